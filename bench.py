@@ -1,0 +1,518 @@
+"""Benchmark of the continuous-batching decode step over a paged KV cache.
+
+One step = a0 host allocator (positions, slots, seq_lens, block tables) + one
+H2D copy of that metadata + a1 RoPE + a2 append + a3 split-KV paged attention
++ a4 LSE merge, on one stream, for every row of the workload.  Steps are
+consecutive decode steps (every row grows by one token per step).
+
+Default workload: ``decode16`` (B=16, L ~ U[128, 2048], 32 query / 8 KV heads,
+d=64, bf16).  Its KV (~36 MB) fits in L2, so L2 is flushed (a 2x-L2 buffer is
+written) before every timed step and only the step itself sits between the
+CUDA events.
+
+Printed JSON line (rank 0):
+  value        whole-job KV throughput: algorithmic attention bytes of all steps
+               / device time of all steps (a0 copy + a1..a4), GB/s
+  attn_gbs     the same bytes / time of a3+a4 only
+  steps_per_s  decode steps per second (device time)
+  roofline     the split-attention kernel (a3): algorithmic bytes per launch /
+               mean launch time, against the measured HBM copy peak
+  e2e          the same metric through ``pkv_decode_step_host`` (host buffers;
+               H2D of q/k/v + metadata and D2H of the output inside the timing)
+  cpu_baseline the float64 oracle timed on this host on a bounded sample
+
+``--impl reference`` times the float64 oracle (the only reference this method
+has) on the host cores for the same workload and metric.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["paged_kv_decode_10_gb300/csrc/attention_kernel.cuh",
+                  "paged_kv_decode_10_gb300/csrc/attention_mma.cu",
+                  "paged_kv_decode_10_gb300/csrc/attention_simt_bf16.cu",
+                  "paged_kv_decode_10_gb300/csrc/attention_simt_f32.cu",
+                  "paged_kv_decode_10_gb300/csrc/attention.cu",
+                  "paged_kv_decode_10_gb300/csrc/common.cuh"]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
+    ap.add_argument("--workload", default="decode16")
+    ap.add_argument("--flags", type=int, default=0, help="1 = CUDA-core attention consumer")
+    ap.add_argument("--parts", type=int, default=0, help="attention partition (0 = default)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-flush", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# shared helpers
+# ---------------------------------------------------------------------------
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload, kernel_hash):
+    """DRAM bytes per launch of the split kernel from the committed ncu summary,
+    only if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(workload)
+    except Exception:
+        return None
+    if not rec or rec.get("kernel_hash") != kernel_hash:
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def attn_bytes(lens_after, Hq, Hkv, d, elem):
+    """Algorithmic bytes of one attention pass (a3+a4): every cached K and V
+    element once, q in, out written, block-table entries and seq_lens read."""
+    lens_after = np.asarray(lens_after, np.int64)
+    kv = int(lens_after.sum()) * Hkv * d * 2 * elem
+    qo = 2 * len(lens_after) * Hq * d * elem
+    tables = int(((lens_after + 15) // 16).sum()) * 4
+    return kv + qo + tables + 4 * len(lens_after)
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# oracle on the host (cpu baseline and the reference arm)
+# ---------------------------------------------------------------------------
+def _oracle_row_job(job):
+    """Runs inside a spawned worker: one row of the step through the oracle."""
+    from oracle.step import decode_step
+    q, k, v, pos, slot, lens, n, kc, vc, scale, dtype = job
+    t0 = time.perf_counter()
+    decode_step(q, k, v, pos, [slot], lens, np.arange(n)[None, :], kc, vc, scale=scale,
+                base=10000.0, dtype=dtype)
+    return time.perf_counter() - t0
+
+
+def oracle_jobs(w, caches, tokens, meta, rows):
+    import torch
+    pos, slots, lens, tables = meta
+    jobs, nbytes = [], 0
+    elem = 2 if w.dtype == "bf16" else 4
+    for b in rows:
+        n = -(-int(lens[b]) // 16)
+        blocks = torch.from_numpy(tables[b, :n].astype(np.int64))
+        kc = caches[0][blocks].double().numpy()
+        vc = caches[1][blocks].double().numpy()
+        j = int(pos[b]) // 16
+        jobs.append(tuple(t[b:b + 1].double().numpy() for t in tokens) +
+                    (pos[b:b + 1], j * 16 + int(slots[b]) % 16, lens[b:b + 1], n, kc, vc,
+                     w.scale, w.dtype))
+        nbytes += attn_bytes([lens[b]], w.Hq, w.Hkv, w.d, elem)
+    return jobs, nbytes
+
+
+def oracle_pool(cores):
+    import multiprocessing as mp
+    env_keys = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+    saved = {k: os.environ.get(k) for k in env_keys}
+    for k in env_keys:
+        os.environ[k] = "1"
+    pool = mp.get_context("spawn").Pool(cores)
+    for k, v in saved.items():
+        if v is None:
+            os.environ.pop(k, None)
+        else:
+            os.environ[k] = v
+    return pool
+
+
+def run_oracle_sample(pool, cores, jobs, nbytes):
+    """Returns (GB/s, compute seconds per core, rows)."""
+    secs = pool.map(_oracle_row_job, jobs, chunksize=1)
+    per_core = sum(secs) / cores
+    return nbytes / per_core / 1e9, per_core, len(jobs)
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+def setup(w, device, parts, flags, steps_total):
+    import torch
+    from paged_kv_decode_10_gb300 import engine, workloads
+    pool_bytes = w.num_blocks * w.Hkv * 16 * w.d * (2 if w.dtype == "bf16" else 4)
+    gen_dev = "cpu" if pool_bytes < (1 << 30) else device
+    k_cache, v_cache = workloads.make_caches(w, gen_dev)
+    bt = w.max_blocks_per_seq(extra_tokens=steps_total + 64)
+    dec = engine.PagedDecoder(w.num_blocks, w.Hq, w.Hkv, w.d, w.dtype, w.B, bt,
+                              initial_free=w.free_order, device=device,
+                              num_parts=parts or None, flags=flags,
+                              k_cache=k_cache.to(device), v_cache=v_cache.to(device))
+    ids = [dec.join(int(L)) for L in w.seq_lens]
+    tokens = [workloads.make_new_tokens(w, s, device) for s in range(steps_total)]
+    return dec, ids, tokens, (k_cache, v_cache) if gen_dev == "cpu" else None
+
+
+def run_gpu(args, rank, world):
+    import torch
+    from paged_kv_decode_10_gb300 import binding, workloads
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    w = workloads.make_workload(args.workload)
+    W, K = args.warmup, args.steps
+    dec, ids, tokens, cpu_caches = setup(w, device, args.parts, args.flags, W + K + 1)
+    assert dec.bt_stride * 16 >= int(w.seq_lens.max()) + W + K + 64
+    elem = 2 if w.dtype == "bf16" else 4
+    stream = torch.cuda.current_stream(device)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush_buf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=device)
+
+    # the oracle sample for the cpu baseline is the first step's state
+    if not args.no_cpu and rank == 0 and cpu_caches is not None:
+        oracle_state = (cpu_caches, [t.cpu() for t in tokens[0]])
+    else:
+        oracle_state = None
+
+    def one_step(s, events=None):
+        B = len(ids)
+        dec.prepare(ids)
+        q, k, v = tokens[s]
+        if events:
+            events[0].record(stream)
+        binding.rope(q, k, dec.positions[:B], w.rope_base, dec.q_rot[:B], dec.k_rot[:B])
+        binding.append(dec.k_rot[:B], v, dec.slots[:B], dec.k_cache, dec.v_cache, dec.err)
+        if events:
+            events[1].record(stream)
+        binding.decode_attn_split(dec.q_rot[:B], dec.k_cache, dec.v_cache, dec.tables[:B],
+                                  dec.seq_lens[:B], dec.scale, dec.num_parts, dec.workspace,
+                                  dec.out[:B], flags=dec.flags, err=dec.err)
+        if events:
+            events[2].record(stream)
+        binding.lse_merge(dec.workspace, dec.seq_lens[:B], dec.bt_stride, B, w.Hq, w.Hkv, w.d,
+                          dec.num_parts, dec.out[:B])
+        if events:
+            events[3].record(stream)
+
+    lens_after = []
+    meta0 = None
+    for s in range(W):
+        one_step(s)
+        if s == 0:
+            meta0 = [np.array(x) for x in dec.last_metadata]
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    for i in range(K):
+        if not args.no_flush:
+            flush_buf.add_(1)
+        e = evs[i]
+        e[4].record(stream)                   # before a0's H2D copy
+        one_step(W + i, e[:4])
+        lens_after.append(np.array(dec.last_metadata[2]))
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    step_ms = [e[4].elapsed_time(e[3]) for e in evs]
+    split_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    attn_ms = [e[1].elapsed_time(e[3]) for e in evs]
+    total_s = sum(step_ms) / 1e3
+    if world > 1:
+        t = torch.tensor([total_s], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_s = float(t.item())
+    bytes_steps = [attn_bytes(la, w.Hq, w.Hkv, w.d, elem) for la in lens_after]
+    kv_only = [int(np.asarray(la, np.int64).sum()) * w.Hkv * w.d * 2 * elem for la in lens_after]
+    total_bytes = sum(bytes_steps) * world
+    value = total_bytes / total_s / 1e9
+    attn_gbs = sum(bytes_steps) / (sum(attn_ms) / 1e3) / 1e9
+    # split kernel alone: everything but the output write (done partly by a4)
+    split_bytes = [b - len(la) * w.Hq * w.d * elem for b, la in zip(bytes_steps, lens_after)]
+    split_gbs = (sum(split_bytes) / len(split_bytes)) / (statistics.mean(split_ms) / 1e3) / 1e9
+    assert dec.device_errors() == 0, "device error flag set during the bench"
+
+    peak, peak_kind = measured_peak()
+    khash = kernel_source_hash()
+    traffic = profiled_traffic(args.workload, khash)
+    result = {
+        "metric": "paged decode-attn achieved HBM GB/s (% of GB300 peak); batched decode steps/s",
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(total_s * 1e3 / K, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic (seeded N(0,1) q/k/v and KV pool; seeded ragged lengths and "
+                "scattered block tables)",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.d,
+                   "block_size": 16, "mean_kv_len": float(np.mean(lens_after[0])),
+                   "pool_blocks": w.num_blocks, "num_parts": dec.num_parts,
+                   "consumer": "simt" if (args.flags & 1 or w.dtype == "f32") else "mma.sync",
+                   "l2": "flushed before every timed step" if not args.no_flush else "not flushed",
+                   "parallelism": "replicas" if world > 1 else "single-gpu"},
+        "steps_per_s": round(K / (sum(step_ms) / 1e3), 1),
+        "attn_gbs": round(attn_gbs, 2),
+        "pct_of_peak": round(100 * attn_gbs / peak, 2),
+        "kv_bytes_per_step": int(statistics.mean(kv_only)),
+        "roofline": {"bound": "hbm", "kernel": "attn_split_kernel (a3)",
+                     "achieved": round(split_gbs, 2), "peak": peak, "peak_kind": peak_kind,
+                     "unit": "GB/s", "frac": round(split_gbs / peak, 4),
+                     "traffic": traffic,
+                     "algorithmic_bytes_per_launch": int(statistics.mean(split_bytes)),
+                     "mean_launch_us": round(1e3 * statistics.mean(split_ms), 3),
+                     "kernel_hash": khash},
+        "gpu_launches": 4 * K,
+        "clocks": clocks,
+    }
+    return result, dec, ids, tokens, oracle_state, meta0, w
+
+
+def run_e2e(args, dec, ids, tokens, w):
+    """Same metric through pkv_decode_step_host: host allocator, H2D of the
+    step's inputs from pinned memory, the step, D2H of the output, wait."""
+    import torch
+    from paged_kv_decode_10_gb300 import binding
+    device = dec.device
+    B = len(ids)
+    elem = 2 if w.dtype == "bf16" else 4
+    pinned = [t.cpu().pin_memory() for t in tokens[-1]]
+    out_h = torch.empty((B, w.Hq, w.d), dtype=dec.tdtype).pin_memory()
+    meta_h = (torch.empty(B, dtype=torch.int32).pin_memory(),
+              torch.empty(B, dtype=torch.int64).pin_memory(),
+              torch.empty(B, dtype=torch.int32).pin_memory(),
+              torch.empty((B, dec.bt_stride), dtype=torch.int32).pin_memory())
+    dq = torch.empty_like(tokens[-1][0])
+    dk = torch.empty_like(tokens[-1][1])
+    dv = torch.empty_like(tokens[-1][2])
+    args_s = dec.step_args(B, dq, dk, dv)
+    io = binding.host_io(*pinned, *meta_h, out_h)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush_buf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=device)
+    h2d = sum(t.numel() * t.element_size() for t in pinned) + \
+        sum(t.numel() * t.element_size() for t in meta_h)
+    d2h = out_h.numel() * out_h.element_size()
+    n = max(3, min(args.steps, 50))
+    secs, nbytes = 0.0, 0
+    for i in range(n + 3):
+        flush_buf.add_(1)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        views = tuple(m.numpy() for m in meta_h)
+        dec.alloc.prepare_step(ids, dec.bt_stride, out=(views[0], views[1], views[2], views[3]))
+        binding.decode_step_host(args_s, io)
+        dt = time.perf_counter() - t0
+        if i >= 3:
+            secs += dt
+            nbytes += attn_bytes(views[2], w.Hq, w.Hkv, w.d, elem)
+    return {"value": round(nbytes / secs / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "steps": n, "ms_per_step": round(1e3 * secs / n, 4)}
+
+
+def cpu_baseline(w, oracle_state, meta0, budget_s):
+    cores = min(16, host_cores())
+    caches, toks = oracle_state
+    pool = oracle_pool(cores)
+    try:
+        rows = list(range(w.B))
+        jobs, nbytes = oracle_jobs(w, caches, toks, meta0, rows)
+        gbs, per_core, nrows = run_oracle_sample(pool, cores, jobs, nbytes)
+        # repeat whole passes until the budget is used (bounded)
+        reps = 1
+        t_end = time.perf_counter() + budget_s
+        total_per_core = per_core
+        while time.perf_counter() < t_end and reps < 50:
+            _, pc, _ = run_oracle_sample(pool, cores, jobs, nbytes)
+            total_per_core += pc
+            reps += 1
+        gbs = reps * nbytes / total_per_core / 1e9
+    finally:
+        pool.close()
+        pool.join()
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{reps} pass(es) over all {nrows} rows of the first step (float64 "
+                      f"numpy oracle, one spawned single-threaded worker per core; "
+                      f"time = summed worker compute seconds / cores)"}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle on the host cores
+# ---------------------------------------------------------------------------
+def run_reference(args, rank, world):
+    import torch
+    from oracle.allocator import BlockAllocatorModel
+    from paged_kv_decode_10_gb300 import workloads
+    if rank != 0:
+        return None
+    w = workloads.make_workload(args.workload)
+    caches = workloads.make_caches(w, "cpu")
+    toks = workloads.make_new_tokens(w, 0, "cpu")
+    bt = w.max_blocks_per_seq()
+    model = BlockAllocatorModel(w.num_blocks, max_seqs=w.B, max_blocks_per_seq=bt,
+                                initial_free=w.free_order)
+    mids = [model.join(int(L)) for L in w.seq_lens]
+    meta = model.prepare_step(mids, bt)
+    cores = min(16, host_cores())
+    pool = oracle_pool(cores)
+    try:
+        jobs, nbytes = oracle_jobs(w, caches, toks, meta, range(w.B))
+        # each bench step is one row of the workload (rows taken in turn)
+        per_row = [(j, attn_bytes([meta[2][b]], w.Hq, w.Hkv, w.d,
+                                  2 if w.dtype == "bf16" else 4)) for b, j in enumerate(jobs)]
+        for i in range(args.warmup):
+            run_oracle_sample(pool, cores, [per_row[i % w.B][0]], per_row[i % w.B][1])
+        secs, total = 0.0, 0
+        for i in range(args.steps):
+            job, nb = per_row[i % w.B]
+            _, per_core, _ = run_oracle_sample(pool, 1, [job], nb)
+            secs += per_core
+            total += nb
+    finally:
+        pool.close()
+        pool.join()
+    value = total / secs / 1e9
+    return {"impl": "reference", "metric": "paged decode-attn achieved HBM GB/s (% of GB300 "
+            "peak); batched decode steps/s", "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * secs / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
+                       "head_dim": w.d, "block_size": 16},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+                             "kind": "oracle",
+                             "sample": "one row of the workload's first decode step per bench "
+                                       "step, rows in turn (float64 numpy oracle, single "
+                                       "thread)"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if world > 1 and rank != 0:
+            return
+        res = run_reference(args, rank, world)
+        print(json.dumps(res), flush=True)
+        return
+    import torch
+    if world > 1:
+        torch.distributed.init_process_group(
+            backend="nccl", init_method="env://")
+    from paged_kv_decode_10_gb300 import build
+    build.build()
+    result, dec, ids, tokens, oracle_state, meta0, w = run_gpu(args, rank, world)
+    if rank == 0:
+        if not args.no_e2e:
+            result["e2e"] = run_e2e(args, dec, ids, tokens, w)
+        if not args.no_cpu and oracle_state is not None and world == 1:
+            result["cpu_baseline"] = cpu_baseline(w, oracle_state, meta0, args.cpu_seconds)
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

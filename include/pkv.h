@@ -1,0 +1,259 @@
+/*
+ * pkv.h -- C ABI of the paged-KV continuous-batching decode step (GB300, sm_103a).
+ *
+ * One decode step appends one token to every row of a batch and attends over
+ * each row's cached keys/values.  It has four device parts and one host part:
+ *
+ *   a0  host block allocator: positions, slot_mapping, seq_lens, block tables
+ *   a1  pkv_rope               rotate-half RoPE of the new q and k at per-row positions
+ *   a2  pkv_append             write rotated k and raw v into the cache slot
+ *   a3  pkv_decode_attn_split  grouped-query attention through block tables,
+ *                              split over a page-balanced partition, online softmax
+ *   a4  pkv_lse_merge          log-sum-exp merge of the split partials
+ *
+ * Sources: "neurogrid releases" v0.7.0 (paged KV cache in fixed 16-token blocks,
+ * O(1) block allocator with per-sequence block tables, paged attention with GQA),
+ * v0.6.0 (flash decode: online softmax over KV tiles), v0.8.0 (kv_len =
+ * position + 1 computed on the GPU, zero device-to-host copies, every kernel on
+ * one caller stream); helexa issue 121 "continuous batching -- batched decode +
+ * engine", slice 1 (per-row RoPE positions, rotate-half, keys stored post-RoPE,
+ * additive (B,1,1,S) mask over each row's padding gap); "cortex-engine writeup",
+ * block-sparse attention kernel (a row with zero softmax denominator outputs
+ * zeros instead of NaN).
+ *
+ * Conventions
+ *  - Every call returns PKV_OK (0) or a PKV_ERR_* code; pkv_last_error()
+ *    returns a message for the calling thread's last failure.
+ *  - The library never allocates device memory.  The caller owns every device
+ *    buffer and the CUDA stream.  Device calls are asynchronous on `stream`
+ *    (a cudaStream_t passed as void*, NULL = legacy default stream), make no
+ *    device-to-host copy and check cudaGetLastError after each launch.
+ *  - Every tensor is dense and row-major in the layout stated.  dtype is
+ *    PKV_F32 or PKV_BF16 and applies to q, k, v, the caches and the output.
+ *  - dev_err_flag (nullable, device int32): kernels that meet an out-of-range
+ *    block id, slot or length atomically OR a PKV_DEVERR_* bit into it and skip
+ *    that access instead of faulting.  The caller clears it.
+ *  - The allocator is host-only and not thread-safe: one owner per allocator.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define PKV_OK 0
+#define PKV_ERR_INVALID_ARG 1   /* null pointer, bad size, bad stride, duplicate row */
+#define PKV_ERR_OUT_OF_BLOCKS 2 /* the free list cannot satisfy the request; nothing changed */
+#define PKV_ERR_UNKNOWN_SEQ 3   /* sequence id not live */
+#define PKV_ERR_UNSUPPORTED 4   /* dtype, head_dim, group size or block size not built */
+#define PKV_ERR_CUDA 5          /* a CUDA runtime/driver call failed; see pkv_last_error */
+
+#define PKV_F32 0
+#define PKV_BF16 1
+
+#define PKV_BLOCK_SIZE 16       /* tokens per KV block ("neurogrid releases" v0.7.0) */
+
+/* bits OR-ed into dev_err_flag */
+#define PKV_DEVERR_BAD_BLOCK 1  /* a block table entry outside [0, num_blocks) */
+#define PKV_DEVERR_BAD_SLOT 2   /* a slot outside [0, num_blocks * 16) */
+#define PKV_DEVERR_BAD_LEN 4    /* seq_len < 0, or longer than bt_stride*16 or bias_stride */
+#define PKV_DEVERR_TIMEOUT 8    /* an internal pipeline wait gave up (never expected) */
+
+/* flags for the attention calls */
+#define PKV_ATTN_SIMT 1         /* use the CUDA-core consumer instead of mma.sync (bf16 only;
+                                   f32 always uses CUDA cores) */
+
+/* Message for the calling thread's last failed call ("" if none). */
+const char *pkv_last_error(void);
+/* ABI version of this header (bumped on any signature change). */
+int pkv_abi_version(void);
+
+/* ======================================================================== */
+/* a0: host block allocator                                                  */
+/* ======================================================================== */
+/*
+ * Policy ("neurogrid releases" v0.7.0: O(1) alloc/free, per-sequence block
+ * tables; v0.8.0: kv_len = position + 1):
+ *  - The free list is a stack, seeded bottom-to-top with `initial_free` (a
+ *    permutation of 0..num_blocks-1; NULL = 0,1,2,...).  Pop takes the top.
+ *  - join pops ceil(prefix_len/16) blocks in table order and takes the
+ *    smallest free sequence id; leave pushes the sequence's blocks in table
+ *    order and frees its id.
+ *  - prepare_step appends one token to each listed sequence: position = L
+ *    (cached length before the step); if L % 16 == 0 a block is popped first;
+ *    slot = table[L/16]*16 + L%16; the length becomes L+1.
+ *  - A request that cannot be met returns PKV_ERR_OUT_OF_BLOCKS and changes
+ *    nothing.  Each pop/push is O(1).
+ */
+typedef struct pkv_alloc pkv_alloc;
+
+/* block_size must be 16.  max_blocks_per_seq bounds each block table.
+ * On success *out owns the allocator (free with pkv_alloc_destroy). */
+int pkv_alloc_create(int32_t num_blocks, int32_t block_size, int32_t max_seqs,
+                     int32_t max_blocks_per_seq, const int32_t *initial_free,
+                     pkv_alloc **out);
+void pkv_alloc_destroy(pkv_alloc *a);
+
+/* A new sequence whose first prefix_len tokens are already in its blocks
+ * (their contents are written by the caller, e.g. by a prefill). */
+int pkv_seq_join(pkv_alloc *a, int32_t prefix_len, int32_t *seq_id);
+int pkv_seq_leave(pkv_alloc *a, int32_t seq_id);
+
+/*
+ * Host part of one decode step for the B listed (distinct, live) sequences.
+ * Outputs (host arrays, row b = seq_ids[b]):
+ *   positions[B]      int32  position of the new token (= cached length before)
+ *   slot_mapping[B]   int64  cache slot of the new token
+ *   seq_lens[B]       int32  length after the append (what attention reads)
+ *   block_tables[B*bt_stride] int32, row-major, padded with -1
+ * Atomic: on any error nothing changes.
+ */
+int pkv_prepare_step(pkv_alloc *a, const int32_t *seq_ids, int32_t B,
+                     int32_t *positions, int64_t *slot_mapping, int32_t *seq_lens,
+                     int32_t *block_tables, int32_t bt_stride);
+
+int pkv_seq_len(const pkv_alloc *a, int32_t seq_id, int32_t *len);
+/* Copies up to cap block ids of the sequence's table into out; *n = table length. */
+int pkv_seq_blocks(const pkv_alloc *a, int32_t seq_id, int32_t *out, int32_t cap,
+                   int32_t *n);
+int pkv_num_free(const pkv_alloc *a, int32_t *n);
+/* Copies the free stack bottom-to-top (up to cap entries); *n = its size. */
+int pkv_alloc_dump(const pkv_alloc *a, int32_t *free_stack, int32_t cap, int32_t *n);
+
+/* ======================================================================== */
+/* a1: RoPE (helexa issue 121, slice 1: batch_cos_sin at per-row positions,   */
+/*     rotate-half apply)                                                    */
+/* ======================================================================== */
+/*
+ * q [B,Hq,d], k [B,Hkv,d] -> q_out [B,Hq,d], k_out [B,Hkv,d] (device, dtype).
+ * For pair i < d/2 at position p = positions[b]:
+ *   theta = p * base^(-2i/d)
+ *   out[i]     = x[i] cos(theta) - x[i+d/2] sin(theta)
+ *   out[i+d/2] = x[i+d/2] cos(theta) + x[i] sin(theta)
+ * theta is formed and reduced modulo 2*pi in double precision, then rotated
+ * in float32 and rounded once to dtype.  In-place (q_out == q) is allowed.
+ * d even, 2 <= d <= 256.
+ */
+int pkv_rope(const void *q, const void *k, void *q_out, void *k_out,
+             const int32_t *positions, int32_t B, int32_t Hq, int32_t Hkv, int32_t d,
+             float base, int32_t dtype, void *stream);
+
+/* ======================================================================== */
+/* a2: append ("neurogrid releases" v0.7.0: fixed 16-token blocks)           */
+/* ======================================================================== */
+/*
+ * k_cache, v_cache: [num_blocks, Hkv, 16, d] (device, dtype).
+ * For each row b with slot = slot_mapping[b] >= 0:
+ *   k_cache[slot/16, h, slot%16, :] = k_rot[b, h, :]
+ *   v_cache[slot/16, h, slot%16, :] = v[b, h, :]
+ * A negative slot appends nothing (padding row).  A slot >= num_blocks*16 sets
+ * PKV_DEVERR_BAD_SLOT and is skipped.  d*sizeof(dtype) must be a multiple of 16.
+ */
+int pkv_append(const void *k_rot, const void *v, const int64_t *slot_mapping,
+               void *k_cache, void *v_cache, int32_t B, int32_t Hkv, int32_t d,
+               int32_t num_blocks, int32_t dtype, int32_t *dev_err_flag, void *stream);
+
+/* ======================================================================== */
+/* a3 + a4: split-KV paged GQA decode attention and its LSE merge            */
+/* ("neurogrid releases" v0.7.0 paged attention with GQA, v0.6.0 flash       */
+/*  decode; "cortex-engine writeup" zero-denominator guard)                  */
+/* ======================================================================== */
+/*
+ * Row b attends over its first seq_lens[b] tokens (the token appended in this
+ * step included).  Token t of row b is row t%16 of block
+ * block_tables[b*bt_stride + t/16].  Query head h uses KV head h / (Hq/Hkv).
+ *   s_t   = (q_rot[b,h] . k_t) * scale + attn_bias[b*bias_stride + t]
+ *   out   = sum_t softmax(s)_t v_t            (float32 accumulation)
+ * attn_bias (device float32, nullable) is additive; -inf excludes a token (the
+ * value at an excluded token must still be finite).  A row with no tokens, or
+ * whose tokens are all excluded, outputs zeros.
+ *
+ * Partition: the pages of all (row, KV head) units, in row-major order, form
+ * one list of P pages; part c of num_parts owns pages
+ * [floor(c*P/num_parts), floor((c+1)*P/num_parts)) and runs as one CTA.  A
+ * unit whose pages lie in one part is written to `out` directly by
+ * pkv_decode_attn_split; every other unit leaves one float32 (o, lse) partial
+ * per part it touches in `workspace`, and pkv_lse_merge combines them
+ * (M = max lse; out = sum exp(lse_s - M) o_s / sum exp(lse_s - M)) and also
+ * writes the zeros of empty rows.  The two calls must run in this order with
+ * the same arguments; `out` is complete only after pkv_lse_merge.
+ *
+ * Supported: dtype PKV_BF16 or PKV_F32; d in {64, 128}; Hq/Hkv in {1,2,4,8};
+ * B <= 65536.  q_rot [B,Hq,d]; out [B,Hq,d] (device, dtype).
+ * num_parts <= 0 selects pkv_attn_default_parts for the current device.
+ */
+int pkv_attn_default_parts(int32_t d, int32_t dtype, int32_t flags, int32_t *num_parts);
+int pkv_attn_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t d,
+                             int32_t num_parts, size_t *bytes);
+
+int pkv_decode_attn_split(const void *q_rot, const void *k_cache, const void *v_cache,
+                          int32_t num_blocks, const int32_t *block_tables,
+                          int32_t bt_stride, const int32_t *seq_lens,
+                          const float *attn_bias, int32_t bias_stride, int32_t B,
+                          int32_t Hq, int32_t Hkv, int32_t d, float scale,
+                          int32_t num_parts, void *workspace, size_t workspace_bytes,
+                          void *out, int32_t dtype, int32_t flags,
+                          int32_t *dev_err_flag, void *stream);
+
+/* bt_stride and bias_stride (0 when no bias was given) are the values passed to
+ * pkv_decode_attn_split: they decide which rows are valid, exactly as there. */
+int pkv_lse_merge(const void *workspace, size_t workspace_bytes, const int32_t *seq_lens,
+                  int32_t bt_stride, int32_t bias_stride, int32_t B, int32_t Hq,
+                  int32_t Hkv, int32_t d, int32_t num_parts, void *out, int32_t dtype,
+                  void *stream);
+
+/* ======================================================================== */
+/* the whole device step: a1 -> a2 -> a3 -> a4 on one stream                */
+/* ======================================================================== */
+typedef struct pkv_step_args {
+  const void *q, *k, *v;             /* new tokens: [B,Hq,d], [B,Hkv,d], [B,Hkv,d] */
+  void *q_rot, *k_rot;               /* RoPE outputs (device scratch owned by the caller) */
+  void *k_cache, *v_cache;           /* [num_blocks,Hkv,16,d] */
+  int32_t num_blocks;
+  const int32_t *positions;          /* [B] */
+  const int64_t *slot_mapping;       /* [B] */
+  const int32_t *seq_lens;           /* [B] lengths after the append */
+  const int32_t *block_tables;       /* [B*bt_stride] */
+  int32_t bt_stride;
+  const float *attn_bias;            /* nullable, [B*bias_stride] */
+  int32_t bias_stride;
+  int32_t B, Hq, Hkv, d;
+  float scale, rope_base;
+  int32_t dtype, flags, num_parts;
+  void *workspace;                   /* pkv_attn_workspace_bytes(...) bytes */
+  size_t workspace_bytes;
+  void *out;                         /* [B,Hq,d] */
+  int32_t *dev_err_flag;             /* nullable */
+} pkv_step_args;
+
+/* All device pointers in *args; asynchronous on stream. */
+int pkv_decode_step(const pkv_step_args *args, void *stream);
+
+/* Host-side buffers for pkv_decode_step_host (pinned memory recommended). */
+typedef struct pkv_step_host_io {
+  const void *q, *k, *v;             /* [B,Hq,d], [B,Hkv,d], [B,Hkv,d] */
+  const int32_t *positions;
+  const int64_t *slot_mapping;
+  const int32_t *seq_lens;
+  const int32_t *block_tables;       /* [B*bt_stride] */
+  void *out;                         /* [B,Hq,d] */
+} pkv_step_host_io;
+
+/*
+ * End-to-end step from host memory: copies the host inputs into the device
+ * buffers named by *dev (q, k, v, positions, slot_mapping, seq_lens,
+ * block_tables), runs pkv_decode_step, copies dev->out back to host->out and
+ * waits for the stream.  Returns after the result is in host memory.
+ */
+int pkv_decode_step_host(const pkv_step_args *dev, const pkv_step_host_io *host,
+                         void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PKV_H */

@@ -1,0 +1,379 @@
+"""ctypes binding of ``libpkv.so`` (the C ABI declared in ``include/pkv.h``).
+
+Argument marshalling only: torch tensors become device pointers, the current
+torch CUDA stream becomes the ``cudaStream_t`` argument, numpy arrays hold the
+allocator's host outputs.  Every computation runs in the library's CUDA kernels
+or in its C++ allocator; if the library has not been built this module raises
+instead of falling back to anything else.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+OK, ERR_INVALID_ARG, ERR_OUT_OF_BLOCKS, ERR_UNKNOWN_SEQ, ERR_UNSUPPORTED, ERR_CUDA = range(6)
+F32, BF16 = 0, 1
+BLOCK_SIZE = 16
+DEVERR_BAD_BLOCK, DEVERR_BAD_SLOT, DEVERR_BAD_LEN, DEVERR_TIMEOUT = 1, 2, 4, 8
+ATTN_SIMT = 1
+
+_c_i32 = ctypes.c_int32
+_c_i64 = ctypes.c_int64
+_vp = ctypes.c_void_p
+_p_i32 = ctypes.POINTER(ctypes.c_int32)
+_p_i64 = ctypes.POINTER(ctypes.c_int64)
+_p_f32 = ctypes.POINTER(ctypes.c_float)
+_size_t = ctypes.c_size_t
+
+
+class PkvError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"pkv error {code}: {msg}")
+        self.code = code
+
+
+class OutOfBlocks(PkvError):
+    pass
+
+
+class UnknownSequence(PkvError):
+    pass
+
+
+class StepArgs(ctypes.Structure):
+    _fields_ = [
+        ("q", _vp), ("k", _vp), ("v", _vp),
+        ("q_rot", _vp), ("k_rot", _vp),
+        ("k_cache", _vp), ("v_cache", _vp),
+        ("num_blocks", _c_i32),
+        ("positions", _vp), ("slot_mapping", _vp), ("seq_lens", _vp),
+        ("block_tables", _vp), ("bt_stride", _c_i32),
+        ("attn_bias", _vp), ("bias_stride", _c_i32),
+        ("B", _c_i32), ("Hq", _c_i32), ("Hkv", _c_i32), ("d", _c_i32),
+        ("scale", ctypes.c_float), ("rope_base", ctypes.c_float),
+        ("dtype", _c_i32), ("flags", _c_i32), ("num_parts", _c_i32),
+        ("workspace", _vp), ("workspace_bytes", _size_t),
+        ("out", _vp), ("dev_err_flag", _vp),
+    ]
+
+
+class StepHostIO(ctypes.Structure):
+    _fields_ = [
+        ("q", _vp), ("k", _vp), ("v", _vp),
+        ("positions", _vp), ("slot_mapping", _vp), ("seq_lens", _vp),
+        ("block_tables", _vp), ("out", _vp),
+    ]
+
+
+# name -> (restype, argtypes); every symbol declared in include/pkv.h
+SIGNATURES = {
+    "pkv_last_error": (ctypes.c_char_p, []),
+    "pkv_abi_version": (ctypes.c_int, []),
+    "pkv_alloc_create": (ctypes.c_int, [_c_i32, _c_i32, _c_i32, _c_i32, _p_i32,
+                                        ctypes.POINTER(_vp)]),
+    "pkv_alloc_destroy": (None, [_vp]),
+    "pkv_seq_join": (ctypes.c_int, [_vp, _c_i32, _p_i32]),
+    "pkv_seq_leave": (ctypes.c_int, [_vp, _c_i32]),
+    "pkv_prepare_step": (ctypes.c_int, [_vp, _p_i32, _c_i32, _p_i32, _p_i64, _p_i32, _p_i32,
+                                        _c_i32]),
+    "pkv_seq_len": (ctypes.c_int, [_vp, _c_i32, _p_i32]),
+    "pkv_seq_blocks": (ctypes.c_int, [_vp, _c_i32, _p_i32, _c_i32, _p_i32]),
+    "pkv_num_free": (ctypes.c_int, [_vp, _p_i32]),
+    "pkv_alloc_dump": (ctypes.c_int, [_vp, _p_i32, _c_i32, _p_i32]),
+    "pkv_rope": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _c_i32, _c_i32, _c_i32, _c_i32,
+                                ctypes.c_float, _c_i32, _vp]),
+    "pkv_append": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _c_i32, _c_i32, _c_i32, _c_i32,
+                                  _c_i32, _vp, _vp]),
+    "pkv_attn_default_parts": (ctypes.c_int, [_c_i32, _c_i32, _c_i32, _p_i32]),
+    "pkv_attn_workspace_bytes": (ctypes.c_int, [_c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
+                                                ctypes.POINTER(_size_t)]),
+    "pkv_decode_attn_split": (ctypes.c_int, [_vp, _vp, _vp, _c_i32, _vp, _c_i32, _vp, _vp,
+                                             _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
+                                             ctypes.c_float, _c_i32, _vp, _size_t, _vp, _c_i32,
+                                             _c_i32, _vp, _vp]),
+    "pkv_lse_merge": (ctypes.c_int, [_vp, _size_t, _vp, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
+                                     _c_i32, _c_i32, _vp, _c_i32, _vp]),
+    "pkv_decode_step": (ctypes.c_int, [ctypes.POINTER(StepArgs), _vp]),
+    "pkv_decode_step_host": (ctypes.c_int, [ctypes.POINTER(StepArgs),
+                                            ctypes.POINTER(StepHostIO), _vp]),
+}
+
+_LIB = None
+
+
+def library_path():
+    return _build.LIB
+
+
+def load():
+    """Load the built library (raises if it has not been built)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"CUDA library {path} is missing: build it with "
+            "`python -m paged_kv_decode_10_gb300.build` (no CPU fallback exists)")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _LIB = lib
+    return lib
+
+
+def _check(rc):
+    if rc == OK:
+        return
+    msg = load().pkv_last_error().decode(errors="replace")
+    if rc == ERR_OUT_OF_BLOCKS:
+        raise OutOfBlocks(rc, msg)
+    if rc == ERR_UNKNOWN_SEQ:
+        raise UnknownSequence(rc, msg)
+    raise PkvError(rc, msg)
+
+
+# --------------------------------------------------------------------------
+# host allocator
+# --------------------------------------------------------------------------
+def _np_ptr(a, ctype):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+class BlockAllocator:
+    """Host block allocator (C++); policy in ``include/pkv.h``."""
+
+    def __init__(self, num_blocks, max_seqs, max_blocks_per_seq, initial_free=None):
+        lib = load()
+        handle = _vp()
+        init = None
+        if initial_free is not None:
+            self._init = np.ascontiguousarray(initial_free, dtype=np.int32)
+            init = _np_ptr(self._init, ctypes.c_int32)
+        _check(lib.pkv_alloc_create(num_blocks, BLOCK_SIZE, max_seqs, max_blocks_per_seq, init,
+                                    ctypes.byref(handle)))
+        self._h = handle
+        self._lib = lib
+        self.num_blocks = num_blocks
+
+    def close(self):
+        if self._h:
+            self._lib.pkv_alloc_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def join(self, prefix_len):
+        sid = ctypes.c_int32()
+        _check(self._lib.pkv_seq_join(self._h, int(prefix_len), ctypes.byref(sid)))
+        return sid.value
+
+    def leave(self, seq_id):
+        _check(self._lib.pkv_seq_leave(self._h, int(seq_id)))
+
+    def prepare_step(self, seq_ids, bt_stride, out=None):
+        """Returns ``positions, slot_mapping, seq_lens, block_tables`` (numpy).
+        ``out`` may supply preallocated (e.g. pinned) arrays to fill."""
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int32)
+        B = len(ids)
+        if out is None:
+            out = (np.empty(B, np.int32), np.empty(B, np.int64), np.empty(B, np.int32),
+                   np.empty((B, bt_stride), np.int32))
+        pos, slots, lens, tables = out
+        _check(self._lib.pkv_prepare_step(self._h, _np_ptr(ids, ctypes.c_int32), B,
+                                          _np_ptr(pos, ctypes.c_int32),
+                                          _np_ptr(slots, ctypes.c_int64),
+                                          _np_ptr(lens, ctypes.c_int32),
+                                          _np_ptr(tables, ctypes.c_int32), int(bt_stride)))
+        return pos, slots, lens, tables
+
+    def seq_len(self, seq_id):
+        n = ctypes.c_int32()
+        _check(self._lib.pkv_seq_len(self._h, int(seq_id), ctypes.byref(n)))
+        return n.value
+
+    def seq_blocks(self, seq_id):
+        n = ctypes.c_int32()
+        _check(self._lib.pkv_seq_blocks(self._h, int(seq_id), None, 0, ctypes.byref(n)))
+        buf = np.empty(n.value, np.int32)
+        _check(self._lib.pkv_seq_blocks(self._h, int(seq_id), _np_ptr(buf, ctypes.c_int32),
+                                        n.value, ctypes.byref(n)))
+        return buf.tolist()
+
+    def num_free(self):
+        n = ctypes.c_int32()
+        _check(self._lib.pkv_num_free(self._h, ctypes.byref(n)))
+        return n.value
+
+    def free_stack(self):
+        n = ctypes.c_int32()
+        _check(self._lib.pkv_alloc_dump(self._h, None, 0, ctypes.byref(n)))
+        buf = np.empty(n.value, np.int32)
+        _check(self._lib.pkv_alloc_dump(self._h, _np_ptr(buf, ctypes.c_int32), n.value,
+                                        ctypes.byref(n)))
+        return buf.tolist()
+
+
+# --------------------------------------------------------------------------
+# device calls (torch tensors in, torch tensors out)
+# --------------------------------------------------------------------------
+def _torch():
+    import torch
+    return torch
+
+
+def dtype_code(t):
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise PkvError(ERR_UNSUPPORTED, f"dtype {t.dtype}")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise PkvError(ERR_INVALID_ARG, "tensor must be on a CUDA device")
+    if not t.is_contiguous():
+        raise PkvError(ERR_INVALID_ARG, "tensor must be contiguous")
+    return _vp(t.data_ptr())
+
+
+def _stream(stream=None):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return _vp(s.cuda_stream)
+
+
+def rope(q, k, positions, base=10000.0, q_out=None, k_out=None, stream=None):
+    """a1: rotate-half RoPE of ``q [B,Hq,d]`` and ``k [B,Hkv,d]`` at ``positions [B]`` (int32)."""
+    torch = _torch()
+    q_out = torch.empty_like(q) if q_out is None else q_out
+    k_out = torch.empty_like(k) if k_out is None else k_out
+    B, Hq, d = q.shape
+    _check(load().pkv_rope(_ptr(q), _ptr(k), _ptr(q_out), _ptr(k_out), _ptr(positions), B, Hq,
+                           k.shape[1], d, float(base), dtype_code(q), _stream(stream)))
+    return q_out, k_out
+
+
+def append(k_rot, v, slot_mapping, k_cache, v_cache, err=None, stream=None):
+    """a2: write ``k_rot``/``v`` ``[B,Hkv,d]`` into cache slots ``slot_mapping [B]`` (int64)."""
+    B, Hkv, d = k_rot.shape
+    _check(load().pkv_append(_ptr(k_rot), _ptr(v), _ptr(slot_mapping), _ptr(k_cache),
+                             _ptr(v_cache), B, Hkv, d, k_cache.shape[0], dtype_code(k_rot),
+                             _ptr(err), _stream(stream)))
+
+
+def default_parts(d, dtype, flags=0):
+    n = ctypes.c_int32()
+    _check(load().pkv_attn_default_parts(d, dtype, flags, ctypes.byref(n)))
+    return n.value
+
+
+def workspace_bytes(B, Hq, Hkv, d, num_parts):
+    n = _size_t()
+    _check(load().pkv_attn_workspace_bytes(B, Hq, Hkv, d, num_parts, ctypes.byref(n)))
+    return n.value
+
+
+def alloc_workspace(B, Hq, Hkv, d, num_parts, device=None):
+    torch = _torch()
+    nbytes = workspace_bytes(B, Hq, Hkv, d, num_parts)
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def decode_attn_split(q_rot, k_cache, v_cache, block_tables, seq_lens, scale, num_parts,
+                      workspace, out, attn_bias=None, flags=0, err=None, stream=None):
+    """a3: split-KV paged GQA attention (fills ``out`` for single-part units and
+    the workspace partials for the rest)."""
+    B, Hq, d = q_rot.shape
+    Hkv = k_cache.shape[1]
+    bias_stride = attn_bias.shape[1] if attn_bias is not None else 0
+    _check(load().pkv_decode_attn_split(
+        _ptr(q_rot), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0], _ptr(block_tables),
+        block_tables.shape[1], _ptr(seq_lens), _ptr(attn_bias), bias_stride, B, Hq, Hkv, d,
+        float(scale), int(num_parts), _ptr(workspace), workspace.numel(), _ptr(out),
+        dtype_code(q_rot), int(flags), _ptr(err), _stream(stream)))
+
+
+def lse_merge(workspace, seq_lens, bt_stride, B, Hq, Hkv, d, num_parts, out, bias_stride=0,
+              stream=None):
+    """a4: LSE merge of the split partials into ``out``."""
+    _check(load().pkv_lse_merge(_ptr(workspace), workspace.numel(), _ptr(seq_lens),
+                                int(bt_stride), int(bias_stride), B, Hq, Hkv, d, int(num_parts),
+                                _ptr(out), dtype_code(out), _stream(stream)))
+
+
+def decode_attention(q_rot, k_cache, v_cache, block_tables, seq_lens, scale, num_parts=None,
+                     workspace=None, out=None, attn_bias=None, flags=0, err=None, stream=None):
+    """a3 + a4: returns ``out [B,Hq,d]``."""
+    torch = _torch()
+    B, Hq, d = q_rot.shape
+    Hkv = k_cache.shape[1]
+    if num_parts is None:
+        num_parts = default_parts(d, dtype_code(q_rot), flags)
+    if workspace is None:
+        workspace = alloc_workspace(B, Hq, Hkv, d, num_parts, q_rot.device)
+    if out is None:
+        out = torch.empty_like(q_rot)
+    decode_attn_split(q_rot, k_cache, v_cache, block_tables, seq_lens, scale, num_parts,
+                      workspace, out, attn_bias, flags, err, stream)
+    lse_merge(workspace, seq_lens, block_tables.shape[1], B, Hq, Hkv, d, num_parts, out,
+              attn_bias.shape[1] if attn_bias is not None else 0, stream)
+    return out
+
+
+def make_step_args(q, k, v, q_rot, k_rot, k_cache, v_cache, positions, slot_mapping, seq_lens,
+                   block_tables, scale, rope_base, num_parts, workspace, out, attn_bias=None,
+                   flags=0, err=None):
+    """Fills the ``pkv_step_args`` struct (all device tensors)."""
+    a = StepArgs()
+    a.q, a.k, a.v = _ptr(q), _ptr(k), _ptr(v)
+    a.q_rot, a.k_rot = _ptr(q_rot), _ptr(k_rot)
+    a.k_cache, a.v_cache = _ptr(k_cache), _ptr(v_cache)
+    a.num_blocks = k_cache.shape[0]
+    a.positions, a.slot_mapping, a.seq_lens = _ptr(positions), _ptr(slot_mapping), _ptr(seq_lens)
+    a.block_tables, a.bt_stride = _ptr(block_tables), block_tables.shape[1]
+    a.attn_bias = _ptr(attn_bias)
+    a.bias_stride = attn_bias.shape[1] if attn_bias is not None else 0
+    a.B, a.Hq, a.d = q.shape
+    a.Hkv = k.shape[1]
+    a.scale, a.rope_base = float(scale), float(rope_base)
+    a.dtype, a.flags, a.num_parts = dtype_code(q), int(flags), int(num_parts)
+    a.workspace, a.workspace_bytes = _ptr(workspace), workspace.numel()
+    a.out = _ptr(out)
+    a.dev_err_flag = _ptr(err)
+    return a
+
+
+def decode_step_args(args, stream=None):
+    """Runs a1 -> a4 from a prepared ``StepArgs``."""
+    _check(load().pkv_decode_step(ctypes.byref(args), _stream(stream)))
+
+
+def decode_step_host(args, host_io, stream=None):
+    """End-to-end step from host buffers (see ``pkv_decode_step_host``)."""
+    _check(load().pkv_decode_step_host(ctypes.byref(args), ctypes.byref(host_io),
+                                       _stream(stream)))
+
+
+def host_io(q, k, v, positions, slot_mapping, seq_lens, block_tables, out):
+    """``pkv_step_host_io`` over host (CPU, ideally pinned) torch tensors."""
+    io = StepHostIO()
+    for name, t in (("q", q), ("k", k), ("v", v), ("positions", positions),
+                    ("slot_mapping", slot_mapping), ("seq_lens", seq_lens),
+                    ("block_tables", block_tables), ("out", out)):
+        if t.is_cuda or not t.is_contiguous():
+            raise PkvError(ERR_INVALID_ARG, f"{name} must be a contiguous host tensor")
+        setattr(io, name, _vp(t.data_ptr()))
+    return io

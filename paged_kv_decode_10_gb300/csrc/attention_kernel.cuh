@@ -1,0 +1,728 @@
+// a3: split-KV paged grouped-query decode attention (sm_103a).
+//
+// What it computes ("neurogrid releases" v0.7.0: paged attention reading K/V
+// through block_table indirection with GQA; v0.6.0: flash decode, online
+// softmax over KV tiles without materialising the score matrix;
+// "cortex-engine writeup", block-sparse attention: zero denominator -> zero
+// output):  out[b,h] = sum_t softmax_t(q[b,h].k_t * scale + bias[b,t]) v_t over
+// the first seq_lens[b] tokens of row b, with query head h reading KV head
+// h / G.
+//
+// How it runs on GB300:
+//  * Work list.  The pages of every (row, KV head) unit, row-major, form one
+//    list of P pages.  CTA c (one per part, grid = num_parts) owns the page
+//    range [c*P/C, (c+1)*P/C): every CTA streams the same number of bytes to
+//    within one 16-token page, whatever the length mix.  A unit split across
+//    CTAs leaves one (o, lse) partial per CTA; the LSE merge kernel combines
+//    them.  A unit inside one CTA is written to the output directly.
+//  * Producer warp.  Walks the CTA's pages, prefetches block ids 32 at a time
+//    and issues 2-D TMA tensor loads (128-byte swizzle) of each 16-token K and
+//    V page into a ring of NS shared-memory stages, each guarded by a
+//    full/empty mbarrier pair.  Every K/V byte is read from HBM once, because a
+//    CTA holds all G query heads of its KV head.
+//  * Consumer warps.  Page x of the range goes to consumer warp x % NW.  Each
+//    warp keeps its own online-softmax state (running max m, sum l,
+//    accumulator) for the G heads and, at the end of each unit segment, the
+//    warps combine their states through shared memory.
+//      - MMA consumer (bf16): S^T = K Q^T and O^T += V^T P^T with
+//        mma.sync.m16n8k16 (16 tokens x 8 head columns, f32 accumulate);
+//        K/V fragments come from ldmatrix (.trans for V) on the swizzled
+//        stage, P^T from movmatrix.  Head columns beyond G hold zero queries.
+//      - SIMT consumer (bf16 / f32): each lane owns d/32 dimensions; the G
+//        partial dot products of a token are reduce-scattered across the warp
+//        so each lane ends with one head's score; P goes through a small
+//        shared buffer for the P.V update.
+//  * Softmax runs in base 2 (scores pre-multiplied by log2 e); partial lse
+//    values in the workspace are base-2.
+#pragma once
+#include <cuda.h>
+
+#include "common.cuh"
+
+namespace pkv {
+
+struct AttnParams {
+  const void *q;            // [B, Hq, D] rotated queries
+  const int32_t *block_tables;
+  const int32_t *seq_lens;
+  const float *bias;        // nullable [B, bias_stride]
+  float *o_part;            // [(U + C), G, D]
+  float *lse_part;          // [(U + C), G]
+  int32_t *meta;            // [U, 2]: first part, number of parts
+  void *out;                // [B, Hq, D]
+  int32_t *err;
+  int bt_stride, bias_stride;
+  int B, Hq, Hkv, G;
+  int num_blocks, num_parts;
+  float scale_log2;         // softmax scale * log2(e)
+};
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr long long kWaitLimitCycles = 1ll << 31;   // about one second
+
+// Pages of row b, or 0 for an invalid length (which also sets *bad).
+__device__ __forceinline__ int row_pages(const int32_t *seq_lens, int b, int bt_stride,
+                                         bool has_bias, int bias_stride, bool *bad) {
+  const int L = seq_lens[b];
+  const bool ok = L >= 0 && L <= bt_stride * kBlockTokens && (!has_bias || L <= bias_stride);
+  *bad = !ok;
+  return ok ? (L + kBlockTokens - 1) / kBlockTokens : 0;
+}
+
+// Part that owns global page x: the largest c with floor(c*P/C) <= x.
+__device__ __forceinline__ int part_of(long long x, long long P, int C) {
+  return static_cast<int>(((x + 1) * C - 1) / P);
+}
+
+struct UnitCursor {
+  int b, g, n;      // row, KV head, pages per unit of this row
+  long long off;    // first global page of unit (b, g)
+};
+
+__device__ __forceinline__ void next_unit(UnitCursor &u, const AttnParams &p) {
+  u.off += u.n;
+  if (++u.g < p.Hkv) return;
+  u.g = 0;
+  bool bad;
+  for (++u.b; u.b < p.B; ++u.b) {
+    u.n = row_pages(p.seq_lens, u.b, p.bt_stride, p.bias != nullptr, p.bias_stride, &bad);
+    if (u.n > 0) return;
+  }
+  u.n = 0;
+}
+
+// Compile-time geometry of one kernel variant.
+template <typename T, int D, int NW, int NS>
+struct Geo {
+  static constexpr int kElem = sizeof(T);
+  static constexpr int kSubCols = 128 / kElem;                 // elements per 128-B row
+  static constexpr int kSubs = D * kElem / 128;                // 128-B sub-tiles per token row
+  static constexpr int kSubBytes = kBlockTokens * 128;         // one sub-tile of a page
+  static constexpr int kTileBytes = kBlockTokens * D * kElem;  // one K (or V) page
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kThreads = (NW + 1) * 32;
+  static constexpr int kHeadsPad = 8;
+  // shared-memory carve-up (after 1024-byte alignment of the base)
+  static constexpr int kOffRedAcc = NS * kStageBytes;
+  static constexpr int kOffRedM = kOffRedAcc + NW * kHeadsPad * D * 4;
+  static constexpr int kOffRedL = kOffRedM + NW * kHeadsPad * 4;
+  static constexpr int kOffPBuf = kOffRedL + NW * kHeadsPad * 4;
+  static constexpr int kOffABuf = kOffPBuf + NW * kBlockTokens * kHeadsPad * 4;
+  static constexpr int kOffBars = kOffABuf + NW * kHeadsPad * 4;      // 8-aligned
+  static constexpr int kOffBad = kOffBars + 2 * NS * 8;
+  static constexpr int kOffScan = kOffBad + NS * 4;
+  static constexpr int kOffMisc = kOffScan + (kThreads / 32) * 4;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;            // + alignment slack
+  static_assert(kSubs >= 1 && D * kElem % 128 == 0, "row must be whole 128-B lines");
+  static_assert(NS % NW == 0, "a stage must always feed the same consumer warp");
+};
+
+// Byte offset inside a page tile of (token row, 16-byte chunk j16) under the
+// 128-byte TMA swizzle: chunk index XOR (row % 8) inside each 128-B line.
+__device__ __forceinline__ uint32_t swz(int row, int j16) {
+  return static_cast<uint32_t>((j16 >> 3) * (kBlockTokens * 128) + row * 128 +
+                               (((j16 & 7) ^ (row & 7)) << 4));
+}
+
+// ---------------------------------------------------------------------------
+// consumers
+// ---------------------------------------------------------------------------
+template <int D>
+struct MmaState {
+  uint32_t qb[D / 16][2];
+  float acc[D / 16][4];
+  float m[2], l[2];
+};
+
+template <typename T, int D>
+__device__ __forceinline__ void mma_begin(MmaState<D> &s, const AttnParams &p, int b, int g,
+                                          int lane) {
+  const int r = lane >> 2, c = lane & 3;
+  const bool real = r < p.G;
+  const __nv_bfloat16 *qrow = static_cast<const __nv_bfloat16 *>(p.q) +
+                              (static_cast<size_t>(b) * p.Hq + g * p.G + (real ? r : 0)) * D;
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) {
+    const uint32_t *w = reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 2 * c);
+    s.qb[ks][0] = real ? w[0] : 0u;
+    s.qb[ks][1] = real ? w[4] : 0u;
+  }
+#pragma unroll
+  for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) s.acc[mt][e] = 0.f;
+  s.m[0] = s.m[1] = -INFINITY;
+  s.l[0] = s.l[1] = 0.f;
+}
+
+// One 16-token page: tokens t0 .. t0+15 of which the first `valid` count.
+template <int D>
+__device__ __forceinline__ void mma_page(MmaState<D> &s, const AttnParams &p, uint32_t ktile,
+                                         uint32_t vtile, int valid, int b, int t0, int lane) {
+  const int r = lane >> 2, c = lane & 3;
+  const int mq = lane >> 3;
+  const int krow = (lane & 7) + (mq & 1) * 8, kj = mq >> 1;
+  const int vrow = (lane & 7) + (mq >> 1) * 8, vj = mq & 1;
+  // S^T[token, head] = sum_d K[token, d] Q[head, d]; two accumulators shorten the chain.
+  float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) {
+    uint32_t a0, a1, a2, a3;
+    ldsm_x4(ktile + swz(krow, ks * 2 + kj), a0, a1, a2, a3);
+    if (ks & 1)
+      mma_bf16_16816(sb, a0, a1, a2, a3, s.qb[ks][0], s.qb[ks][1]);
+    else
+      mma_bf16_16816(sa, a0, a1, a2, a3, s.qb[ks][0], s.qb[ks][1]);
+  }
+  float sc[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) sc[e] = (sa[e] + sb[e]) * p.scale_log2;
+  // sc[0]: (token r, head 2c)  sc[1]: (r, 2c+1)  sc[2]: (r+8, 2c)  sc[3]: (r+8, 2c+1)
+  if (p.bias) {
+    const float *bias = p.bias + static_cast<size_t>(b) * p.bias_stride + t0;
+    if (r < valid) {
+      const float x = bias[r] * kLog2e;
+      sc[0] += x;
+      sc[1] += x;
+    }
+    if (r + 8 < valid) {
+      const float x = bias[r + 8] * kLog2e;
+      sc[2] += x;
+      sc[3] += x;
+    }
+  }
+  if (r >= valid) sc[0] = sc[1] = -INFINITY;
+  if (r + 8 >= valid) sc[2] = sc[3] = -INFINITY;
+  float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+  }
+  const float mn0 = fmaxf(s.m[0], mx0), mn1 = fmaxf(s.m[1], mx1);
+  const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
+  const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
+  const float al0 = ex2(s.m[0] - mu0), al1 = ex2(s.m[1] - mu1);
+  s.m[0] = mn0;
+  s.m[1] = mn1;
+  const uint32_t p01 = pack_bf16(ex2(sc[0] - mu0), ex2(sc[1] - mu1));
+  const uint32_t p23 = pack_bf16(ex2(sc[2] - mu0), ex2(sc[3] - mu1));
+  // the normaliser sums the same bf16-rounded weights the P.V product uses
+  s.l[0] = s.l[0] * al0 + bf16_lo(p01) + bf16_lo(p23);
+  s.l[1] = s.l[1] * al1 + bf16_hi(p01) + bf16_hi(p23);
+#pragma unroll
+  for (int mt = 0; mt < D / 16; ++mt) {
+    s.acc[mt][0] *= al0;
+    s.acc[mt][1] *= al1;
+    s.acc[mt][2] *= al0;
+    s.acc[mt][3] *= al1;
+  }
+  const uint32_t b0 = movmatrix_trans(p01);   // P^T rows: tokens 2c, 2c+1; column: head r
+  const uint32_t b1 = movmatrix_trans(p23);   // tokens 2c+8, 2c+9
+  // Tokens past `valid` may hold stale cache contents; zero their V lanes so
+  // 0 * (non-finite) never reaches the accumulator.
+  uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+  if (valid < kBlockTokens) {
+    mlo = (2 * c < valid ? 0x0000ffffu : 0u) | (2 * c + 1 < valid ? 0xffff0000u : 0u);
+    mhi = (2 * c + 8 < valid ? 0x0000ffffu : 0u) | (2 * c + 9 < valid ? 0xffff0000u : 0u);
+  }
+#pragma unroll
+  for (int mt = 0; mt < D / 16; ++mt) {
+    uint32_t a0, a1, a2, a3;
+    ldsm_x4_trans(vtile + swz(vrow, mt * 2 + vj), a0, a1, a2, a3);
+    mma_bf16_16816(s.acc[mt], a0 & mlo, a1 & mlo, a2 & mhi, a3 & mhi, b0, b1);
+  }
+}
+
+// Writes the warp's state to the reduction buffers (heads padded to 8).
+template <int D>
+__device__ __forceinline__ void mma_stash(MmaState<D> &s, float *red_acc, float *red_m,
+                                          float *red_l, int lane) {
+  const int r = lane >> 2, c = lane & 3;
+  float l0 = s.l[0], l1 = s.l[1];
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+  }
+  if (r == 0) {
+    red_m[2 * c] = s.m[0];
+    red_m[2 * c + 1] = s.m[1];
+    red_l[2 * c] = l0;
+    red_l[2 * c + 1] = l1;
+  }
+#pragma unroll
+  for (int mt = 0; mt < D / 16; ++mt) {
+    const int d0 = mt * 16 + r;
+    red_acc[(2 * c) * D + d0] = s.acc[mt][0];
+    red_acc[(2 * c + 1) * D + d0] = s.acc[mt][1];
+    red_acc[(2 * c) * D + d0 + 8] = s.acc[mt][2];
+    red_acc[(2 * c + 1) * D + d0 + 8] = s.acc[mt][3];
+  }
+}
+
+// ---- SIMT consumer ----------------------------------------------------------
+// Sum over the warp of v[h] for h = lane / (32/G): reduce-scatter halves the
+// set of heads at each butterfly step, then the remaining lanes of a head add.
+template <int G>
+__device__ __forceinline__ float reduce_scatter(float (&v)[G], int lane) {
+#pragma unroll
+  for (int n = G, o = 16; n > 1; n >>= 1, o >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float send = upper ? v[i] : v[i + n / 2];
+      const float keep = upper ? v[i + n / 2] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  float x = v[0];
+#pragma unroll
+  for (int o = 16 / G; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+template <typename T, int D, int G>
+struct SimtState {
+  static constexpr int DPL = D / 32;
+  float qf[G][DPL];
+  float acc[G][DPL];
+  float m, l;
+};
+
+// Loads the lane's DPL consecutive elements of token row `row` from a tile.
+template <typename T, int DPL>
+__device__ __forceinline__ void simt_load_row(const char *tile, int row, int lane,
+                                              float (&x)[DPL]) {
+  const int byte = lane * DPL * static_cast<int>(sizeof(T));
+  const char *ptr = tile + swz(row, byte >> 4) + (byte & 15);
+  if constexpr (sizeof(T) == 2) {
+    if constexpr (DPL == 4) {
+      const uint2 w = *reinterpret_cast<const uint2 *>(ptr);
+      x[0] = bf16_lo(w.x);
+      x[1] = bf16_hi(w.x);
+      x[2] = bf16_lo(w.y);
+      x[3] = bf16_hi(w.y);
+    } else {
+      const uint32_t w = *reinterpret_cast<const uint32_t *>(ptr);
+      x[0] = bf16_lo(w);
+      x[1] = bf16_hi(w);
+    }
+  } else {
+    if constexpr (DPL == 4) {
+      const float4 w = *reinterpret_cast<const float4 *>(ptr);
+      x[0] = w.x;
+      x[1] = w.y;
+      x[2] = w.z;
+      x[3] = w.w;
+    } else {
+      const float2 w = *reinterpret_cast<const float2 *>(ptr);
+      x[0] = w.x;
+      x[1] = w.y;
+    }
+  }
+}
+
+template <typename T, int D, int G>
+__device__ __forceinline__ void simt_begin(SimtState<T, D, G> &s, const AttnParams &p, int b,
+                                           int g, int lane) {
+  constexpr int DPL = D / 32;
+  const T *q = static_cast<const T *>(p.q) + (static_cast<size_t>(b) * p.Hq + g * p.G) * D;
+#pragma unroll
+  for (int h = 0; h < G; ++h)
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) {
+      s.qf[h][e] = h < p.G ? to_f32(q[h * D + lane * DPL + e]) * p.scale_log2 : 0.f;
+      s.acc[h][e] = 0.f;
+    }
+  s.m = -INFINITY;
+  s.l = 0.f;
+}
+
+template <typename T, int D, int G>
+__device__ __forceinline__ void simt_page(SimtState<T, D, G> &s, const AttnParams &p,
+                                          const char *ktile, const char *vtile, int valid, int b,
+                                          int t0, int lane, float *pbuf, float *abuf) {
+  constexpr int DPL = D / 32;
+  constexpr int LPH = 32 / G;
+  float sc[kBlockTokens];
+#pragma unroll
+  for (int i = 0; i < kBlockTokens; ++i) {
+    float k[DPL];
+    simt_load_row<T, DPL>(ktile, i, lane, k);
+    float part[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float a = 0.f;
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) a = fmaf(s.qf[h][e], k[e], a);
+      part[h] = a;
+    }
+    sc[i] = reduce_scatter<G>(part, lane);
+  }
+  const float *bias = p.bias ? p.bias + static_cast<size_t>(b) * p.bias_stride + t0 : nullptr;
+  float mx = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < kBlockTokens; ++i) {
+    if (i < valid) {
+      if (bias) sc[i] += bias[i] * kLog2e;
+    } else {
+      sc[i] = -INFINITY;
+    }
+    mx = fmaxf(mx, sc[i]);
+  }
+  const float mn = fmaxf(s.m, mx);
+  const float mu = mn == -INFINITY ? 0.f : mn;
+  const float alpha = ex2(s.m - mu);
+  s.m = mn;
+  float psum = 0.f;
+  const int hl = lane / LPH;
+  const bool writer = (lane % LPH) == 0;
+#pragma unroll
+  for (int i = 0; i < kBlockTokens; ++i) {
+    const float pi = ex2(sc[i] - mu);
+    psum += pi;
+    if (writer) pbuf[i * 8 + hl] = pi;
+  }
+  s.l = s.l * alpha + psum;
+  if (writer) abuf[hl] = alpha;
+  __syncwarp();
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    const float a = abuf[h];
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) s.acc[h][e] *= a;
+  }
+  for (int i = 0; i < valid; ++i) {
+    float v[DPL];
+    simt_load_row<T, DPL>(vtile, i, lane, v);
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float ph = pbuf[i * 8 + h];
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) s.acc[h][e] = fmaf(ph, v[e], s.acc[h][e]);
+    }
+  }
+  __syncwarp();
+}
+
+template <typename T, int D, int G>
+__device__ __forceinline__ void simt_stash(SimtState<T, D, G> &s, float *red_acc, float *red_m,
+                                           float *red_l, int lane) {
+  constexpr int DPL = D / 32;
+  constexpr int LPH = 32 / G;
+  if (lane % LPH == 0) {
+    red_m[lane / LPH] = s.m;
+    red_l[lane / LPH] = s.l;
+  }
+#pragma unroll
+  for (int h = 0; h < G; ++h)
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) red_acc[h * D + lane * DPL + e] = s.acc[h][e];
+}
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+// KIND 0: MMA consumer (T must be bf16, G <= 8 at run time).
+// KIND 1: SIMT consumer with compile-time group G.
+template <typename T, int D, int NW, int NS, int KIND, int G>
+__global__ void __launch_bounds__((NW + 1) * 32, 1)
+    attn_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                      const __grid_constant__ CUtensorMap tmap_v, const AttnParams p) {
+  using Q = Geo<T, D, NW, NS>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char *smem = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  float *red_acc = reinterpret_cast<float *>(smem + Q::kOffRedAcc);
+  float *red_m = reinterpret_cast<float *>(smem + Q::kOffRedM);
+  float *red_l = reinterpret_cast<float *>(smem + Q::kOffRedL);
+  float *pbuf_all = reinterpret_cast<float *>(smem + Q::kOffPBuf);
+  float *abuf_all = reinterpret_cast<float *>(smem + Q::kOffABuf);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + Q::kOffBars);
+  uint64_t *empty = full + NS;
+  volatile int *stage_bad = reinterpret_cast<volatile int *>(smem + Q::kOffBad);
+  int *scan = reinterpret_cast<int *>(smem + Q::kOffScan);
+  volatile int *misc = reinterpret_cast<volatile int *>(smem + Q::kOffMisc);  // b0, rowoff0, abort
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int C = p.num_parts;
+  const bool has_bias = p.bias != nullptr;
+
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    misc[0] = -1;
+    misc[1] = 0;
+    misc[2] = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == NW && lane == 0) {
+    prefetch_tmap(&tmap_k);
+    prefetch_tmap(&tmap_v);
+  }
+
+  // ---- page counts of all rows: per-thread chunk sums, block-wide scan ----
+  const int nthreads = Q::kThreads;
+  const int chunk = (p.B + nthreads - 1) / nthreads;
+  const int r0 = min(p.B, tid * chunk), r1 = min(p.B, r0 + chunk);
+  int mysum = 0;
+  for (int b = r0; b < r1; ++b) {
+    bool bad;
+    mysum += row_pages(p.seq_lens, b, p.bt_stride, has_bias, p.bias_stride, &bad);
+    if (bad && blockIdx.x == 0) set_dev_err(p.err, PKV_DEVERR_BAD_LEN);
+  }
+  int incl = mysum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) scan[warp] = incl;
+  __syncthreads();
+  int before = 0, total = 0;
+  for (int w = 0; w < nthreads / 32; ++w) {
+    const int t = scan[w];
+    if (w < warp) before += t;
+    total += t;
+  }
+  const long long excl = before + incl - mysum;
+  const long long P = static_cast<long long>(total) * p.Hkv;
+  const long long start = P * blockIdx.x / C;
+  const long long end = P * (blockIdx.x + 1) / C;
+  if (start < end && mysum > 0 && start >= excl * p.Hkv && start < (excl + mysum) * p.Hkv) {
+    long long acc = excl;
+    for (int b = r0; b < r1; ++b) {
+      bool bad;
+      const int n = row_pages(p.seq_lens, b, p.bt_stride, has_bias, p.bias_stride, &bad);
+      if (start < (acc + n) * p.Hkv) {
+        misc[0] = b;
+        misc[1] = static_cast<int>(acc);
+        break;
+      }
+      acc += n;
+    }
+  }
+  __syncthreads();
+  if (start >= end) return;
+  if (misc[0] < 0) {   // the row scan found no owner of `start` (never expected)
+    if (tid == 0) set_dev_err(p.err, PKV_DEVERR_TIMEOUT);
+    return;
+  }
+
+  UnitCursor u0;
+  {
+    u0.b = misc[0];
+    const long long rowoff = misc[1];
+    bool bad;
+    u0.n = row_pages(p.seq_lens, u0.b, p.bt_stride, has_bias, p.bias_stride, &bad);
+    u0.g = static_cast<int>((start - rowoff * p.Hkv) / u0.n);
+    u0.off = rowoff * p.Hkv + static_cast<long long>(u0.g) * u0.n;
+  }
+
+  if (warp == NW) {
+    // ======================= producer warp =======================
+    UnitCursor u = u0;
+    long long cur = start;
+    int x = 0;
+    bool aborted = false;
+    while (cur < end && !aborted) {
+      const int j0 = static_cast<int>(cur - u.off);
+      const int j1 = static_cast<int>(min(static_cast<long long>(u.n), end - u.off));
+      const int32_t *bt = p.block_tables + static_cast<size_t>(u.b) * p.bt_stride;
+      int ids = (j0 + lane < j1) ? bt[j0 + lane] : -1;
+      for (int jb = j0; jb < j1 && !aborted; jb += 32) {
+        const int cur_ids = ids;
+        ids = (jb + 32 + lane < j1) ? bt[jb + 32 + lane] : -1;
+        const int cnt = min(32, j1 - jb);
+        for (int i = 0; i < cnt; ++i) {
+          const int blk = __shfl_sync(0xffffffffu, cur_ids, i);
+          if (lane == 0) {
+            const int xx = x + (jb - j0) + i;
+            const int st = xx % NS;
+            const uint32_t ph = static_cast<uint32_t>(xx / NS) & 1u;
+            if (misc[2] || !mbar_wait_bounded(&empty[st], ph ^ 1u, kWaitLimitCycles)) {
+              misc[2] = 1;
+              set_dev_err(p.err, PKV_DEVERR_TIMEOUT);
+            }
+            const bool ok = !misc[2] && blk >= 0 && blk < p.num_blocks;
+            stage_bad[st] = ok ? 0 : 1;
+            if (ok) {
+              mbar_arrive_expect_tx(&full[st], Q::kStageBytes);
+              const uint32_t kdst = smem_u32(smem + st * Q::kStageBytes);
+              const uint32_t vdst = kdst + Q::kTileBytes;
+              const int y = (blk * p.Hkv + u.g) * kBlockTokens;
+#pragma unroll
+              for (int sub = 0; sub < Q::kSubs; ++sub) {
+                tma_load_2d(kdst + sub * Q::kSubBytes, &tmap_k, sub * Q::kSubCols, y, &full[st]);
+                tma_load_2d(vdst + sub * Q::kSubBytes, &tmap_v, sub * Q::kSubCols, y, &full[st]);
+              }
+            } else {
+              if (!misc[2]) set_dev_err(p.err, PKV_DEVERR_BAD_BLOCK);
+              mbar_arrive(&full[st]);
+            }
+          }
+        }
+        aborted = __shfl_sync(0xffffffffu, misc[2], 0) != 0;
+      }
+      x += j1 - j0;
+      cur += j1 - j0;
+      if (cur < end) next_unit(u, p);
+    }
+    if (aborted && lane == 0) {
+      // never expected: let any copy still in flight land before the CTA exits
+      for (int xx = max(0, x - NS); xx < x; ++xx)
+        mbar_wait_bounded(&full[xx % NS], static_cast<uint32_t>(xx / NS) & 1u, kWaitLimitCycles);
+    }
+    return;
+  }
+
+  // ======================= consumer warps =======================
+  float *my_acc = red_acc + warp * Q::kHeadsPad * D;
+  float *my_m = red_m + warp * Q::kHeadsPad;
+  float *my_l = red_l + warp * Q::kHeadsPad;
+  float *pbuf = pbuf_all + warp * kBlockTokens * Q::kHeadsPad;
+  float *abuf = abuf_all + warp * Q::kHeadsPad;
+  constexpr int kConsumers = NW * 32;
+
+  UnitCursor u = u0;
+  long long cur = start;
+  int x = 0;
+  while (cur < end) {
+    const int j0 = static_cast<int>(cur - u.off);
+    const int j1 = static_cast<int>(min(static_cast<long long>(u.n), end - u.off));
+    const int L = p.seq_lens[u.b];
+    // ---- this warp's pages of the segment ----
+    if constexpr (KIND == 0) {
+      MmaState<D> s;
+      mma_begin<T, D>(s, p, u.b, u.g, lane);
+      int j = j0 + ((warp - x % NW) + NW) % NW;
+      for (; j < j1; j += NW) {
+        const int xx = x + (j - j0);
+        const int st = xx % NS;
+        const uint32_t ph = static_cast<uint32_t>(xx / NS) & 1u;
+        bool ready = !misc[2];
+        if (ready && !mbar_wait_bounded(&full[st], ph, kWaitLimitCycles)) {
+          misc[2] = 1;
+          set_dev_err(p.err, PKV_DEVERR_TIMEOUT);
+          ready = false;
+        }
+        if (ready && !stage_bad[st]) {
+          const uint32_t kt = smem_u32(smem + st * Q::kStageBytes);
+          mma_page<D>(s, p, kt, kt + Q::kTileBytes, min(kBlockTokens, L - j * kBlockTokens), u.b,
+                      j * kBlockTokens, lane);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+      }
+      mma_stash<D>(s, my_acc, my_m, my_l, lane);
+    } else {
+      SimtState<T, D, G> s;
+      simt_begin<T, D, G>(s, p, u.b, u.g, lane);
+      int j = j0 + ((warp - x % NW) + NW) % NW;
+      for (; j < j1; j += NW) {
+        const int xx = x + (j - j0);
+        const int st = xx % NS;
+        const uint32_t ph = static_cast<uint32_t>(xx / NS) & 1u;
+        bool ready = !misc[2];
+        if (ready && !mbar_wait_bounded(&full[st], ph, kWaitLimitCycles)) {
+          misc[2] = 1;
+          set_dev_err(p.err, PKV_DEVERR_TIMEOUT);
+          ready = false;
+        }
+        if (ready && !stage_bad[st]) {
+          const char *kt = reinterpret_cast<const char *>(smem + st * Q::kStageBytes);
+          simt_page<T, D, G>(s, p, kt, kt + Q::kTileBytes, min(kBlockTokens, L - j * kBlockTokens),
+                             u.b, j * kBlockTokens, lane, pbuf, abuf);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+      }
+      simt_stash<T, D, G>(s, my_acc, my_m, my_l, lane);
+    }
+    // ---- combine the consumer warps' states for this segment ----
+    asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
+    const int u_idx = u.b * p.Hkv + u.g;
+    const int c_first = part_of(u.off, P, C);
+    const int c_last = part_of(u.off + u.n - 1, P, C);
+    const int nseg = c_last - c_first + 1;
+    const int gq = p.G;
+    for (int e = tid; e < gq * D; e += kConsumers) {
+      const int h = e / D, dim = e - h * D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) M = fmaxf(M, red_m[w * Q::kHeadsPad + h]);
+      float Lsum = 0.f, O = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+          const float f = ex2(red_m[w * Q::kHeadsPad + h] - M);
+          Lsum += f * red_l[w * Q::kHeadsPad + h];
+          O += f * red_acc[(w * Q::kHeadsPad + h) * D + dim];
+        }
+      }
+      const float o = Lsum > 0.f ? O / Lsum : 0.f;
+      if (nseg == 1) {
+        T *out = static_cast<T *>(p.out) +
+                 (static_cast<size_t>(u.b) * p.Hq + u.g * gq + h) * D + dim;
+        *out = from_f32<T>(o);
+      } else {
+        const size_t idx = static_cast<size_t>(u_idx) + blockIdx.x;
+        p.o_part[(idx * gq + h) * D + dim] = o;
+        if (dim == 0) p.lse_part[idx * gq + h] = Lsum > 0.f ? M + log2f(Lsum) : -INFINITY;
+      }
+    }
+    if (tid == 0 && j0 == 0) {
+      p.meta[2 * u_idx] = c_first;
+      p.meta[2 * u_idx + 1] = nseg;
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
+    x += j1 - j0;
+    cur += j1 - j0;
+    if (cur < end) next_unit(u, p);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host-side launch table entry for one compiled variant
+// ---------------------------------------------------------------------------
+struct AttnVariant {
+  cudaError_t (*launch)(const CUtensorMap &, const CUtensorMap &, const AttnParams &,
+                        cudaStream_t);
+  cudaError_t (*occupancy)(int *blocks_per_sm);
+  int smem_bytes;
+  int threads;
+};
+
+template <typename T, int D, int NW, int NS, int KIND, int G>
+struct AttnLauncher {
+  using Q = Geo<T, D, NW, NS>;
+  static cudaError_t launch(const CUtensorMap &tk, const CUtensorMap &tv, const AttnParams &p,
+                            cudaStream_t s) {
+    auto kern = attn_split_kernel<T, D, NW, NS, KIND, G>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Q::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    kern<<<p.num_parts, Q::kThreads, Q::kSmemBytes, s>>>(tk, tv, p);
+    return cudaGetLastError();
+  }
+  static cudaError_t occupancy(int *n) {
+    auto kern = attn_split_kernel<T, D, NW, NS, KIND, G>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Q::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, kern, Q::kThreads, Q::kSmemBytes);
+  }
+  static AttnVariant variant() { return AttnVariant{&launch, &occupancy, Q::kSmemBytes, Q::kThreads}; }
+};
+
+// Variant lookup, one per translation unit (returns false if not built).
+bool attn_variant_mma(int D, AttnVariant *v);
+bool attn_variant_simt_bf16(int D, int G, AttnVariant *v);
+bool attn_variant_simt_f32(int D, int G, AttnVariant *v);
+
+}  // namespace pkv

@@ -1,0 +1,122 @@
+"""One continuous-batching decoder over a paged KV pool: the whole step.
+
+``PagedDecoder`` owns the device KV pool, the host block allocator and the
+per-step buffers.  ``step`` runs a0 on the host (allocator: positions,
+slot_mapping, seq_lens, block tables, written into pinned buffers), one
+host-to-device copy of that metadata, then a1-a4 through ``pkv_decode_step`` on
+one CUDA stream.  Nothing is copied back to the host ("neurogrid releases"
+v0.8.0: position, seq_len and kv_len live in GPU buffers; no D2H copies).
+
+Joins and leaves only edit the allocator's block tables ("neurogrid releases"
+v0.7.0: on-demand blocks, O(1) alloc/free); no KV is moved when the batch
+changes, which is what replaces the extract/re-assemble rebatch of the helexa
+continuous-batching PR.
+"""
+import math
+
+import numpy as np
+
+from . import binding
+
+
+class PagedDecoder:
+    def __init__(self, num_blocks, Hq, Hkv, d, dtype, max_seqs, max_blocks_per_seq,
+                 initial_free=None, device="cuda", num_parts=None, rope_base=10000.0,
+                 scale=None, flags=0, k_cache=None, v_cache=None):
+        import torch
+        self.torch = torch
+        self.device = torch.device(device)
+        self.Hq, self.Hkv, self.d = Hq, Hkv, d
+        self.dtype = dtype
+        self.tdtype = {"bf16": torch.bfloat16, "f32": torch.float32}[dtype]
+        self.max_seqs = max_seqs
+        self.bt_stride = max_blocks_per_seq
+        self.rope_base = rope_base
+        self.scale = 1.0 / math.sqrt(d) if scale is None else scale
+        self.flags = flags
+        shape = (num_blocks, Hkv, binding.BLOCK_SIZE, d)
+        self.k_cache = k_cache if k_cache is not None else torch.empty(
+            shape, dtype=self.tdtype, device=self.device)
+        self.v_cache = v_cache if v_cache is not None else torch.empty(
+            shape, dtype=self.tdtype, device=self.device)
+        self.num_blocks = num_blocks
+        self.alloc = binding.BlockAllocator(num_blocks, max_seqs, max_blocks_per_seq,
+                                            initial_free)
+        code = binding.F32 if dtype == "f32" else binding.BF16
+        self.num_parts = num_parts or binding.default_parts(d, code, flags)
+        self.workspace = binding.alloc_workspace(max_seqs, Hq, Hkv, d, self.num_parts,
+                                                 self.device)
+        dev = dict(device=self.device)
+        self.positions = torch.empty(max_seqs, dtype=torch.int32, **dev)
+        self.slots = torch.empty(max_seqs, dtype=torch.int64, **dev)
+        self.seq_lens = torch.empty(max_seqs, dtype=torch.int32, **dev)
+        self.tables = torch.empty((max_seqs, self.bt_stride), dtype=torch.int32, **dev)
+        self.q_rot = torch.empty((max_seqs, Hq, d), dtype=self.tdtype, **dev)
+        self.k_rot = torch.empty((max_seqs, Hkv, d), dtype=self.tdtype, **dev)
+        self.out = torch.empty((max_seqs, Hq, d), dtype=self.tdtype, **dev)
+        self.err = torch.zeros(1, dtype=torch.int32, **dev)
+        # two pinned metadata sets so the host can fill step i+1 while step i's
+        # copy is still queued
+        self._host = []
+        for _ in range(2):
+            hs = dict(pin_memory=True)
+            self._host.append(dict(
+                pos=torch.empty(max_seqs, dtype=torch.int32, **hs),
+                slots=torch.empty(max_seqs, dtype=torch.int64, **hs),
+                lens=torch.empty(max_seqs, dtype=torch.int32, **hs),
+                tables=torch.empty((max_seqs, self.bt_stride), dtype=torch.int32, **hs),
+                event=None))
+        self._turn = 0
+        self.last_metadata = None
+
+    # -- batch membership ----------------------------------------------------
+    def join(self, prefix_len):
+        return self.alloc.join(prefix_len)
+
+    def leave(self, seq_id):
+        self.alloc.leave(seq_id)
+
+    # -- a0 ----------------------------------------------------------------
+    def prepare(self, seq_ids, stream=None):
+        """Host allocator step + one async H2D copy of the metadata."""
+        torch = self.torch
+        B = len(seq_ids)
+        h = self._host[self._turn]
+        self._turn ^= 1
+        if h["event"] is not None:
+            h["event"].synchronize()
+        views = (h["pos"][:B].numpy(), h["slots"][:B].numpy(), h["lens"][:B].numpy(),
+                 h["tables"][:B].numpy())
+        self.alloc.prepare_step(seq_ids, self.bt_stride, out=views)
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        with torch.cuda.stream(s):
+            self.positions[:B].copy_(h["pos"][:B], non_blocking=True)
+            self.slots[:B].copy_(h["slots"][:B], non_blocking=True)
+            self.seq_lens[:B].copy_(h["lens"][:B], non_blocking=True)
+            self.tables[:B].copy_(h["tables"][:B], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(s)
+        h["event"] = ev
+        self.last_metadata = views
+        return views
+
+    # -- a1..a4 --------------------------------------------------------------
+    def step_args(self, B, q, k, v, attn_bias=None):
+        return binding.make_step_args(
+            q, k, v, self.q_rot[:B], self.k_rot[:B], self.k_cache, self.v_cache,
+            self.positions[:B], self.slots[:B], self.seq_lens[:B], self.tables[:B],
+            self.scale, self.rope_base, self.num_parts, self.workspace, self.out[:B],
+            attn_bias, self.flags, self.err)
+
+    def step(self, seq_ids, q, k, v, attn_bias=None, stream=None):
+        """One decode step for the listed sequences; returns ``out[:B]`` (device)."""
+        B = len(seq_ids)
+        self.prepare(seq_ids, stream)
+        binding.decode_step_args(self.step_args(B, q, k, v, attn_bias), stream)
+        return self.out[:B]
+
+    def device_errors(self):
+        """Reads and clears the device error flag (a D2H copy: not for the hot loop)."""
+        val = int(self.err.item())
+        self.err.zero_()
+        return val

@@ -27,3 +27,11 @@ def cuda_lib():
         pytest.skip("no CUDA device")
     from paged_kv_decode_10_gb300 import binding
     return binding.load()
+
+
+@pytest.fixture(scope="session")
+def host_lib():
+    """The library built in-tree (compiled here if needed) for host-only calls."""
+    from paged_kv_decode_10_gb300 import binding, build
+    build.build()
+    return binding.load()

@@ -1,0 +1,348 @@
+"""GPU parity of the decode step (through the C ABI) against the float64 oracle.
+
+Tolerances: attention output max-abs 1e-5 for float32 inputs and 2e-2 for bf16
+inputs (float32 accumulation); rotated q/k within one ulp of the storage type;
+allocator outputs, slot writes of V and untouched cache bytes bit-exact.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from helpers import (TOL, assert_out_close, assert_rope_close, dev, f64, gpu_single_step,
+                     oracle_metadata, oracle_rows)
+from oracle.step import decode_step
+from paged_kv_decode_10_gb300 import binding, engine, workloads
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_full_step(w, res, rows=None):
+    caches = workloads.make_caches(w, "cpu")
+    tokens = workloads.make_new_tokens(w, 0, "cpu")
+    meta = oracle_metadata(w)
+    for got, ref in zip(res["meta"], meta):
+        np.testing.assert_array_equal(got, ref)          # a0 bit-exact
+    rows = range(w.B) if rows is None else rows
+    ref = oracle_rows(w, caches, tokens, meta, rows)
+    out = f64(res["out"])
+    worst = 0.0
+    for b in rows:
+        assert_rope_close(f64(res["q_rot"][b]), ref[b]["q_rot"], w.dtype)
+        assert_rope_close(f64(res["k_rot"][b]), ref[b]["k_rot"], w.dtype)
+        worst = max(worst, assert_out_close(out[b], ref[b]["out"], w.dtype, f"row {b}"))
+    # append: V slot bit-exact, K slot = the kernel's own k_rot, everything else untouched
+    pos, slots, lens, tables = meta
+    k0, v0 = caches
+    k1, v1 = res["k_cache"], res["v_cache"]
+    touched = torch.zeros(k0.shape[0] * 16, dtype=torch.bool)
+    touched[torch.from_numpy(slots)] = True
+    touched = touched.view(k0.shape[0], 16)
+    for b in range(w.B):
+        blk, row = divmod(int(slots[b]), 16)
+        assert torch.equal(v1[blk, :, row], tokens[2][b])
+        assert torch.equal(k1[blk, :, row], res["k_rot"][b])
+    keep = ~touched[:, None, :, None].expand_as(k0)
+    assert torch.equal(k1[keep], k0[keep]) and torch.equal(v1[keep], v0[keep])
+    assert res["err"] == 0
+    return worst
+
+
+def test_tiny_fp32_step():
+    w = workloads.make_workload("tiny")
+    _check_full_step(w, gpu_single_step(w))
+
+
+def test_tiny_fp32_step_simt_vs_parts():
+    w = workloads.make_workload("tiny")
+    for parts in (1, 2, 5, 64):
+        _check_full_step(w, gpu_single_step(w, num_parts=parts))
+
+
+def test_decode16_bf16_step():
+    w = workloads.make_workload("decode16")
+    _check_full_step(w, gpu_single_step(w))
+
+
+def test_decode16_bf16_simt_consumer():
+    w = workloads.make_workload("decode16")
+    _check_full_step(w, gpu_single_step(w, flags=binding.ATTN_SIMT))
+
+
+def test_ragged64_bf16_step():
+    w = workloads.make_workload("ragged64")
+    _check_full_step(w, gpu_single_step(w))
+
+
+def test_long131k_bf16_step():
+    w = workloads.make_workload("long131k")
+    res = gpu_single_step(w)
+    _check_full_step(w, res)
+
+
+def test_long131k_bf16_simt_consumer():
+    w = workloads.make_workload("long131k")
+    _check_full_step(w, gpu_single_step(w, flags=binding.ATTN_SIMT))
+
+
+@pytest.mark.parametrize("parts", [1, 3, 152, 1000, 5000])
+def test_split_count_invariance(parts):
+    """Any partition of the pages into parts gives the same output (the LSE
+    merge of any number of splits equals one split)."""
+    w = workloads.make_workload("decode16")
+    _check_full_step(w, gpu_single_step(w, num_parts=parts))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (8, 2), (16, 2)])
+def test_shapes_and_ragged_tails(dtype, d, hq, hkv):
+    """Lengths around page boundaries (0, 1, 15, 16, 17, 31, 32, 33 cached tokens)
+    for every built head_dim / group size and both dtypes."""
+    lens = [0, 1, 15, 16, 17, 31, 32, 33, 100, 257]
+    w = workloads.custom_workload("edges", lens, hq, hkv, d, dtype, seed=5)
+    for flags in ([0, binding.ATTN_SIMT] if dtype == "bf16" else [0]):
+        for parts in (None, 3):
+            _check_full_step(w, gpu_single_step(w, num_parts=parts, flags=flags))
+
+
+def test_empty_prefix_returns_new_value():
+    """A row with no cached tokens attends only to its own new token: out = v."""
+    w = workloads.custom_workload("fresh", [0, 0, 0], 8, 2, 128, "bf16", seed=6)
+    res = gpu_single_step(w)
+    v = workloads.make_new_tokens(w, 0, "cpu")[2]
+    for b in range(3):
+        for h in range(8):
+            assert torch.equal(res["out"][b, h], v[b, h // 4])
+
+
+def test_constant_values_give_constant_output():
+    """V identical to c everywhere -> out == c for every row and head (pins the
+    softmax normaliser and the split merge on the GPU)."""
+    w = workloads.make_workload("ragged64")
+    k_cache, v_cache = workloads.make_caches(w, "cpu")
+    q, k, v = workloads.make_new_tokens(w, 0, "cpu")
+    c = 0.375
+    v_cache.fill_(c)
+    v.fill_(c)
+    res = gpu_single_step(w, caches=(k_cache, v_cache), tokens=(q, k, v))
+    assert torch.all(res["out"] == c)
+
+
+def test_ragged_batch_equals_rows_alone():
+    """helexa issue 121: the ragged lockstep batch equals each row decoded alone."""
+    w = workloads.make_workload("decode16")
+    caches = workloads.make_caches(w, "cpu")
+    tokens = workloads.make_new_tokens(w, 0, "cpu")
+    full = gpu_single_step(w, caches=caches, tokens=tokens)
+    meta = full["meta"]
+    d = dev()
+    k_cache, v_cache = (c.to(d) for c in caches)
+    q, k, v = (t.to(d) for t in tokens)
+    pos, slots, lens, tables = (torch.from_numpy(np.ascontiguousarray(m)).to(d) for m in meta)
+    for b in range(w.B):
+        q_rot, k_rot = binding.rope(q[b:b + 1], k[b:b + 1], pos[b:b + 1])
+        kc, vc = k_cache.clone(), v_cache.clone()
+        binding.append(k_rot, v[b:b + 1], slots[b:b + 1], kc, vc)
+        out = binding.decode_attention(q_rot, kc, vc, tables[b:b + 1], lens[b:b + 1], w.scale)
+        torch.cuda.synchronize()
+        diff = (out[0].float().cpu() - full["out"][b].float()).abs().max().item()
+        assert diff <= TOL["bf16"], (b, diff)
+
+
+def test_block_table_permutation_invariance():
+    """The same logical sequences stored under two different block layouts give
+    the same output (paged equals contiguous)."""
+    w = workloads.make_workload("decode16")
+    caches = workloads.make_caches(w, "cpu")
+    tokens = workloads.make_new_tokens(w, 0, "cpu")
+    a = gpu_single_step(w, caches=caches, tokens=tokens)
+    # relabel blocks: physical block p of layout A becomes block perm[p] of layout B
+    perm = torch.from_numpy(np.random.default_rng(3).permutation(w.num_blocks))
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(w.num_blocks)
+    kb, vb = torch.empty_like(caches[0]), torch.empty_like(caches[1])
+    kb[perm], vb[perm] = caches[0], caches[1]
+    w2 = workloads.Workload(**{**w.__dict__})
+    w2.free_order = perm.numpy()[w.free_order].astype(np.int32)
+    b = gpu_single_step(w2, caches=(kb, vb), tokens=tokens)
+    diff = (a["out"].float() - b["out"].float()).abs().max().item()
+    assert diff <= TOL["bf16"]
+
+
+def test_padded_batch_with_mask_equals_unpadded():
+    """helexa issue 121, slice 1: rows right-padded to the batch max with a
+    finite gap, an additive -inf mask over [prefix_len, padded_len), the new
+    token after the gap and RoPE at the real position, equal the unpadded batch."""
+    w = workloads.make_workload("tiny")
+    caches = workloads.make_caches(w, "cpu")
+    tokens = workloads.make_new_tokens(w, 0, "cpu")
+    unpadded = gpu_single_step(w, caches=caches, tokens=tokens)
+    d = dev()
+    lens = [int(x) for x in w.seq_lens]
+    P = max(lens)
+    nb = 3 * (-(-(P + 1) // 16))
+    alloc = binding.BlockAllocator(nb, 3, 4, np.arange(nb, dtype=np.int32)[::-1].copy())
+    ids = [alloc.join(P) for _ in range(3)]
+    _, slots, seq_lens, tables = alloc.prepare_step(ids, 4)
+    # dense padded pool: real prefix, then a finite gap of garbage
+    pos_u, _, _, tab_u = unpadded["meta"]
+    kp = torch.randn(nb, w.Hkv, 16, w.d) * 50
+    vp = torch.randn(nb, w.Hkv, 16, w.d) * 50
+    for b, L in enumerate(lens):
+        for t in range(L):
+            src = (int(tab_u[b, t // 16]), t % 16)
+            dst = (int(tables[b, t // 16]), t % 16)
+            kp[dst[0], :, dst[1]] = caches[0][src[0], :, src[1]]
+            vp[dst[0], :, dst[1]] = caches[1][src[0], :, src[1]]
+    bias = torch.zeros(3, P + 1)
+    for b, L in enumerate(lens):
+        bias[b, L:P] = -math.inf
+    q, k, v = (t.to(d) for t in tokens)
+    positions = torch.tensor(lens, dtype=torch.int32, device=d)      # RoPE at real position
+    kp, vp = kp.to(d), vp.to(d)
+    q_rot, k_rot = binding.rope(q, k, positions)
+    binding.append(k_rot, v, torch.from_numpy(slots).to(d), kp, vp)
+    out = binding.decode_attention(q_rot, kp, vp, torch.from_numpy(tables).to(d),
+                                   torch.from_numpy(seq_lens).to(d), w.scale,
+                                   attn_bias=bias.to(d))
+    torch.cuda.synchronize()
+    assert (seq_lens == P + 1).all()
+    diff = (out.cpu() - unpadded["out"]).abs().max().item()
+    assert diff <= TOL["f32"], diff
+
+
+def test_fully_masked_row_outputs_zero():
+    w = workloads.custom_workload("masked", [40, 5], 8, 2, 64, "f32", seed=9)
+    d = dev()
+    caches = workloads.make_caches(w, "cpu")
+    q, _, _ = workloads.make_new_tokens(w, 0, "cpu")
+    meta = oracle_metadata(w)
+    tables = torch.from_numpy(meta[3]).to(d)
+    lens = torch.from_numpy(meta[2]).to(d)
+    bias = torch.zeros(2, 64, device=d)
+    bias[1, :] = -math.inf
+    out = binding.decode_attention(q.to(d), caches[0].to(d), caches[1].to(d), tables, lens,
+                                   w.scale, attn_bias=bias, num_parts=7)
+    torch.cuda.synchronize()
+    assert torch.all(out[1] == 0) and torch.isfinite(out).all()
+    assert out[0].abs().sum() > 0
+
+
+def test_device_error_flags_instead_of_faults():
+    """Out-of-range block ids, slots and lengths are reported in the flag word
+    and skipped (no access outside the buffers)."""
+    w = workloads.custom_workload("bad", [20, 20], 8, 2, 128, "bf16", seed=10)
+    d = dev()
+    k_cache, v_cache = (c.to(d) for c in workloads.make_caches(w, "cpu"))
+    q, k, v = (t.to(d) for t in workloads.make_new_tokens(w, 0, "cpu"))
+    meta = oracle_metadata(w)
+    err = torch.zeros(1, dtype=torch.int32, device=d)
+    tables = torch.from_numpy(meta[3]).to(d)
+    tables[1, 0] = w.num_blocks + 1000
+    lens = torch.from_numpy(meta[2]).to(d)
+    binding.decode_attention(q, k_cache, v_cache, tables, lens, w.scale, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & binding.DEVERR_BAD_BLOCK
+    err.zero_()
+    slots = torch.tensor([0, w.num_blocks * 16 + 5], dtype=torch.int64, device=d)
+    kc = k_cache.clone()
+    binding.append(k, v, slots, kc, v_cache.clone(), err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == binding.DEVERR_BAD_SLOT
+    err.zero_()
+    lens2 = lens.clone()
+    lens2[0] = tables.shape[1] * 16 + 1
+    out = binding.decode_attention(q, k_cache, v_cache, torch.from_numpy(meta[3]).to(d), lens2,
+                                   w.scale, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & binding.DEVERR_BAD_LEN
+    assert torch.all(out[0] == 0)
+
+
+def test_host_entry_point_matches_device_path():
+    """pkv_decode_step_host (host buffers in, host result out) equals the device call."""
+    w = workloads.make_workload("decode16")
+    caches = workloads.make_caches(w, "cpu")
+    tokens = workloads.make_new_tokens(w, 0, "cpu")
+    ref = gpu_single_step(w, caches=caches, tokens=tokens)
+    d = dev()
+    bt = w.max_blocks_per_seq()
+    dec = engine.PagedDecoder(w.num_blocks, w.Hq, w.Hkv, w.d, w.dtype, w.B, bt,
+                              initial_free=w.free_order, device=d,
+                              k_cache=caches[0].to(d), v_cache=caches[1].to(d))
+    ids = [dec.join(int(L)) for L in w.seq_lens]
+    pos, slots, lens, tables = dec.alloc.prepare_step(ids, bt)
+    q, k, v = tokens
+    dq, dk, dv = torch.empty_like(q, device=d), torch.empty_like(k, device=d), torch.empty_like(v, device=d)
+    args = dec.step_args(w.B, dq, dk, dv)
+    out_h = torch.empty_like(q).pin_memory()
+    pinned = [torch.from_numpy(np.ascontiguousarray(x)).pin_memory() for x in (pos, slots, lens, tables)]
+    io = binding.host_io(q.pin_memory(), k.pin_memory(), v.pin_memory(), *pinned, out_h)
+    binding.decode_step_host(args, io)
+    assert torch.equal(out_h, ref["out"])
+
+
+def _churn_case(dtype, d, hq, hkv, seed):
+    r = np.random.default_rng(seed)
+    B, steps, n_move = 8, 8, 2
+    lens = r.integers(10, 60, size=B)
+    nb = 200
+    order = r.permutation(nb).astype(np.int32)
+    return r, B, steps, n_move, lens, nb, order
+
+
+@pytest.mark.parametrize("dtype,d,hq,hkv", [("bf16", 128, 32, 8), ("f32", 64, 8, 2),
+                                            ("bf16", 64, 16, 2)])
+def test_multi_step_churn_matches_oracle(dtype, d, hq, hkv):
+    """Lockstep decode with rows leaving and joining between steps: each step's
+    output and the allocator state match the oracle replaying the same history
+    (block reuse after leave included)."""
+    from oracle.allocator import BlockAllocatorModel
+    r, B, steps, n_move, lens, nb, order = _churn_case(dtype, d, hq, hkv, 11)
+    dv = dev()
+    tdt = {"bf16": torch.bfloat16, "f32": torch.float32}[dtype]
+    gen = torch.Generator().manual_seed(123)
+    k_pool = torch.randn(nb, hkv, 16, d, generator=gen).to(tdt)
+    v_pool = torch.randn(nb, hkv, 16, d, generator=gen).to(tdt)
+    bt = 16
+    dec = engine.PagedDecoder(nb, hq, hkv, d, dtype, B, bt, initial_free=order, device=dv,
+                              num_parts=11, k_cache=k_pool.to(dv), v_cache=v_pool.to(dv))
+    model = BlockAllocatorModel(nb, max_seqs=B, max_blocks_per_seq=bt, initial_free=order)
+    ids = [dec.join(int(L)) for L in lens]
+    assert ids == [model.join(int(L)) for L in lens]
+    k_ref, v_ref = f64(k_pool), f64(v_pool)
+    scale = 1 / math.sqrt(d)
+    for step in range(steps):
+        if step:
+            leave = r.choice(B, size=n_move, replace=False)
+            for row in leave:
+                dec.leave(ids[row])
+                model.leave(ids[row])
+            for row in leave:
+                pre = int(r.integers(0, 40))
+                ids[row] = dec.join(pre)
+                assert ids[row] == model.join(pre)
+                # synthetic prefill stand-in: fresh prefix contents for the joiner
+                blocks = model.seq_blocks(ids[row])
+                fill_k = torch.randn(len(blocks), hkv, 16, d, generator=gen).to(tdt)
+                fill_v = torch.randn(len(blocks), hkv, 16, d, generator=gen).to(tdt)
+                idx = torch.tensor(blocks, dtype=torch.long)
+                dec.k_cache[idx.to(dv)] = fill_k.to(dv)
+                dec.v_cache[idx.to(dv)] = fill_v.to(dv)
+                k_ref[blocks], v_ref[blocks] = f64(fill_k), f64(fill_v)
+        q = torch.randn(B, hq, d, generator=gen).to(tdt)
+        k = torch.randn(B, hkv, d, generator=gen).to(tdt)
+        v = torch.randn(B, hkv, d, generator=gen).to(tdt)
+        out = dec.step(ids, q.to(dv), k.to(dv), v.to(dv))
+        torch.cuda.synchronize()
+        pos, slots, seq_lens, tables = model.prepare_step(ids, bt)
+        for got, want in zip(dec.last_metadata, (pos, slots, seq_lens, tables)):
+            np.testing.assert_array_equal(got, want)
+        ref = decode_step(f64(q), f64(k), f64(v), pos, slots, seq_lens, tables, k_ref, v_ref,
+                          scale=scale, base=10000.0, dtype=dtype)
+        k_ref, v_ref = ref["k_cache"], ref["v_cache"]
+        assert_out_close(f64(out), ref["out"], dtype, f"step {step}")
+        assert dec.alloc.free_stack() == model.free
+    assert dec.device_errors() == 0

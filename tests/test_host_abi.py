@@ -1,0 +1,147 @@
+"""Host-side checks of the C ABI: exported symbols and the C++ block allocator
+against the hand-derived trace and against the allocator model (bit-exact)."""
+import json
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle.allocator import BlockAllocatorModel, OutOfBlocks
+from oracle.allocator import UnknownSequence as ModelUnknown
+
+HERE = os.path.dirname(__file__)
+HEADER = os.path.join(os.path.dirname(HERE), "include", "pkv.h")
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_function(host_lib):
+    from paged_kv_decode_10_gb300 import binding
+    names = header_functions()
+    assert len(names) >= 18
+    for name in names:
+        assert hasattr(host_lib, name), name
+        assert name in binding.SIGNATURES, name
+    assert host_lib.pkv_abi_version() == 1
+
+
+def _run_trace(alloc_cls, errors):
+    with open(os.path.join(HERE, "golden", "allocator_trace.json")) as f:
+        g = json.load(f)
+    a = alloc_cls(g)
+    for op in g["ops"]:
+        err = op.get("error")
+        if op["op"] == "join":
+            if err:
+                with pytest.raises(errors["out_of_blocks"]):
+                    a.join(op["prefix"])
+            else:
+                assert a.join(op["prefix"]) == op["seq_id"]
+        elif op["op"] == "leave":
+            if err:
+                with pytest.raises(errors["unknown_seq"]):
+                    a.leave(op["seq_id"])
+            else:
+                a.leave(op["seq_id"])
+        else:
+            if err:
+                with pytest.raises(errors["out_of_blocks"]):
+                    a.prepare_step(op["seq_ids"], g["bt_stride"])
+            else:
+                pos, slots, lens, tables = a.prepare_step(op["seq_ids"], g["bt_stride"])
+                assert pos.tolist() == op["positions"]
+                assert slots.tolist() == op["slots"]
+                assert lens.tolist() == op["seq_lens"]
+                assert tables.tolist() == op["tables"]
+        assert a.free_stack() == op["free_after"], op
+    for sid, blocks in g["final_tables"].items():
+        assert a.seq_blocks(int(sid)) == blocks
+        assert a.seq_len(int(sid)) == g["final_lengths"][sid]
+
+
+def test_cpp_allocator_golden_trace(host_lib):
+    from paged_kv_decode_10_gb300 import binding
+
+    def make(g):
+        return binding.BlockAllocator(g["num_blocks"], g["max_seqs"], g["bt_stride"],
+                                      g["initial_free"])
+    _run_trace(make, {"out_of_blocks": binding.OutOfBlocks,
+                      "unknown_seq": binding.UnknownSequence})
+
+
+class _ModelAdapter(BlockAllocatorModel):
+    def free_stack(self):
+        return list(self.free)
+
+
+def test_model_allocator_golden_trace_adapter():
+    _run_trace(lambda g: _ModelAdapter(g["num_blocks"], g["block_size"], g["max_seqs"],
+                                       initial_free=g["initial_free"]),
+               {"out_of_blocks": OutOfBlocks, "unknown_seq": ModelUnknown})
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_cpp_allocator_matches_model_under_churn(host_lib, seed):
+    from paged_kv_decode_10_gb300 import binding
+    r = np.random.default_rng(seed)
+    nb, max_seqs, bt = 400, 24, 40
+    order = r.permutation(nb).astype(np.int32)
+    cpp = binding.BlockAllocator(nb, max_seqs, bt, order)
+    model = BlockAllocatorModel(nb, max_seqs=max_seqs, max_blocks_per_seq=bt,
+                                initial_free=order)
+    live = []
+    for _ in range(600):
+        act = r.integers(0, 4)
+        if act == 0 and len(live) < max_seqs:
+            L = int(r.integers(0, 200))
+            try:
+                s_m = model.join(L)
+            except OutOfBlocks:
+                with pytest.raises(binding.OutOfBlocks):
+                    cpp.join(L)
+                continue
+            assert cpp.join(L) == s_m
+            live.append(s_m)
+        elif act == 1 and live:
+            s = live.pop(int(r.integers(0, len(live))))
+            model.leave(s)
+            cpp.leave(s)
+        elif live:
+            ids = [s for s in live if model.seq_len(s) < (bt - 1) * 16]
+            r.shuffle(ids)
+            try:
+                ref = model.prepare_step(ids, bt)
+            except OutOfBlocks:
+                with pytest.raises(binding.OutOfBlocks):
+                    cpp.prepare_step(ids, bt)
+                continue
+            got = cpp.prepare_step(ids, bt)
+            for a_, b_ in zip(ref, got):
+                np.testing.assert_array_equal(a_, b_)
+        assert cpp.free_stack() == model.free
+        assert cpp.num_free() == model.num_free()
+        for s in live:
+            assert cpp.seq_blocks(s) == model.seq_blocks(s)
+            assert cpp.seq_len(s) == model.seq_len(s)
+
+
+def test_cpp_allocator_rejects_bad_input(host_lib):
+    from paged_kv_decode_10_gb300 import binding
+    with pytest.raises(binding.PkvError):
+        binding.BlockAllocator(4, 2, 2, [0, 1, 1, 2])          # not a permutation
+    a = binding.BlockAllocator(8, 2, 2)
+    s = a.join(3)
+    with pytest.raises(binding.PkvError):
+        a.prepare_step([s, s], 2)                             # duplicate row
+    with pytest.raises(binding.UnknownSequence):
+        a.prepare_step([1], 2)
+    with pytest.raises(binding.PkvError):
+        a.join(33)                                            # wider than a table
+    with pytest.raises(binding.UnknownSequence):
+        a.leave(5)
+    assert a.seq_len(s) == 3 and a.num_free() == 7
