@@ -250,80 +250,100 @@ def run_gpu(args, rank, world):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     w = workloads.make_workload(args.workload)
-    W, K = args.warmup, args.steps
-    dec, ids, tokens, cpu_caches = setup(w, device, args.parts, args.flags, W + K + 1)
-    assert dec.bt_stride * 16 >= int(w.seq_lens.max()) + W + K + 64
+    W, K, GW = args.warmup, args.steps, 2
+    dec, ids, tokens, cpu_caches = setup(w, device, args.parts, args.flags, W + GW + K + 1)
+    assert dec.bt_stride * 16 >= int(w.seq_lens.max()) + W + GW + K + 64
+    B = len(ids)
     elem = 2 if w.dtype == "bf16" else 4
     stream = torch.cuda.current_stream(device)
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    flush_buf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=device)
+    # read in full before every timed step: evicts the KV from L2 (without
+    # leaving dirty lines to write back) and keeps the GPU busy while the host
+    # prepares the next step
+    flush_buf = torch.ones(max(4 * l2, 512 << 20) // 8, dtype=torch.int64, device=device)
 
-    # the oracle sample for the cpu baseline is the first step's state
+    def flush():
+        if not args.no_flush:
+            flush_buf.sum()
+
+    oracle_state = None
     if not args.no_cpu and rank == 0 and cpu_caches is not None:
         oracle_state = (cpu_caches, [t.cpu() for t in tokens[0]])
-    else:
-        oracle_state = None
 
-    def one_step(s, events=None):
-        B = len(ids)
-        dec.prepare(ids)
-        q, k, v = tokens[s]
-        if events:
-            events[0].record(stream)
-        binding.rope(q, k, dec.positions[:B], w.rope_base, dec.q_rot[:B], dec.k_rot[:B])
-        binding.append(dec.k_rot[:B], v, dec.slots[:B], dec.k_cache, dec.v_cache, dec.err)
-        if events:
-            events[1].record(stream)
-        binding.decode_attn_split(dec.q_rot[:B], dec.k_cache, dec.v_cache, dec.tables[:B],
-                                  dec.seq_lens[:B], dec.scale, dec.num_parts, dec.workspace,
-                                  dec.out[:B], flags=dec.flags, err=dec.err)
-        if events:
-            events[2].record(stream)
-        binding.lse_merge(dec.workspace, dec.seq_lens[:B], dec.bt_stride, B, w.Hq, w.Hkv, w.d,
-                          dec.num_parts, dec.out[:B])
-        if events:
-            events[3].record(stream)
-
-    lens_after = []
+    # warm-up: eager steps through the C ABI (one pkv_decode_step call each)
     meta0 = None
     for s in range(W):
-        one_step(s)
+        q, k, v = tokens[s]
+        dec.step(ids, q, k, v)
         if s == 0:
             meta0 = [np.array(x) for x in dec.last_metadata]
+    # the timed step: one CUDA graph (metadata H2D + rope/append + attention)
+    dec.capture(B)
+
+    def stage(s):
+        q, k, v = tokens[s]
+        dec.q_in[:B].copy_(q)
+        dec.k_in[:B].copy_(k)
+        dec.v_in[:B].copy_(v)
+
+    for s in range(W, W + GW):
+        stage(s)
+        dec.prepare_host(ids)
+        dec.replay_step()
     torch.cuda.synchronize()
     sampler = ClockSampler(local)
     sampler.start()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    lens_after = []
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     for i in range(K):
-        if not args.no_flush:
-            flush_buf.add_(1)
-        e = evs[i]
-        e[4].record(stream)                   # before a0's H2D copy
-        one_step(W + i, e[:4])
-        lens_after.append(np.array(dec.last_metadata[2]))
+        stage(W + GW + i)
+        flush()
+        lens_after.append(np.array(dec.prepare_host(ids)[2]))
+        evs[i][0].record(stream)
+        dec.replay_step()
+        evs[i][1].record(stream)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
-    step_ms = [e[4].elapsed_time(e[3]) for e in evs]
-    split_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    attn_ms = [e[1].elapsed_time(e[3]) for e in evs]
+    step_ms = [a.elapsed_time(b) for a, b in evs]
     total_s = sum(step_ms) / 1e3
     if world > 1:
         t = torch.tensor([total_s], dtype=torch.float64, device=device)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         total_s = float(t.item())
+
+    # the attention kernel timed alone on the final state, same launch
+    # configuration as in the step (split + fused LSE merge: a3 + a4)
+    # (captured once so that the launch costs no host time inside the events)
+    attn_graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(device)
+    cap.wait_stream(stream)
+    with torch.cuda.graph(attn_graph, stream=cap):
+        binding.decode_attn_split(dec.q_rot[:B], dec.k_cache, dec.v_cache, dec.tables[:B],
+                                  dec.seq_lens[:B], dec.scale, dec.num_parts, dec.workspace,
+                                  dec.out[:B], flags=dec.flags, err=dec.err)
+    stream.wait_stream(cap)
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    for i in range(K):
+        flush()
+        kev[i][0].record(stream)
+        attn_graph.replay()
+        kev[i][1].record(stream)
+    torch.cuda.synchronize()
+    attn_ms = [e[0].elapsed_time(e[1]) for e in kev]
+    last_lens = lens_after[-1]
+
     bytes_steps = [attn_bytes(la, w.Hq, w.Hkv, w.d, elem) for la in lens_after]
     kv_only = [int(np.asarray(la, np.int64).sum()) * w.Hkv * w.d * 2 * elem for la in lens_after]
     total_bytes = sum(bytes_steps) * world
     value = total_bytes / total_s / 1e9
-    attn_gbs = sum(bytes_steps) / (sum(attn_ms) / 1e3) / 1e9
-    # split kernel alone: everything but the output write (done partly by a4)
-    split_bytes = [b - len(la) * w.Hq * w.d * elem for b, la in zip(bytes_steps, lens_after)]
-    split_gbs = (sum(split_bytes) / len(split_bytes)) / (statistics.mean(split_ms) / 1e3) / 1e9
+    attn_b = attn_bytes(last_lens, w.Hq, w.Hkv, w.d, elem)
+    attn_gbs = attn_b / (statistics.mean(attn_ms) / 1e3) / 1e9
     assert dec.device_errors() == 0, "device error flag set during the bench"
 
     peak, peak_kind = measured_peak()
@@ -347,20 +367,21 @@ def run_gpu(args, rank, world):
                    "block_size": 16, "mean_kv_len": float(np.mean(lens_after[0])),
                    "pool_blocks": w.num_blocks, "num_parts": dec.num_parts,
                    "consumer": "simt" if (args.flags & 1 or w.dtype == "f32") else "mma.sync",
+                   "step": "one CUDA graph: metadata H2D + fused rope/append + split-KV attention with fused LSE merge",
                    "l2": "flushed before every timed step" if not args.no_flush else "not flushed",
                    "parallelism": "replicas" if world > 1 else "single-gpu"},
         "steps_per_s": round(K / (sum(step_ms) / 1e3), 1),
         "attn_gbs": round(attn_gbs, 2),
         "pct_of_peak": round(100 * attn_gbs / peak, 2),
         "kv_bytes_per_step": int(statistics.mean(kv_only)),
-        "roofline": {"bound": "hbm", "kernel": "attn_split_kernel (a3)",
-                     "achieved": round(split_gbs, 2), "peak": peak, "peak_kind": peak_kind,
-                     "unit": "GB/s", "frac": round(split_gbs / peak, 4),
+        "roofline": {"bound": "hbm", "kernel": "attn_split_kernel (a3 + fused a4)",
+                     "achieved": round(attn_gbs, 2), "peak": peak, "peak_kind": peak_kind,
+                     "unit": "GB/s", "frac": round(attn_gbs / peak, 4),
                      "traffic": traffic,
-                     "algorithmic_bytes_per_launch": int(statistics.mean(split_bytes)),
-                     "mean_launch_us": round(1e3 * statistics.mean(split_ms), 3),
+                     "algorithmic_bytes_per_launch": int(attn_b),
+                     "mean_launch_us": round(1e3 * statistics.mean(attn_ms), 3),
                      "kernel_hash": khash},
-        "gpu_launches": 4 * K,
+        "gpu_launches": 2 * K,
         "clocks": clocks,
     }
     return result, dec, ids, tokens, oracle_state, meta0, w
@@ -386,14 +407,14 @@ def run_e2e(args, dec, ids, tokens, w):
     args_s = dec.step_args(B, dq, dk, dv)
     io = binding.host_io(*pinned, *meta_h, out_h)
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    flush_buf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=device)
+    flush_buf = torch.ones(max(2 * l2, 256 << 20) // 8, dtype=torch.int64, device=device)
     h2d = sum(t.numel() * t.element_size() for t in pinned) + \
         sum(t.numel() * t.element_size() for t in meta_h)
     d2h = out_h.numel() * out_h.element_size()
     n = max(3, min(args.steps, 50))
     secs, nbytes = 0.0, 0
     for i in range(n + 3):
-        flush_buf.add_(1)
+        flush_buf.sum()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         views = tuple(m.numpy() for m in meta_h)

@@ -67,6 +67,8 @@ extern "C" {
 /* flags for the attention calls */
 #define PKV_ATTN_SIMT 1         /* use the CUDA-core consumer instead of mma.sync (bf16 only;
                                    f32 always uses CUDA cores) */
+#define PKV_ATTN_SEPARATE_MERGE 2 /* leave the split partials for pkv_lse_merge instead of
+                                     merging them in the split kernel's epilogue */
 
 /* Message for the calling thread's last failed call ("" if none). */
 const char *pkv_last_error(void);
@@ -158,6 +160,17 @@ int pkv_append(const void *k_rot, const void *v, const int64_t *slot_mapping,
                void *k_cache, void *v_cache, int32_t B, int32_t Hkv, int32_t d,
                int32_t num_blocks, int32_t dtype, int32_t *dev_err_flag, void *stream);
 
+/*
+ * a1 + a2 fused: one launch that rotates q and k as pkv_rope does and writes
+ * the rotated key and the raw value into the cache slot as pkv_append does
+ * (k_out still receives the rotated key).  Same argument rules as the two calls.
+ */
+int pkv_rope_append(const void *q, const void *k, const void *v, void *q_out, void *k_out,
+                    const int32_t *positions, const int64_t *slot_mapping, void *k_cache,
+                    void *v_cache, int32_t B, int32_t Hq, int32_t Hkv, int32_t d,
+                    int32_t num_blocks, float base, int32_t dtype, int32_t *dev_err_flag,
+                    void *stream);
+
 /* ======================================================================== */
 /* a3 + a4: split-KV paged GQA decode attention and its LSE merge            */
 /* ("neurogrid releases" v0.7.0 paged attention with GQA, v0.6.0 flash       */
@@ -176,12 +189,20 @@ int pkv_append(const void *k_rot, const void *v, const int64_t *slot_mapping,
  * Partition: the pages of all (row, KV head) units, in row-major order, form
  * one list of P pages; part c of num_parts owns pages
  * [floor(c*P/num_parts), floor((c+1)*P/num_parts)) and runs as one CTA.  A
- * unit whose pages lie in one part is written to `out` directly by
- * pkv_decode_attn_split; every other unit leaves one float32 (o, lse) partial
- * per part it touches in `workspace`, and pkv_lse_merge combines them
- * (M = max lse; out = sum exp(lse_s - M) o_s / sum exp(lse_s - M)) and also
- * writes the zeros of empty rows.  The two calls must run in this order with
- * the same arguments; `out` is complete only after pkv_lse_merge.
+ * unit whose pages lie in one part is written to `out` directly.  Every other
+ * unit leaves one float32 (o, lse) partial per part it touches in `workspace`;
+ * the LSE merge (M = max lse; out = sum exp(lse_s - M) o_s / sum exp(lse_s - M))
+ * then combines them.  By default the merge runs in the epilogue of
+ * pkv_decode_attn_split (the last part to finish a unit merges it), so `out`
+ * is complete when the call's kernel ends.  With PKV_ATTN_SEPARATE_MERGE the
+ * split kernel stops at the partials and pkv_lse_merge must follow with the
+ * same arguments.  pkv_lse_merge may also be called after a fused call: it
+ * recomputes the same merge from the partials left in the workspace.
+ *
+ * Workspace: pkv_attn_workspace_bytes(...) bytes, 256-byte aligned, owned by
+ * the caller, ZERO-FILLED ONCE after allocation (it holds the fused merge's
+ * per-unit counters, which every call leaves at zero).  Calls that share a
+ * workspace must not overlap on the GPU.
  *
  * Supported: dtype PKV_BF16 or PKV_F32; d in {64, 128}; Hq/Hkv in {1,2,4,8};
  * B <= 65536.  q_rot [B,Hq,d]; out [B,Hq,d] (device, dtype).
@@ -231,7 +252,9 @@ typedef struct pkv_step_args {
   int32_t *dev_err_flag;             /* nullable */
 } pkv_step_args;
 
-/* All device pointers in *args; asynchronous on stream. */
+/* All device pointers in *args; asynchronous on stream.  Runs pkv_rope_append,
+ * pkv_decode_attn_split and, when flags has PKV_ATTN_SEPARATE_MERGE,
+ * pkv_lse_merge.  q_rot/k_rot receive the rotated q and k. */
 int pkv_decode_step(const pkv_step_args *args, void *stream);
 
 /* Host-side buffers for pkv_decode_step_host (pinned memory recommended). */

@@ -18,6 +18,7 @@ F32, BF16 = 0, 1
 BLOCK_SIZE = 16
 DEVERR_BAD_BLOCK, DEVERR_BAD_SLOT, DEVERR_BAD_LEN, DEVERR_TIMEOUT = 1, 2, 4, 8
 ATTN_SIMT = 1
+ATTN_SEPARATE_MERGE = 2
 
 _c_i32 = ctypes.c_int32
 _c_i64 = ctypes.c_int64
@@ -84,6 +85,9 @@ SIGNATURES = {
     "pkv_alloc_dump": (ctypes.c_int, [_vp, _p_i32, _c_i32, _p_i32]),
     "pkv_rope": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _c_i32, _c_i32, _c_i32, _c_i32,
                                 ctypes.c_float, _c_i32, _vp]),
+    "pkv_rope_append": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_i32,
+                                       _c_i32, _c_i32, _c_i32, _c_i32, ctypes.c_float, _c_i32,
+                                       _vp, _vp]),
     "pkv_append": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _c_i32, _c_i32, _c_i32, _c_i32,
                                   _c_i32, _vp, _vp]),
     "pkv_attn_default_parts": (ctypes.c_int, [_c_i32, _c_i32, _c_i32, _p_i32]),
@@ -266,6 +270,20 @@ def rope(q, k, positions, base=10000.0, q_out=None, k_out=None, stream=None):
     return q_out, k_out
 
 
+def rope_append(q, k, v, positions, slot_mapping, k_cache, v_cache, base=10000.0, q_out=None,
+                k_out=None, err=None, stream=None):
+    """a1 + a2 fused: rotate q/k and write the rotated k and raw v into the cache slots."""
+    torch = _torch()
+    q_out = torch.empty_like(q) if q_out is None else q_out
+    k_out = torch.empty_like(k) if k_out is None else k_out
+    B, Hq, d = q.shape
+    _check(load().pkv_rope_append(_ptr(q), _ptr(k), _ptr(v), _ptr(q_out), _ptr(k_out),
+                                  _ptr(positions), _ptr(slot_mapping), _ptr(k_cache),
+                                  _ptr(v_cache), B, Hq, k.shape[1], d, k_cache.shape[0],
+                                  float(base), dtype_code(q), _ptr(err), _stream(stream)))
+    return q_out, k_out
+
+
 def append(k_rot, v, slot_mapping, k_cache, v_cache, err=None, stream=None):
     """a2: write ``k_rot``/``v`` ``[B,Hkv,d]`` into cache slots ``slot_mapping [B]`` (int64)."""
     B, Hkv, d = k_rot.shape
@@ -289,7 +307,8 @@ def workspace_bytes(B, Hq, Hkv, d, num_parts):
 def alloc_workspace(B, Hq, Hkv, d, num_parts, device=None):
     torch = _torch()
     nbytes = workspace_bytes(B, Hq, Hkv, d, num_parts)
-    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device or "cuda")
+    # zero-filled once: the fused merge's counters start (and stay) at zero
+    return torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device or "cuda")
 
 
 def decode_attn_split(q_rot, k_cache, v_cache, block_tables, seq_lens, scale, num_parts,
@@ -328,8 +347,9 @@ def decode_attention(q_rot, k_cache, v_cache, block_tables, seq_lens, scale, num
         out = torch.empty_like(q_rot)
     decode_attn_split(q_rot, k_cache, v_cache, block_tables, seq_lens, scale, num_parts,
                       workspace, out, attn_bias, flags, err, stream)
-    lse_merge(workspace, seq_lens, block_tables.shape[1], B, Hq, Hkv, d, num_parts, out,
-              attn_bias.shape[1] if attn_bias is not None else 0, stream)
+    if flags & ATTN_SEPARATE_MERGE:
+        lse_merge(workspace, seq_lens, block_tables.shape[1], B, Hq, Hkv, d, num_parts, out,
+                  attn_bias.shape[1] if attn_bias is not None else 0, stream)
     return out
 
 

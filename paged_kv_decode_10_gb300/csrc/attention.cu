@@ -22,23 +22,36 @@ constexpr int kMaxB = 65536;
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct Workspace {
-  int32_t *meta;
-  float *lse;
-  float *o;
+  int32_t *counters;       // [U + C]
+  int32_t *unit_counters;  // [U]
+  int32_t *meta;           // [U x 2 + 2]
+  float *lse, *o;          // [(U + C) x G], [(U + C) x G x D]
+  float *lse2, *o2;        // the same shapes, merged groups
   size_t bytes;
 };
 
-// [meta: U x 2 int32][lse: (U + C) x G f32][o: (U + C) x G x D f32]
+// [counters][unit_counters][meta][lse][o][lse2][o2], each region 256-byte aligned
 Workspace workspace_layout(void *base, int B, int Hq, int Hkv, int D, int C) {
   const size_t U = static_cast<size_t>(B) * Hkv;
   const size_t G = static_cast<size_t>(Hq / Hkv);
   const size_t S = U + static_cast<size_t>(C);
-  const size_t meta_b = align256(U * 2 * sizeof(int32_t));
-  const size_t lse_b = align256(S * G * sizeof(float));
-  const size_t o_b = align256(S * G * static_cast<size_t>(D) * sizeof(float));
+  const size_t sizes[7] = {align256(S * sizeof(int32_t)), align256(U * sizeof(int32_t)),
+                           align256((U * 2 + 2) * sizeof(int32_t)),
+                           align256(S * G * sizeof(float)),
+                           align256(S * G * static_cast<size_t>(D) * sizeof(float)),
+                           align256(S * G * sizeof(float)),
+                           align256(S * G * static_cast<size_t>(D) * sizeof(float))};
   char *p = static_cast<char *>(base);
-  return Workspace{reinterpret_cast<int32_t *>(p), reinterpret_cast<float *>(p + meta_b),
-                   reinterpret_cast<float *>(p + meta_b + lse_b), meta_b + lse_b + o_b};
+  char *r[7];
+  size_t off = 0;
+  for (int i = 0; i < 7; ++i) {
+    r[i] = p + off;
+    off += sizes[i];
+  }
+  return Workspace{reinterpret_cast<int32_t *>(r[0]), reinterpret_cast<int32_t *>(r[1]),
+                   reinterpret_cast<int32_t *>(r[2]), reinterpret_cast<float *>(r[3]),
+                   reinterpret_cast<float *>(r[4]), reinterpret_cast<float *>(r[5]),
+                   reinterpret_cast<float *>(r[6]), off};
 }
 
 // ---- cuTensorMapEncodeTiled through the runtime's driver entry point ------
@@ -168,20 +181,16 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const float *__restrict_
     for (int e = threadIdx.x; e < G * D; e += blockDim.x) o[e] = from_f32<T>(NAN);
     return;
   }
+  const int Uall = gridDim.x;
+  const long long P = static_cast<long long>(static_cast<uint32_t>(meta[2 * Uall])) |
+                      (static_cast<long long>(meta[2 * Uall + 1]) << 32);
   const size_t first = static_cast<size_t>(u) + c0;
-  for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
-    const int h = e / D, dim = e - h * D;
-    float M = -INFINITY;
-    for (int s = 0; s < nseg; ++s) M = fmaxf(M, lse_part[(first + s) * G + h]);
-    float num = 0.f, den = 0.f;
-    if (M != -INFINITY) {
-      for (int s = 0; s < nseg; ++s) {
-        const float w = ex2(lse_part[(first + s) * G + h] - M);
-        den += w;
-        num = fmaf(w, o_part[((first + s) * G + h) * D + dim], num);
-      }
-    }
-    o[e] = from_f32<T>(den > 0.f ? num / den : 0.f);
+  auto skip = [&](int i) { return num_parts > P && part_empty(c0 + i, P, num_parts); };
+  for (int col = threadIdx.x; col < G * D / 4; col += blockDim.x) {
+    const int h = col / (D / 4), d4 = col - h * (D / 4);
+    float l;
+    store4<T>(o + h * D + 4 * d4,
+              merge_column(o_part, lse_part, first, nseg, 1, G, D, h, d4, skip, &l));
   }
 }
 
@@ -265,6 +274,11 @@ extern "C" int pkv_decode_attn_split(const void *q_rot, const void *k_cache, con
   p.o_part = ws.o;
   p.lse_part = ws.lse;
   p.meta = ws.meta;
+  p.counters = ws.counters;
+  p.unit_counters = ws.unit_counters;
+  p.o_group = ws.o2;
+  p.lse_group = ws.lse2;
+  p.fuse_merge = (flags & PKV_ATTN_SEPARATE_MERGE) ? 0 : 1;
   p.out = out;
   p.err = dev_err_flag;
   p.bt_stride = bt_stride;
@@ -324,17 +338,16 @@ extern "C" int pkv_decode_step(const pkv_step_args *a, void *stream) {
     rc = default_parts(a->d, a->dtype, a->flags, a->Hq / a->Hkv, &num_parts);
     if (rc != PKV_OK) return rc;
   }
-  int rc = pkv_rope(a->q, a->k, a->q_rot, a->k_rot, a->positions, a->B, a->Hq, a->Hkv, a->d,
-                    a->rope_base, a->dtype, stream);
-  if (rc != PKV_OK) return rc;
-  rc = pkv_append(a->k_rot, a->v, a->slot_mapping, a->k_cache, a->v_cache, a->B, a->Hkv, a->d,
-                  a->num_blocks, a->dtype, a->dev_err_flag, stream);
+  int rc = pkv_rope_append(a->q, a->k, a->v, a->q_rot, a->k_rot, a->positions, a->slot_mapping,
+                           a->k_cache, a->v_cache, a->B, a->Hq, a->Hkv, a->d, a->num_blocks,
+                           a->rope_base, a->dtype, a->dev_err_flag, stream);
   if (rc != PKV_OK) return rc;
   rc = pkv_decode_attn_split(a->q_rot, a->k_cache, a->v_cache, a->num_blocks, a->block_tables,
                              a->bt_stride, a->seq_lens, a->attn_bias, a->bias_stride, a->B, a->Hq,
                              a->Hkv, a->d, a->scale, num_parts, a->workspace, a->workspace_bytes,
                              a->out, a->dtype, a->flags, a->dev_err_flag, stream);
   if (rc != PKV_OK) return rc;
+  if (!(a->flags & PKV_ATTN_SEPARATE_MERGE)) return PKV_OK;
   return pkv_lse_merge(a->workspace, a->workspace_bytes, a->seq_lens, a->bt_stride,
                        a->attn_bias ? a->bias_stride : 0, a->B, a->Hq, a->Hkv, a->d, num_parts,
                        a->out, a->dtype, stream);

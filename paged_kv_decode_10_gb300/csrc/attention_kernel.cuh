@@ -48,12 +48,17 @@ struct AttnParams {
   const float *bias;        // nullable [B, bias_stride]
   float *o_part;            // [(U + C), G, D]
   float *lse_part;          // [(U + C), G]
-  int32_t *meta;            // [U, 2]: first part, number of parts
+  int32_t *meta;            // [U, 2]: first part, number of parts spanned; then P (int64)
+  int32_t *counters;        // [U + C] finished-part counters per merge group (kept at 0)
+  int32_t *unit_counters;   // [U] finished-group counters per unit (kept at 0)
+  float *o_group;           // [(U + C), G, D] merged groups of a unit's partials
+  float *lse_group;         // [(U + C), G]
   void *out;                // [B, Hq, D]
   int32_t *err;
   int bt_stride, bias_stride;
   int B, Hq, Hkv, G;
   int num_blocks, num_parts;
+  int fuse_merge;           // 1: the last part of a unit merges it (a4 in the epilogue)
   float scale_log2;         // softmax scale * log2(e)
 };
 
@@ -72,6 +77,91 @@ __device__ __forceinline__ int row_pages(const int32_t *seq_lens, int b, int bt_
 // Part that owns global page x: the largest c with floor(c*P/C) <= x.
 __device__ __forceinline__ int part_of(long long x, long long P, int C) {
   return static_cast<int>(((x + 1) * C - 1) / P);
+}
+
+// The fused merge combines a unit's partials in groups of kMergeGroup parts
+// (the last part of a group to finish merges the group), then the last group
+// merger combines the group results: no CTA ever merges more than
+// max(kMergeGroup, groups) partials, whatever the split count.
+constexpr int kMergeGroup = 16;
+
+// A part owns no page when C > P and its page range is empty.
+__device__ __forceinline__ bool part_empty(long long c, long long P, int C) {
+  return (P * c / C) == (P * (c + 1) / C);
+}
+
+// Parts c0 .. c0+n-1 that own at least one page (all of them when C <= P).
+__device__ __forceinline__ int real_parts(int c0, int n, long long P, int C) {
+  if (C <= P) return n;
+  int r = 0;
+  for (int s = 0; s < n; ++s) r += !part_empty(c0 + s, P, C);
+  return r;
+}
+
+// Merge groups of a unit spanning parts c0 .. c0+nseg-1 that own a page.
+__device__ __forceinline__ int real_groups(int c0, int nseg, long long P, int C) {
+  const int ng = (nseg + kMergeGroup - 1) / kMergeGroup;
+  if (C <= P) return ng;
+  int r = 0;
+  for (int k = 0; k < ng; ++k)
+    r += real_parts(c0 + k * kMergeGroup, min(kMergeGroup, nseg - k * kMergeGroup), P, C) > 0;
+  return r;
+}
+
+// a4, the LSE merge of one float4 column (head h, dims 4*d4 .. 4*d4+3) over the
+// partials i < n stored at slots slot0 + i*stride (skip(i): no partial there).
+// A partial is (o_s normalised, base-2 lse_s):
+//   out = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M),  M = max_s lse_s,
+// and the merged lse is M + log2(sum_s 2^(lse_s - M)).  Nothing unmasked
+// anywhere -> zeros and lse = -inf.  Loads bypass L1: other CTAs of this grid
+// wrote the partials.
+template <typename Skip>
+__device__ __forceinline__ float4 merge_column(const float *o, const float *lse, size_t slot0,
+                                               int n, int stride, int G, int D, int h, int d4,
+                                               Skip skip, float *lse_out) {
+  float M = -INFINITY;
+  for (int i = 0; i < n; ++i)
+    if (!skip(i)) M = fmaxf(M, __ldcg(lse + (slot0 + static_cast<size_t>(i) * stride) * G + h));
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float den = 0.f;
+  if (M != -INFINITY) {
+    for (int i = 0; i < n; ++i) {
+      if (skip(i)) continue;
+      const size_t s = slot0 + static_cast<size_t>(i) * stride;
+      const float w = ex2(__ldcg(lse + s * G + h) - M);
+      const float4 v = __ldcg(reinterpret_cast<const float4 *>(o + (s * G + h) * D) + d4);
+      den += w;
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z);
+      acc.w = fmaf(w, v.w, acc.w);
+    }
+  }
+  if (den > 0.f) {
+    const float r = 1.f / den;
+    acc.x *= r;
+    acc.y *= r;
+    acc.z *= r;
+    acc.w *= r;
+    *lse_out = M + log2f(den);
+  } else {
+    *lse_out = -INFINITY;
+  }
+  return acc;
+}
+
+template <typename T>
+__device__ __forceinline__ void store4(T *dst, float4 v);
+template <>
+__device__ __forceinline__ void store4<float>(float *dst, float4 v) {
+  *reinterpret_cast<float4 *>(dst) = v;
+}
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16 *dst, float4 v) {
+  uint2 w;
+  w.x = pack_bf16(v.x, v.y);
+  w.y = pack_bf16(v.z, v.w);
+  *reinterpret_cast<uint2 *>(dst) = w;
 }
 
 struct UnitCursor {
@@ -507,6 +597,20 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
       acc += n;
     }
   }
+  // rows with no token (or an invalid length) output zeros; part c clears rows
+  // c, c + C, ...
+  for (int b = blockIdx.x; b < p.B; b += C) {
+    bool bad;
+    if (row_pages(p.seq_lens, b, p.bt_stride, has_bias, p.bias_stride, &bad) == 0) {
+      T *o = static_cast<T *>(p.out) + static_cast<size_t>(b) * p.Hq * D;
+      for (int e = tid; e < p.Hq * D; e += nthreads) o[e] = from_f32<T>(0.f);
+    }
+  }
+  if (blockIdx.x == 0 && tid == 0) {
+    // total page count, for the merge to tell empty parts (C > P) from real ones
+    p.meta[2 * p.B * p.Hkv] = static_cast<int32_t>(P & 0xffffffffll);
+    p.meta[2 * p.B * p.Hkv + 1] = static_cast<int32_t>(P >> 32);
+  }
   __syncthreads();
   if (start >= end) return;
   if (misc[0] < 0) {   // the row scan found no owner of `start` (never expected)
@@ -679,6 +783,66 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
     if (tid == 0 && j0 == 0) {
       p.meta[2 * u_idx] = c_first;
       p.meta[2 * u_idx + 1] = nseg;
+    }
+    if (nseg > 1 && p.fuse_merge) {
+      // a4 in the epilogue (threadfence-reduction pattern, two levels; every
+      // counter is reset by the CTA that consumes it)
+      const int grp = (static_cast<int>(blockIdx.x) - c_first) / kMergeGroup;
+      const int g0 = c_first + grp * kMergeGroup;
+      const int gcount = min(kMergeGroup, nseg - grp * kMergeGroup);
+      const int ngroups = (nseg + kMergeGroup - 1) / kMergeGroup;
+      const int ncol = gq * D / 4;
+      T *out_u = static_cast<T *>(p.out) + (static_cast<size_t>(u.b) * p.Hq + u.g * gq) * D;
+      __threadfence();
+      asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
+      if (tid == 0) {
+        const int prev = atomicAdd(&p.counters[u_idx + g0], 1);
+        misc[3] = (prev == real_parts(g0, gcount, P, C) - 1) ? 1 : 0;
+      }
+      asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
+      if (misc[3]) {
+        __threadfence();
+        const size_t slot0 = static_cast<size_t>(u_idx) + g0;
+        auto skip1 = [&](int i) { return C > P && part_empty(g0 + i, P, C); };
+        for (int col = tid; col < ncol; col += kConsumers) {
+          const int h = col / (D / 4), d4 = col - h * (D / 4);
+          float l;
+          const float4 r = merge_column(p.o_part, p.lse_part, slot0, gcount, 1, gq, D, h, d4,
+                                        skip1, &l);
+          if (ngroups == 1) {
+            store4<T>(out_u + h * D + 4 * d4, r);
+          } else {
+            *reinterpret_cast<float4 *>(p.o_group + (slot0 * gq + h) * D + 4 * d4) = r;
+            if (d4 == 0) p.lse_group[slot0 * gq + h] = l;
+          }
+        }
+        if (tid == 0) p.counters[u_idx + g0] = 0;
+        if (ngroups > 1) {
+          __threadfence();
+          asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
+          if (tid == 0) {
+            const int prev = atomicAdd(&p.unit_counters[u_idx], 1);
+            misc[3] = (prev == real_groups(c_first, nseg, P, C) - 1) ? 1 : 0;
+          }
+          asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
+          if (misc[3]) {
+            __threadfence();
+            auto skip2 = [&](int k) {
+              return C > P && real_parts(c_first + k * kMergeGroup,
+                                         min(kMergeGroup, nseg - k * kMergeGroup), P, C) == 0;
+            };
+            for (int col = tid; col < ncol; col += kConsumers) {
+              const int h = col / (D / 4), d4 = col - h * (D / 4);
+              float l;
+              const float4 r = merge_column(p.o_group, p.lse_group,
+                                            static_cast<size_t>(u_idx) + c_first, ngroups,
+                                            kMergeGroup, gq, D, h, d4, skip2, &l);
+              store4<T>(out_u + h * D + 4 * d4, r);
+            }
+            if (tid == 0) p.unit_counters[u_idx] = 0;
+          }
+        }
+      }
     }
     asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
     x += j1 - j0;

@@ -55,6 +55,11 @@ class PagedDecoder:
         self.k_rot = torch.empty((max_seqs, Hkv, d), dtype=self.tdtype, **dev)
         self.out = torch.empty((max_seqs, Hq, d), dtype=self.tdtype, **dev)
         self.err = torch.zeros(1, dtype=torch.int32, **dev)
+        # fixed input buffers for graph replay (the producer of q/k/v writes here)
+        self.q_in = torch.empty((max_seqs, Hq, d), dtype=self.tdtype, **dev)
+        self.k_in = torch.empty((max_seqs, Hkv, d), dtype=self.tdtype, **dev)
+        self.v_in = torch.empty((max_seqs, Hkv, d), dtype=self.tdtype, **dev)
+        self._graphs = None
         # two pinned metadata sets so the host can fill step i+1 while step i's
         # copy is still queued
         self._host = []
@@ -113,6 +118,54 @@ class PagedDecoder:
         B = len(seq_ids)
         self.prepare(seq_ids, stream)
         binding.decode_step_args(self.step_args(B, q, k, v, attn_bias), stream)
+        return self.out[:B]
+
+    # -- CUDA graph of the whole device step ("neurogrid releases" v0.8.0) ---
+    def capture(self, B, attn_bias=None):
+        """Captures, for a fixed batch size B, one CUDA graph per pinned
+        metadata set: the metadata H2D copies followed by a1..a4 reading
+        ``q_in/k_in/v_in[:B]``.  ``replay_step`` then costs one graph launch."""
+        torch = self.torch
+        binding.default_parts(self.d, binding.F32 if self.dtype == "f32" else binding.BF16,
+                              self.flags)   # sets kernel attributes outside capture
+        args = self.step_args(B, self.q_in[:B], self.k_in[:B], self.v_in[:B], attn_bias)
+        stream = torch.cuda.Stream(self.device)
+        stream.wait_stream(torch.cuda.current_stream(self.device))
+        graphs = []
+        for h in self._host:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                self.positions[:B].copy_(h["pos"][:B], non_blocking=True)
+                self.slots[:B].copy_(h["slots"][:B], non_blocking=True)
+                self.seq_lens[:B].copy_(h["lens"][:B], non_blocking=True)
+                self.tables[:B].copy_(h["tables"][:B], non_blocking=True)
+                binding.decode_step_args(args, stream)
+            graphs.append(g)
+        torch.cuda.current_stream(self.device).wait_stream(stream)
+        self._graphs = (B, graphs, args)
+
+    def prepare_host(self, seq_ids):
+        """a0 into the pinned set the next replay will copy from."""
+        h = self._host[self._turn]
+        if h["event"] is not None:
+            h["event"].synchronize()
+        B = len(seq_ids)
+        views = (h["pos"][:B].numpy(), h["slots"][:B].numpy(), h["lens"][:B].numpy(),
+                 h["tables"][:B].numpy())
+        self.alloc.prepare_step(seq_ids, self.bt_stride, out=views)
+        self.last_metadata = views
+        return views
+
+    def replay_step(self):
+        """Launches the captured step for the metadata of the last prepare_host."""
+        torch = self.torch
+        B, graphs, _ = self._graphs
+        turn = self._turn
+        self._turn ^= 1
+        graphs[turn].replay()
+        ev = torch.cuda.Event()
+        ev.record(torch.cuda.current_stream(self.device))
+        self._host[turn]["event"] = ev
         return self.out[:B]
 
     def device_errors(self):

@@ -346,3 +346,73 @@ def test_multi_step_churn_matches_oracle(dtype, d, hq, hkv):
         assert_out_close(f64(out), ref["out"], dtype, f"step {step}")
         assert dec.alloc.free_stack() == model.free
     assert dec.device_errors() == 0
+
+
+def test_fused_rope_append_equals_separate_calls():
+    w = workloads.make_workload("ragged64")
+    d = dev()
+    k_cache, v_cache = (c.to(d) for c in workloads.make_caches(w, "cpu"))
+    q, k, v = (t.to(d) for t in workloads.make_new_tokens(w, 0, "cpu"))
+    pos, slots, _, _ = (torch.from_numpy(np.ascontiguousarray(m)).to(d)
+                        for m in oracle_metadata(w))
+    kc1, vc1 = k_cache.clone(), v_cache.clone()
+    q1, k1 = binding.rope(q, k, pos)
+    binding.append(k1, v, slots, kc1, vc1)
+    kc2, vc2 = k_cache.clone(), v_cache.clone()
+    q2, k2 = binding.rope_append(q, k, v, pos, slots, kc2, vc2)
+    torch.cuda.synchronize()
+    assert torch.equal(q1, q2) and torch.equal(k1, k2)
+    assert torch.equal(kc1, kc2) and torch.equal(vc1, vc2)
+
+
+@pytest.mark.parametrize("name,parts", [("tiny", None), ("tiny", 1000), ("decode16", 7),
+                                        ("long131k", None)])
+def test_separate_merge_equals_fused(name, parts):
+    """a4 as its own launch (pkv_lse_merge) gives the same output as the merge
+    fused into the split kernel's epilogue, and re-merging is idempotent."""
+    w = workloads.make_workload(name)
+    fused = gpu_single_step(w, num_parts=parts)
+    sep = gpu_single_step(w, num_parts=parts, flags=binding.ATTN_SEPARATE_MERGE)
+    # the fused merge combines groups of 16 partials first: same value up to
+    # float32 summation order, i.e. within one ulp of the output type
+    close = 1e-6 if w.dtype == "f32" else 1e-2
+    assert (fused["out"].float() - sep["out"].float()).abs().max() <= close
+    _check_full_step(w, sep)
+    dec = fused["decoder"]
+    B = w.B
+    # re-merging rewrites the multi-part units with the same values and leaves
+    # the single-part units alone
+    again = fused["out"].to(d := dev())
+    binding.lse_merge(dec.workspace, dec.seq_lens[:B], dec.bt_stride, B, w.Hq, w.Hkv, w.d,
+                      dec.num_parts, again)
+    torch.cuda.synchronize()
+    assert (again.cpu().float() - fused["out"].float()).abs().max() <= close
+
+
+def test_graph_replay_matches_eager_steps():
+    """The captured step (metadata H2D + rope/append + attention in one CUDA
+    graph) gives bit-identical outputs and caches to the eager C ABI calls."""
+    w = workloads.make_workload("decode16")
+    d = dev()
+    caches = workloads.make_caches(w, "cpu")
+    bt = w.max_blocks_per_seq(extra_tokens=8)
+    decs = []
+    for _ in range(2):
+        dec = engine.PagedDecoder(w.num_blocks, w.Hq, w.Hkv, w.d, w.dtype, w.B, bt,
+                                  initial_free=w.free_order, device=d,
+                                  k_cache=caches[0].to(d), v_cache=caches[1].to(d))
+        decs.append((dec, [dec.join(int(L)) for L in w.seq_lens]))
+    (eager, ids_e), (graph, ids_g) = decs
+    graph.capture(w.B)
+    for step in range(4):
+        q, k, v = (t.to(d) for t in workloads.make_new_tokens(w, step, "cpu"))
+        out_e = eager.step(ids_e, q, k, v).clone()
+        graph.q_in[:w.B].copy_(q)
+        graph.k_in[:w.B].copy_(k)
+        graph.v_in[:w.B].copy_(v)
+        graph.prepare_host(ids_g)
+        out_g = graph.replay_step().clone()
+        torch.cuda.synchronize()
+        assert torch.equal(out_e, out_g), step
+    assert torch.equal(eager.k_cache, graph.k_cache) and torch.equal(eager.v_cache, graph.v_cache)
+    assert eager.device_errors() == 0 and graph.device_errors() == 0
