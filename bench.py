@@ -270,9 +270,26 @@ def run_gpu(args, rank, world):
     if not args.no_cpu and rank == 0 and cpu_caches is not None:
         oracle_state = (cpu_caches, [t.cpu() for t in tokens[0]])
 
+    churn_s = []
+
+    def churn(s):
+        """Continuous batching: before step s >= 1 the planned rows leave and new
+        rows join in their places (host allocator only; no KV moves).  The
+        joiner's prefix blocks keep whatever KV they held (a stand-in prefill)."""
+        if not w.churn or s == 0:
+            return
+        leave, prefixes = w.churn[(s - 1) % len(w.churn)]
+        t0 = time.perf_counter()
+        for row in leave:
+            dec.leave(ids[row])
+        for row, pre in zip(leave, prefixes):
+            ids[row] = dec.join(int(pre))
+        churn_s.append(time.perf_counter() - t0)
+
     # warm-up: eager steps through the C ABI (one pkv_decode_step call each)
     meta0 = None
     for s in range(W):
+        churn(s)
         q, k, v = tokens[s]
         dec.step(ids, q, k, v)
         if s == 0:
@@ -287,6 +304,7 @@ def run_gpu(args, rank, world):
         dec.v_in[:B].copy_(v)
 
     for s in range(W, W + GW):
+        churn(s)
         stage(s)
         dec.prepare_host(ids)
         dec.replay_step()
@@ -299,10 +317,14 @@ def run_gpu(args, rank, world):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    t_host = 0.0
     for i in range(K):
+        churn(W + GW + i)
         stage(W + GW + i)
         flush()
+        t0 = time.perf_counter()
         lens_after.append(np.array(dec.prepare_host(ids)[2]))
+        t_host += time.perf_counter() - t0
         evs[i][0].record(stream)
         dec.replay_step()
         evs[i][1].record(stream)
@@ -381,6 +403,8 @@ def run_gpu(args, rank, world):
                      "algorithmic_bytes_per_launch": int(attn_b),
                      "mean_launch_us": round(1e3 * statistics.mean(attn_ms), 3),
                      "kernel_hash": khash},
+        "host_a0_us_per_step": round(1e6 * t_host / K, 2),
+        "host_churn_us_per_step": round(1e6 * statistics.mean(churn_s), 2) if churn_s else None,
         "gpu_launches": 2 * K,
         "clocks": clocks,
     }

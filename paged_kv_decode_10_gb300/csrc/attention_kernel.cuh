@@ -634,6 +634,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
     long long cur = start;
     int x = 0;
     bool aborted = false;
+    bool waited_prev = false;
     while (cur < end && !aborted) {
       const int j0 = static_cast<int>(cur - u.off);
       const int j1 = static_cast<int>(min(static_cast<long long>(u.n), end - u.off));
@@ -656,6 +657,12 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
             const bool ok = !misc[2] && blk >= 0 && blk < p.num_blocks;
             stage_bad[st] = ok ? 0 : 1;
             if (ok) {
+              // the last page of a unit holds the token appended by the kernel
+              // before this one: wait for that grid (once) before reading it
+              if (jb + i == u.n - 1 && !waited_prev) {
+                pdl_wait();
+                waited_prev = true;
+              }
               mbar_arrive_expect_tx(&full[st], Q::kStageBytes);
               const uint32_t kdst = smem_u32(smem + st * Q::kStageBytes);
               const uint32_t vdst = kdst + Q::kTileBytes;
@@ -703,6 +710,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
     // ---- this warp's pages of the segment ----
     if constexpr (KIND == 0) {
       MmaState<D> s;
+      pdl_wait();   // q_rot comes from the kernel before this one
       mma_begin<T, D>(s, p, u.b, u.g, lane);
       int j = j0 + ((warp - x % NW) + NW) % NW;
       for (; j < j1; j += NW) {
@@ -726,6 +734,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
       mma_stash<D>(s, my_acc, my_m, my_l, lane);
     } else {
       SimtState<T, D, G> s;
+      pdl_wait();   // q_rot comes from the kernel before this one
       simt_begin<T, D, G>(s, p, u.b, u.g, lane);
       int j = j0 + ((warp - x % NW) + NW) % NW;
       for (; j < j1; j += NW) {
@@ -871,7 +880,21 @@ struct AttnLauncher {
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Q::kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<p.num_parts, Q::kThreads, Q::kSmemBytes, s>>>(tk, tv, p);
+    // launched as a programmatic dependent: the prologue (row scan, barrier
+    // set-up, block-id prefetch, TMA of pages that do not hold this step's
+    // token) overlaps the RoPE/append kernel before it
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.num_parts);
+    cfg.blockDim = dim3(Q::kThreads);
+    cfg.dynamicSmemBytes = Q::kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }
   static cudaError_t occupancy(int *n) {

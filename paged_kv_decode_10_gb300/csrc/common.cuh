@@ -140,6 +140,16 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
   return d;
 }
 
+// ---- programmatic dependent launch (sm_90+) --------------------------------
+// The dependent kernel may start before this grid ends; it must call
+// pdl_wait() before touching anything this grid writes.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Waits until every prerequisite grid has finished and its writes are visible
+// (returns at once when the kernel was not launched as a dependent).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void set_dev_err(int32_t *flag, int bits) {
   if (flag) atomicOr(flag, bits);
 }

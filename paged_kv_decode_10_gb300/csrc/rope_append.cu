@@ -1,9 +1,17 @@
-// a1 RoPE and a2 append of the decode step.
+// a1 RoPE and a2 append of the decode step (separately and fused).
 //
 // RoPE: helexa issue 121, slice 1 -- cos/sin gathered at arbitrary per-row
 // positions ((B,1,half)) and applied with the rotate-half convention; keys are
 // stored post-RoPE.  Append: "neurogrid releases" v0.7.0 -- the KV cache is a
 // pool of fixed 16-token blocks; the new token's K/V go to slot_mapping[b].
+//
+// Angles.  theta_i = p * base^(-2i/d) can reach 1.3e5 rad at p = 131072, where
+// a float32 product would be off by ~0.008 rad.  The kernel instead works in
+// turns with 64-bit fixed point: F_i = round(2^64 * base^(-2i/d) / (2 pi))
+// (host, double precision), and p * F_i mod 2^64 (an exact integer product
+// that wraps) is the fractional turn of theta_i.  Read as a signed 64-bit
+// value and scaled by 2 pi / 2^64 it is theta_i reduced to [-pi, pi), exact to
+// float32 rounding, and sincosf then only sees reduced arguments.
 #include <cmath>
 #include <cstdint>
 
@@ -12,90 +20,130 @@
 namespace pkv {
 namespace {
 
-constexpr double kTwoPi = 6.283185307179586476925286766559;
 constexpr int kMaxHalf = 128;
 
-// base^(-2i/d) for i < d/2, computed on the host in double precision.
-struct RopeFreqs {
-  double inv[kMaxHalf];
+struct RopeTurns {
+  unsigned long long f[kMaxHalf];   // 2^64 * base^(-2i/d) / (2 pi)
 };
 
-// One CTA per batch row.  Threads first build cos/sin of every pair at the
-// row's position (angle p * inv_freq formed and reduced modulo 2*pi in double
-// precision, so positions of 10^5 keep float32-accurate angles), then rotate
-// every head of q and k.  With APPEND the rotated key and the raw value are
-// also written into the row's cache slot (a1 and a2 fused).
-template <typename T, bool APPEND>
+template <typename T, int VEC>
+struct Vec;
+template <> struct Vec<float, 4> { using type = float4; };
+template <> struct Vec<__nv_bfloat16, 4> { using type = uint2; };
+template <> struct Vec<float, 1> { using type = float; };
+template <> struct Vec<__nv_bfloat16, 1> { using type = __nv_bfloat16; };
+
+template <typename T, int VEC>
+__device__ __forceinline__ void unpack(const typename Vec<T, VEC>::type &w, float (&x)[VEC]) {
+  if constexpr (VEC == 1) {
+    x[0] = to_f32(w);
+  } else if constexpr (sizeof(T) == 4) {
+    x[0] = w.x; x[1] = w.y; x[2] = w.z; x[3] = w.w;
+  } else {
+    x[0] = bf16_lo(w.x); x[1] = bf16_hi(w.x); x[2] = bf16_lo(w.y); x[3] = bf16_hi(w.y);
+  }
+}
+
+template <typename T, int VEC>
+__device__ __forceinline__ typename Vec<T, VEC>::type pack(const float (&x)[VEC]) {
+  typename Vec<T, VEC>::type w;
+  if constexpr (VEC == 1) {
+    w = from_f32<T>(x[0]);
+  } else if constexpr (sizeof(T) == 4) {
+    w = make_float4(x[0], x[1], x[2], x[3]);
+  } else {
+    w.x = pack_bf16(x[0], x[1]);
+    w.y = pack_bf16(x[2], x[3]);
+  }
+  return w;
+}
+
+// One CTA per batch row, one work item per thread so every load of the row is
+// issued in one round.  Items: VEC consecutive rotation pairs of one head of q
+// or k ((Hq + Hkv) * half / VEC of them) and, with APPEND, 16-byte chunks of
+// the row's values (copied into the cache slot).  cos/sin of the row's
+// position are built first in shared memory.
+template <typename T, int VEC, bool APPEND>
 __global__ void rope_kernel(const T *__restrict__ q, const T *__restrict__ k,
                             const T *__restrict__ v, T *__restrict__ q_out,
                             T *__restrict__ k_out, const int32_t *__restrict__ positions,
                             const int64_t *__restrict__ slots, T *__restrict__ k_cache,
                             T *__restrict__ v_cache, int Hq, int Hkv, int d, int64_t num_slots,
-                            int32_t *err, const RopeFreqs freqs) {
+                            int32_t *err, const RopeTurns turns) {
+  using W = typename Vec<T, VEC>::type;
   extern __shared__ float cs[];  // cos[half], sin[half]
+  // the attention kernel that follows may start its own prologue now; it waits
+  // for this grid before reading q_rot or the appended slot
+  pdl_launch_dependents();
   const int b = blockIdx.x;
   const int half = d >> 1;
-  const double p = static_cast<double>(positions[b]);
-  for (int i = threadIdx.x; i < half; i += blockDim.x) {
-    const double theta = p * freqs.inv[i];
-    const double turns = rint(theta * (1.0 / kTwoPi));
-    const double r = fma(-turns, kTwoPi, theta);
-    float s, c;
-    sincosf(static_cast<float>(r), &s, &c);
-    cs[i] = c;
+  const int tid = threadIdx.x;
+  const int rot_items = (Hq + Hkv) * (half / VEC);
+  const int v_chunks = APPEND ? Hkv * d * static_cast<int>(sizeof(T)) / 16 : 0;
+
+  // issue this thread's loads before anything waits
+  const uint32_t pos = static_cast<uint32_t>(positions[b]);
+  int64_t slot = -1;
+  if (APPEND) slot = slots[b];
+  W x1w{}, x2w{};
+  int h = 0, c = 0;
+  const bool rot = tid < rot_items;
+  if (rot) {
+    h = tid / (half / VEC);
+    c = (tid - h * (half / VEC)) * VEC;
+    const T *src = h < Hq ? q + (static_cast<size_t>(b) * Hq + h) * d
+                          : k + (static_cast<size_t>(b) * Hkv + (h - Hq)) * d;
+    x1w = *reinterpret_cast<const W *>(src + c);
+    x2w = *reinterpret_cast<const W *>(src + half + c);
+  }
+  uint4 vw{};
+  const bool vcopy = APPEND && tid < v_chunks;
+  if (vcopy) vw = reinterpret_cast<const uint4 *>(v + static_cast<size_t>(b) * Hkv * d)[tid];
+
+  for (int i = tid; i < half; i += blockDim.x) {
+    const unsigned long long ph = static_cast<unsigned long long>(pos) * turns.f[i];
+    const float ang = static_cast<float>(static_cast<long long>(ph)) * 3.4061215800865545e-19f;
+    float s, co;
+    sincosf(ang, &s, &co);
+    cs[i] = co;
     cs[half + i] = s;
   }
-  int64_t slot = -1;
-  if (APPEND) {
-    slot = slots[b];
-    if (slot >= num_slots) {
-      if (threadIdx.x == 0) set_dev_err(err, PKV_DEVERR_BAD_SLOT);
-      slot = -1;
-    }
+  if (APPEND && slot >= num_slots) {
+    if (tid == 0) set_dev_err(err, PKV_DEVERR_BAD_SLOT);
+    slot = -1;
   }
-  // cache row of the slot for KV head 0; head h adds h * 16 * d
-  const int64_t blk = slot / kBlockTokens;
-  T *kdst0 = APPEND && slot >= 0
-                 ? k_cache + ((blk * Hkv) * kBlockTokens + (slot - blk * kBlockTokens)) * d
-                 : nullptr;
-  T *vdst0 = APPEND && slot >= 0
-                 ? v_cache + ((blk * Hkv) * kBlockTokens + (slot - blk * kBlockTokens)) * d
-                 : nullptr;
   __syncthreads();
-  const int heads = Hq + Hkv;
-  for (int e = threadIdx.x; e < heads * half; e += blockDim.x) {
-    const int h = e / half;
-    const int i = e - h * half;
-    const T *src;
-    T *dst;
-    T *cdst = nullptr;
-    if (h < Hq) {
-      src = q + (static_cast<size_t>(b) * Hq + h) * d;
-      dst = q_out + (static_cast<size_t>(b) * Hq + h) * d;
-    } else {
-      const int hk = h - Hq;
-      src = k + (static_cast<size_t>(b) * Hkv + hk) * d;
-      dst = k_out + (static_cast<size_t>(b) * Hkv + hk) * d;
-      if (kdst0) cdst = kdst0 + static_cast<size_t>(hk) * kBlockTokens * d;
+
+  const int64_t blk = slot / kBlockTokens;
+  const size_t row0 =
+      APPEND && slot >= 0
+          ? static_cast<size_t>((blk * Hkv) * kBlockTokens + (slot - blk * kBlockTokens)) * d
+          : 0;
+  if (rot) {
+    float x1[VEC], x2[VEC], y1[VEC], y2[VEC];
+    unpack<T, VEC>(x1w, x1);
+    unpack<T, VEC>(x2w, x2);
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) {
+      const float co = cs[c + e], s = cs[half + c + e];
+      y1[e] = x1[e] * co - x2[e] * s;
+      y2[e] = x2[e] * co + x1[e] * s;
     }
-    const float x1 = to_f32(src[i]);
-    const float x2 = to_f32(src[i + half]);
-    const float c = cs[i], s = cs[half + i];
-    const T y1 = from_f32<T>(x1 * c - x2 * s);
-    const T y2 = from_f32<T>(x2 * c + x1 * s);
-    dst[i] = y1;
-    dst[i + half] = y2;
-    if (cdst) {
-      cdst[i] = y1;
-      cdst[i + half] = y2;
+    const W o1 = pack<T, VEC>(y1), o2 = pack<T, VEC>(y2);
+    T *dst = h < Hq ? q_out + (static_cast<size_t>(b) * Hq + h) * d
+                    : k_out + (static_cast<size_t>(b) * Hkv + (h - Hq)) * d;
+    *reinterpret_cast<W *>(dst + c) = o1;
+    *reinterpret_cast<W *>(dst + half + c) = o2;
+    if (APPEND && slot >= 0 && h >= Hq) {
+      T *cdst = k_cache + row0 + static_cast<size_t>(h - Hq) * kBlockTokens * d;
+      *reinterpret_cast<W *>(cdst + c) = o1;
+      *reinterpret_cast<W *>(cdst + half + c) = o2;
     }
   }
-  if (vdst0) {
-    for (int e = threadIdx.x; e < Hkv * d; e += blockDim.x) {
-      const int hk = e / d, i = e - hk * d;
-      vdst0[static_cast<size_t>(hk) * kBlockTokens * d + i] =
-          v[(static_cast<size_t>(b) * Hkv + hk) * d + i];
-    }
+  if (vcopy && slot >= 0) {
+    const int per_head = d * static_cast<int>(sizeof(T)) / 16;
+    const int hk = tid / per_head, ch = tid - hk * per_head;
+    reinterpret_cast<uint4 *>(v_cache + row0 + static_cast<size_t>(hk) * kBlockTokens * d)[ch] = vw;
   }
 }
 
@@ -120,7 +168,8 @@ __global__ void append_kernel(const uint4 *__restrict__ k_rot, const uint4 *__re
     }
     const int64_t blk = slot / kBlockTokens;
     const int64_t off = slot - blk * kBlockTokens;
-    const size_t dst = ((static_cast<size_t>(blk) * Hkv + h) * kBlockTokens + off) * chunks_per_row + c;
+    const size_t dst =
+        ((static_cast<size_t>(blk) * Hkv + h) * kBlockTokens + off) * chunks_per_row + c;
     const size_t src = (static_cast<size_t>(b) * Hkv + h) * chunks_per_row + c;
     k_cache[dst] = k_rot[src];
     v_cache[dst] = v[src];
@@ -129,12 +178,17 @@ __global__ void append_kernel(const uint4 *__restrict__ k_rot, const uint4 *__re
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-}  // namespace
-}  // namespace pkv
+template <typename T, int VEC, bool APPEND>
+void launch_rope(int B, int threads, size_t smem, cudaStream_t s, const void *q, const void *k,
+                 const void *v, void *q_out, void *k_out, const int32_t *positions,
+                 const int64_t *slots, void *k_cache, void *v_cache, int Hq, int Hkv, int d,
+                 int64_t num_slots, int32_t *err, const RopeTurns &turns) {
+  rope_kernel<T, VEC, APPEND><<<B, threads, smem, s>>>(
+      static_cast<const T *>(q), static_cast<const T *>(k), static_cast<const T *>(v),
+      static_cast<T *>(q_out), static_cast<T *>(k_out), positions, slots,
+      static_cast<T *>(k_cache), static_cast<T *>(v_cache), Hq, Hkv, d, num_slots, err, turns);
+}
 
-using namespace pkv;
-
-namespace {
 int rope_launch(const void *q, const void *k, const void *v, void *q_out, void *k_out,
                 const int32_t *positions, const int64_t *slots, void *k_cache, void *v_cache,
                 int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int32_t num_blocks, float base,
@@ -147,34 +201,60 @@ int rope_launch(const void *q, const void *k, const void *v, void *q_out, void *
   PKV_REQUIRE(positions, PKV_ERR_INVALID_ARG, "positions is NULL");
   PKV_REQUIRE((Hq == 0 || (q && q_out)) && (Hkv == 0 || (k && k_out)), PKV_ERR_INVALID_ARG,
               "NULL tensor");
-  if (append)
+  const int elem = static_cast<int>(dtype_size(dtype));
+  const int vec = (d % 8 == 0) ? 4 : 1;
+  if (vec == 4)
+    PKV_REQUIRE((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                 reinterpret_cast<uintptr_t>(q_out) | reinterpret_cast<uintptr_t>(k_out)) %
+                        (4 * elem) == 0,
+                PKV_ERR_INVALID_ARG, "q/k tensors must be aligned to 4 elements");
+  if (append) {
     PKV_REQUIRE(v && slots && k_cache && v_cache && num_blocks >= 0, PKV_ERR_INVALID_ARG,
                 "NULL append argument");
-  RopeFreqs f;
-  for (int i = 0; i < d / 2; ++i)
-    f.inv[i] = std::pow(static_cast<double>(base), -2.0 * i / static_cast<double>(d));
+    PKV_REQUIRE(d * elem % 16 == 0 && aligned16(v) && aligned16(k_cache) && aligned16(v_cache),
+                PKV_ERR_INVALID_ARG, "append needs 16-byte rows and 16-byte aligned tensors");
+  }
+  RopeTurns t;
+  for (int i = 0; i < d / 2; ++i) {
+    const double f = std::pow(static_cast<double>(base), -2.0 * i / static_cast<double>(d)) /
+                     (2.0 * 3.141592653589793238462643383279502884);
+    t.f[i] = static_cast<unsigned long long>(std::ldexp(f, 64));
+  }
+  const int rot_items = (Hq + Hkv) * (d / 2 / vec);
+  const int v_chunks = append ? Hkv * d * elem / 16 : 0;
+  int items = rot_items > v_chunks ? rot_items : v_chunks;
+  if (items < d / 2) items = d / 2;
+  PKV_REQUIRE(items <= 1024, PKV_ERR_UNSUPPORTED, "too many heads for one CTA per row (%d items)",
+              items);
+  const int threads = (items + 31) / 32 * 32;
   const size_t smem = sizeof(float) * d;
   const int64_t num_slots = static_cast<int64_t>(num_blocks) * kBlockTokens;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+#define PKV_ROPE_ARGS                                                                     \
+  B, threads, smem, s, q, k, v, q_out, k_out, positions, slots, k_cache, v_cache, Hq, Hkv, d, \
+      num_slots, err, t
   if (dtype == PKV_BF16) {
     using T = __nv_bfloat16;
-    auto kern = append ? rope_kernel<T, true> : rope_kernel<T, false>;
-    kern<<<B, 128, smem, s>>>(static_cast<const T *>(q), static_cast<const T *>(k),
-                              static_cast<const T *>(v), static_cast<T *>(q_out),
-                              static_cast<T *>(k_out), positions, slots, static_cast<T *>(k_cache),
-                              static_cast<T *>(v_cache), Hq, Hkv, d, num_slots, err, f);
+    if (vec == 4)
+      append ? launch_rope<T, 4, true>(PKV_ROPE_ARGS) : launch_rope<T, 4, false>(PKV_ROPE_ARGS);
+    else
+      append ? launch_rope<T, 1, true>(PKV_ROPE_ARGS) : launch_rope<T, 1, false>(PKV_ROPE_ARGS);
   } else {
     using T = float;
-    auto kern = append ? rope_kernel<T, true> : rope_kernel<T, false>;
-    kern<<<B, 128, smem, s>>>(static_cast<const T *>(q), static_cast<const T *>(k),
-                              static_cast<const T *>(v), static_cast<T *>(q_out),
-                              static_cast<T *>(k_out), positions, slots, static_cast<T *>(k_cache),
-                              static_cast<T *>(v_cache), Hq, Hkv, d, num_slots, err, f);
+    if (vec == 4)
+      append ? launch_rope<T, 4, true>(PKV_ROPE_ARGS) : launch_rope<T, 4, false>(PKV_ROPE_ARGS);
+    else
+      append ? launch_rope<T, 1, true>(PKV_ROPE_ARGS) : launch_rope<T, 1, false>(PKV_ROPE_ARGS);
   }
+#undef PKV_ROPE_ARGS
   PKV_LAUNCH_CHECK("rope_kernel");
   return PKV_OK;
 }
+
 }  // namespace
+}  // namespace pkv
+
+using namespace pkv;
 
 extern "C" int pkv_rope(const void *q, const void *k, void *q_out, void *k_out,
                         const int32_t *positions, int32_t B, int32_t Hq, int32_t Hkv, int32_t d,

@@ -2,10 +2,12 @@
 
 ``PagedDecoder`` owns the device KV pool, the host block allocator and the
 per-step buffers.  ``step`` runs a0 on the host (allocator: positions,
-slot_mapping, seq_lens, block tables, written into pinned buffers), one
-host-to-device copy of that metadata, then a1-a4 through ``pkv_decode_step`` on
+slot_mapping, seq_lens, block tables, written into one pinned buffer), one
+host-to-device copy of that buffer, then a1-a4 through ``pkv_decode_step`` on
 one CUDA stream.  Nothing is copied back to the host ("neurogrid releases"
 v0.8.0: position, seq_len and kv_len live in GPU buffers; no D2H copies).
+``capture``/``replay_step`` put the copy and the kernels of a step in one CUDA
+graph (v0.8.0: the whole decode replayed as one graph).
 
 Joins and leaves only edit the allocator's block tables ("neurogrid releases"
 v0.7.0: on-demand blocks, O(1) alloc/free); no KV is moved when the batch
@@ -14,9 +16,17 @@ continuous-batching PR.
 """
 import math
 
-import numpy as np
-
 from . import binding
+
+
+def _metadata_layout(B, bt_stride):
+    """Byte offsets of slot_mapping (int64), positions, seq_lens and block tables
+    (int32) in one packed buffer for batch size B, and its size."""
+    slots = 0
+    pos = 8 * B
+    lens = pos + 4 * B
+    tables = (lens + 4 * B + 15) // 16 * 16
+    return slots, pos, lens, tables, tables + 4 * B * bt_stride
 
 
 class PagedDecoder:
@@ -47,10 +57,8 @@ class PagedDecoder:
         self.workspace = binding.alloc_workspace(max_seqs, Hq, Hkv, d, self.num_parts,
                                                  self.device)
         dev = dict(device=self.device)
-        self.positions = torch.empty(max_seqs, dtype=torch.int32, **dev)
-        self.slots = torch.empty(max_seqs, dtype=torch.int64, **dev)
-        self.seq_lens = torch.empty(max_seqs, dtype=torch.int32, **dev)
-        self.tables = torch.empty((max_seqs, self.bt_stride), dtype=torch.int32, **dev)
+        cap = _metadata_layout(max_seqs, self.bt_stride)[-1]
+        self._meta_dev = torch.empty(cap, dtype=torch.uint8, **dev)
         self.q_rot = torch.empty((max_seqs, Hq, d), dtype=self.tdtype, **dev)
         self.k_rot = torch.empty((max_seqs, Hkv, d), dtype=self.tdtype, **dev)
         self.out = torch.empty((max_seqs, Hq, d), dtype=self.tdtype, **dev)
@@ -60,19 +68,26 @@ class PagedDecoder:
         self.k_in = torch.empty((max_seqs, Hkv, d), dtype=self.tdtype, **dev)
         self.v_in = torch.empty((max_seqs, Hkv, d), dtype=self.tdtype, **dev)
         self._graphs = None
-        # two pinned metadata sets so the host can fill step i+1 while step i's
-        # copy is still queued
-        self._host = []
-        for _ in range(2):
-            hs = dict(pin_memory=True)
-            self._host.append(dict(
-                pos=torch.empty(max_seqs, dtype=torch.int32, **hs),
-                slots=torch.empty(max_seqs, dtype=torch.int64, **hs),
-                lens=torch.empty(max_seqs, dtype=torch.int32, **hs),
-                tables=torch.empty((max_seqs, self.bt_stride), dtype=torch.int32, **hs),
-                event=None))
+        # two pinned metadata buffers so the host can fill step i+1 while step
+        # i's copy is still queued
+        self._host = [dict(raw=torch.empty(cap, dtype=torch.uint8, pin_memory=True), event=None)
+                      for _ in range(2)]
         self._turn = 0
         self.last_metadata = None
+        self._set_device_views(max_seqs)
+
+    # -- packed metadata views ----------------------------------------------
+    def _views(self, raw, B):
+        torch = self.torch
+        o_slots, o_pos, o_lens, o_tab, end = _metadata_layout(B, self.bt_stride)
+        return (raw[o_pos:o_pos + 4 * B].view(torch.int32),
+                raw[o_slots:o_slots + 8 * B].view(torch.int64),
+                raw[o_lens:o_lens + 4 * B].view(torch.int32),
+                raw[o_tab:end].view(torch.int32).view(B, self.bt_stride)), end
+
+    def _set_device_views(self, B):
+        (self.positions, self.slots, self.seq_lens, self.tables), _ = self._views(
+            self._meta_dev, B)
 
     # -- batch membership ----------------------------------------------------
     def join(self, prefix_len):
@@ -82,34 +97,41 @@ class PagedDecoder:
         self.alloc.leave(seq_id)
 
     # -- a0 ----------------------------------------------------------------
-    def prepare(self, seq_ids, stream=None):
-        """Host allocator step + one async H2D copy of the metadata."""
-        torch = self.torch
-        B = len(seq_ids)
+    def prepare_host(self, seq_ids):
+        """a0 into the pinned buffer that the next copy (or replay) reads."""
         h = self._host[self._turn]
-        self._turn ^= 1
         if h["event"] is not None:
             h["event"].synchronize()
-        views = (h["pos"][:B].numpy(), h["slots"][:B].numpy(), h["lens"][:B].numpy(),
-                 h["tables"][:B].numpy())
-        self.alloc.prepare_step(seq_ids, self.bt_stride, out=views)
+        B = len(seq_ids)
+        views, _ = self._views(h["raw"], B)
+        npv = tuple(t.numpy() for t in views)
+        self.alloc.prepare_step(seq_ids, self.bt_stride, out=npv)
+        self.last_metadata = npv
+        return npv
+
+    def prepare(self, seq_ids, stream=None):
+        """Host allocator step + one async H2D copy of the packed metadata."""
+        torch = self.torch
+        B = len(seq_ids)
+        npv = self.prepare_host(seq_ids)
+        h = self._host[self._turn]
+        self._turn ^= 1
+        nbytes = _metadata_layout(B, self.bt_stride)[-1]
         s = stream if stream is not None else torch.cuda.current_stream(self.device)
         with torch.cuda.stream(s):
-            self.positions[:B].copy_(h["pos"][:B], non_blocking=True)
-            self.slots[:B].copy_(h["slots"][:B], non_blocking=True)
-            self.seq_lens[:B].copy_(h["lens"][:B], non_blocking=True)
-            self.tables[:B].copy_(h["tables"][:B], non_blocking=True)
+            self._meta_dev[:nbytes].copy_(h["raw"][:nbytes], non_blocking=True)
             ev = torch.cuda.Event()
             ev.record(s)
         h["event"] = ev
-        self.last_metadata = views
-        return views
+        self._set_device_views(B)
+        return npv
 
     # -- a1..a4 --------------------------------------------------------------
     def step_args(self, B, q, k, v, attn_bias=None):
+        self._set_device_views(B)
         return binding.make_step_args(
             q, k, v, self.q_rot[:B], self.k_rot[:B], self.k_cache, self.v_cache,
-            self.positions[:B], self.slots[:B], self.seq_lens[:B], self.tables[:B],
+            self.positions, self.slots, self.seq_lens, self.tables,
             self.scale, self.rope_base, self.num_parts, self.workspace, self.out[:B],
             attn_bias, self.flags, self.err)
 
@@ -123,38 +145,24 @@ class PagedDecoder:
     # -- CUDA graph of the whole device step ("neurogrid releases" v0.8.0) ---
     def capture(self, B, attn_bias=None):
         """Captures, for a fixed batch size B, one CUDA graph per pinned
-        metadata set: the metadata H2D copies followed by a1..a4 reading
+        metadata buffer: its H2D copy followed by a1..a4 reading
         ``q_in/k_in/v_in[:B]``.  ``replay_step`` then costs one graph launch."""
         torch = self.torch
         binding.default_parts(self.d, binding.F32 if self.dtype == "f32" else binding.BF16,
                               self.flags)   # sets kernel attributes outside capture
         args = self.step_args(B, self.q_in[:B], self.k_in[:B], self.v_in[:B], attn_bias)
+        nbytes = _metadata_layout(B, self.bt_stride)[-1]
         stream = torch.cuda.Stream(self.device)
         stream.wait_stream(torch.cuda.current_stream(self.device))
         graphs = []
         for h in self._host:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
-                self.positions[:B].copy_(h["pos"][:B], non_blocking=True)
-                self.slots[:B].copy_(h["slots"][:B], non_blocking=True)
-                self.seq_lens[:B].copy_(h["lens"][:B], non_blocking=True)
-                self.tables[:B].copy_(h["tables"][:B], non_blocking=True)
+                self._meta_dev[:nbytes].copy_(h["raw"][:nbytes], non_blocking=True)
                 binding.decode_step_args(args, stream)
             graphs.append(g)
         torch.cuda.current_stream(self.device).wait_stream(stream)
         self._graphs = (B, graphs, args)
-
-    def prepare_host(self, seq_ids):
-        """a0 into the pinned set the next replay will copy from."""
-        h = self._host[self._turn]
-        if h["event"] is not None:
-            h["event"].synchronize()
-        B = len(seq_ids)
-        views = (h["pos"][:B].numpy(), h["slots"][:B].numpy(), h["lens"][:B].numpy(),
-                 h["tables"][:B].numpy())
-        self.alloc.prepare_step(seq_ids, self.bt_stride, out=views)
-        self.last_metadata = views
-        return views
 
     def replay_step(self):
         """Launches the captured step for the metadata of the last prepare_host."""
