@@ -206,7 +206,8 @@ int pkv_rope_append(const void *q, const void *k, const void *v, void *q_out, vo
  *
  * Supported: dtype PKV_BF16 or PKV_F32; d in {64, 128}; Hq/Hkv in {1,2,4,8};
  * B <= 65536.  q_rot [B,Hq,d]; out [B,Hq,d] (device, dtype).
- * num_parts <= 0 selects pkv_attn_default_parts for the current device.
+ * num_parts <= 0 selects pkv_attn_default_parts for the current device;
+ * at most 4096 parts.
  */
 int pkv_attn_default_parts(int32_t d, int32_t dtype, int32_t flags, int32_t *num_parts);
 int pkv_attn_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t d,

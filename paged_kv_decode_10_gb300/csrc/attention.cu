@@ -18,6 +18,9 @@ namespace pkv {
 namespace {
 
 constexpr int kMaxB = 65536;
+// the fused merge keeps up to ceil((num_parts + 1) / 16) group weights per head
+// in the CTA's reduction buffer (2048 floats at d = 64)
+constexpr int kMaxParts = 4096;
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -216,7 +219,8 @@ extern "C" int pkv_attn_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int3
                                         int32_t num_parts, size_t *bytes) {
   clear_error();
   PKV_REQUIRE(bytes, PKV_ERR_INVALID_ARG, "bytes is NULL");
-  PKV_REQUIRE(num_parts > 0, PKV_ERR_INVALID_ARG, "num_parts must be positive");
+  PKV_REQUIRE(num_parts > 0 && num_parts <= kMaxParts, PKV_ERR_INVALID_ARG,
+              "num_parts must be in [1, %d]", kMaxParts);
   const int rc = check_shapes(B, Hq, Hkv, d, PKV_F32);
   if (rc != PKV_OK) return rc;
   *bytes = workspace_layout(nullptr, B, Hq, Hkv, d, num_parts).bytes;
@@ -255,6 +259,8 @@ extern "C" int pkv_decode_attn_split(const void *q_rot, const void *k_cache, con
     rc = default_parts(d, dtype, flags, G, &num_parts);
     if (rc != PKV_OK) return rc;
   }
+  PKV_REQUIRE(num_parts <= kMaxParts, PKV_ERR_INVALID_ARG, "num_parts must be <= %d",
+              kMaxParts);
   const Workspace ws = workspace_layout(workspace, B, Hq, Hkv, d, num_parts);
   PKV_REQUIRE(workspace_bytes >= ws.bytes, PKV_ERR_INVALID_ARG,
               "workspace of %zu bytes < %zu needed", workspace_bytes, ws.bytes);

@@ -150,6 +150,65 @@ __device__ __forceinline__ float4 merge_column(const float *o, const float *lse,
   return acc;
 }
 
+// a4 done cooperatively by the nthr consumer threads of a CTA (named barrier 1):
+// merges the partials i < n at slots slot0 + i*stride for every column of the
+// unit.  All lse values are gathered in one round into shared memory `sw`
+// (n*G floats), turned into weights there, and the weighted sum of o issues its
+// loads independently (unrolled), so the merge costs a few L2 round trips
+// whatever n is.  store(h, d4, o4, lse) receives each merged float4 column.
+template <typename Skip, typename Store>
+__device__ __forceinline__ void merge_cta(const float *o, const float *lse, size_t slot0, int n,
+                                          int stride, int G, int D, Skip skip, float *sw,
+                                          float *sM, int tid, int nthr, Store store) {
+  for (int i = tid; i < n * G; i += nthr) {
+    const int s = i / G, h = i - s * G;
+    sw[i] = skip(s) ? -INFINITY : __ldcg(lse + (slot0 + static_cast<size_t>(s) * stride) * G + h);
+  }
+  asm volatile("bar.sync 1, %0;" ::"r"(nthr) : "memory");
+  if (tid < G) {
+    float M = -INFINITY;
+    for (int s = 0; s < n; ++s) M = fmaxf(M, sw[s * G + tid]);
+    float den = 0.f;
+    for (int s = 0; s < n; ++s) {
+      const float w = M == -INFINITY ? 0.f : ex2(sw[s * G + tid] - M);
+      sw[s * G + tid] = w;
+      den += w;
+    }
+    sM[tid] = M;
+    sM[G + tid] = den;
+  }
+  asm volatile("bar.sync 1, %0;" ::"r"(nthr) : "memory");
+  const int cols = D / 4;
+  for (int col = tid; col < G * cols; col += nthr) {
+    const int h = col / cols, d4 = col - h * cols;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+    for (int s = 0; s < n; ++s) {
+      const float w = sw[s * G + h];
+      if (w != 0.f) {
+        const float4 v = __ldcg(
+            reinterpret_cast<const float4 *>(o + ((slot0 + static_cast<size_t>(s) * stride) * G + h) * D) + d4);
+        acc.x = fmaf(w, v.x, acc.x);
+        acc.y = fmaf(w, v.y, acc.y);
+        acc.z = fmaf(w, v.z, acc.z);
+        acc.w = fmaf(w, v.w, acc.w);
+      }
+    }
+    const float den = sM[G + h];
+    float l = -INFINITY;
+    if (den > 0.f) {
+      const float r = 1.f / den;
+      acc.x *= r;
+      acc.y *= r;
+      acc.z *= r;
+      acc.w *= r;
+      l = sM[h] + log2f(den);
+    }
+    store(h, d4, acc, l);
+  }
+  asm volatile("bar.sync 1, %0;" ::"r"(nthr) : "memory");
+}
+
 template <typename T>
 __device__ __forceinline__ void store4(T *dst, float4 v);
 template <>
@@ -800,8 +859,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
       const int g0 = c_first + grp * kMergeGroup;
       const int gcount = min(kMergeGroup, nseg - grp * kMergeGroup);
       const int ngroups = (nseg + kMergeGroup - 1) / kMergeGroup;
-      const int ncol = gq * D / 4;
       T *out_u = static_cast<T *>(p.out) + (static_cast<size_t>(u.b) * p.Hq + u.g * gq) * D;
+      auto to_out = [&](int h, int d4, float4 r, float) { store4<T>(out_u + h * D + 4 * d4, r); };
       __threadfence();
       asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
       if (tid == 0) {
@@ -813,17 +872,16 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
         __threadfence();
         const size_t slot0 = static_cast<size_t>(u_idx) + g0;
         auto skip1 = [&](int i) { return C > P && part_empty(g0 + i, P, C); };
-        for (int col = tid; col < ncol; col += kConsumers) {
-          const int h = col / (D / 4), d4 = col - h * (D / 4);
-          float l;
-          const float4 r = merge_column(p.o_part, p.lse_part, slot0, gcount, 1, gq, D, h, d4,
-                                        skip1, &l);
-          if (ngroups == 1) {
-            store4<T>(out_u + h * D + 4 * d4, r);
-          } else {
+        if (ngroups == 1) {
+          merge_cta(p.o_part, p.lse_part, slot0, gcount, 1, gq, D, skip1, red_acc, red_m, tid,
+                    kConsumers, to_out);
+        } else {
+          auto to_group = [&](int h, int d4, float4 r, float l) {
             *reinterpret_cast<float4 *>(p.o_group + (slot0 * gq + h) * D + 4 * d4) = r;
             if (d4 == 0) p.lse_group[slot0 * gq + h] = l;
-          }
+          };
+          merge_cta(p.o_part, p.lse_part, slot0, gcount, 1, gq, D, skip1, red_acc, red_m, tid,
+                    kConsumers, to_group);
         }
         if (tid == 0) p.counters[u_idx + g0] = 0;
         if (ngroups > 1) {
@@ -840,14 +898,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
               return C > P && real_parts(c_first + k * kMergeGroup,
                                          min(kMergeGroup, nseg - k * kMergeGroup), P, C) == 0;
             };
-            for (int col = tid; col < ncol; col += kConsumers) {
-              const int h = col / (D / 4), d4 = col - h * (D / 4);
-              float l;
-              const float4 r = merge_column(p.o_group, p.lse_group,
-                                            static_cast<size_t>(u_idx) + c_first, ngroups,
-                                            kMergeGroup, gq, D, h, d4, skip2, &l);
-              store4<T>(out_u + h * D + 4 * d4, r);
-            }
+            merge_cta(p.o_group, p.lse_group, static_cast<size_t>(u_idx) + c_first, ngroups,
+                      kMergeGroup, gq, D, skip2, red_acc, red_m, tid, kConsumers, to_out);
             if (tid == 0) p.unit_counters[u_idx] = 0;
           }
         }
