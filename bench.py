@@ -321,10 +321,10 @@ def run_gpu(args, rank, world):
     for i in range(K):
         churn(W + GW + i)
         stage(W + GW + i)
-        flush()
         t0 = time.perf_counter()
         lens_after.append(np.array(dec.prepare_host(ids)[2]))
         t_host += time.perf_counter() - t0
+        flush()   # still running on the GPU when the replay below is enqueued
         evs[i][0].record(stream)
         dec.replay_step()
         evs[i][1].record(stream)

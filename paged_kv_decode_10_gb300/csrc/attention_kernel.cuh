@@ -156,7 +156,7 @@ __device__ __forceinline__ float4 merge_column(const float *o, const float *lse,
 // (n*G floats), turned into weights there, and the weighted sum of o issues its
 // loads independently (unrolled), so the merge costs a few L2 round trips
 // whatever n is.  store(h, d4, o4, lse) receives each merged float4 column.
-template <typename Skip, typename Store>
+template <int MAXC, typename Skip, typename Store>
 __device__ __forceinline__ void merge_cta(const float *o, const float *lse, size_t slot0, int n,
                                           int stride, int G, int D, Skip skip, float *sw,
                                           float *sM, int tid, int nthr, Store store) {
@@ -178,33 +178,63 @@ __device__ __forceinline__ void merge_cta(const float *o, const float *lse, size
     sM[G + tid] = den;
   }
   asm volatile("bar.sync 1, %0;" ::"r"(nthr) : "memory");
+  // each thread owns up to MAXC float4 columns; the loads of U partials x MAXC
+  // columns (8 in all) are issued before any of them is consumed
   const int cols = D / 4;
-  for (int col = tid; col < G * cols; col += nthr) {
-    const int h = col / cols, d4 = col - h * cols;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-    for (int s = 0; s < n; ++s) {
-      const float w = sw[s * G + h];
-      if (w != 0.f) {
-        const float4 v = __ldcg(
-            reinterpret_cast<const float4 *>(o + ((slot0 + static_cast<size_t>(s) * stride) * G + h) * D) + d4);
-        acc.x = fmaf(w, v.x, acc.x);
-        acc.y = fmaf(w, v.y, acc.y);
-        acc.z = fmaf(w, v.z, acc.z);
-        acc.w = fmaf(w, v.w, acc.w);
+  const int ncol = G * cols;
+  float4 acc[MAXC];
+  int hh[MAXC], dd[MAXC];
+  bool on[MAXC];
+#pragma unroll
+  for (int k = 0; k < MAXC; ++k) {
+    const int col = tid + k * nthr;
+    on[k] = col < ncol;
+    hh[k] = on[k] ? col / cols : 0;
+    dd[k] = on[k] ? col - hh[k] * cols : 0;
+    acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  constexpr int U = MAXC >= 8 ? 1 : 8 / MAXC;   // 8 loads in flight per thread
+  for (int s0 = 0; s0 < n; s0 += U) {
+    float4 v[U][MAXC];
+    float w[U][MAXC];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int s = s0 + u;
+#pragma unroll
+      for (int k = 0; k < MAXC; ++k) {
+        w[u][k] = (s < n && on[k]) ? sw[s * G + hh[k]] : 0.f;
+        v[u][k] = w[u][k] != 0.f
+                      ? __ldcg(reinterpret_cast<const float4 *>(
+                                   o + ((slot0 + static_cast<size_t>(s) * stride) * G + hh[k]) * D) +
+                               dd[k])
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
-    const float den = sM[G + h];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int k = 0; k < MAXC; ++k) {
+        acc[k].x = fmaf(w[u][k], v[u][k].x, acc[k].x);
+        acc[k].y = fmaf(w[u][k], v[u][k].y, acc[k].y);
+        acc[k].z = fmaf(w[u][k], v[u][k].z, acc[k].z);
+        acc[k].w = fmaf(w[u][k], v[u][k].w, acc[k].w);
+      }
+  }
+#pragma unroll
+  for (int k = 0; k < MAXC; ++k) {
+    if (!on[k]) continue;
+    const float den = sM[G + hh[k]];
     float l = -INFINITY;
+    float4 r = acc[k];
     if (den > 0.f) {
-      const float r = 1.f / den;
-      acc.x *= r;
-      acc.y *= r;
-      acc.z *= r;
-      acc.w *= r;
-      l = sM[h] + log2f(den);
+      const float inv = 1.f / den;
+      r.x *= inv;
+      r.y *= inv;
+      r.z *= inv;
+      r.w *= inv;
+      l = sM[hh[k]] + log2f(den);
     }
-    store(h, d4, acc, l);
+    store(hh[k], dd[k], r, l);
   }
   asm volatile("bar.sync 1, %0;" ::"r"(nthr) : "memory");
 }
@@ -758,6 +788,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
   float *pbuf = pbuf_all + warp * kBlockTokens * Q::kHeadsPad;
   float *abuf = abuf_all + warp * Q::kHeadsPad;
   constexpr int kConsumers = NW * 32;
+  constexpr int kMergeCols = (8 * (D / 4) + kConsumers - 1) / kConsumers;
 
   UnitCursor u = u0;
   long long cur = start;
@@ -873,14 +904,14 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
         const size_t slot0 = static_cast<size_t>(u_idx) + g0;
         auto skip1 = [&](int i) { return C > P && part_empty(g0 + i, P, C); };
         if (ngroups == 1) {
-          merge_cta(p.o_part, p.lse_part, slot0, gcount, 1, gq, D, skip1, red_acc, red_m, tid,
+          merge_cta<kMergeCols>(p.o_part, p.lse_part, slot0, gcount, 1, gq, D, skip1, red_acc, red_m, tid,
                     kConsumers, to_out);
         } else {
           auto to_group = [&](int h, int d4, float4 r, float l) {
             *reinterpret_cast<float4 *>(p.o_group + (slot0 * gq + h) * D + 4 * d4) = r;
             if (d4 == 0) p.lse_group[slot0 * gq + h] = l;
           };
-          merge_cta(p.o_part, p.lse_part, slot0, gcount, 1, gq, D, skip1, red_acc, red_m, tid,
+          merge_cta<kMergeCols>(p.o_part, p.lse_part, slot0, gcount, 1, gq, D, skip1, red_acc, red_m, tid,
                     kConsumers, to_group);
         }
         if (tid == 0) p.counters[u_idx + g0] = 0;
@@ -898,7 +929,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
               return C > P && real_parts(c_first + k * kMergeGroup,
                                          min(kMergeGroup, nseg - k * kMergeGroup), P, C) == 0;
             };
-            merge_cta(p.o_group, p.lse_group, static_cast<size_t>(u_idx) + c_first, ngroups,
+            merge_cta<kMergeCols>(p.o_group, p.lse_group, static_cast<size_t>(u_idx) + c_first, ngroups,
                       kMergeGroup, gq, D, skip2, red_acc, red_m, tid, kConsumers, to_out);
             if (tid == 0) p.unit_counters[u_idx] = 0;
           }
