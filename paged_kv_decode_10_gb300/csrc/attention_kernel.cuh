@@ -74,9 +74,31 @@ __device__ __forceinline__ int row_pages(const int32_t *seq_lens, int b, int bt_
   return ok ? (L + kBlockTokens - 1) / kBlockTokens : 0;
 }
 
-// Part that owns global page x: the largest c with floor(c*P/C) <= x.
+// floor(a / b) for 0 <= a, 0 < b and a / b < 2^40, without a 64-bit integer
+// division (a long software sequence on the GPU): a float reciprocal estimate,
+// one refinement on the exact remainder (error then <= 3), and exact
+// remainder corrections.
+__device__ __forceinline__ long long div_floor(long long a, long long b) {
+  const float rb = 1.0f / static_cast<float>(b);
+  long long q = static_cast<long long>(static_cast<float>(a) * rb);
+  long long r = a - q * b;
+  q += static_cast<long long>(static_cast<float>(r) * rb);
+  r = a - q * b;
+  while (r < 0) {
+    --q;
+    r += b;
+  }
+  while (r >= b) {
+    ++q;
+    r -= b;
+  }
+  return q;
+}
+
+// Part that owns global page x: the largest c with floor(c*P/C) <= x, i.e.
+// with c*P < (x+1)*C.
 __device__ __forceinline__ int part_of(long long x, long long P, int C) {
-  return static_cast<int>(((x + 1) * C - 1) / P);
+  return static_cast<int>(div_floor((x + 1) * C - 1, P));
 }
 
 // The fused merge combines a unit's partials in groups of kMergeGroup parts
@@ -87,7 +109,7 @@ constexpr int kMergeGroup = 16;
 
 // A part owns no page when C > P and its page range is empty.
 __device__ __forceinline__ bool part_empty(long long c, long long P, int C) {
-  return (P * c / C) == (P * (c + 1) / C);
+  return div_floor(P * c, C) == div_floor(P * (c + 1), C);
 }
 
 // Parts c0 .. c0+n-1 that own at least one page (all of them when C <= P).
@@ -671,8 +693,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
   }
   const long long excl = before + incl - mysum;
   const long long P = static_cast<long long>(total) * p.Hkv;
-  const long long start = P * blockIdx.x / C;
-  const long long end = P * (blockIdx.x + 1) / C;
+  const long long start = div_floor(P * blockIdx.x, C);
+  const long long end = div_floor(P * (blockIdx.x + 1), C);
   if (start < end && mysum > 0 && start >= excl * p.Hkv && start < (excl + mysum) * p.Hkv) {
     long long acc = excl;
     for (int b = r0; b < r1; ++b) {
@@ -713,7 +735,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
     const long long rowoff = misc[1];
     bool bad;
     u0.n = row_pages(p.seq_lens, u0.b, p.bt_stride, has_bias, p.bias_stride, &bad);
-    u0.g = static_cast<int>((start - rowoff * p.Hkv) / u0.n);
+    u0.g = static_cast<int>(div_floor(start - rowoff * p.Hkv, u0.n));
     u0.off = rowoff * p.Hkv + static_cast<long long>(u0.g) * u0.n;
   }
 
@@ -854,29 +876,50 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
     const int c_last = part_of(u.off + u.n - 1, P, C);
     const int nseg = c_last - c_first + 1;
     const int gq = p.G;
-    for (int e = tid; e < gq * D; e += kConsumers) {
-      const int h = e / D, dim = e - h * D;
+    // per-head rescale factors of the NW warp states, once (G threads); each
+    // output element is then NW fused multiply-adds
+    float *fac = pbuf_all;   // [NW][8] factors, then 1/l [8], lse [8]
+    if (tid < gq) {
       float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < NW; ++w) M = fmaxf(M, red_m[w * Q::kHeadsPad + h]);
-      float Lsum = 0.f, O = 0.f;
-      if (M != -INFINITY) {
+      for (int w = 0; w < NW; ++w) M = fmaxf(M, red_m[w * Q::kHeadsPad + tid]);
+      float L = 0.f;
 #pragma unroll
-        for (int w = 0; w < NW; ++w) {
-          const float f = ex2(red_m[w * Q::kHeadsPad + h] - M);
-          Lsum += f * red_l[w * Q::kHeadsPad + h];
-          O += f * red_acc[(w * Q::kHeadsPad + h) * D + dim];
-        }
+      for (int w = 0; w < NW; ++w) {
+        const float f = M == -INFINITY ? 0.f : ex2(red_m[w * Q::kHeadsPad + tid] - M);
+        fac[w * Q::kHeadsPad + tid] = f;
+        L += f * red_l[w * Q::kHeadsPad + tid];
       }
-      const float o = Lsum > 0.f ? O / Lsum : 0.f;
+      fac[NW * Q::kHeadsPad + tid] = L > 0.f ? 1.f / L : 0.f;
+      fac[NW * Q::kHeadsPad + 8 + tid] = L > 0.f ? M + log2f(L) : -INFINITY;
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
+    for (int e4 = tid; e4 < gq * (D / 4); e4 += kConsumers) {
+      const int h = e4 / (D / 4), d4 = e4 - h * (D / 4);
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        const float f = fac[w * Q::kHeadsPad + h];
+        const float4 a =
+            *reinterpret_cast<const float4 *>(red_acc + (w * Q::kHeadsPad + h) * D + 4 * d4);
+        o.x = fmaf(f, a.x, o.x);
+        o.y = fmaf(f, a.y, o.y);
+        o.z = fmaf(f, a.z, o.z);
+        o.w = fmaf(f, a.w, o.w);
+      }
+      const float inv = fac[NW * Q::kHeadsPad + h];
+      o.x *= inv;
+      o.y *= inv;
+      o.z *= inv;
+      o.w *= inv;
       if (nseg == 1) {
-        T *out = static_cast<T *>(p.out) +
-                 (static_cast<size_t>(u.b) * p.Hq + u.g * gq + h) * D + dim;
-        *out = from_f32<T>(o);
+        store4<T>(static_cast<T *>(p.out) + (static_cast<size_t>(u.b) * p.Hq + u.g * gq + h) * D +
+                      4 * d4,
+                  o);
       } else {
         const size_t idx = static_cast<size_t>(u_idx) + blockIdx.x;
-        p.o_part[(idx * gq + h) * D + dim] = o;
-        if (dim == 0) p.lse_part[idx * gq + h] = Lsum > 0.f ? M + log2f(Lsum) : -INFINITY;
+        *reinterpret_cast<float4 *>(p.o_part + (idx * gq + h) * D + 4 * d4) = o;
+        if (d4 == 0) p.lse_part[idx * gq + h] = fac[NW * Q::kHeadsPad + 8 + h];
       }
     }
     if (tid == 0 && j0 == 0) {
