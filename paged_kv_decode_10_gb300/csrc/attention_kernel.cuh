@@ -74,26 +74,9 @@ __device__ __forceinline__ int row_pages(const int32_t *seq_lens, int b, int bt_
   return ok ? (L + kBlockTokens - 1) / kBlockTokens : 0;
 }
 
-// floor(a / b) for 0 <= a, 0 < b and a / b < 2^40, without a 64-bit integer
-// division (a long software sequence on the GPU): a float reciprocal estimate,
-// one refinement on the exact remainder (error then <= 3), and exact
-// remainder corrections.
-__device__ __forceinline__ long long div_floor(long long a, long long b) {
-  const float rb = 1.0f / static_cast<float>(b);
-  long long q = static_cast<long long>(static_cast<float>(a) * rb);
-  long long r = a - q * b;
-  q += static_cast<long long>(static_cast<float>(r) * rb);
-  r = a - q * b;
-  while (r < 0) {
-    --q;
-    r += b;
-  }
-  while (r >= b) {
-    ++q;
-    r -= b;
-  }
-  return q;
-}
+// floor(a / b) for a >= 0, b > 0 (the compiler's 64-bit division measured
+// faster here than float-estimate variants).
+__device__ __forceinline__ long long div_floor(long long a, long long b) { return a / b; }
 
 // Part that owns global page x: the largest c with floor(c*P/C) <= x, i.e.
 // with c*P < (x+1)*C.
@@ -741,11 +724,11 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
 
   if (warp == NW) {
     // ======================= producer warp =======================
+    constexpr int kBatch = NS >= 8 ? 4 : (NS >= 2 ? NS / 2 : 1);
     UnitCursor u = u0;
     long long cur = start;
     int x = 0;
     bool aborted = false;
-    bool waited_prev = false;
     while (cur < end && !aborted) {
       const int j0 = static_cast<int>(cur - u.off);
       const int j1 = static_cast<int>(min(static_cast<long long>(u.n), end - u.off));
@@ -755,25 +738,27 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
         const int cur_ids = ids;
         ids = (jb + 32 + lane < j1) ? bt[jb + 32 + lane] : -1;
         const int cnt = min(32, j1 - jb);
-        for (int i = 0; i < cnt; ++i) {
-          const int blk = __shfl_sync(0xffffffffu, cur_ids, i);
-          if (lane == 0) {
-            const int xx = x + (jb - j0) + i;
+        // pages go out kBatch at a time, lane l < kBatch taking page i + l, so
+        // the barrier waits, arrivals and TMA issues of a batch share warp
+        // instructions (one page per lane-instruction costs ~600 cycles)
+        for (int i = 0; i < cnt; i += kBatch) {
+          const int blk = __shfl_sync(0xffffffffu, cur_ids, (i + lane) & 31);
+          if (lane < kBatch && i + lane < cnt) {
+            const int xx = x + (jb - j0) + i + lane;
             const int st = xx % NS;
             const uint32_t ph = static_cast<uint32_t>(xx / NS) & 1u;
-            if (misc[2] || !mbar_wait_bounded(&empty[st], ph ^ 1u, kWaitLimitCycles)) {
+            bool dead = misc[2] != 0;
+            if (!dead && !mbar_wait_bounded(&empty[st], ph ^ 1u, kWaitLimitCycles)) {
               misc[2] = 1;
+              dead = true;
               set_dev_err(p.err, PKV_DEVERR_TIMEOUT);
             }
-            const bool ok = !misc[2] && blk >= 0 && blk < p.num_blocks;
+            const bool ok = !dead && blk >= 0 && blk < p.num_blocks;
             stage_bad[st] = ok ? 0 : 1;
             if (ok) {
               // the last page of a unit holds the token appended by the kernel
-              // before this one: wait for that grid (once) before reading it
-              if (jb + i == u.n - 1 && !waited_prev) {
-                pdl_wait();
-                waited_prev = true;
-              }
+              // before this one: wait for that grid before reading it
+              if (jb + i + lane == u.n - 1) pdl_wait();
               mbar_arrive_expect_tx(&full[st], Q::kStageBytes);
               const uint32_t kdst = smem_u32(smem + st * Q::kStageBytes);
               const uint32_t vdst = kdst + Q::kTileBytes;
@@ -784,10 +769,11 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
                 tma_load_2d(vdst + sub * Q::kSubBytes, &tmap_v, sub * Q::kSubCols, y, &full[st]);
               }
             } else {
-              if (!misc[2]) set_dev_err(p.err, PKV_DEVERR_BAD_BLOCK);
+              if (!dead) set_dev_err(p.err, PKV_DEVERR_BAD_BLOCK);
               mbar_arrive(&full[st]);
             }
           }
+          __syncwarp();
         }
         aborted = __shfl_sync(0xffffffffu, misc[2], 0) != 0;
       }
@@ -1005,6 +991,9 @@ struct AttnLauncher {
     auto kern = attn_split_kernel<T, D, NW, NS, KIND, G>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Q::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     // launched as a programmatic dependent: the prologue (row scan, barrier
     // set-up, block-id prefetch, TMA of pages that do not hold this step's

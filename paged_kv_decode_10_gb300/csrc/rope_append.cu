@@ -183,6 +183,10 @@ void launch_rope(int B, int threads, size_t smem, cudaStream_t s, const void *q,
                  const void *v, void *q_out, void *k_out, const int32_t *positions,
                  const int64_t *slots, void *k_cache, void *v_cache, int Hq, int Hkv, int d,
                  int64_t num_slots, int32_t *err, const RopeTurns &turns) {
+  // same L1/shared split as the attention kernel that follows, so the SMs need
+  // no reconfiguration between the two launches of a step
+  cudaFuncSetAttribute(rope_kernel<T, VEC, APPEND>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                       cudaSharedmemCarveoutMaxShared);
   rope_kernel<T, VEC, APPEND><<<B, threads, smem, s>>>(
       static_cast<const T *>(q), static_cast<const T *>(k), static_cast<const T *>(v),
       static_cast<T *>(q_out), static_cast<T *>(k_out), positions, slots,
