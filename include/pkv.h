@@ -222,6 +222,33 @@ int pkv_decode_attn_split(const void *q_rot, const void *k_cache, const void *v_
                           void *out, int32_t dtype, int32_t flags,
                           int32_t *dev_err_flag, void *stream);
 
+/*
+ * Attention without a caller-provided workspace.  This call has no
+ * counterpart in the pages the method comes from; it exists for callers that
+ * cannot allocate device memory (code running under another runtime's memory
+ * manager, plugins that are handed only their input and output tensors, or
+ * paths that must never reach an allocator).  It computes the same result as
+ * pkv_decode_attn_split followed by its fused merge (same arguments, minus
+ * the workspace) and takes its scratch from a 16 MiB array compiled into this
+ * library; calls needing more scratch than that fail with
+ * PKV_ERR_UNSUPPORTED.  It performs no device allocation or free.
+ *  - Every GPU that loads the library holds the 16 MiB array until the
+ *    process exits.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress); make that first call before any stream capture.
+ *  - All calls share the one array, which keeps the previous call's contents;
+ *    each call clears the bytes it uses first (an asynchronous memset on
+ *    `stream`).  Calls that overlap on the GPU (other streams, other host
+ *    threads) race on the array and give wrong results: serialise them.
+ *  - PKV_ATTN_SEPARATE_MERGE is rejected (the merge always runs in-kernel).
+ */
+int pkv_decode_attn_static(const void *q_rot, const void *k_cache, const void *v_cache,
+                           int32_t num_blocks, const int32_t *block_tables, int32_t bt_stride,
+                           const int32_t *seq_lens, const float *attn_bias, int32_t bias_stride,
+                           int32_t B, int32_t Hq, int32_t Hkv, int32_t d, float scale,
+                           int32_t num_parts, void *out, int32_t dtype, int32_t flags,
+                           int32_t *dev_err_flag, void *stream);
+
 /* bt_stride and bias_stride (0 when no bias was given) are the values passed to
  * pkv_decode_attn_split: they decide which rows are valid, exactly as there. */
 int pkv_lse_merge(const void *workspace, size_t workspace_bytes, const int32_t *seq_lens,

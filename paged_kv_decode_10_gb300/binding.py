@@ -97,6 +97,10 @@ SIGNATURES = {
                                              _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
                                              ctypes.c_float, _c_i32, _vp, _size_t, _vp, _c_i32,
                                              _c_i32, _vp, _vp]),
+    "pkv_decode_attn_static": (ctypes.c_int, [_vp, _vp, _vp, _c_i32, _vp, _c_i32, _vp, _vp,
+                                              _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
+                                              ctypes.c_float, _c_i32, _vp, _c_i32, _c_i32, _vp,
+                                              _vp]),
     "pkv_lse_merge": (ctypes.c_int, [_vp, _size_t, _vp, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
                                      _c_i32, _c_i32, _vp, _c_i32, _vp]),
     "pkv_decode_step": (ctypes.c_int, [ctypes.POINTER(StepArgs), _vp]),
@@ -323,6 +327,22 @@ def decode_attn_split(q_rot, k_cache, v_cache, block_tables, seq_lens, scale, nu
         block_tables.shape[1], _ptr(seq_lens), _ptr(attn_bias), bias_stride, B, Hq, Hkv, d,
         float(scale), int(num_parts), _ptr(workspace), workspace.numel(), _ptr(out),
         dtype_code(q_rot), int(flags), _ptr(err), _stream(stream)))
+
+
+def decode_attention_static(q_rot, k_cache, v_cache, block_tables, seq_lens, scale, out,
+                            num_parts=0, attn_bias=None, flags=0, err=None, stream=None):
+    """a3 + fused a4 with the library's built-in scratch array instead of a
+    workspace, for callers that cannot allocate device memory (see
+    ``pkv_decode_attn_static`` in ``include/pkv.h``)."""
+    B, Hq, d = q_rot.shape
+    Hkv = k_cache.shape[1]
+    bias_stride = attn_bias.shape[1] if attn_bias is not None else 0
+    _check(load().pkv_decode_attn_static(
+        _ptr(q_rot), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0], _ptr(block_tables),
+        block_tables.shape[1], _ptr(seq_lens), _ptr(attn_bias), bias_stride, B, Hq, Hkv, d,
+        float(scale), int(num_parts), _ptr(out), dtype_code(q_rot), int(flags), _ptr(err),
+        _stream(stream)))
+    return out
 
 
 def lse_merge(workspace, seq_lens, bt_stride, B, Hq, Hkv, d, num_parts, out, bias_stride=0,
