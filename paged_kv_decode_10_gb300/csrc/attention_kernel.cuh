@@ -798,6 +798,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
   constexpr int kConsumers = NW * 32;
   constexpr int kMergeCols = (8 * (D / 4) + kConsumers - 1) / kConsumers;
 
+  int pend_u[2], pend_c[2], pend_n[2], pend_b[2], pend_g[2];   // at most two (see below)
+  int npend = 0;
   UnitCursor u = u0;
   long long cur = start;
   int x = 0;
@@ -912,16 +914,35 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
       p.meta[2 * u_idx] = c_first;
       p.meta[2 * u_idx + 1] = nseg;
     }
-    if (nseg > 1 && p.fuse_merge) {
+    if (nseg > 1 && p.fuse_merge && npend < 2) {
+      // only the first and last segment of a part can belong to a unit split
+      // across parts: remember it and merge after streaming, so merges never
+      // stall the consumer warps while the producer keeps the ring full
+      pend_u[npend] = u_idx;
+      pend_c[npend] = c_first;
+      pend_n[npend] = nseg;
+      pend_b[npend] = u.b;
+      pend_g[npend] = u.g;
+      ++npend;
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
+    x += j1 - j0;
+    cur += j1 - j0;
+    if (cur < end) next_unit(u, p);
+  }
+  if (npend > 0) __threadfence();
+  for (int q = 0; q < npend; ++q) {
+    const int u_idx = pend_u[q], c_first = pend_c[q], nseg = pend_n[q];
+    const int gq = p.G;
+    {
       // a4 in the epilogue (threadfence-reduction pattern, two levels; every
       // counter is reset by the CTA that consumes it)
       const int grp = (static_cast<int>(blockIdx.x) - c_first) / kMergeGroup;
       const int g0 = c_first + grp * kMergeGroup;
       const int gcount = min(kMergeGroup, nseg - grp * kMergeGroup);
       const int ngroups = (nseg + kMergeGroup - 1) / kMergeGroup;
-      T *out_u = static_cast<T *>(p.out) + (static_cast<size_t>(u.b) * p.Hq + u.g * gq) * D;
+      T *out_u = static_cast<T *>(p.out) + (static_cast<size_t>(pend_b[q]) * p.Hq + pend_g[q] * gq) * D;
       auto to_out = [&](int h, int d4, float4 r, float) { store4<T>(out_u + h * D + 4 * d4, r); };
-      __threadfence();
       asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
       if (tid == 0) {
         const int prev = atomicAdd(&p.counters[u_idx + g0], 1);
@@ -965,10 +986,6 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
         }
       }
     }
-    asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
-    x += j1 - j0;
-    cur += j1 - j0;
-    if (cur < end) next_unit(u, p);
   }
 }
 
