@@ -69,6 +69,8 @@ extern "C" {
                                    f32 always uses CUDA cores) */
 #define PKV_ATTN_SEPARATE_MERGE 2 /* leave the split partials for pkv_lse_merge instead of
                                      merging them in the split kernel's epilogue */
+#define PKV_STEP_FUSED 4          /* pkv_decode_step: run a1+a2 inside the attention kernel
+                                     (one launch per step) instead of as their own kernel */
 
 /* Message for the calling thread's last failed call ("" if none). */
 const char *pkv_last_error(void);
@@ -137,8 +139,9 @@ int pkv_alloc_dump(const pkv_alloc *a, int32_t *free_stack, int32_t cap, int32_t
  *   theta = p * base^(-2i/d)
  *   out[i]     = x[i] cos(theta) - x[i+d/2] sin(theta)
  *   out[i+d/2] = x[i+d/2] cos(theta) + x[i] sin(theta)
- * theta is formed and reduced modulo 2*pi in double precision, then rotated
- * in float32 and rounded once to dtype.  In-place (q_out == q) is allowed.
+ * theta is formed modulo 2*pi exactly (64-bit fixed-point turns from a
+ * double-precision host table), then rotated in float32 and rounded once to
+ * dtype.  In-place (q_out == q) is allowed.
  * d even, 2 <= d <= 256.
  */
 int pkv_rope(const void *q, const void *k, void *q_out, void *k_out,
@@ -280,9 +283,18 @@ typedef struct pkv_step_args {
   int32_t *dev_err_flag;             /* nullable */
 } pkv_step_args;
 
-/* All device pointers in *args; asynchronous on stream.  Runs pkv_rope_append,
- * pkv_decode_attn_split and, when flags has PKV_ATTN_SEPARATE_MERGE,
- * pkv_lse_merge.  q_rot/k_rot receive the rotated q and k. */
+/* All pointers in *args are device pointers or host memory the GPU can read
+ * (pinned / mapped; positions, slot_mapping, seq_lens and block_tables may live
+ * there so that a step needs no host-to-device copy); asynchronous on stream.
+ * Runs pkv_rope_append, then pkv_decode_attn_split launched as a programmatic
+ * dependent (its prologue overlaps the RoPE kernel), and pkv_lse_merge when
+ * flags has PKV_ATTN_SEPARATE_MERGE.  With PKV_STEP_FUSED the whole step is
+ * one kernel instead: the attention kernel also rotates q and k and appends
+ * the rotated key and the value (the part that owns a row's last page writes
+ * that row's slot before it loads the page; rows with seq_len 0 are not
+ * appended).  Both forms give bit-identical results.  q_rot/k_rot receive the
+ * rotated q and k.  Each row's slot must be its position seq_len-1 in its own
+ * blocks, as pkv_prepare_step produces. */
 int pkv_decode_step(const pkv_step_args *args, void *stream);
 
 /* Host-side buffers for pkv_decode_step_host (pinned memory recommended). */

@@ -19,6 +19,7 @@ BLOCK_SIZE = 16
 DEVERR_BAD_BLOCK, DEVERR_BAD_SLOT, DEVERR_BAD_LEN, DEVERR_TIMEOUT = 1, 2, 4, 8
 ATTN_SIMT = 1
 ATTN_SEPARATE_MERGE = 2
+STEP_FUSED = 4
 
 _c_i32 = ctypes.c_int32
 _c_i64 = ctypes.c_int64

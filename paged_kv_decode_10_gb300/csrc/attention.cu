@@ -227,15 +227,17 @@ extern "C" int pkv_attn_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int3
   return PKV_OK;
 }
 
-extern "C" int pkv_decode_attn_split(const void *q_rot, const void *k_cache, const void *v_cache,
-                                     int32_t num_blocks, const int32_t *block_tables,
-                                     int32_t bt_stride, const int32_t *seq_lens,
-                                     const float *attn_bias, int32_t bias_stride, int32_t B,
-                                     int32_t Hq, int32_t Hkv, int32_t d, float scale,
-                                     int32_t num_parts, void *workspace, size_t workspace_bytes,
-                                     void *out, int32_t dtype, int32_t flags,
-                                     int32_t *dev_err_flag, void *stream) {
-  clear_error();
+namespace {
+
+// a3 (+ a4 fused) launch; with `step` the whole-step kernel that also does a1
+// + a2 from step->q/k/v, positions and slot_mapping (q_rot then only receives
+// the rotated queries).
+int attn_launch(const void *q_rot, const void *k_cache, const void *v_cache, int32_t num_blocks,
+                const int32_t *block_tables, int32_t bt_stride, const int32_t *seq_lens,
+                const float *attn_bias, int32_t bias_stride, int32_t B, int32_t Hq, int32_t Hkv,
+                int32_t d, float scale, int32_t num_parts, void *workspace,
+                size_t workspace_bytes, void *out, int32_t dtype, int32_t flags,
+                int32_t *dev_err_flag, void *stream, const pkv_step_args *step) {
   int rc = check_shapes(B, Hq, Hkv, d, dtype);
   if (rc != PKV_OK) return rc;
   if (B == 0) return PKV_OK;
@@ -296,10 +298,46 @@ extern "C" int pkv_decode_attn_split(const void *q_rot, const void *k_cache, con
   p.num_blocks = num_blocks;
   p.num_parts = num_parts;
   p.scale_log2 = scale * kLog2e;
-  const cudaError_t e = v.launch(tk, tv, p, static_cast<cudaStream_t>(stream));
+  cudaError_t e;
+  if (step) {
+    PKV_REQUIRE(step->q && step->k && step->v && step->k_rot && step->positions &&
+                    step->slot_mapping,
+                PKV_ERR_INVALID_ARG, "NULL step argument");
+    PKV_REQUIRE(step->rope_base > 0.0f, PKV_ERR_INVALID_ARG, "rope base must be positive");
+    p.q_new = step->q;
+    p.k_new = step->k;
+    p.v_new = step->v;
+    p.positions = step->positions;
+    p.slots = step->slot_mapping;
+    p.k_cache_w = const_cast<void *>(k_cache);
+    p.v_cache_w = const_cast<void *>(v_cache);
+    p.q_rot_out = const_cast<void *>(q_rot);
+    p.k_rot_out = step->k_rot;
+    p.num_slots = static_cast<long long>(num_blocks) * kBlockTokens;
+    fill_rope_turns(step->rope_base, d, p.turns);
+    e = v.launch_step(tk, tv, p, static_cast<cudaStream_t>(stream));
+  } else {
+    e = v.launch(tk, tv, p, static_cast<cudaStream_t>(stream));
+  }
   PKV_REQUIRE(e == cudaSuccess, PKV_ERR_CUDA, "attn_split_kernel launch: %s",
               cudaGetErrorString(e));
   return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" int pkv_decode_attn_split(const void *q_rot, const void *k_cache, const void *v_cache,
+                                     int32_t num_blocks, const int32_t *block_tables,
+                                     int32_t bt_stride, const int32_t *seq_lens,
+                                     const float *attn_bias, int32_t bias_stride, int32_t B,
+                                     int32_t Hq, int32_t Hkv, int32_t d, float scale,
+                                     int32_t num_parts, void *workspace, size_t workspace_bytes,
+                                     void *out, int32_t dtype, int32_t flags,
+                                     int32_t *dev_err_flag, void *stream) {
+  clear_error();
+  return attn_launch(q_rot, k_cache, v_cache, num_blocks, block_tables, bt_stride, seq_lens,
+                     attn_bias, bias_stride, B, Hq, Hkv, d, scale, num_parts, workspace,
+                     workspace_bytes, out, dtype, flags, dev_err_flag, stream, nullptr);
 }
 
 extern "C" int pkv_lse_merge(const void *workspace, size_t workspace_bytes,
@@ -344,14 +382,24 @@ extern "C" int pkv_decode_step(const pkv_step_args *a, void *stream) {
     rc = default_parts(a->d, a->dtype, a->flags, a->Hq / a->Hkv, &num_parts);
     if (rc != PKV_OK) return rc;
   }
-  int rc = pkv_rope_append(a->q, a->k, a->v, a->q_rot, a->k_rot, a->positions, a->slot_mapping,
-                           a->k_cache, a->v_cache, a->B, a->Hq, a->Hkv, a->d, a->num_blocks,
-                           a->rope_base, a->dtype, a->dev_err_flag, stream);
-  if (rc != PKV_OK) return rc;
-  rc = pkv_decode_attn_split(a->q_rot, a->k_cache, a->v_cache, a->num_blocks, a->block_tables,
-                             a->bt_stride, a->seq_lens, a->attn_bias, a->bias_stride, a->B, a->Hq,
-                             a->Hkv, a->d, a->scale, num_parts, a->workspace, a->workspace_bytes,
-                             a->out, a->dtype, a->flags, a->dev_err_flag, stream);
+  int rc;
+  if (!(a->flags & PKV_STEP_FUSED)) {
+    rc = pkv_rope_append(a->q, a->k, a->v, a->q_rot, a->k_rot, a->positions, a->slot_mapping,
+                         a->k_cache, a->v_cache, a->B, a->Hq, a->Hkv, a->d, a->num_blocks,
+                         a->rope_base, a->dtype, a->dev_err_flag, stream);
+    if (rc != PKV_OK) return rc;
+    rc = pkv_decode_attn_split(a->q_rot, a->k_cache, a->v_cache, a->num_blocks, a->block_tables,
+                               a->bt_stride, a->seq_lens, a->attn_bias, a->bias_stride, a->B,
+                               a->Hq, a->Hkv, a->d, a->scale, num_parts, a->workspace,
+                               a->workspace_bytes, a->out, a->dtype, a->flags, a->dev_err_flag,
+                               stream);
+  } else {
+    // PKV_STEP_FUSED: the whole step in one launch
+    rc = attn_launch(a->q_rot, a->k_cache, a->v_cache, a->num_blocks, a->block_tables,
+                     a->bt_stride, a->seq_lens, a->attn_bias, a->bias_stride, a->B, a->Hq, a->Hkv,
+                     a->d, a->scale, num_parts, a->workspace, a->workspace_bytes, a->out,
+                     a->dtype, a->flags, a->dev_err_flag, stream, a);
+  }
   if (rc != PKV_OK) return rc;
   if (!(a->flags & PKV_ATTN_SEPARATE_MERGE)) return PKV_OK;
   return pkv_lse_merge(a->workspace, a->workspace_bytes, a->seq_lens, a->bt_stride,

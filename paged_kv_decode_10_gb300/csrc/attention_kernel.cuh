@@ -60,6 +60,15 @@ struct AttnParams {
   int num_blocks, num_parts;
   int fuse_merge;           // 1: the last part of a unit merges it (a4 in the epilogue)
   float scale_log2;         // softmax scale * log2(e)
+  // whole-step kernels only (a1 + a2 fused in): the step's new tokens, where
+  // they go, and where their rotated copies are reported
+  const void *q_new, *k_new, *v_new;   // [B,Hq,D], [B,Hkv,D], [B,Hkv,D]
+  const int32_t *positions;            // [B] RoPE positions
+  const int64_t *slots;                // [B] cache slots of the new tokens
+  void *k_cache_w, *v_cache_w;         // the caches, written at the slots
+  void *q_rot_out, *k_rot_out;         // [B,Hq,D], [B,Hkv,D]
+  long long num_slots;                 // num_blocks * 16
+  unsigned long long turns[128];       // RoPE fixed-point turns (fill_rope_turns)
 };
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -507,6 +516,154 @@ __device__ __forceinline__ void simt_load_row(const char *tile, int row, int lan
   }
 }
 
+// ---- whole-step kernels: a1 + a2 inside the attention kernel ---------------
+// Rotated queries of unit (b, g) built by the consumer threads into shared
+// memory qs [G][D] (storage type T, rounded once as pkv_rope does); the part
+// that owns the unit's first page also reports them in q_rot_out.  Every load
+// (position, both halves of each pair) is issued before any is used, and each
+// thread forms the angles of its own pairs, so this costs one memory round
+// trip and one barrier.
+template <typename T, int D, int NTHR>
+__device__ __forceinline__ void fused_rotate_q(const AttnParams &p, int b, int g, bool report,
+                                               T *qs, int tid) {
+  constexpr int half = D / 2;
+  constexpr int KM = (8 * half + NTHR - 1) / NTHR;   // pairs per thread (G <= 8)
+  const int npairs = p.G * half;
+  const T *q = static_cast<const T *>(p.q_new) + (static_cast<size_t>(b) * p.Hq + g * p.G) * D;
+  const uint32_t pos = static_cast<uint32_t>(p.positions[b]);
+  float x1[KM], x2[KM];
+#pragma unroll
+  for (int k = 0; k < KM; ++k) {
+    const int e = tid + k * NTHR;
+    const int h = e / half, i = e - h * half;
+    x1[k] = e < npairs ? to_f32(q[h * D + i]) : 0.f;
+    x2[k] = e < npairs ? to_f32(q[h * D + half + i]) : 0.f;
+  }
+  T *qo = static_cast<T *>(p.q_rot_out) + (static_cast<size_t>(b) * p.Hq + g * p.G) * D;
+#pragma unroll
+  for (int k = 0; k < KM; ++k) {
+    const int e = tid + k * NTHR;
+    if (e < npairs) {
+      const int h = e / half, i = e - h * half;
+      float c, s, y1, y2;
+      rope_cossin(pos, p.turns[i], &c, &s);
+      rope_rotate(x1[k], x2[k], c, s, &y1, &y2);
+      const T t1 = from_f32<T>(y1), t2 = from_f32<T>(y2);
+      qs[h * D + i] = t1;
+      qs[h * D + half + i] = t2;
+      if (report) {
+        qo[h * D + i] = t1;
+        qo[h * D + half + i] = t2;
+      }
+    }
+  }
+  asm volatile("bar.sync 1, %0;" ::"r"(NTHR) : "memory");
+}
+
+// The new token of unit (b, g), appended by the 32 lanes of the producer warp
+// of the part that owns the unit's last page -- the only part that reads that
+// page.  fetch() loads everything at the start of the segment; put() (called
+// just before the batch that loads the last page) rotates the key, writes key
+// and value into the cache slot (and the key into k_rot_out) and fences the
+// generic-proxy stores ahead of the page's TMA (async-proxy) load.
+template <typename T, int D>
+struct FusedAppend {
+  static constexpr int KP = (D / 2 + 31) / 32;   // pairs per lane
+  static constexpr int KV = (D + 31) / 32;       // values per lane
+  float x1[KP], x2[KP], v[KV];
+  long long slot;
+  uint32_t pos;
+
+  __device__ __forceinline__ void fetch(const AttnParams &p, int b, int g, int lane) {
+    constexpr int half = D / 2;
+    slot = p.slots[b];
+    pos = static_cast<uint32_t>(p.positions[b]);
+    const T *kn = static_cast<const T *>(p.k_new) + (static_cast<size_t>(b) * p.Hkv + g) * D;
+    const T *vn = static_cast<const T *>(p.v_new) + (static_cast<size_t>(b) * p.Hkv + g) * D;
+#pragma unroll
+    for (int k = 0; k < KP; ++k) {
+      const int i = lane + 32 * k;
+      x1[k] = i < half ? to_f32(kn[i]) : 0.f;
+      x2[k] = i < half ? to_f32(kn[half + i]) : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < KV; ++k) {
+      const int i = lane + 32 * k;
+      v[k] = i < D ? to_f32(vn[i]) : 0.f;
+    }
+  }
+
+  __device__ __forceinline__ void put(const AttnParams &p, int b, int g, int lane) {
+    constexpr int half = D / 2;
+    if (slot >= p.num_slots) {
+      if (lane == 0) set_dev_err(p.err, PKV_DEVERR_BAD_SLOT);
+    } else if (slot >= 0) {
+      const long long blk = slot / kBlockTokens;
+      const size_t row =
+          (static_cast<size_t>(blk * p.Hkv + g) * kBlockTokens + (slot - blk * kBlockTokens)) * D;
+      T *kc = static_cast<T *>(p.k_cache_w) + row;
+      T *vc = static_cast<T *>(p.v_cache_w) + row;
+      T *ko = static_cast<T *>(p.k_rot_out) + (static_cast<size_t>(b) * p.Hkv + g) * D;
+#pragma unroll
+      for (int k = 0; k < KP; ++k) {
+        const int i = lane + 32 * k;
+        if (i < half) {
+          float c, s, y1, y2;
+          rope_cossin(pos, p.turns[i], &c, &s);
+          rope_rotate(x1[k], x2[k], c, s, &y1, &y2);
+          const T t1 = from_f32<T>(y1), t2 = from_f32<T>(y2);
+          kc[i] = t1;
+          kc[half + i] = t2;
+          ko[i] = t1;
+          ko[half + i] = t2;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < KV; ++k) {
+        const int i = lane + 32 * k;
+        if (i < D) vc[i] = from_f32<T>(v[k]);
+      }
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
+    __syncwarp();
+  }
+};
+
+template <int D>
+__device__ __forceinline__ void mma_begin_smem(MmaState<D> &s, const __nv_bfloat16 *qs, int G,
+                                               int lane) {
+  const int r = lane >> 2, c = lane & 3;
+  const bool real = r < G;
+  const __nv_bfloat16 *qrow = qs + (real ? r : 0) * D;
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) {
+    const uint32_t *w = reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 2 * c);
+    s.qb[ks][0] = real ? w[0] : 0u;
+    s.qb[ks][1] = real ? w[4] : 0u;
+  }
+#pragma unroll
+  for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) s.acc[mt][e] = 0.f;
+  s.m[0] = s.m[1] = -INFINITY;
+  s.l[0] = s.l[1] = 0.f;
+}
+
+template <typename T, int D, int G>
+__device__ __forceinline__ void simt_begin_smem(SimtState<T, D, G> &s, const T *qs, int Greal,
+                                                float scale_log2, int lane) {
+  constexpr int DPL = D / 32;
+#pragma unroll
+  for (int h = 0; h < G; ++h)
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) {
+      s.qf[h][e] = h < Greal ? to_f32(qs[h * D + lane * DPL + e]) * scale_log2 : 0.f;
+      s.acc[h][e] = 0.f;
+    }
+  s.m = -INFINITY;
+  s.l = 0.f;
+}
+
 template <typename T, int D, int G>
 __device__ __forceinline__ void simt_begin(SimtState<T, D, G> &s, const AttnParams &p, int b,
                                            int g, int lane) {
@@ -610,10 +767,13 @@ __device__ __forceinline__ void simt_stash(SimtState<T, D, G> &s, float *red_acc
 // ---------------------------------------------------------------------------
 // KIND 0: MMA consumer (T must be bf16, G <= 8 at run time).
 // KIND 1: SIMT consumer with compile-time group G.
-template <typename T, int D, int NW, int NS, int KIND, int G>
+// FUSE: whole-step kernel -- also rotates the step's q/k and appends k/v
+// (a1 + a2), so a decode step is one launch.
+template <typename T, int D, int NW, int NS, int KIND, int G, bool FUSE>
 __global__ void __launch_bounds__((NW + 1) * 32, 1)
     attn_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                      const __grid_constant__ CUtensorMap tmap_v, const AttnParams p) {
+                      const __grid_constant__ CUtensorMap tmap_v,
+                      const __grid_constant__ AttnParams p) {
   using Q = Geo<T, D, NW, NS>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>(
@@ -734,6 +894,10 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
       const int j1 = static_cast<int>(min(static_cast<long long>(u.n), end - u.off));
       const int32_t *bt = p.block_tables + static_cast<size_t>(u.b) * p.bt_stride;
       int ids = (j0 + lane < j1) ? bt[j0 + lane] : -1;
+      FusedAppend<T, D> app;
+      if constexpr (FUSE) {
+        if (j1 == u.n) app.fetch(p, u.b, u.g, lane);   // this part owns the last page
+      }
       for (int jb = j0; jb < j1 && !aborted; jb += 32) {
         const int cur_ids = ids;
         ids = (jb + 32 + lane < j1) ? bt[jb + 32 + lane] : -1;
@@ -742,6 +906,12 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
         // the barrier waits, arrivals and TMA issues of a batch share warp
         // instructions (one page per lane-instruction costs ~600 cycles)
         for (int i = 0; i < cnt; i += kBatch) {
+          if constexpr (FUSE) {
+            // this part owns the unit's last page: append the step's token
+            // before the batch that loads that page
+            if (j1 == u.n && jb + i <= u.n - 1 && u.n - 1 < jb + i + kBatch)
+              app.put(p, u.b, u.g, lane);
+          }
           const int blk = __shfl_sync(0xffffffffu, cur_ids, (i + lane) & 31);
           if (lane < kBatch && i + lane < cnt) {
             const int xx = x + (jb - j0) + i + lane;
@@ -758,7 +928,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
             if (ok) {
               // the last page of a unit holds the token appended by the kernel
               // before this one: wait for that grid before reading it
-              if (jb + i + lane == u.n - 1) pdl_wait();
+              if (!FUSE && jb + i + lane == u.n - 1) pdl_wait();
               mbar_arrive_expect_tx(&full[st], Q::kStageBytes);
               const uint32_t kdst = smem_u32(smem + st * Q::kStageBytes);
               const uint32_t vdst = kdst + Q::kTileBytes;
@@ -810,8 +980,16 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
     // ---- this warp's pages of the segment ----
     if constexpr (KIND == 0) {
       MmaState<D> s;
-      pdl_wait();   // q_rot comes from the kernel before this one
-      mma_begin<T, D>(s, p, u.b, u.g, lane);
+      if constexpr (FUSE) {
+        T *qs = reinterpret_cast<T *>(red_acc);
+        fused_rotate_q<T, D, kConsumers>(p, u.b, u.g, j0 == 0, qs, tid);
+        mma_begin_smem<D>(s, reinterpret_cast<const __nv_bfloat16 *>(qs), p.G, lane);
+        // qs sits in the reduction buffer: nobody stashes before all have read
+        asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
+      } else {
+        pdl_wait();   // q_rot comes from the kernel before this one
+        mma_begin<T, D>(s, p, u.b, u.g, lane);
+      }
       int j = j0 + ((warp - x % NW) + NW) % NW;
       for (; j < j1; j += NW) {
         const int xx = x + (j - j0);
@@ -834,8 +1012,15 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
       mma_stash<D>(s, my_acc, my_m, my_l, lane);
     } else {
       SimtState<T, D, G> s;
-      pdl_wait();   // q_rot comes from the kernel before this one
-      simt_begin<T, D, G>(s, p, u.b, u.g, lane);
+      if constexpr (FUSE) {
+        T *qs = reinterpret_cast<T *>(red_acc);
+        fused_rotate_q<T, D, kConsumers>(p, u.b, u.g, j0 == 0, qs, tid);
+        simt_begin_smem<T, D, G>(s, qs, p.G, p.scale_log2, lane);
+        asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
+      } else {
+        pdl_wait();   // q_rot comes from the kernel before this one
+        simt_begin<T, D, G>(s, p, u.b, u.g, lane);
+      }
       int j = j0 + ((warp - x % NW) + NW) % NW;
       for (; j < j1; j += NW) {
         const int xx = x + (j - j0);
@@ -995,6 +1180,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
 struct AttnVariant {
   cudaError_t (*launch)(const CUtensorMap &, const CUtensorMap &, const AttnParams &,
                         cudaStream_t);
+  cudaError_t (*launch_step)(const CUtensorMap &, const CUtensorMap &, const AttnParams &,
+                             cudaStream_t);
   cudaError_t (*occupancy)(int *blocks_per_sm);
   int smem_bytes;
   int threads;
@@ -1003,9 +1190,10 @@ struct AttnVariant {
 template <typename T, int D, int NW, int NS, int KIND, int G>
 struct AttnLauncher {
   using Q = Geo<T, D, NW, NS>;
-  static cudaError_t launch(const CUtensorMap &tk, const CUtensorMap &tv, const AttnParams &p,
-                            cudaStream_t s) {
-    auto kern = attn_split_kernel<T, D, NW, NS, KIND, G>;
+  template <bool FUSE>
+  static cudaError_t launch_impl(const CUtensorMap &tk, const CUtensorMap &tv,
+                                 const AttnParams &p, cudaStream_t s) {
+    auto kern = attn_split_kernel<T, D, NW, NS, KIND, G, FUSE>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Q::kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -1014,7 +1202,7 @@ struct AttnLauncher {
     if (e != cudaSuccess) return e;
     // launched as a programmatic dependent: the prologue (row scan, barrier
     // set-up, block-id prefetch, TMA of pages that do not hold this step's
-    // token) overlaps the RoPE/append kernel before it
+    // token) overlaps the RoPE/append kernel before it (when there is one)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.num_parts);
     cfg.blockDim = dim3(Q::kThreads);
@@ -1024,19 +1212,29 @@ struct AttnLauncher {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = FUSE ? 0 : 1;
     e = cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }
+  static cudaError_t launch(const CUtensorMap &tk, const CUtensorMap &tv, const AttnParams &p,
+                            cudaStream_t s) {
+    return launch_impl<false>(tk, tv, p, s);
+  }
+  static cudaError_t launch_step(const CUtensorMap &tk, const CUtensorMap &tv,
+                                 const AttnParams &p, cudaStream_t s) {
+    return launch_impl<true>(tk, tv, p, s);
+  }
   static cudaError_t occupancy(int *n) {
-    auto kern = attn_split_kernel<T, D, NW, NS, KIND, G>;
+    auto kern = attn_split_kernel<T, D, NW, NS, KIND, G, false>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Q::kSmemBytes);
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, kern, Q::kThreads, Q::kSmemBytes);
   }
-  static AttnVariant variant() { return AttnVariant{&launch, &occupancy, Q::kSmemBytes, Q::kThreads}; }
+  static AttnVariant variant() {
+    return AttnVariant{&launch, &launch_step, &occupancy, Q::kSmemBytes, Q::kThreads};
+  }
 };
 
 // Variant lookup, one per translation unit (returns false if not built).

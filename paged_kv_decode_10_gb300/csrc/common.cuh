@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <cmath>
+
 #include "pkv.h"
 #include "status.h"
 
@@ -138,6 +140,34 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
   uint32_t d;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
   return d;
+}
+
+// ---- rotate-half RoPE arithmetic, shared by every kernel that rotates ------
+// Angle of pair i at position p in 64-bit fixed-point turns: `turn` is
+// round(2^64 * base^(-2i/d) / (2 pi)) and p * turn mod 2^64 (an exact wrapping
+// product) is the fractional turn of theta_i = p * base^(-2i/d).  Read as a
+// signed value and scaled by 2 pi / 2^64 it is theta_i reduced to [-pi, pi).
+__device__ __forceinline__ void rope_cossin(uint32_t pos, unsigned long long turn, float *c,
+                                            float *s) {
+  const unsigned long long ph = static_cast<unsigned long long>(pos) * turn;
+  const float ang = static_cast<float>(static_cast<long long>(ph)) * 3.4061215800865545e-19f;
+  sincosf(ang, s, c);
+}
+// (x1, x2) -> (x1 c - x2 s, x2 c + x1 s) with a fixed operation order, so every
+// kernel produces bit-identical rotated values.
+__device__ __forceinline__ void rope_rotate(float x1, float x2, float c, float s, float *y1,
+                                            float *y2) {
+  *y1 = fmaf(x1, c, -__fmul_rn(x2, s));
+  *y2 = fmaf(x2, c, __fmul_rn(x1, s));
+}
+
+// Host: the fixed-point turn table of pairs i < d/2.
+inline void fill_rope_turns(float base, int d, unsigned long long *turns) {
+  for (int i = 0; i < d / 2; ++i) {
+    const double f = std::pow(static_cast<double>(base), -2.0 * i / static_cast<double>(d)) /
+                     (2.0 * 3.141592653589793238462643383279502884);
+    turns[i] = static_cast<unsigned long long>(std::ldexp(f, 64));
+  }
 }
 
 // ---- programmatic dependent launch (sm_90+) --------------------------------

@@ -6,12 +6,9 @@
 // pool of fixed 16-token blocks; the new token's K/V go to slot_mapping[b].
 //
 // Angles.  theta_i = p * base^(-2i/d) can reach 1.3e5 rad at p = 131072, where
-// a float32 product would be off by ~0.008 rad.  The kernel instead works in
-// turns with 64-bit fixed point: F_i = round(2^64 * base^(-2i/d) / (2 pi))
-// (host, double precision), and p * F_i mod 2^64 (an exact integer product
-// that wraps) is the fractional turn of theta_i.  Read as a signed 64-bit
-// value and scaled by 2 pi / 2^64 it is theta_i reduced to [-pi, pi), exact to
-// float32 rounding, and sincosf then only sees reduced arguments.
+// a float32 product would be off by ~0.008 rad; the angle is formed in 64-bit
+// fixed-point turns instead (rope_cossin in common.cuh), exact to float32
+// rounding, and sincosf then only sees reduced arguments.
 #include <cmath>
 #include <cstdint>
 
@@ -101,10 +98,8 @@ __global__ void rope_kernel(const T *__restrict__ q, const T *__restrict__ k,
   if (vcopy) vw = reinterpret_cast<const uint4 *>(v + static_cast<size_t>(b) * Hkv * d)[tid];
 
   for (int i = tid; i < half; i += blockDim.x) {
-    const unsigned long long ph = static_cast<unsigned long long>(pos) * turns.f[i];
-    const float ang = static_cast<float>(static_cast<long long>(ph)) * 3.4061215800865545e-19f;
     float s, co;
-    sincosf(ang, &s, &co);
+    rope_cossin(pos, turns.f[i], &co, &s);
     cs[i] = co;
     cs[half + i] = s;
   }
@@ -124,11 +119,7 @@ __global__ void rope_kernel(const T *__restrict__ q, const T *__restrict__ k,
     unpack<T, VEC>(x1w, x1);
     unpack<T, VEC>(x2w, x2);
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) {
-      const float co = cs[c + e], s = cs[half + c + e];
-      y1[e] = x1[e] * co - x2[e] * s;
-      y2[e] = x2[e] * co + x1[e] * s;
-    }
+    for (int e = 0; e < VEC; ++e) rope_rotate(x1[e], x2[e], cs[c + e], cs[half + c + e], &y1[e], &y2[e]);
     const W o1 = pack<T, VEC>(y1), o2 = pack<T, VEC>(y2);
     T *dst = h < Hq ? q_out + (static_cast<size_t>(b) * Hq + h) * d
                     : k_out + (static_cast<size_t>(b) * Hkv + (h - Hq)) * d;
@@ -219,11 +210,7 @@ int rope_launch(const void *q, const void *k, const void *v, void *q_out, void *
                 PKV_ERR_INVALID_ARG, "append needs 16-byte rows and 16-byte aligned tensors");
   }
   RopeTurns t;
-  for (int i = 0; i < d / 2; ++i) {
-    const double f = std::pow(static_cast<double>(base), -2.0 * i / static_cast<double>(d)) /
-                     (2.0 * 3.141592653589793238462643383279502884);
-    t.f[i] = static_cast<unsigned long long>(std::ldexp(f, 64));
-  }
+  fill_rope_turns(base, d, t.f);
   const int rot_items = (Hq + Hkv) * (d / 2 / vec);
   const int v_chunks = append ? Hkv * d * elem / 16 : 0;
   int items = rot_items > v_chunks ? rot_items : v_chunks;

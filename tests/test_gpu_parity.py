@@ -416,3 +416,18 @@ def test_graph_replay_matches_eager_steps():
         assert torch.equal(out_e, out_g), step
     assert torch.equal(eager.k_cache, graph.k_cache) and torch.equal(eager.v_cache, graph.v_cache)
     assert eager.device_errors() == 0 and graph.device_errors() == 0
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode16", "ragged64", "long131k"])
+def test_whole_step_kernel_equals_split_launch(name):
+    """The one-launch step (RoPE and append inside the attention kernel) gives
+    bit-identical q_rot, k_rot, caches and output to the default two launches
+    (pkv_rope_append, then the attention kernel)."""
+    w = workloads.make_workload(name)
+    caches = workloads.make_caches(w, "cpu")
+    tokens = workloads.make_new_tokens(w, 0, "cpu")
+    fused = gpu_single_step(w, caches=caches, tokens=tokens, flags=binding.STEP_FUSED)
+    split = gpu_single_step(w, caches=caches, tokens=tokens)
+    for key in ("out", "q_rot", "k_rot", "k_cache", "v_cache"):
+        assert torch.equal(fused[key], split[key]), key
+    assert fused["err"] == 0 and split["err"] == 0
