@@ -62,6 +62,9 @@ def parse_args():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-flush", action="store_true")
+    ap.add_argument("--metadata", default="mapped", choices=["copy", "mapped"],
+                    help="per-step metadata: copied to the device, or read in place from "
+                         "pinned host memory")
     return ap.parse_args()
 
 
@@ -227,7 +230,7 @@ def host_cores():
 # ---------------------------------------------------------------------------
 # the GPU arm
 # ---------------------------------------------------------------------------
-def setup(w, device, parts, flags, steps_total):
+def setup(w, device, parts, flags, steps_total, metadata):
     import torch
     from paged_kv_decode_10_gb300 import engine, workloads
     pool_bytes = w.num_blocks * w.Hkv * 16 * w.d * (2 if w.dtype == "bf16" else 4)
@@ -237,7 +240,8 @@ def setup(w, device, parts, flags, steps_total):
     dec = engine.PagedDecoder(w.num_blocks, w.Hq, w.Hkv, w.d, w.dtype, w.B, bt,
                               initial_free=w.free_order, device=device,
                               num_parts=parts or None, flags=flags,
-                              k_cache=k_cache.to(device), v_cache=v_cache.to(device))
+                              k_cache=k_cache.to(device), v_cache=v_cache.to(device),
+                              metadata=metadata)
     ids = [dec.join(int(L)) for L in w.seq_lens]
     tokens = [workloads.make_new_tokens(w, s, device) for s in range(steps_total)]
     return dec, ids, tokens, (k_cache, v_cache) if gen_dev == "cpu" else None
@@ -251,7 +255,8 @@ def run_gpu(args, rank, world):
     torch.cuda.set_device(device)
     w = workloads.make_workload(args.workload)
     W, K, GW = args.warmup, args.steps, 2
-    dec, ids, tokens, cpu_caches = setup(w, device, args.parts, args.flags, W + GW + K + 1)
+    dec, ids, tokens, cpu_caches = setup(w, device, args.parts, args.flags, W + GW + K + 1,
+                                          args.metadata)
     assert dec.bt_stride * 16 >= int(w.seq_lens.max()) + W + GW + K + 64
     B = len(ids)
     elem = 2 if w.dtype == "bf16" else 4
@@ -339,25 +344,36 @@ def run_gpu(args, rank, world):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         total_s = float(t.item())
 
-    # the step's kernel timed alone on the final state, same launch configuration
-    # as in the step (captured once so the launch costs no host time inside the events)
-    attn_graph = torch.cuda.CUDAGraph()
+    # The dominant kernel (split-KV attention with its fused merge) timed alone
+    # on the final step's state, in the step's launch configuration, and the
+    # step's kernels (RoPE/append + attention) without the host side; each is
+    # captured once so that no host launch time falls between the events.
+    # Re-running the final step is idempotent (the same token re-appended).
+    step_args = dec.step_args(B, dec.q_in[:B], dec.k_in[:B], dec.v_in[:B])
     cap = torch.cuda.Stream(device)
     cap.wait_stream(stream)
-    step_args = dec.step_args(B, dec.q_in[:B], dec.k_in[:B], dec.v_in[:B])
+    attn_graph, kern_graph = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     with torch.cuda.graph(attn_graph, stream=cap):
-        # the step's single kernel (RoPE + append + attention + merge), rerun on
-        # the final step's inputs (re-appending the same token is idempotent)
+        binding.decode_attention(dec.q_rot[:B], dec.k_cache, dec.v_cache, dec.tables,
+                                 dec.seq_lens, scale=dec.scale, num_parts=dec.num_parts,
+                                 workspace=dec.workspace, out=dec.out[:B], flags=dec.flags,
+                                 err=dec.err, stream=cap)
+    with torch.cuda.graph(kern_graph, stream=cap):
         binding.decode_step_args(step_args, cap)
     stream.wait_stream(cap)
-    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
-    for i in range(K):
-        flush()
-        kev[i][0].record(stream)
-        attn_graph.replay()
-        kev[i][1].record(stream)
-    torch.cuda.synchronize()
-    attn_ms = [e[0].elapsed_time(e[1]) for e in kev]
+
+    def time_graph(g):
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+        for i in range(K):
+            flush()
+            ev[i][0].record(stream)
+            g.replay()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        return [e[0].elapsed_time(e[1]) for e in ev]
+
+    attn_ms = time_graph(attn_graph)
+    kern_ms = time_graph(kern_graph)
     last_lens = lens_after[-1]
 
     bytes_steps = [attn_bytes(la, w.Hq, w.Hkv, w.d, elem) for la in lens_after]
@@ -389,14 +405,20 @@ def run_gpu(args, rank, world):
                    "block_size": 16, "mean_kv_len": float(np.mean(lens_after[0])),
                    "pool_blocks": w.num_blocks, "num_parts": dec.num_parts,
                    "consumer": "simt" if (args.flags & 1 or w.dtype == "f32") else "mma.sync",
-                   "step": "one CUDA graph: metadata H2D + one kernel (RoPE, append, split-KV attention, LSE merge)",
+                   "step": "one CUDA graph: " + (
+                       "metadata H2D copy + " if args.metadata == "copy" else
+                       "metadata read in place from pinned host memory + ") + (
+                       "one kernel (RoPE, append, split-KV attention, LSE merge)"
+                       if args.flags & 4 else
+                       "RoPE/append kernel + split-KV attention kernel with fused LSE merge "
+                       "(programmatic dependent launch)"),
                    "l2": "flushed before every timed step" if not args.no_flush else "not flushed",
                    "parallelism": "replicas" if world > 1 else "single-gpu"},
         "steps_per_s": round(K / (sum(step_ms) / 1e3), 1),
         "attn_gbs": round(attn_gbs, 2),
         "pct_of_peak": round(100 * attn_gbs / peak, 2),
         "kv_bytes_per_step": int(statistics.mean(kv_only)),
-        "roofline": {"bound": "hbm", "kernel": "attn_split_kernel, whole step (a1 + a2 + a3 + fused a4)",
+        "roofline": {"bound": "hbm", "kernel": "attn_split_kernel (a3 + fused a4), timed alone",
                      "achieved": round(attn_gbs, 2), "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": round(attn_gbs / peak, 4),
                      "traffic": traffic,
@@ -405,7 +427,8 @@ def run_gpu(args, rank, world):
                      "kernel_hash": khash},
         "host_a0_us_per_step": round(1e6 * t_host / K, 2),
         "host_churn_us_per_step": round(1e6 * statistics.mean(churn_s), 2) if churn_s else None,
-        "gpu_launches": K,
+        "step_kernels_us": round(1e3 * statistics.mean(kern_ms), 3),
+        "gpu_launches": K * ((1 if args.flags & 4 else 2) + (1 if args.flags & 2 else 0)),
         "clocks": clocks,
     }
     return result, dec, ids, tokens, oracle_state, meta0, w
@@ -428,7 +451,11 @@ def run_e2e(args, dec, ids, tokens, w):
     dq = torch.empty_like(tokens[-1][0])
     dk = torch.empty_like(tokens[-1][1])
     dv = torch.empty_like(tokens[-1][2])
-    args_s = dec.step_args(B, dq, dk, dv)
+    meta_d = [torch.empty_like(m, device=device) for m in meta_h]
+    args_s = binding.make_step_args(
+        dq, dk, dv, dec.q_rot[:B], dec.k_rot[:B], dec.k_cache, dec.v_cache, *meta_d,
+        dec.scale, dec.rope_base, dec.num_parts, dec.workspace, dec.out[:B],
+        flags=dec.flags, err=dec.err)
     io = binding.host_io(*pinned, *meta_h, out_h)
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     flush_buf = torch.ones(max(2 * l2, 256 << 20) // 8, dtype=torch.int64, device=device)

@@ -129,6 +129,13 @@ int pkv_num_free(const pkv_alloc *a, int32_t *n);
 /* Copies the free stack bottom-to-top (up to cap entries); *n = its size. */
 int pkv_alloc_dump(const pkv_alloc *a, int32_t *free_stack, int32_t cap, int32_t *n);
 
+/* Device calls.  Tensors are device memory, except that the integer index
+ * arrays (positions, slot_mapping, seq_lens, block_tables) may instead be
+ * page-locked host memory at its mapped address (pkv_mapped_pointer): the
+ * kernels then read them in place over the CPU-GPU link, and the host must not
+ * rewrite them until those kernels have finished.  All calls are asynchronous
+ * on `stream` (a cudaStream_t; NULL = the legacy default stream). */
+
 /* ======================================================================== */
 /* a1: RoPE (helexa issue 121, slice 1: batch_cos_sin at per-row positions,   */
 /*     rotate-half apply)                                                    */
@@ -296,6 +303,15 @@ typedef struct pkv_step_args {
  * rotated q and k.  Each row's slot must be its position seq_len-1 in its own
  * blocks, as pkv_prepare_step produces. */
 int pkv_decode_step(const pkv_step_args *args, void *stream);
+
+/* The address under which kernels read the page-locked host buffer at
+ * host_ptr (allocated pinned, or registered with the mapped flag), so that the
+ * per-step metadata of pkv_decode_step can stay in host memory and be read by
+ * the kernels over the CPU-GPU link instead of being copied first.  The buffer
+ * must not change until the kernels that read it have finished.  Returns
+ * PKV_ERR_INVALID_ARG for a NULL pointer and PKV_ERR_CUDA when the memory is
+ * not mapped for the current device. */
+int pkv_mapped_pointer(const void *host_ptr, void **device_ptr);
 
 /* Host-side buffers for pkv_decode_step_host (pinned memory recommended). */
 typedef struct pkv_step_host_io {

@@ -105,6 +105,7 @@ SIGNATURES = {
     "pkv_lse_merge": (ctypes.c_int, [_vp, _size_t, _vp, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
                                      _c_i32, _c_i32, _vp, _c_i32, _vp]),
     "pkv_decode_step": (ctypes.c_int, [ctypes.POINTER(StepArgs), _vp]),
+    "pkv_mapped_pointer": (ctypes.c_int, [_vp, ctypes.POINTER(_vp)]),
     "pkv_decode_step_host": (ctypes.c_int, [ctypes.POINTER(StepArgs),
                                             ctypes.POINTER(StepHostIO), _vp]),
 }
@@ -258,6 +259,25 @@ def _ptr(t):
     return _vp(t.data_ptr())
 
 
+def mapped_pointer(t):
+    """Device-side address of a contiguous pinned CPU tensor (``pkv_mapped_pointer``)."""
+    if t.is_cuda or not t.is_pinned():
+        raise PkvError(ERR_INVALID_ARG, "tensor must be in pinned host memory")
+    if not t.is_contiguous():
+        raise PkvError(ERR_INVALID_ARG, "tensor must be contiguous")
+    out = _vp()
+    _check(load().pkv_mapped_pointer(_vp(t.data_ptr()), ctypes.byref(out)))
+    return out
+
+
+def _meta_ptr(t):
+    """Step metadata may be a device tensor or a pinned host tensor the kernels
+    read in place."""
+    if t is not None and not t.is_cuda:
+        return mapped_pointer(t)
+    return _ptr(t)
+
+
 def _stream(stream=None):
     torch = _torch()
     s = stream if stream is not None else torch.cuda.current_stream()
@@ -270,7 +290,7 @@ def rope(q, k, positions, base=10000.0, q_out=None, k_out=None, stream=None):
     q_out = torch.empty_like(q) if q_out is None else q_out
     k_out = torch.empty_like(k) if k_out is None else k_out
     B, Hq, d = q.shape
-    _check(load().pkv_rope(_ptr(q), _ptr(k), _ptr(q_out), _ptr(k_out), _ptr(positions), B, Hq,
+    _check(load().pkv_rope(_ptr(q), _ptr(k), _ptr(q_out), _ptr(k_out), _meta_ptr(positions), B, Hq,
                            k.shape[1], d, float(base), dtype_code(q), _stream(stream)))
     return q_out, k_out
 
@@ -283,7 +303,7 @@ def rope_append(q, k, v, positions, slot_mapping, k_cache, v_cache, base=10000.0
     k_out = torch.empty_like(k) if k_out is None else k_out
     B, Hq, d = q.shape
     _check(load().pkv_rope_append(_ptr(q), _ptr(k), _ptr(v), _ptr(q_out), _ptr(k_out),
-                                  _ptr(positions), _ptr(slot_mapping), _ptr(k_cache),
+                                  _meta_ptr(positions), _meta_ptr(slot_mapping), _ptr(k_cache),
                                   _ptr(v_cache), B, Hq, k.shape[1], d, k_cache.shape[0],
                                   float(base), dtype_code(q), _ptr(err), _stream(stream)))
     return q_out, k_out
@@ -292,7 +312,7 @@ def rope_append(q, k, v, positions, slot_mapping, k_cache, v_cache, base=10000.0
 def append(k_rot, v, slot_mapping, k_cache, v_cache, err=None, stream=None):
     """a2: write ``k_rot``/``v`` ``[B,Hkv,d]`` into cache slots ``slot_mapping [B]`` (int64)."""
     B, Hkv, d = k_rot.shape
-    _check(load().pkv_append(_ptr(k_rot), _ptr(v), _ptr(slot_mapping), _ptr(k_cache),
+    _check(load().pkv_append(_ptr(k_rot), _ptr(v), _meta_ptr(slot_mapping), _ptr(k_cache),
                              _ptr(v_cache), B, Hkv, d, k_cache.shape[0], dtype_code(k_rot),
                              _ptr(err), _stream(stream)))
 
@@ -324,8 +344,8 @@ def decode_attn_split(q_rot, k_cache, v_cache, block_tables, seq_lens, scale, nu
     Hkv = k_cache.shape[1]
     bias_stride = attn_bias.shape[1] if attn_bias is not None else 0
     _check(load().pkv_decode_attn_split(
-        _ptr(q_rot), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0], _ptr(block_tables),
-        block_tables.shape[1], _ptr(seq_lens), _ptr(attn_bias), bias_stride, B, Hq, Hkv, d,
+        _ptr(q_rot), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0], _meta_ptr(block_tables),
+        block_tables.shape[1], _meta_ptr(seq_lens), _ptr(attn_bias), bias_stride, B, Hq, Hkv, d,
         float(scale), int(num_parts), _ptr(workspace), workspace.numel(), _ptr(out),
         dtype_code(q_rot), int(flags), _ptr(err), _stream(stream)))
 
@@ -339,8 +359,8 @@ def decode_attention_static(q_rot, k_cache, v_cache, block_tables, seq_lens, sca
     Hkv = k_cache.shape[1]
     bias_stride = attn_bias.shape[1] if attn_bias is not None else 0
     _check(load().pkv_decode_attn_static(
-        _ptr(q_rot), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0], _ptr(block_tables),
-        block_tables.shape[1], _ptr(seq_lens), _ptr(attn_bias), bias_stride, B, Hq, Hkv, d,
+        _ptr(q_rot), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0], _meta_ptr(block_tables),
+        block_tables.shape[1], _meta_ptr(seq_lens), _ptr(attn_bias), bias_stride, B, Hq, Hkv, d,
         float(scale), int(num_parts), _ptr(out), dtype_code(q_rot), int(flags), _ptr(err),
         _stream(stream)))
     return out
@@ -349,7 +369,7 @@ def decode_attention_static(q_rot, k_cache, v_cache, block_tables, seq_lens, sca
 def lse_merge(workspace, seq_lens, bt_stride, B, Hq, Hkv, d, num_parts, out, bias_stride=0,
               stream=None):
     """a4: LSE merge of the split partials into ``out``."""
-    _check(load().pkv_lse_merge(_ptr(workspace), workspace.numel(), _ptr(seq_lens),
+    _check(load().pkv_lse_merge(_ptr(workspace), workspace.numel(), _meta_ptr(seq_lens),
                                 int(bt_stride), int(bias_stride), B, Hq, Hkv, d, int(num_parts),
                                 _ptr(out), dtype_code(out), _stream(stream)))
 
@@ -377,14 +397,17 @@ def decode_attention(q_rot, k_cache, v_cache, block_tables, seq_lens, scale, num
 def make_step_args(q, k, v, q_rot, k_rot, k_cache, v_cache, positions, slot_mapping, seq_lens,
                    block_tables, scale, rope_base, num_parts, workspace, out, attn_bias=None,
                    flags=0, err=None):
-    """Fills the ``pkv_step_args`` struct (all device tensors)."""
+    """Fills the ``pkv_step_args`` struct.  All tensors are on the device except
+    that positions, slot_mapping, seq_lens and block_tables may be pinned host
+    tensors, which the kernels then read in place."""
     a = StepArgs()
     a.q, a.k, a.v = _ptr(q), _ptr(k), _ptr(v)
     a.q_rot, a.k_rot = _ptr(q_rot), _ptr(k_rot)
     a.k_cache, a.v_cache = _ptr(k_cache), _ptr(v_cache)
     a.num_blocks = k_cache.shape[0]
-    a.positions, a.slot_mapping, a.seq_lens = _ptr(positions), _ptr(slot_mapping), _ptr(seq_lens)
-    a.block_tables, a.bt_stride = _ptr(block_tables), block_tables.shape[1]
+    a.positions, a.slot_mapping = _meta_ptr(positions), _meta_ptr(slot_mapping)
+    a.seq_lens = _meta_ptr(seq_lens)
+    a.block_tables, a.bt_stride = _meta_ptr(block_tables), block_tables.shape[1]
     a.attn_bias = _ptr(attn_bias)
     a.bias_stride = attn_bias.shape[1] if attn_bias is not None else 0
     a.B, a.Hq, a.d = q.shape

@@ -407,6 +407,13 @@ extern "C" int pkv_decode_step(const pkv_step_args *a, void *stream) {
                        a->out, a->dtype, stream);
 }
 
+extern "C" int pkv_mapped_pointer(const void *host_ptr, void **device_ptr) {
+  clear_error();
+  PKV_REQUIRE(host_ptr && device_ptr, PKV_ERR_INVALID_ARG, "NULL pointer");
+  PKV_CUDA_CHECK(cudaHostGetDevicePointer(device_ptr, const_cast<void *>(host_ptr), 0));
+  return PKV_OK;
+}
+
 extern "C" int pkv_decode_step_host(const pkv_step_args *dev, const pkv_step_host_io *host,
                                     void *stream) {
   clear_error();

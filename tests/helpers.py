@@ -27,7 +27,8 @@ def storage_spacing(x, dtype):
     return np.ldexp(1.0, np.maximum(e - 1, -126) - (bits - 1))
 
 
-def gpu_single_step(w, num_parts=None, flags=0, caches=None, tokens=None, bt=None):
+def gpu_single_step(w, num_parts=None, flags=0, caches=None, tokens=None, bt=None,
+                    metadata="copy"):
     """One decode step of workload ``w`` on the GPU; every row joins with its
     cached length and is stepped once.  Returns host copies of everything."""
     d = dev()
@@ -40,7 +41,8 @@ def gpu_single_step(w, num_parts=None, flags=0, caches=None, tokens=None, bt=Non
     bt = bt or w.max_blocks_per_seq()
     dec = engine.PagedDecoder(w.num_blocks, w.Hq, w.Hkv, w.d, w.dtype, w.B, bt,
                               initial_free=w.free_order, device=d, num_parts=num_parts,
-                              flags=flags, k_cache=k_cache.to(d), v_cache=v_cache.to(d))
+                              flags=flags, k_cache=k_cache.to(d), v_cache=v_cache.to(d),
+                              metadata=metadata)
     ids = [dec.join(int(L)) for L in w.seq_lens]
     out = dec.step(ids, q.to(d), k.to(d), v.to(d))
     torch.cuda.synchronize()

@@ -389,18 +389,21 @@ def test_separate_merge_equals_fused(name, parts):
     assert (again.cpu().float() - fused["out"].float()).abs().max() <= close
 
 
-def test_graph_replay_matches_eager_steps():
-    """The captured step (metadata H2D + rope/append + attention in one CUDA
-    graph) gives bit-identical outputs and caches to the eager C ABI calls."""
+@pytest.mark.parametrize("metadata", ["copy", "mapped"])
+def test_graph_replay_matches_eager_steps(metadata):
+    """The captured step (metadata H2D, or none when the kernels read the pinned
+    metadata in place, + rope/append + attention in one CUDA graph) gives
+    bit-identical outputs and caches to the eager C ABI calls."""
     w = workloads.make_workload("decode16")
     d = dev()
     caches = workloads.make_caches(w, "cpu")
     bt = w.max_blocks_per_seq(extra_tokens=8)
     decs = []
-    for _ in range(2):
+    for mode in ("copy", metadata):
         dec = engine.PagedDecoder(w.num_blocks, w.Hq, w.Hkv, w.d, w.dtype, w.B, bt,
                                   initial_free=w.free_order, device=d,
-                                  k_cache=caches[0].to(d), v_cache=caches[1].to(d))
+                                  k_cache=caches[0].to(d), v_cache=caches[1].to(d),
+                                  metadata=mode)
         decs.append((dec, [dec.join(int(L)) for L in w.seq_lens]))
     (eager, ids_e), (graph, ids_g) = decs
     graph.capture(w.B)
@@ -431,3 +434,59 @@ def test_whole_step_kernel_equals_split_launch(name):
     for key in ("out", "q_rot", "k_rot", "k_cache", "v_cache"):
         assert torch.equal(fused[key], split[key]), key
     assert fused["err"] == 0 and split["err"] == 0
+
+
+@pytest.mark.parametrize("name,flags", [("tiny", 0), ("ragged64", 0), ("ragged64", 4),
+                                        ("long131k", 0), ("tiny", 1)])
+def test_mapped_metadata_equals_device_copy(name, flags):
+    """Kernels reading positions, slots, seq_lens and block tables in place from
+    pinned host memory give bit-identical results to reading a device copy."""
+    w = workloads.make_workload(name)
+    caches = workloads.make_caches(w, "cpu")
+    tokens = workloads.make_new_tokens(w, 0, "cpu")
+    a = gpu_single_step(w, caches=caches, tokens=tokens, flags=flags)
+    b = gpu_single_step(w, caches=caches, tokens=tokens, flags=flags, metadata="mapped")
+    for key in ("out", "q_rot", "k_rot", "k_cache", "v_cache"):
+        assert torch.equal(a[key], b[key]), key
+    assert a["err"] == 0 and b["err"] == 0
+
+
+def test_mapped_metadata_churn_eager_and_graph():
+    """Rows leave and join between steps; eager steps and graph replays of a
+    decoder with in-place host metadata track a device-copy decoder exactly
+    (the two pinned buffers alternate, so a refill never races a running step)."""
+    w = workloads.make_workload("decode16")
+    d = dev()
+    caches = workloads.make_caches(w, "cpu")
+    bt = w.max_blocks_per_seq(extra_tokens=64)
+    r = np.random.default_rng(7)
+    decs = []
+    for mode in ("copy", "mapped", "mapped"):
+        dec = engine.PagedDecoder(w.num_blocks, w.Hq, w.Hkv, w.d, w.dtype, w.B, bt,
+                                  initial_free=w.free_order, device=d,
+                                  k_cache=caches[0].to(d), v_cache=caches[1].to(d),
+                                  metadata=mode)
+        decs.append([dec, [dec.join(int(L)) for L in w.seq_lens]])
+    decs[2][0].capture(w.B)
+    for step in range(6):
+        if step in (2, 4):
+            row = int(r.integers(0, w.B))
+            pre = int(r.integers(1, 40))
+            for entry in decs:
+                entry[0].leave(entry[1][row])
+                entry[1][row] = entry[0].join(pre)
+        q, k, v = (t.to(d) for t in workloads.make_new_tokens(w, step, "cpu"))
+        outs = [decs[0][0].step(decs[0][1], q, k, v).clone(),
+                decs[1][0].step(decs[1][1], q, k, v).clone()]
+        g = decs[2][0]
+        g.q_in[:w.B].copy_(q)
+        g.k_in[:w.B].copy_(k)
+        g.v_in[:w.B].copy_(v)
+        g.prepare_host(decs[2][1])
+        outs.append(g.replay_step().clone())
+        torch.cuda.synchronize()
+        assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2]), step
+    for dec, _ in decs[1:]:
+        assert torch.equal(dec.k_cache, decs[0][0].k_cache)
+        assert torch.equal(dec.v_cache, decs[0][0].v_cache)
+        assert dec.device_errors() == 0
