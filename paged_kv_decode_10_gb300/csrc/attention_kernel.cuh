@@ -164,95 +164,6 @@ __device__ __forceinline__ float4 merge_column(const float *o, const float *lse,
   return acc;
 }
 
-// a4 done cooperatively by the nthr consumer threads of a CTA (named barrier 1):
-// merges the partials i < n at slots slot0 + i*stride for every column of the
-// unit.  All lse values are gathered in one round into shared memory `sw`
-// (n*G floats), turned into weights there, and the weighted sum of o issues its
-// loads independently (unrolled), so the merge costs a few L2 round trips
-// whatever n is.  store(h, d4, o4, lse) receives each merged float4 column.
-template <int MAXC, typename Skip, typename Store>
-__device__ __forceinline__ void merge_cta(const float *o, const float *lse, size_t slot0, int n,
-                                          int stride, int G, int D, Skip skip, float *sw,
-                                          float *sM, int tid, int nthr, Store store) {
-  for (int i = tid; i < n * G; i += nthr) {
-    const int s = i / G, h = i - s * G;
-    sw[i] = skip(s) ? -INFINITY : __ldcg(lse + (slot0 + static_cast<size_t>(s) * stride) * G + h);
-  }
-  asm volatile("bar.sync 1, %0;" ::"r"(nthr) : "memory");
-  if (tid < G) {
-    float M = -INFINITY;
-    for (int s = 0; s < n; ++s) M = fmaxf(M, sw[s * G + tid]);
-    float den = 0.f;
-    for (int s = 0; s < n; ++s) {
-      const float w = M == -INFINITY ? 0.f : ex2(sw[s * G + tid] - M);
-      sw[s * G + tid] = w;
-      den += w;
-    }
-    sM[tid] = M;
-    sM[G + tid] = den;
-  }
-  asm volatile("bar.sync 1, %0;" ::"r"(nthr) : "memory");
-  // each thread owns up to MAXC float4 columns; the loads of U partials x MAXC
-  // columns (8 in all) are issued before any of them is consumed
-  const int cols = D / 4;
-  const int ncol = G * cols;
-  float4 acc[MAXC];
-  int hh[MAXC], dd[MAXC];
-  bool on[MAXC];
-#pragma unroll
-  for (int k = 0; k < MAXC; ++k) {
-    const int col = tid + k * nthr;
-    on[k] = col < ncol;
-    hh[k] = on[k] ? col / cols : 0;
-    dd[k] = on[k] ? col - hh[k] * cols : 0;
-    acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  constexpr int U = MAXC >= 8 ? 1 : 8 / MAXC;   // 8 loads in flight per thread
-  for (int s0 = 0; s0 < n; s0 += U) {
-    float4 v[U][MAXC];
-    float w[U][MAXC];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int s = s0 + u;
-#pragma unroll
-      for (int k = 0; k < MAXC; ++k) {
-        w[u][k] = (s < n && on[k]) ? sw[s * G + hh[k]] : 0.f;
-        v[u][k] = w[u][k] != 0.f
-                      ? __ldcg(reinterpret_cast<const float4 *>(
-                                   o + ((slot0 + static_cast<size_t>(s) * stride) * G + hh[k]) * D) +
-                               dd[k])
-                      : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u)
-#pragma unroll
-      for (int k = 0; k < MAXC; ++k) {
-        acc[k].x = fmaf(w[u][k], v[u][k].x, acc[k].x);
-        acc[k].y = fmaf(w[u][k], v[u][k].y, acc[k].y);
-        acc[k].z = fmaf(w[u][k], v[u][k].z, acc[k].z);
-        acc[k].w = fmaf(w[u][k], v[u][k].w, acc[k].w);
-      }
-  }
-#pragma unroll
-  for (int k = 0; k < MAXC; ++k) {
-    if (!on[k]) continue;
-    const float den = sM[G + hh[k]];
-    float l = -INFINITY;
-    float4 r = acc[k];
-    if (den > 0.f) {
-      const float inv = 1.f / den;
-      r.x *= inv;
-      r.y *= inv;
-      r.z *= inv;
-      r.w *= inv;
-      l = sM[hh[k]] + log2f(den);
-    }
-    store(hh[k], dd[k], r, l);
-  }
-  asm volatile("bar.sync 1, %0;" ::"r"(nthr) : "memory");
-}
-
 template <typename T>
 __device__ __forceinline__ void store4(T *dst, float4 v);
 template <>
@@ -265,6 +176,120 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16 *dst, float4
   w.x = pack_bf16(v.x, v.y);
   w.y = pack_bf16(v.z, v.w);
   *reinterpret_cast<uint2 *>(dst) = w;
+}
+
+// One merge of the fused a4: the partials i < n stored at slots
+// slot0 + i*stride of (o, lse).  Level 1 merges up to kMergeGroup partials of
+// consecutive parts c0 + i; level 2 merges the group results of a unit whose
+// parts c0 .. c0+nseg-1 formed several groups.  The result goes to the group
+// buffers at grp_slot (a level-1 merge of a multi-group unit) or to the unit's
+// output rows.
+struct MergeJob {
+  const float *o, *lse;
+  size_t slot0;
+  int n, stride;
+  int c0, nseg, level;
+  float *o_grp, *lse_grp;   // non-null: write the merged group here
+  size_t grp_slot;
+  void *out;                // else: the unit's [G, D] output rows
+};
+
+// Partial i of job J does not exist: its part (level 1), or every part of its
+// group (level 2), owns no page (only possible when C > P).
+__device__ __forceinline__ bool merge_skip(const MergeJob &J, int i, long long P, int C) {
+  if (C <= P) return false;
+  if (J.level == 1) return part_empty(J.c0 + i, P, C);
+  return real_parts(J.c0 + i * kMergeGroup, min(kMergeGroup, J.nseg - i * kMergeGroup), P, C) == 0;
+}
+
+// The merge of one float4 column (head h, dims 4*d4 .. 4*d4+3) of job J by one
+// thread.  The lse and o loads of K partials are issued together, so a merge of
+// n <= K partials costs one L2 round trip; longer ones rescale a running
+// maximum chunk by chunk.  Loads bypass L1: other CTAs wrote the partials.
+template <typename T, int K>
+__device__ __forceinline__ void merge_job_column(const MergeJob J, int G, int D, int h, int d4,
+                                                 long long P, int C) {
+  float M = -INFINITY, den = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = 0; s0 < J.n; s0 += K) {
+    float l[K];
+    float4 v[K];
+#pragma unroll
+    for (int u = 0; u < K; ++u) {
+      const int s = s0 + u;
+      const bool on = s < J.n && !merge_skip(J, s, P, C);
+      const size_t slot = J.slot0 + static_cast<size_t>(s) * J.stride;
+      l[u] = on ? __ldcg(J.lse + slot * G + h) : -INFINITY;
+      v[u] = on ? __ldcg(reinterpret_cast<const float4 *>(J.o + (slot * G + h) * D) + d4)
+                : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float m = M;
+#pragma unroll
+    for (int u = 0; u < K; ++u) m = fmaxf(m, l[u]);
+    if (m == -INFINITY) continue;
+    const float r = ex2(M - m);   // 0 while nothing was accumulated
+    den *= r;
+    acc.x *= r;
+    acc.y *= r;
+    acc.z *= r;
+    acc.w *= r;
+#pragma unroll
+    for (int u = 0; u < K; ++u) {
+      const float w = ex2(l[u] - m);
+      if (w != 0.f) {
+        den += w;
+        acc.x = fmaf(w, v[u].x, acc.x);
+        acc.y = fmaf(w, v[u].y, acc.y);
+        acc.z = fmaf(w, v[u].z, acc.z);
+        acc.w = fmaf(w, v[u].w, acc.w);
+      }
+    }
+    M = m;
+  }
+  float lse = -INFINITY;
+  if (den > 0.f) {
+    const float inv = 1.f / den;
+    acc.x *= inv;
+    acc.y *= inv;
+    acc.z *= inv;
+    acc.w *= inv;
+    lse = M + log2f(den);
+  }
+  if (J.o_grp) {
+    *(reinterpret_cast<float4 *>(J.o_grp + (J.grp_slot * G + h) * D) + d4) = acc;
+    if (d4 == 0) J.lse_grp[J.grp_slot * G + h] = lse;
+  } else {
+    store4<T>(static_cast<T *>(J.out) + h * D + 4 * d4, acc);
+  }
+}
+
+// The jobs' columns spread over the nthr consumer threads: with two jobs of a
+// small unit every thread has one column, and all loads are in flight at once.
+template <typename T>
+__device__ __forceinline__ void merge_jobs(const MergeJob J0, const MergeJob J1, int njobs,
+                                           int G, int D, long long P, int C, int tid, int nthr) {
+  const int cols = G * (D / 4);
+  for (int item = tid; item < njobs * cols; item += nthr) {
+    const int q = item >= cols ? 1 : 0;
+    const int col = item - q * cols;
+    const int h = col / (D / 4), d4 = col - h * (D / 4);
+    merge_job_column<T, 8>(q ? J1 : J0, G, D, h, d4, P, C);
+  }
+}
+
+// Release / acquire at GPU scope around the merge counters (the partials that
+// other threads of this CTA wrote before a CTA barrier are covered: fences are
+// cumulative).
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+__device__ __forceinline__ int atom_add_relaxed_gpu(int32_t *p, int v) {
+  int old;
+  asm volatile("atom.relaxed.gpu.global.add.s32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(p), "r"(v)
+               : "memory");
+  return old;
 }
 
 struct UnitCursor {
@@ -305,7 +330,7 @@ struct Geo {
   static constexpr int kOffBad = kOffBars + 2 * NS * 8;
   static constexpr int kOffScan = kOffBad + NS * 4;
   static constexpr int kOffMisc = kOffScan + (kThreads / 32) * 4;
-  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;            // + alignment slack
+  static constexpr int kSmemBytes = kOffMisc + 32 + 1024;            // + alignment slack
   static_assert(kSubs >= 1 && D * kElem % 128 == 0, "row must be whole 128-B lines");
   static_assert(NS % NW == 0, "a stage must always feed the same consumer warp");
 };
@@ -966,7 +991,6 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
   float *pbuf = pbuf_all + warp * kBlockTokens * Q::kHeadsPad;
   float *abuf = abuf_all + warp * Q::kHeadsPad;
   constexpr int kConsumers = NW * 32;
-  constexpr int kMergeCols = (8 * (D / 4) + kConsumers - 1) / kConsumers;
 
   int pend_u[2], pend_c[2], pend_n[2], pend_b[2], pend_g[2];   // at most two (see below)
   int npend = 0;
@@ -1115,63 +1139,96 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
     cur += j1 - j0;
     if (cur < end) next_unit(u, p);
   }
-  if (npend > 0) __threadfence();
-  for (int q = 0; q < npend; ++q) {
-    const int u_idx = pend_u[q], c_first = pend_c[q], nseg = pend_n[q];
-    const int gq = p.G;
-    {
-      // a4 in the epilogue (threadfence-reduction pattern, two levels; every
-      // counter is reset by the CTA that consumes it)
-      const int grp = (static_cast<int>(blockIdx.x) - c_first) / kMergeGroup;
-      const int g0 = c_first + grp * kMergeGroup;
-      const int gcount = min(kMergeGroup, nseg - grp * kMergeGroup);
-      const int ngroups = (nseg + kMergeGroup - 1) / kMergeGroup;
-      T *out_u = static_cast<T *>(p.out) + (static_cast<size_t>(pend_b[q]) * p.Hq + pend_g[q] * gq) * D;
-      auto to_out = [&](int h, int d4, float4 r, float) { store4<T>(out_u + h * D + 4 * d4, r); };
-      asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
-      if (tid == 0) {
-        const int prev = atomicAdd(&p.counters[u_idx + g0], 1);
-        misc[3] = (prev == real_parts(g0, gcount, P, C) - 1) ? 1 : 0;
-      }
-      asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
-      if (misc[3]) {
-        __threadfence();
-        const size_t slot0 = static_cast<size_t>(u_idx) + g0;
-        auto skip1 = [&](int i) { return C > P && part_empty(g0 + i, P, C); };
-        if (ngroups == 1) {
-          merge_cta<kMergeCols>(p.o_part, p.lse_part, slot0, gcount, 1, gq, D, skip1, red_acc, red_m, tid,
-                    kConsumers, to_out);
-        } else {
-          auto to_group = [&](int h, int d4, float4 r, float l) {
-            *reinterpret_cast<float4 *>(p.o_group + (slot0 * gq + h) * D + 4 * d4) = r;
-            if (d4 == 0) p.lse_group[slot0 * gq + h] = l;
-          };
-          merge_cta<kMergeCols>(p.o_part, p.lse_part, slot0, gcount, 1, gq, D, skip1, red_acc, red_m, tid,
-                    kConsumers, to_group);
-        }
-        if (tid == 0) p.counters[u_idx + g0] = 0;
-        if (ngroups > 1) {
-          __threadfence();
-          asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
-          if (tid == 0) {
-            const int prev = atomicAdd(&p.unit_counters[u_idx], 1);
-            misc[3] = (prev == real_groups(c_first, nseg, P, C) - 1) ? 1 : 0;
-          }
-          asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
-          if (misc[3]) {
-            __threadfence();
-            auto skip2 = [&](int k) {
-              return C > P && real_parts(c_first + k * kMergeGroup,
-                                         min(kMergeGroup, nseg - k * kMergeGroup), P, C) == 0;
-            };
-            merge_cta<kMergeCols>(p.o_group, p.lse_group, static_cast<size_t>(u_idx) + c_first, ngroups,
-                      kMergeGroup, gq, D, skip2, red_acc, red_m, tid, kConsumers, to_out);
-            if (tid == 0) p.unit_counters[u_idx] = 0;
-          }
-        }
-      }
-    }
+  if (npend == 0) return;
+  // ---- a4 in the epilogue: the last part to finish a merge group merges it,
+  // the last group merger of a unit merges the groups (threadfence-reduction
+  // pattern; every counter is reset by the CTA that consumes it).  Both
+  // pending units go through each phase together, so the counters cost one
+  // round trip and the merges one or two more. ----
+  // (the segment loop ended with a consumer barrier: all partials are written)
+  MergeJob job[2];
+  int first_g[2], ngroups[2];
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int qq = q < npend ? q : 0;
+    const int u_idx = pend_u[qq], c_first = pend_c[qq], nseg = pend_n[qq];
+    const int grp = (static_cast<int>(blockIdx.x) - c_first) / kMergeGroup;
+    first_g[q] = c_first + grp * kMergeGroup;
+    ngroups[q] = (nseg + kMergeGroup - 1) / kMergeGroup;
+    MergeJob &J = job[q];
+    J.o = p.o_part;
+    J.lse = p.lse_part;
+    J.slot0 = static_cast<size_t>(u_idx) + first_g[q];
+    J.n = min(kMergeGroup, nseg - grp * kMergeGroup);
+    J.stride = 1;
+    J.c0 = first_g[q];
+    J.nseg = nseg;
+    J.level = 1;
+    J.o_grp = ngroups[q] > 1 ? p.o_group : nullptr;
+    J.lse_grp = p.lse_group;
+    J.grp_slot = J.slot0;
+    J.out = static_cast<T *>(p.out) + (static_cast<size_t>(pend_b[qq]) * p.Hq + pend_g[qq] * p.G) * D;
   }
+  if (tid == 0) {
+    fence_acq_rel_gpu();   // release this part's partials
+    int prev[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+      if (q < npend) prev[q] = atom_add_relaxed_gpu(&p.counters[pend_u[q] + first_g[q]], 1);
+    fence_acq_rel_gpu();   // acquire the other parts' partials
+    int last = 0;
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+      if (q < npend && prev[q] == real_parts(first_g[q], job[q].n, P, C) - 1) {
+        last |= 1 << q;
+        p.counters[pend_u[q] + first_g[q]] = 0;
+      }
+    misc[4] = last;
+  }
+  asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
+  const int last1 = misc[4];
+  if (last1 == 0) return;
+  merge_jobs<T>((last1 & 1) ? job[0] : job[1], job[1], last1 == 3 ? 2 : 1, p.G, D, P, C, tid, kConsumers);
+  // level 2 for the units that have several groups
+  int multi = 0;
+#pragma unroll
+  for (int q = 0; q < 2; ++q)
+    if ((last1 >> q & 1) && ngroups[q] > 1) multi |= 1 << q;
+  if (multi == 0) return;
+  asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");   // group results written
+  if (tid == 0) {
+    fence_acq_rel_gpu();
+    int prev[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+      if (multi >> q & 1) prev[q] = atom_add_relaxed_gpu(&p.unit_counters[pend_u[q]], 1);
+    fence_acq_rel_gpu();
+    int last = 0;
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+      if ((multi >> q & 1) && prev[q] == real_groups(pend_c[q], pend_n[q], P, C) - 1) {
+        last |= 1 << q;
+        p.unit_counters[pend_u[q]] = 0;
+      }
+    misc[5] = last;
+  }
+  asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
+  const int last2 = misc[5];
+  if (last2 == 0) return;
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    MergeJob &J = job[q];
+    J.o = p.o_group;
+    J.lse = p.lse_group;
+    J.slot0 = static_cast<size_t>(pend_u[q < npend ? q : 0]) + pend_c[q < npend ? q : 0];
+    J.n = ngroups[q];
+    J.stride = kMergeGroup;
+    J.c0 = pend_c[q < npend ? q : 0];
+    J.level = 2;
+    J.o_grp = nullptr;
+  }
+  merge_jobs<T>((last2 & 1) ? job[0] : job[1], job[1], last2 == 3 ? 2 : 1, p.G, D, P, C, tid,
+                kConsumers);
 }
 
 // ---------------------------------------------------------------------------
