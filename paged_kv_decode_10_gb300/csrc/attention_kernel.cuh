@@ -105,21 +105,27 @@ __device__ __forceinline__ bool part_empty(long long c, long long P, int C) {
 }
 
 // Parts c0 .. c0+n-1 that own at least one page (all of them when C <= P).
-__device__ __forceinline__ int real_parts(int c0, int n, long long P, int C) {
-  if (C <= P) return n;
+// The counting loops only run when C > P and are kept out of line so that the
+// common path stays short (the epilogue's code is fetched cold).
+static __device__ __noinline__ int count_real_parts(int c0, int n, long long P, int C) {
   int r = 0;
   for (int s = 0; s < n; ++s) r += !part_empty(c0 + s, P, C);
   return r;
 }
+__device__ __forceinline__ int real_parts(int c0, int n, long long P, int C) {
+  return C <= P ? n : count_real_parts(c0, n, P, C);
+}
 
 // Merge groups of a unit spanning parts c0 .. c0+nseg-1 that own a page.
-__device__ __forceinline__ int real_groups(int c0, int nseg, long long P, int C) {
+static __device__ __noinline__ int count_real_groups(int c0, int nseg, long long P, int C) {
   const int ng = (nseg + kMergeGroup - 1) / kMergeGroup;
-  if (C <= P) return ng;
   int r = 0;
   for (int k = 0; k < ng; ++k)
-    r += real_parts(c0 + k * kMergeGroup, min(kMergeGroup, nseg - k * kMergeGroup), P, C) > 0;
+    r += count_real_parts(c0 + k * kMergeGroup, min(kMergeGroup, nseg - k * kMergeGroup), P, C) > 0;
   return r;
+}
+__device__ __forceinline__ int real_groups(int c0, int nseg, long long P, int C) {
+  return C <= P ? (nseg + kMergeGroup - 1) / kMergeGroup : count_real_groups(c0, nseg, P, C);
 }
 
 // a4, the LSE merge of one float4 column (head h, dims 4*d4 .. 4*d4+3) over the
@@ -196,10 +202,13 @@ struct MergeJob {
 
 // Partial i of job J does not exist: its part (level 1), or every part of its
 // group (level 2), owns no page (only possible when C > P).
-__device__ __forceinline__ bool merge_skip(const MergeJob &J, int i, long long P, int C) {
-  if (C <= P) return false;
+static __device__ __noinline__ bool merge_skip_slow(const MergeJob &J, int i, long long P, int C) {
   if (J.level == 1) return part_empty(J.c0 + i, P, C);
-  return real_parts(J.c0 + i * kMergeGroup, min(kMergeGroup, J.nseg - i * kMergeGroup), P, C) == 0;
+  return count_real_parts(J.c0 + i * kMergeGroup, min(kMergeGroup, J.nseg - i * kMergeGroup), P,
+                          C) == 0;
+}
+__device__ __forceinline__ bool merge_skip(const MergeJob &J, int i, long long P, int C) {
+  return C > P && merge_skip_slow(J, i, P, C);
 }
 
 // The merge of one float4 column (head h, dims 4*d4 .. 4*d4+3) of job J by one
@@ -910,6 +919,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
   if (warp == NW) {
     // ======================= producer warp =======================
     constexpr int kBatch = NS >= 8 ? 4 : (NS >= 2 ? NS / 2 : 1);
+    const uint64_t l2_stream = l2_policy_evict_first();
     UnitCursor u = u0;
     long long cur = start;
     int x = 0;
@@ -960,8 +970,10 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
               const int y = (blk * p.Hkv + u.g) * kBlockTokens;
 #pragma unroll
               for (int sub = 0; sub < Q::kSubs; ++sub) {
-                tma_load_2d(kdst + sub * Q::kSubBytes, &tmap_k, sub * Q::kSubCols, y, &full[st]);
-                tma_load_2d(vdst + sub * Q::kSubBytes, &tmap_v, sub * Q::kSubCols, y, &full[st]);
+                tma_load_2d_hint(kdst + sub * Q::kSubBytes, &tmap_k, sub * Q::kSubCols, y,
+                                 &full[st], l2_stream);
+                tma_load_2d_hint(vdst + sub * Q::kSubBytes, &tmap_v, sub * Q::kSubCols, y,
+                                 &full[st], l2_stream);
               }
             } else {
               if (!dead) set_dev_err(p.err, PKV_DEVERR_BAD_BLOCK);
