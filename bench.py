@@ -276,11 +276,22 @@ def run_gpu(args, rank, world):
         oracle_state = (cpu_caches, [t.cpu() for t in tokens[0]])
 
     churn_s = []
+    prefill_log = []     # (tokens, start event, end event) per churn step
+    if w.churn:
+        # synthetic raw prefix keys/values of the joiners (the prefill's input)
+        max_t = max(int(np.sum(p)) for _, p in w.churn)
+        gen = torch.Generator(device=device).manual_seed(1000 + w.seed)
+        pre_k = torch.randn((max_t, w.Hkv, w.d), generator=gen, device=device).to(dec.tdtype)
+        pre_v = torch.randn((max_t, w.Hkv, w.d), generator=gen, device=device).to(dec.tdtype)
+        pre_pos = torch.empty(max_t, dtype=torch.int32).pin_memory()
+        pre_slot = torch.empty(max_t, dtype=torch.int64).pin_memory()
+        pre_done = [None]
 
     def churn(s):
         """Continuous batching: before step s >= 1 the planned rows leave and new
-        rows join in their places (host allocator only; no KV moves).  The
-        joiner's prefix blocks keep whatever KV they held (a stand-in prefill)."""
+        rows join in their places (host allocator; no KV moves), and the joiners'
+        prefix KV is written into their new blocks by the prefill kernel
+        (pkv_seq_slots + pkv_prefill_kv, timed on its own after an L2 flush)."""
         if not w.churn or s == 0:
             return
         leave, prefixes = w.churn[(s - 1) % len(w.churn)]
@@ -290,6 +301,22 @@ def run_gpu(args, rank, world):
         for row, pre in zip(leave, prefixes):
             ids[row] = dec.join(int(pre))
         churn_s.append(time.perf_counter() - t0)
+        if pre_done[0] is not None:
+            pre_done[0].synchronize()   # the last prefill still reads the pinned arrays
+        n = 0
+        pos_np, slot_np = pre_pos.numpy(), pre_slot.numpy()
+        for row, pre in zip(leave, prefixes):
+            dec.alloc.seq_slots(ids[row], 0, int(pre), out=(pos_np[n:n + int(pre)],
+                                                            slot_np[n:n + int(pre)]))
+            n += int(pre)
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        binding.prefill_kv(pre_k[:n], pre_v[:n], pre_pos[:n], pre_slot[:n], dec.k_cache,
+                           dec.v_cache, base=dec.rope_base, err=dec.err, stream=stream)
+        e1.record(stream)
+        pre_done[0] = e1
+        prefill_log.append((s, n, e0, e1))
 
     # warm-up: eager steps through the C ABI (one pkv_decode_step call each)
     meta0 = None
@@ -428,10 +455,28 @@ def run_gpu(args, rank, world):
         "host_a0_us_per_step": round(1e6 * t_host / K, 2),
         "host_churn_us_per_step": round(1e6 * statistics.mean(churn_s), 2) if churn_s else None,
         "step_kernels_us": round(1e3 * statistics.mean(kern_ms), 3),
+        "prefill": prefill_summary([x[1:] for x in prefill_log if x[0] >= W + GW], w, elem,
+                                   peak),
         "gpu_launches": K * ((1 if args.flags & 4 else 2) + (1 if args.flags & 2 else 0)),
         "clocks": clocks,
     }
     return result, dec, ids, tokens, oracle_state, meta0, w
+
+
+def prefill_summary(log, w, elem, peak):
+    """Joiners' prefix KV writes of a churn run: tokens per call and the
+    achieved bandwidth of pkv_prefill_kv (reads raw k and v, writes both into
+    the cache, reads positions and slots: 4*Hkv*d*elem + 12 bytes per token)."""
+    if not log:
+        return None
+    toks = [n for n, _, _ in log]
+    us = [1e3 * a.elapsed_time(b) for _, a, b in log]
+    nbytes = [n * (4 * w.Hkv * w.d * elem + 12) for n in toks]
+    gbs = sum(nbytes) / (sum(us) * 1e-6) / 1e9
+    return {"kernel": "rope_kernel (pkv_prefill_kv)", "calls": len(log),
+            "tokens_per_call": round(statistics.mean(toks), 1),
+            "us_per_call": round(statistics.mean(us), 3), "achieved_gbs": round(gbs, 2),
+            "frac": round(gbs / peak, 4), "l2": "flushed before every call"}
 
 
 def run_e2e(args, dec, ids, tokens, w):

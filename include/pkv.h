@@ -125,6 +125,13 @@ int pkv_seq_len(const pkv_alloc *a, int32_t seq_id, int32_t *len);
 /* Copies up to cap block ids of the sequence's table into out; *n = table length. */
 int pkv_seq_blocks(const pkv_alloc *a, int32_t seq_id, int32_t *out, int32_t cap,
                    int32_t *n);
+/* Positions and cache slots of tokens [start, start+count) of a live sequence
+ * (already covered by its blocks: start+count <= its length), for writing a
+ * prefix chunk with pkv_prefill_kv.  positions[i] = start+i,
+ * slot_mapping[i] = table[p/16]*16 + p%16.  PKV_ERR_INVALID_ARG if the range
+ * is negative or beyond the length; nothing is changed. */
+int pkv_seq_slots(const pkv_alloc *a, int32_t seq_id, int32_t start, int32_t count,
+                  int32_t *positions, int64_t *slot_mapping);
 int pkv_num_free(const pkv_alloc *a, int32_t *n);
 /* Copies the free stack bottom-to-top (up to cap entries); *n = its size. */
 int pkv_alloc_dump(const pkv_alloc *a, int32_t *free_stack, int32_t cap, int32_t *n);
@@ -180,6 +187,21 @@ int pkv_rope_append(const void *q, const void *k, const void *v, void *q_out, vo
                     void *v_cache, int32_t B, int32_t Hq, int32_t Hkv, int32_t d,
                     int32_t num_blocks, float base, int32_t dtype, int32_t *dev_err_flag,
                     void *stream);
+
+/*
+ * Prefix KV of joining sequences (chunked prefill's cache write): T tokens,
+ * each with its raw key k[t, Hkv, d], value v[t, Hkv, d], position
+ * positions[t] and cache slot slot_mapping[t] (pkv_seq_slots gives both for a
+ * chunk of one sequence; chunks of several sequences may be concatenated).
+ * The key is rotated at its position exactly as pkv_rope_append rotates a
+ * decode token (bit-identical rows), then both are written to the slot.
+ * Same argument rules as pkv_rope_append; there is no query and no rotated-key
+ * output.  Writes nothing but the T slots; a negative slot writes nothing.
+ */
+int pkv_prefill_kv(const void *k, const void *v, const int32_t *positions,
+                   const int64_t *slot_mapping, void *k_cache, void *v_cache, int32_t T,
+                   int32_t Hkv, int32_t d, int32_t num_blocks, float base, int32_t dtype,
+                   int32_t *dev_err_flag, void *stream);
 
 /* ======================================================================== */
 /* a3 + a4: split-KV paged GQA decode attention and its LSE merge            */

@@ -20,6 +20,11 @@ allocator must reproduce bit for bit:
   the length becomes ``L + 1``, which is the ``seq_len`` attention reads.
 * A request that needs more blocks than are free fails with ``OutOfBlocks`` and
   changes nothing.
+* ``seq_slots(seq_id, start, count)`` names where tokens ``[start, start+count)``
+  of a sequence live (position ``p``, slot ``table[p // 16] * 16 + p % 16``);
+  this is how a joiner's prefix, whose blocks ``join`` popped, is written (the
+  "chunked-prefill" path of helexa issue 121's engine, which our reading
+  turns into a cache write of the prefix keys and values).
 """
 import numpy as np
 
@@ -105,6 +110,20 @@ class BlockAllocatorModel:
             seq_lens[b] = pos + 1
             tables[b, :len(self.tables[s])] = self.tables[s]
         return positions, slots, seq_lens, tables
+
+    def seq_slots(self, seq_id, start, count):
+        """Positions and slots (int32, int64 numpy arrays) of tokens
+        ``[start, start+count)`` of a live sequence; they must lie within its
+        length."""
+        if seq_id not in self.tables:
+            raise UnknownSequence(seq_id)
+        if start < 0 or count < 0 or start + count > self.lengths[seq_id]:
+            raise ValueError("token range outside the sequence")
+        table = self.tables[seq_id]
+        positions = np.arange(start, start + count, dtype=np.int32)
+        slots = np.array([table[p // self.block_size] * self.block_size + p % self.block_size
+                          for p in range(start, start + count)], dtype=np.int64)
+        return positions, slots
 
     # -- inspection ---------------------------------------------------------
     def num_free(self):

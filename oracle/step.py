@@ -72,6 +72,30 @@ def decode_step(q, k_new, v_new, positions, slot_mapping, seq_lens, block_tables
     return result
 
 
+def prefill_kv(k, v, positions, slot_mapping, k_cache, v_cache, *, base, dtype,
+               block_size=16):
+    """Write the prefix keys and values of joining sequences into the cache.
+
+    Token t's raw key ``k[t] [Hkv,d]`` is rotated at ``positions[t]`` (the
+    same rotate-half RoPE and rounding to T as a decode step's new key: keys are
+    stored post-RoPE, helexa issue 121 slice 1) and written with ``v[t]`` to
+    slot ``slot_mapping[t]`` (a negative slot writes nothing).  Returns copies of
+    ``k_cache, v_cache``.
+    """
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    k_cache = np.array(k_cache, dtype=np.float64, copy=True)
+    v_cache = np.array(v_cache, dtype=np.float64, copy=True)
+    for t in range(k.shape[0]):
+        slot = int(slot_mapping[t])
+        if slot < 0:
+            continue
+        blk, row = divmod(slot, block_size)
+        k_cache[blk, :, row, :] = round_to(rope_rotate_half(k[t], positions[t], base), dtype)
+        v_cache[blk, :, row, :] = v[t]
+    return k_cache, v_cache
+
+
 def attend_rows(q_rot, k_cache, v_cache, block_tables, seq_lens, rows, *, scale,
                 attn_bias=None, block_size=16):
     """Float64 attention outputs (not rounded) for selected batch ``rows``.

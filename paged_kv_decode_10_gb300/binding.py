@@ -82,6 +82,7 @@ SIGNATURES = {
                                         _c_i32]),
     "pkv_seq_len": (ctypes.c_int, [_vp, _c_i32, _p_i32]),
     "pkv_seq_blocks": (ctypes.c_int, [_vp, _c_i32, _p_i32, _c_i32, _p_i32]),
+    "pkv_seq_slots": (ctypes.c_int, [_vp, _c_i32, _c_i32, _c_i32, _p_i32, _p_i64]),
     "pkv_num_free": (ctypes.c_int, [_vp, _p_i32]),
     "pkv_alloc_dump": (ctypes.c_int, [_vp, _p_i32, _c_i32, _p_i32]),
     "pkv_rope": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _c_i32, _c_i32, _c_i32, _c_i32,
@@ -91,6 +92,8 @@ SIGNATURES = {
                                        _vp, _vp]),
     "pkv_append": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _c_i32, _c_i32, _c_i32, _c_i32,
                                   _c_i32, _vp, _vp]),
+    "pkv_prefill_kv": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_i32, _c_i32, _c_i32,
+                                      _c_i32, ctypes.c_float, _c_i32, _vp, _vp]),
     "pkv_attn_default_parts": (ctypes.c_int, [_c_i32, _c_i32, _c_i32, _p_i32]),
     "pkv_attn_workspace_bytes": (ctypes.c_int, [_c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
                                                 ctypes.POINTER(_size_t)]),
@@ -218,6 +221,17 @@ class BlockAllocator:
                                         n.value, ctypes.byref(n)))
         return buf.tolist()
 
+    def seq_slots(self, seq_id, start, count, out=None):
+        """Positions and cache slots of tokens [start, start+count) of a live
+        sequence (``pkv_seq_slots``); ``out`` may supply the two arrays."""
+        if out is None:
+            out = (np.empty(count, np.int32), np.empty(count, np.int64))
+        pos, slots = out
+        _check(self._lib.pkv_seq_slots(self._h, int(seq_id), int(start), int(count),
+                                       _np_ptr(pos, ctypes.c_int32),
+                                       _np_ptr(slots, ctypes.c_int64)))
+        return pos, slots
+
     def num_free(self):
         n = ctypes.c_int32()
         _check(self._lib.pkv_num_free(self._h, ctypes.byref(n)))
@@ -307,6 +321,17 @@ def rope_append(q, k, v, positions, slot_mapping, k_cache, v_cache, base=10000.0
                                   _ptr(v_cache), B, Hq, k.shape[1], d, k_cache.shape[0],
                                   float(base), dtype_code(q), _ptr(err), _stream(stream)))
     return q_out, k_out
+
+
+def prefill_kv(k, v, positions, slot_mapping, k_cache, v_cache, base=10000.0, err=None,
+               stream=None):
+    """Prefix KV of joining sequences: rotate ``k [T,Hkv,d]`` at ``positions [T]``
+    and write it and ``v`` into ``slot_mapping [T]`` of the caches."""
+    T, Hkv, d = k.shape
+    _check(load().pkv_prefill_kv(_ptr(k), _ptr(v), _meta_ptr(positions),
+                                 _meta_ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache), T, Hkv,
+                                 d, k_cache.shape[0], float(base), dtype_code(k), _ptr(err),
+                                 _stream(stream)))
 
 
 def append(k_rot, v, slot_mapping, k_cache, v_cache, err=None, stream=None):

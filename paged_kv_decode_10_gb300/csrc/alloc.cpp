@@ -205,6 +205,26 @@ extern "C" int pkv_seq_blocks(const pkv_alloc *a, int32_t seq_id, int32_t *out, 
   return PKV_OK;
 }
 
+extern "C" int pkv_seq_slots(const pkv_alloc *a, int32_t seq_id, int32_t start, int32_t count,
+                             int32_t *positions, int64_t *slot_mapping) {
+  pkv::clear_error();
+  PKV_REQUIRE(a, PKV_ERR_INVALID_ARG, "NULL allocator");
+  PKV_REQUIRE(a->is_live(seq_id), PKV_ERR_UNKNOWN_SEQ, "sequence %d is not live", seq_id);
+  PKV_REQUIRE(start >= 0 && count >= 0, PKV_ERR_INVALID_ARG, "negative start or count");
+  const int32_t len = a->lengths[seq_id];
+  PKV_REQUIRE(static_cast<int64_t>(start) + count <= len, PKV_ERR_INVALID_ARG,
+              "tokens [%d, %d) exceed the sequence length %d", start, start + count, len);
+  if (count == 0) return PKV_OK;
+  PKV_REQUIRE(positions && slot_mapping, PKV_ERR_INVALID_ARG, "NULL output");
+  const int32_t *t = a->table(seq_id);
+  for (int32_t i = 0; i < count; ++i) {
+    const int32_t p = start + i;
+    positions[i] = p;
+    slot_mapping[i] = static_cast<int64_t>(t[p / kBlock]) * kBlock + p % kBlock;
+  }
+  return PKV_OK;
+}
+
 extern "C" int pkv_num_free(const pkv_alloc *a, int32_t *n) {
   pkv::clear_error();
   PKV_REQUIRE(a && n, PKV_ERR_INVALID_ARG, "NULL argument");

@@ -122,9 +122,11 @@ __global__ void rope_kernel(const T *__restrict__ q, const T *__restrict__ k,
     for (int e = 0; e < VEC; ++e) rope_rotate(x1[e], x2[e], cs[c + e], cs[half + c + e], &y1[e], &y2[e]);
     const W o1 = pack<T, VEC>(y1), o2 = pack<T, VEC>(y2);
     T *dst = h < Hq ? q_out + (static_cast<size_t>(b) * Hq + h) * d
-                    : k_out + (static_cast<size_t>(b) * Hkv + (h - Hq)) * d;
-    *reinterpret_cast<W *>(dst + c) = o1;
-    *reinterpret_cast<W *>(dst + half + c) = o2;
+                    : (k_out ? k_out + (static_cast<size_t>(b) * Hkv + (h - Hq)) * d : nullptr);
+    if (dst) {   // a prefill does not report the rotated keys
+      *reinterpret_cast<W *>(dst + c) = o1;
+      *reinterpret_cast<W *>(dst + half + c) = o2;
+    }
     if (APPEND && slot >= 0 && h >= Hq) {
       T *cdst = k_cache + row0 + static_cast<size_t>(h - Hq) * kBlockTokens * d;
       *reinterpret_cast<W *>(cdst + c) = o1;
@@ -187,15 +189,15 @@ void launch_rope(int B, int threads, size_t smem, cudaStream_t s, const void *q,
 int rope_launch(const void *q, const void *k, const void *v, void *q_out, void *k_out,
                 const int32_t *positions, const int64_t *slots, void *k_cache, void *v_cache,
                 int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int32_t num_blocks, float base,
-                int32_t dtype, int32_t *err, void *stream, bool append) {
+                int32_t dtype, int32_t *err, void *stream, bool append, bool k_out_optional = false) {
   PKV_REQUIRE(B >= 0 && Hq >= 0 && Hkv >= 0, PKV_ERR_INVALID_ARG, "negative size");
   PKV_REQUIRE(d >= 2 && d <= 2 * kMaxHalf && d % 2 == 0, PKV_ERR_UNSUPPORTED, "head_dim %d", d);
   PKV_REQUIRE(dtype_ok(dtype), PKV_ERR_UNSUPPORTED, "dtype %d", dtype);
   PKV_REQUIRE(base > 0.0f, PKV_ERR_INVALID_ARG, "rope base must be positive");
   if (B == 0 || Hq + Hkv == 0) return PKV_OK;
   PKV_REQUIRE(positions, PKV_ERR_INVALID_ARG, "positions is NULL");
-  PKV_REQUIRE((Hq == 0 || (q && q_out)) && (Hkv == 0 || (k && k_out)), PKV_ERR_INVALID_ARG,
-              "NULL tensor");
+  PKV_REQUIRE((Hq == 0 || (q && q_out)) && (Hkv == 0 || (k && (k_out || k_out_optional))),
+              PKV_ERR_INVALID_ARG, "NULL tensor");
   const int elem = static_cast<int>(dtype_size(dtype));
   const int vec = (d % 8 == 0) ? 4 : 1;
   if (vec == 4)
@@ -263,6 +265,17 @@ extern "C" int pkv_rope_append(const void *q, const void *k, const void *v, void
   clear_error();
   return rope_launch(q, k, v, q_out, k_out, positions, slot_mapping, k_cache, v_cache, B, Hq, Hkv,
                      d, num_blocks, base, dtype, dev_err_flag, stream, true);
+}
+
+extern "C" int pkv_prefill_kv(const void *k, const void *v, const int32_t *positions,
+                              const int64_t *slot_mapping, void *k_cache, void *v_cache, int32_t T,
+                              int32_t Hkv, int32_t d, int32_t num_blocks, float base,
+                              int32_t dtype, int32_t *dev_err_flag, void *stream) {
+  clear_error();
+  // the decode-step kernel with no query heads and no rotated-key report: every
+  // token's key is rotated and stored exactly as a decode append would store it
+  return rope_launch(nullptr, k, v, nullptr, nullptr, positions, slot_mapping, k_cache, v_cache, T,
+                     0, Hkv, d, num_blocks, base, dtype, dev_err_flag, stream, true, true);
 }
 
 extern "C" int pkv_append(const void *k_rot, const void *v, const int64_t *slot_mapping,

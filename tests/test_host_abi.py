@@ -128,6 +128,13 @@ def test_cpp_allocator_matches_model_under_churn(host_lib, seed):
         for s in live:
             assert cpp.seq_blocks(s) == model.seq_blocks(s)
             assert cpp.seq_len(s) == model.seq_len(s)
+            L = model.seq_len(s)
+            if L:
+                start = int(r.integers(0, L))
+                count = int(r.integers(0, L - start + 1))
+                for a_, b_ in zip(model.seq_slots(s, start, count),
+                                  cpp.seq_slots(s, start, count)):
+                    np.testing.assert_array_equal(a_, b_)
 
 
 def test_cpp_allocator_rejects_bad_input(host_lib):
@@ -144,4 +151,10 @@ def test_cpp_allocator_rejects_bad_input(host_lib):
         a.join(33)                                            # wider than a table
     with pytest.raises(binding.UnknownSequence):
         a.leave(5)
+    with pytest.raises(binding.PkvError):
+        a.seq_slots(s, 2, 2)                                  # beyond the length
+    with pytest.raises(binding.PkvError):
+        a.seq_slots(s, -1, 1)
+    with pytest.raises(binding.UnknownSequence):
+        a.seq_slots(1, 0, 1)
     assert a.seq_len(s) == 3 and a.num_free() == 7

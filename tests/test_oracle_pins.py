@@ -18,7 +18,7 @@ from oracle.allocator import BlockAllocatorModel, OutOfBlocks, UnknownSequence
 from oracle.attention import decode_attention_row, gather_sequence, softmax_attention
 from oracle.numerics import round_to_bf16, round_to_f32
 from oracle.rope import rope_rotate_half
-from oracle.step import decode_step
+from oracle.step import decode_step, prefill_kv
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 rng = np.random.default_rng(12345)
@@ -409,3 +409,58 @@ def test_allocator_model_conservation_under_churn():
         assert sorted(owned + a.free) == list(range(nb))
         for s in live:
             assert len(a.seq_blocks(s)) == -(-a.seq_len(s) // 16)
+
+
+def test_allocator_model_prefix_slots_hand_derived():
+    """join(20) on the free stack [5,3,0,1,4,2] (bottom to top) pops 2 then 4, so
+    tokens 14..17 live in block 2 rows 14, 15 and block 4 rows 0, 1."""
+    a = BlockAllocatorModel(6, initial_free=[5, 3, 0, 1, 4, 2])
+    sid = a.join(20)
+    pos, slots = a.seq_slots(sid, 14, 4)
+    assert pos.tolist() == [14, 15, 16, 17]
+    assert slots.tolist() == [46, 47, 64, 65]
+    with pytest.raises(ValueError):
+        a.seq_slots(sid, 18, 3)
+
+
+def test_allocator_model_slots_equal_those_of_decode_appends():
+    """The slot the model names for token p is the slot a decode step assigned
+    when it appended token p."""
+    r = np.random.default_rng(7)
+    a = BlockAllocatorModel(64, initial_free=r.permutation(64))
+    s1, s2 = a.join(0), a.join(5)
+    seen = {s1: [], s2: []}
+    for _ in range(40):
+        _, slots, _, _ = a.prepare_step([s2, s1], 8)
+        seen[s2].append(int(slots[0]))
+        seen[s1].append(int(slots[1]))
+    assert a.seq_slots(s1, 0, 40)[1].tolist() == seen[s1]
+    assert a.seq_slots(s2, 5, 40)[1].tolist() == seen[s2]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_prefill_equals_token_by_token_decode_appends(dtype):
+    """Writing a prefix in one prefill leaves the cache exactly as appending its
+    tokens one decode step at a time does (same rotation, same rounding)."""
+    r = np.random.default_rng(3)
+    nb, hkv, d, n = 8, 2, 16, 37
+    rnd = round_to_f32 if dtype == "f32" else round_to_bf16
+    k = rnd(r.standard_normal((n, hkv, d)))
+    v = rnd(r.standard_normal((n, hkv, d)))
+    kc0 = rnd(r.standard_normal((nb, hkv, 16, d)))
+    vc0 = rnd(r.standard_normal((nb, hkv, 16, d)))
+    a = BlockAllocatorModel(nb, initial_free=r.permutation(nb))
+    sid = a.join(n)
+    pos, slots = a.seq_slots(sid, 0, n)
+    kc, vc = prefill_kv(k, v, pos, slots, kc0, vc0, base=10000.0, dtype=dtype)
+    kd, vd = kc0, vc0
+    for t in range(n):
+        res = decode_step(np.zeros((1, hkv, d)), k[t:t + 1], v[t:t + 1], pos[t:t + 1],
+                          slots[t:t + 1], np.array([t + 1]), np.array([a.seq_blocks(sid)]),
+                          kd, vd, scale=1.0, base=10000.0, dtype=dtype)
+        kd, vd = res["k_cache"], res["v_cache"]
+    np.testing.assert_array_equal(kc, kd)
+    np.testing.assert_array_equal(vc, vd)
+    untouched = np.ones(nb, bool)
+    untouched[a.seq_blocks(sid)] = False
+    np.testing.assert_array_equal(kc[untouched], kc0[untouched])
