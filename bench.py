@@ -62,6 +62,9 @@ def parse_args():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-flush", action="store_true")
+    ap.add_argument("--layers", type=int, default=1,
+                    help="layers per step, each with its own KV pool under the same block "
+                         "tables (one graph per step)")
     ap.add_argument("--metadata", default="mapped", choices=["copy", "mapped"],
                     help="per-step metadata: copied to the device, or read in place from "
                          "pinned host memory")
@@ -230,20 +233,34 @@ def host_cores():
 # ---------------------------------------------------------------------------
 # the GPU arm
 # ---------------------------------------------------------------------------
-def setup(w, device, parts, flags, steps_total, metadata):
+def setup(w, device, parts, flags, steps_total, metadata, n_layers=1):
     import torch
     from paged_kv_decode_10_gb300 import engine, workloads
     pool_bytes = w.num_blocks * w.Hkv * 16 * w.d * (2 if w.dtype == "bf16" else 4)
     gen_dev = "cpu" if pool_bytes < (1 << 30) else device
     k_cache, v_cache = workloads.make_caches(w, gen_dev)
     bt = w.max_blocks_per_seq(extra_tokens=steps_total + 64)
+    if n_layers > 1:
+        # every layer's pool starts as a copy of the same synthetic cache
+        kd, vd = k_cache.to(device), v_cache.to(device)
+        k_dev = kd.unsqueeze(0).expand(n_layers, *kd.shape).contiguous()
+        v_dev = vd.unsqueeze(0).expand(n_layers, *vd.shape).contiguous()
+        del kd, vd
+    else:
+        k_dev, v_dev = k_cache.to(device), v_cache.to(device)
     dec = engine.PagedDecoder(w.num_blocks, w.Hq, w.Hkv, w.d, w.dtype, w.B, bt,
                               initial_free=w.free_order, device=device,
                               num_parts=parts or None, flags=flags,
-                              k_cache=k_cache.to(device), v_cache=v_cache.to(device),
-                              metadata=metadata)
+                              k_cache=k_dev, v_cache=v_dev, metadata=metadata,
+                              n_layers=n_layers)
     ids = [dec.join(int(L)) for L in w.seq_lens]
-    tokens = [workloads.make_new_tokens(w, s, device) for s in range(steps_total)]
+    if n_layers == 1:
+        tokens = [workloads.make_new_tokens(w, s, device) for s in range(steps_total)]
+    else:
+        tokens = []
+        for s in range(steps_total):
+            per = [workloads.make_new_tokens(w, s * n_layers + l, device) for l in range(n_layers)]
+            tokens.append(tuple(torch.stack([t[i] for t in per]) for i in range(3)))
     return dec, ids, tokens, (k_cache, v_cache) if gen_dev == "cpu" else None
 
 
@@ -256,7 +273,7 @@ def run_gpu(args, rank, world):
     w = workloads.make_workload(args.workload)
     W, K, GW = args.warmup, args.steps, 2
     dec, ids, tokens, cpu_caches = setup(w, device, args.parts, args.flags, W + GW + K + 1,
-                                          args.metadata)
+                                          args.metadata, args.layers)
     assert dec.bt_stride * 16 >= int(w.seq_lens.max()) + W + GW + K + 64
     B = len(ids)
     elem = 2 if w.dtype == "bf16" else 4
@@ -273,7 +290,7 @@ def run_gpu(args, rank, world):
 
     oracle_state = None
     if not args.no_cpu and rank == 0 and cpu_caches is not None:
-        oracle_state = (cpu_caches, [t.cpu() for t in tokens[0]])
+        oracle_state = (cpu_caches, [(t[0] if args.layers > 1 else t).cpu() for t in tokens[0]])
 
     churn_s = []
     prefill_log = []     # (tokens, start event, end event) per churn step
@@ -312,11 +329,13 @@ def run_gpu(args, rank, world):
         flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        binding.prefill_kv(pre_k[:n], pre_v[:n], pre_pos[:n], pre_slot[:n], dec.k_cache,
-                           dec.v_cache, base=dec.rope_base, err=dec.err, stream=stream)
+        for layer in range(dec.n_layers):
+            binding.prefill_kv(pre_k[:n], pre_v[:n], pre_pos[:n], pre_slot[:n],
+                               dec.k_caches[layer], dec.v_caches[layer], base=dec.rope_base,
+                               err=dec.err, stream=stream)
         e1.record(stream)
         pre_done[0] = e1
-        prefill_log.append((s, n, e0, e1))
+        prefill_log.append((s, n * dec.n_layers, e0, e1))
 
     # warm-up: eager steps through the C ABI (one pkv_decode_step call each)
     meta0 = None
@@ -331,9 +350,14 @@ def run_gpu(args, rank, world):
 
     def stage(s):
         q, k, v = tokens[s]
-        dec.q_in[:B].copy_(q)
-        dec.k_in[:B].copy_(k)
-        dec.v_in[:B].copy_(v)
+        if args.layers > 1:
+            dec.q_ins[:, :B].copy_(q)
+            dec.k_ins[:, :B].copy_(k)
+            dec.v_ins[:, :B].copy_(v)
+        else:
+            dec.q_in[:B].copy_(q)
+            dec.k_in[:B].copy_(k)
+            dec.v_in[:B].copy_(v)
 
     for s in range(W, W + GW):
         churn(s)
@@ -376,7 +400,10 @@ def run_gpu(args, rank, world):
     # step's kernels (RoPE/append + attention) without the host side; each is
     # captured once so that no host launch time falls between the events.
     # Re-running the final step is idempotent (the same token re-appended).
-    step_args = dec.step_args(B, dec.q_in[:B], dec.k_in[:B], dec.v_in[:B])
+    if args.layers > 1:
+        step_args = dec.layer_args(B, dec.q_ins[:, :B], dec.k_ins[:, :B], dec.v_ins[:, :B])
+    else:
+        step_args = dec.step_args(B, dec.q_in[:B], dec.k_in[:B], dec.v_in[:B])
     cap = torch.cuda.Stream(device)
     cap.wait_stream(stream)
     attn_graph, kern_graph = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
@@ -386,7 +413,10 @@ def run_gpu(args, rank, world):
                                  workspace=dec.workspace, out=dec.out[:B], flags=dec.flags,
                                  err=dec.err, stream=cap)
     with torch.cuda.graph(kern_graph, stream=cap):
-        binding.decode_step_args(step_args, cap)
+        if args.layers > 1:
+            binding.decode_step_layers(step_args, cap)
+        else:
+            binding.decode_step_args(step_args, cap)
     stream.wait_stream(cap)
 
     def time_graph(g):
@@ -403,8 +433,9 @@ def run_gpu(args, rank, world):
     kern_ms = time_graph(kern_graph)
     last_lens = lens_after[-1]
 
-    bytes_steps = [attn_bytes(la, w.Hq, w.Hkv, w.d, elem) for la in lens_after]
-    kv_only = [int(np.asarray(la, np.int64).sum()) * w.Hkv * w.d * 2 * elem for la in lens_after]
+    bytes_steps = [args.layers * attn_bytes(la, w.Hq, w.Hkv, w.d, elem) for la in lens_after]
+    kv_only = [args.layers * int(np.asarray(la, np.int64).sum()) * w.Hkv * w.d * 2 * elem
+               for la in lens_after]
     total_bytes = sum(bytes_steps) * world
     value = total_bytes / total_s / 1e9
     attn_b = attn_bytes(last_lens, w.Hq, w.Hkv, w.d, elem)
@@ -428,7 +459,8 @@ def run_gpu(args, rank, world):
         "dtype": w.dtype,
         "data": "synthetic (seeded N(0,1) q/k/v and KV pool; seeded ragged lengths and "
                 "scattered block tables)",
-        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.d,
+        "config": {"workload": w.name, "layers": args.layers, "B": w.B, "Hq": w.Hq,
+                   "Hkv": w.Hkv, "head_dim": w.d,
                    "block_size": 16, "mean_kv_len": float(np.mean(lens_after[0])),
                    "pool_blocks": w.num_blocks, "num_parts": dec.num_parts,
                    "consumer": "simt" if (args.flags & 1 or w.dtype == "f32") else "mma.sync",
@@ -438,7 +470,9 @@ def run_gpu(args, rank, world):
                        "one kernel (RoPE, append, split-KV attention, LSE merge)"
                        if args.flags & 4 else
                        "RoPE/append kernel + split-KV attention kernel with fused LSE merge "
-                       "(programmatic dependent launch)"),
+                       "(programmatic dependent launch)") + (
+                       f", for each of {args.layers} layers (each layer's kernels launched as "
+                       "dependents of the previous layer's)" if args.layers > 1 else ""),
                    "l2": "flushed before every timed step" if not args.no_flush else "not flushed",
                    "parallelism": "replicas" if world > 1 else "single-gpu"},
         "steps_per_s": round(K / (sum(step_ms) / 1e3), 1),
@@ -457,7 +491,8 @@ def run_gpu(args, rank, world):
         "step_kernels_us": round(1e3 * statistics.mean(kern_ms), 3),
         "prefill": prefill_summary([x[1:] for x in prefill_log if x[0] >= W + GW], w, elem,
                                    peak),
-        "gpu_launches": K * ((1 if args.flags & 4 else 2) + (1 if args.flags & 2 else 0)),
+        "gpu_launches": K * args.layers * ((1 if args.flags & 4 else 2) +
+                                           (1 if args.flags & 2 else 0)),
         "clocks": clocks,
     }
     return result, dec, ids, tokens, oracle_state, meta0, w
@@ -621,7 +656,7 @@ def main():
     build.build()
     result, dec, ids, tokens, oracle_state, meta0, w = run_gpu(args, rank, world)
     if rank == 0:
-        if not args.no_e2e:
+        if not args.no_e2e and args.layers == 1:
             result["e2e"] = run_e2e(args, dec, ids, tokens, w)
         if not args.no_cpu and oracle_state is not None and world == 1:
             result["cpu_baseline"] = cpu_baseline(w, oracle_state, meta0, args.cpu_seconds)

@@ -133,6 +133,11 @@ int pkv_seq_blocks(const pkv_alloc *a, int32_t seq_id, int32_t *out, int32_t cap
 int pkv_seq_slots(const pkv_alloc *a, int32_t seq_id, int32_t start, int32_t count,
                   int32_t *positions, int64_t *slot_mapping);
 int pkv_num_free(const pkv_alloc *a, int32_t *n);
+/* Pool auto-sizing ("neurogrid releases" v0.7.0: the pool is sized from the
+ * VRAM budget): the number of 16-token blocks whose K and V, for every KV head
+ * and every one of n_layers layers, fit in budget_bytes (floor; host only). */
+int pkv_pool_blocks(uint64_t budget_bytes, int32_t n_layers, int32_t Hkv, int32_t d,
+                    int32_t dtype, int32_t *num_blocks);
 /* Copies the free stack bottom-to-top (up to cap entries); *n = its size. */
 int pkv_alloc_dump(const pkv_alloc *a, int32_t *free_stack, int32_t cap, int32_t *n);
 
@@ -325,6 +330,21 @@ typedef struct pkv_step_args {
  * rotated q and k.  Each row's slot must be its position seq_len-1 in its own
  * blocks, as pkv_prepare_step produces. */
 int pkv_decode_step(const pkv_step_args *args, void *stream);
+
+/*
+ * A decode step through n_layers layers, each with its own caches
+ * ("neurogrid releases" v0.7.0: per-layer caches; the block tables, slots,
+ * positions and lengths are the same for every layer, so layers[l] differ in
+ * q, k, v, q_rot, k_rot, k_cache, v_cache, out and workspace).  Layer l runs
+ * after layer l-1 on `stream`: its RoPE/append kernel is launched as a
+ * programmatic dependent of layer l-1's attention kernel (its angles are
+ * formed early; its q/k/v reads and cache writes wait for that kernel), and
+ * its attention kernel as a dependent of its RoPE/append kernel, so each
+ * layer's start overlaps the previous layer's tail.  Consecutive layers must
+ * not share a workspace (two alternating workspaces suffice).
+ * PKV_STEP_FUSED is rejected.  Stops at the first failing layer.
+ */
+int pkv_decode_step_layers(const pkv_step_args *layers, int32_t n_layers, void *stream);
 
 /* The address under which kernels read the page-locked host buffer at
  * host_ptr (allocated pinned, or registered with the mapped flag), so that the

@@ -84,6 +84,7 @@ SIGNATURES = {
     "pkv_seq_blocks": (ctypes.c_int, [_vp, _c_i32, _p_i32, _c_i32, _p_i32]),
     "pkv_seq_slots": (ctypes.c_int, [_vp, _c_i32, _c_i32, _c_i32, _p_i32, _p_i64]),
     "pkv_num_free": (ctypes.c_int, [_vp, _p_i32]),
+    "pkv_pool_blocks": (ctypes.c_int, [ctypes.c_uint64, _c_i32, _c_i32, _c_i32, _c_i32, _p_i32]),
     "pkv_alloc_dump": (ctypes.c_int, [_vp, _p_i32, _c_i32, _p_i32]),
     "pkv_rope": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _c_i32, _c_i32, _c_i32, _c_i32,
                                 ctypes.c_float, _c_i32, _vp]),
@@ -109,6 +110,7 @@ SIGNATURES = {
                                      _c_i32, _c_i32, _vp, _c_i32, _vp]),
     "pkv_decode_step": (ctypes.c_int, [ctypes.POINTER(StepArgs), _vp]),
     "pkv_mapped_pointer": (ctypes.c_int, [_vp, ctypes.POINTER(_vp)]),
+    "pkv_decode_step_layers": (ctypes.c_int, [ctypes.POINTER(StepArgs), _c_i32, _vp]),
     "pkv_decode_step_host": (ctypes.c_int, [ctypes.POINTER(StepArgs),
                                             ctypes.POINTER(StepHostIO), _vp]),
 }
@@ -448,6 +450,29 @@ def make_step_args(q, k, v, q_rot, k_rot, k_cache, v_cache, positions, slot_mapp
 def decode_step_args(args, stream=None):
     """Runs a1 -> a4 from a prepared ``StepArgs``."""
     _check(load().pkv_decode_step(ctypes.byref(args), _stream(stream)))
+
+
+def layer_args_array(layers):
+    """A ctypes array of ``StepArgs``, one per layer, for ``decode_step_layers``."""
+    arr = (StepArgs * len(layers))()
+    for i, a in enumerate(layers):
+        arr[i] = a
+    return arr
+
+
+def decode_step_layers(layers, stream=None):
+    """One decode step through every layer (``pkv_decode_step_layers``);
+    ``layers`` is a list of ``StepArgs`` or an array from ``layer_args_array``."""
+    arr = layers if isinstance(layers, ctypes.Array) else layer_args_array(layers)
+    _check(load().pkv_decode_step_layers(arr, len(arr), _stream(stream)))
+
+
+def pool_blocks(budget_bytes, n_layers, Hkv, d, dtype):
+    """Blocks of a K/V pool for ``n_layers`` layers that fit in ``budget_bytes``."""
+    n = ctypes.c_int32()
+    _check(load().pkv_pool_blocks(int(budget_bytes), int(n_layers), int(Hkv), int(d),
+                                  int(dtype), ctypes.byref(n)))
+    return n.value
 
 
 def decode_step_host(args, host_io, stream=None):

@@ -225,6 +225,20 @@ extern "C" int pkv_seq_slots(const pkv_alloc *a, int32_t seq_id, int32_t start, 
   return PKV_OK;
 }
 
+extern "C" int pkv_pool_blocks(uint64_t budget_bytes, int32_t n_layers, int32_t Hkv, int32_t d,
+                               int32_t dtype, int32_t *num_blocks) {
+  pkv::clear_error();
+  PKV_REQUIRE(num_blocks, PKV_ERR_INVALID_ARG, "NULL output");
+  PKV_REQUIRE(n_layers > 0 && Hkv > 0 && d > 0, PKV_ERR_INVALID_ARG, "non-positive size");
+  PKV_REQUIRE(dtype == PKV_F32 || dtype == PKV_BF16, PKV_ERR_UNSUPPORTED, "dtype %d", dtype);
+  // one block = 16 tokens of K and of V, all KV heads, every layer
+  const uint64_t per_block = static_cast<uint64_t>(n_layers) * 2u * static_cast<uint64_t>(Hkv) *
+                             kBlock * static_cast<uint64_t>(d) * (dtype == PKV_BF16 ? 2u : 4u);
+  const uint64_t n = budget_bytes / per_block;
+  *num_blocks = n > static_cast<uint64_t>(INT32_MAX) ? INT32_MAX : static_cast<int32_t>(n);
+  return PKV_OK;
+}
+
 extern "C" int pkv_num_free(const pkv_alloc *a, int32_t *n) {
   pkv::clear_error();
   PKV_REQUIRE(a && n, PKV_ERR_INVALID_ARG, "NULL argument");

@@ -85,7 +85,7 @@ struct TmapKey {
 };
 
 struct TmapCache {
-  static constexpr int kN = 16;
+  static constexpr int kN = 128;   // a K and a V map per layer of a deep model
   std::mutex mu;
   TmapKey key[kN];
   CUtensorMap map[kN];
@@ -405,6 +405,56 @@ extern "C" int pkv_decode_step(const pkv_step_args *a, void *stream) {
   return pkv_lse_merge(a->workspace, a->workspace_bytes, a->seq_lens, a->bt_stride,
                        a->attn_bias ? a->bias_stride : 0, a->B, a->Hq, a->Hkv, a->d, num_parts,
                        a->out, a->dtype, stream);
+}
+
+extern "C" int pkv_decode_step_layers(const pkv_step_args *layers, int32_t n_layers,
+                                      void *stream) {
+  clear_error();
+  PKV_REQUIRE(n_layers >= 0 && (layers || n_layers == 0), PKV_ERR_INVALID_ARG,
+              "bad layer list");
+  for (int32_t l = 0; l < n_layers; ++l) {   // checked before anything is launched
+    PKV_REQUIRE(!(layers[l].flags & PKV_STEP_FUSED), PKV_ERR_UNSUPPORTED,
+                "PKV_STEP_FUSED is a single-layer form");
+    if (l > 0)
+      PKV_REQUIRE(layers[l].workspace != layers[l - 1].workspace, PKV_ERR_INVALID_ARG,
+                  "layers %d and %d share a workspace", l - 1, l);
+  }
+  for (int32_t l = 0; l < n_layers; ++l) {
+    const pkv_step_args *a = &layers[l];
+    int num_parts = a->num_parts;
+    int rc;
+    if (num_parts <= 0 && a->B > 0) {
+      rc = check_shapes(a->B, a->Hq, a->Hkv, a->d, a->dtype);
+      if (rc != PKV_OK) return rc;
+      rc = default_parts(a->d, a->dtype, a->flags, a->Hq / a->Hkv, &num_parts);
+      if (rc != PKV_OK) return rc;
+    }
+    if (l == 0) {
+      rc = pkv_rope_append(a->q, a->k, a->v, a->q_rot, a->k_rot, a->positions, a->slot_mapping,
+                           a->k_cache, a->v_cache, a->B, a->Hq, a->Hkv, a->d, a->num_blocks,
+                           a->rope_base, a->dtype, a->dev_err_flag, stream);
+    } else {
+      clear_error();
+      rc = rope_append_dependent(a->q, a->k, a->v, a->q_rot, a->k_rot, a->positions,
+                                 a->slot_mapping, a->k_cache, a->v_cache, a->B, a->Hq, a->Hkv,
+                                 a->d, a->num_blocks, a->rope_base, a->dtype, a->dev_err_flag,
+                                 stream);
+    }
+    if (rc != PKV_OK) return rc;
+    rc = pkv_decode_attn_split(a->q_rot, a->k_cache, a->v_cache, a->num_blocks, a->block_tables,
+                               a->bt_stride, a->seq_lens, a->attn_bias, a->bias_stride, a->B,
+                               a->Hq, a->Hkv, a->d, a->scale, num_parts, a->workspace,
+                               a->workspace_bytes, a->out, a->dtype, a->flags, a->dev_err_flag,
+                               stream);
+    if (rc != PKV_OK) return rc;
+    if (a->flags & PKV_ATTN_SEPARATE_MERGE) {
+      rc = pkv_lse_merge(a->workspace, a->workspace_bytes, a->seq_lens, a->bt_stride,
+                         a->attn_bias ? a->bias_stride : 0, a->B, a->Hq, a->Hkv, a->d, num_parts,
+                         a->out, a->dtype, stream);
+      if (rc != PKV_OK) return rc;
+    }
+  }
+  return PKV_OK;
 }
 
 extern "C" int pkv_mapped_pointer(const void *host_ptr, void **device_ptr) {

@@ -827,6 +827,10 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
   const int warp = tid >> 5, lane = tid & 31;
   const int C = p.num_parts;
   const bool has_bias = p.bias != nullptr;
+  // a kernel launched after this one as a programmatic dependent (the next
+  // layer's RoPE/append) may start now; it waits for this grid before it reads
+  // anything this grid produces
+  if (!FUSE) pdl_launch_dependents();
 
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {

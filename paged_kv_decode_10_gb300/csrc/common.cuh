@@ -200,4 +200,13 @@ __device__ __forceinline__ void set_dev_err(int32_t *flag, int bits) {
   if (flag) atomicOr(flag, bits);
 }
 
+// pkv_rope_append launched as a programmatic dependent of the kernel before it
+// on the stream (a previous layer's attention): its q/k/v reads and cache
+// writes wait for that kernel (rope_append.cu).
+int rope_append_dependent(const void *q, const void *k, const void *v, void *q_out, void *k_out,
+                          const int32_t *positions, const int64_t *slot_mapping, void *k_cache,
+                          void *v_cache, int32_t B, int32_t Hq, int32_t Hkv, int32_t d,
+                          int32_t num_blocks, float base, int32_t dtype, int32_t *dev_err_flag,
+                          void *stream);
+
 }  // namespace pkv

@@ -59,8 +59,11 @@ __device__ __forceinline__ typename Vec<T, VEC>::type pack(const float (&x)[VEC]
 // issued in one round.  Items: VEC consecutive rotation pairs of one head of q
 // or k ((Hq + Hkv) * half / VEC of them) and, with APPEND, 16-byte chunks of
 // the row's values (copied into the cache slot).  cos/sin of the row's
-// position are built first in shared memory.
-template <typename T, int VEC, bool APPEND>
+// position are built first in shared memory.  DEP: launched as a programmatic
+// dependent of the previous layer's attention kernel; the new q/k/v are that
+// layer's product, so they are read only after griddepcontrol.wait (the
+// angles are formed before it).
+template <typename T, int VEC, bool APPEND, bool DEP>
 __global__ void rope_kernel(const T *__restrict__ q, const T *__restrict__ k,
                             const T *__restrict__ v, T *__restrict__ q_out,
                             T *__restrict__ k_out, const int32_t *__restrict__ positions,
@@ -88,20 +91,29 @@ __global__ void rope_kernel(const T *__restrict__ q, const T *__restrict__ k,
   if (rot) {
     h = tid / (half / VEC);
     c = (tid - h * (half / VEC)) * VEC;
-    const T *src = h < Hq ? q + (static_cast<size_t>(b) * Hq + h) * d
-                          : k + (static_cast<size_t>(b) * Hkv + (h - Hq)) * d;
-    x1w = *reinterpret_cast<const W *>(src + c);
-    x2w = *reinterpret_cast<const W *>(src + half + c);
   }
   uint4 vw{};
   const bool vcopy = APPEND && tid < v_chunks;
-  if (vcopy) vw = reinterpret_cast<const uint4 *>(v + static_cast<size_t>(b) * Hkv * d)[tid];
+  auto load_inputs = [&]() {
+    if (rot) {
+      const T *src = h < Hq ? q + (static_cast<size_t>(b) * Hq + h) * d
+                            : k + (static_cast<size_t>(b) * Hkv + (h - Hq)) * d;
+      x1w = *reinterpret_cast<const W *>(src + c);
+      x2w = *reinterpret_cast<const W *>(src + half + c);
+    }
+    if (vcopy) vw = reinterpret_cast<const uint4 *>(v + static_cast<size_t>(b) * Hkv * d)[tid];
+  };
+  if constexpr (!DEP) load_inputs();
 
   for (int i = tid; i < half; i += blockDim.x) {
     float s, co;
     rope_cossin(pos, turns.f[i], &co, &s);
     cs[i] = co;
     cs[half + i] = s;
+  }
+  if constexpr (DEP) {
+    pdl_wait();
+    load_inputs();
   }
   if (APPEND && slot >= num_slots) {
     if (tid == 0) set_dev_err(err, PKV_DEVERR_BAD_SLOT);
@@ -175,21 +187,43 @@ template <typename T, int VEC, bool APPEND>
 void launch_rope(int B, int threads, size_t smem, cudaStream_t s, const void *q, const void *k,
                  const void *v, void *q_out, void *k_out, const int32_t *positions,
                  const int64_t *slots, void *k_cache, void *v_cache, int Hq, int Hkv, int d,
-                 int64_t num_slots, int32_t *err, const RopeTurns &turns) {
-  // same L1/shared split as the attention kernel that follows, so the SMs need
-  // no reconfiguration between the two launches of a step
-  cudaFuncSetAttribute(rope_kernel<T, VEC, APPEND>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                 int64_t num_slots, int32_t *err, const RopeTurns &turns, bool dependent) {
+  if (!dependent) {
+    // same L1/shared split as the attention kernel that follows, so the SMs
+    // need no reconfiguration between the two launches of a step
+    cudaFuncSetAttribute(rope_kernel<T, VEC, APPEND, false>,
+                         cudaFuncAttributePreferredSharedMemoryCarveout,
+                         cudaSharedmemCarveoutMaxShared);
+    rope_kernel<T, VEC, APPEND, false><<<B, threads, smem, s>>>(
+        static_cast<const T *>(q), static_cast<const T *>(k), static_cast<const T *>(v),
+        static_cast<T *>(q_out), static_cast<T *>(k_out), positions, slots,
+        static_cast<T *>(k_cache), static_cast<T *>(v_cache), Hq, Hkv, d, num_slots, err, turns);
+    return;
+  }
+  auto kern = rope_kernel<T, VEC, APPEND, true>;
+  cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                        cudaSharedmemCarveoutMaxShared);
-  rope_kernel<T, VEC, APPEND><<<B, threads, smem, s>>>(
-      static_cast<const T *>(q), static_cast<const T *>(k), static_cast<const T *>(v),
-      static_cast<T *>(q_out), static_cast<T *>(k_out), positions, slots,
-      static_cast<T *>(k_cache), static_cast<T *>(v_cache), Hq, Hkv, d, num_slots, err, turns);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(B);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, kern, static_cast<const T *>(q), static_cast<const T *>(k),
+                     static_cast<const T *>(v), static_cast<T *>(q_out), static_cast<T *>(k_out),
+                     positions, slots, static_cast<T *>(k_cache), static_cast<T *>(v_cache), Hq,
+                     Hkv, d, num_slots, err, turns);
 }
 
 int rope_launch(const void *q, const void *k, const void *v, void *q_out, void *k_out,
                 const int32_t *positions, const int64_t *slots, void *k_cache, void *v_cache,
                 int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int32_t num_blocks, float base,
-                int32_t dtype, int32_t *err, void *stream, bool append, bool k_out_optional = false) {
+                int32_t dtype, int32_t *err, void *stream, bool append, bool k_out_optional = false,
+                bool dependent = false) {
   PKV_REQUIRE(B >= 0 && Hq >= 0 && Hkv >= 0, PKV_ERR_INVALID_ARG, "negative size");
   PKV_REQUIRE(d >= 2 && d <= 2 * kMaxHalf && d % 2 == 0, PKV_ERR_UNSUPPORTED, "head_dim %d", d);
   PKV_REQUIRE(dtype_ok(dtype), PKV_ERR_UNSUPPORTED, "dtype %d", dtype);
@@ -225,7 +259,7 @@ int rope_launch(const void *q, const void *k, const void *v, void *q_out, void *
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 #define PKV_ROPE_ARGS                                                                     \
   B, threads, smem, s, q, k, v, q_out, k_out, positions, slots, k_cache, v_cache, Hq, Hkv, d, \
-      num_slots, err, t
+      num_slots, err, t, dependent
   if (dtype == PKV_BF16) {
     using T = __nv_bfloat16;
     if (vec == 4)
@@ -245,6 +279,16 @@ int rope_launch(const void *q, const void *k, const void *v, void *q_out, void *
 }
 
 }  // namespace
+
+int rope_append_dependent(const void *q, const void *k, const void *v, void *q_out, void *k_out,
+                          const int32_t *positions, const int64_t *slot_mapping, void *k_cache,
+                          void *v_cache, int32_t B, int32_t Hq, int32_t Hkv, int32_t d,
+                          int32_t num_blocks, float base, int32_t dtype, int32_t *dev_err_flag,
+                          void *stream) {
+  return rope_launch(q, k, v, q_out, k_out, positions, slot_mapping, k_cache, v_cache, B, Hq, Hkv,
+                     d, num_blocks, base, dtype, dev_err_flag, stream, true, false, true);
+}
+
 }  // namespace pkv
 
 using namespace pkv;

@@ -12,6 +12,13 @@ GPU buffers; no D2H copies).  ``capture``/``replay_step`` put the (copy and)
 kernels of a step in one CUDA graph (v0.8.0: the whole decode replayed as one
 graph).
 
+With ``n_layers > 1`` every layer has its own K/V pool ("neurogrid releases"
+v0.7.0: per-layer caches) indexed by the same block tables; a step runs the
+layers in order through ``pkv_decode_step_layers`` (each layer's kernels
+overlap the previous layer's tail) and one graph holds all of them.
+``pool_blocks_for_vram`` sizes the pool from the free device memory (v0.7.0:
+blocks from available VRAM, 25% budget).
+
 Joins and leaves only edit the allocator's block tables ("neurogrid releases"
 v0.7.0: on-demand blocks, O(1) alloc/free); no KV is moved when the batch
 changes, which is what replaces the extract/re-assemble rebatch of the helexa
@@ -20,6 +27,15 @@ continuous-batching PR.
 import math
 
 from . import binding
+
+
+def pool_blocks_for_vram(n_layers, Hkv, d, dtype, fraction=0.25, device=None):
+    """Blocks that fit in ``fraction`` of the device's free memory, for K and V
+    pools of ``n_layers`` layers."""
+    import torch
+    free, _ = torch.cuda.mem_get_info(device)
+    code = binding.F32 if dtype == "f32" else binding.BF16
+    return binding.pool_blocks(int(free * fraction), n_layers, Hkv, d, code)
 
 
 def _metadata_layout(B, bt_stride):
@@ -35,11 +51,14 @@ def _metadata_layout(B, bt_stride):
 class PagedDecoder:
     def __init__(self, num_blocks, Hq, Hkv, d, dtype, max_seqs, max_blocks_per_seq,
                  initial_free=None, device="cuda", num_parts=None, rope_base=10000.0,
-                 scale=None, flags=0, k_cache=None, v_cache=None, metadata="copy"):
+                 scale=None, flags=0, k_cache=None, v_cache=None, metadata="copy", n_layers=1):
         import torch
         if metadata not in ("copy", "mapped"):
             raise ValueError(f"metadata must be 'copy' or 'mapped', not {metadata!r}")
+        if n_layers < 1:
+            raise ValueError("n_layers must be >= 1")
         self.metadata = metadata
+        self.n_layers = n_layers
         self.torch = torch
         self.device = torch.device(device)
         self.Hq, self.Hkv, self.d = Hq, Hkv, d
@@ -50,11 +69,19 @@ class PagedDecoder:
         self.rope_base = rope_base
         self.scale = 1.0 / math.sqrt(d) if scale is None else scale
         self.flags = flags
-        shape = (num_blocks, Hkv, binding.BLOCK_SIZE, d)
-        self.k_cache = k_cache if k_cache is not None else torch.empty(
+        L = n_layers
+        shape = (L, num_blocks, Hkv, binding.BLOCK_SIZE, d)
+        # caches of every layer: [L, num_blocks, Hkv, 16, d]; a single-layer
+        # decoder also accepts (and exposes) [num_blocks, Hkv, 16, d]
+        if k_cache is not None and k_cache.dim() == 4:
+            k_cache, v_cache = k_cache.unsqueeze(0), v_cache.unsqueeze(0)
+        self.k_caches = k_cache if k_cache is not None else torch.empty(
             shape, dtype=self.tdtype, device=self.device)
-        self.v_cache = v_cache if v_cache is not None else torch.empty(
+        self.v_caches = v_cache if v_cache is not None else torch.empty(
             shape, dtype=self.tdtype, device=self.device)
+        if tuple(self.k_caches.shape) != shape or tuple(self.v_caches.shape) != shape:
+            raise ValueError(f"caches must have shape {shape}")
+        self.k_cache, self.v_cache = self.k_caches[0], self.v_caches[0]
         self.num_blocks = num_blocks
         self.alloc = binding.BlockAllocator(num_blocks, max_seqs, max_blocks_per_seq,
                                             initial_free)
@@ -62,17 +89,23 @@ class PagedDecoder:
         self.num_parts = num_parts or binding.default_parts(d, code, flags)
         self.workspace = binding.alloc_workspace(max_seqs, Hq, Hkv, d, self.num_parts,
                                                  self.device)
+        # consecutive layers alternate between two workspaces
+        self.workspace2 = (binding.alloc_workspace(max_seqs, Hq, Hkv, d, self.num_parts,
+                                                   self.device) if L > 1 else None)
         dev = dict(device=self.device)
         cap = _metadata_layout(max_seqs, self.bt_stride)[-1]
         self._meta_dev = torch.empty(cap if metadata == "copy" else 0, dtype=torch.uint8, **dev)
-        self.q_rot = torch.empty((max_seqs, Hq, d), dtype=self.tdtype, **dev)
-        self.k_rot = torch.empty((max_seqs, Hkv, d), dtype=self.tdtype, **dev)
-        self.out = torch.empty((max_seqs, Hq, d), dtype=self.tdtype, **dev)
+        # per-layer buffers [L, max_seqs, H, d]; the unsuffixed names are layer 0
+        self.q_rots = torch.empty((L, max_seqs, Hq, d), dtype=self.tdtype, **dev)
+        self.k_rots = torch.empty((L, max_seqs, Hkv, d), dtype=self.tdtype, **dev)
+        self.outs = torch.empty((L, max_seqs, Hq, d), dtype=self.tdtype, **dev)
         self.err = torch.zeros(1, dtype=torch.int32, **dev)
         # fixed input buffers for graph replay (the producer of q/k/v writes here)
-        self.q_in = torch.empty((max_seqs, Hq, d), dtype=self.tdtype, **dev)
-        self.k_in = torch.empty((max_seqs, Hkv, d), dtype=self.tdtype, **dev)
-        self.v_in = torch.empty((max_seqs, Hkv, d), dtype=self.tdtype, **dev)
+        self.q_ins = torch.empty((L, max_seqs, Hq, d), dtype=self.tdtype, **dev)
+        self.k_ins = torch.empty((L, max_seqs, Hkv, d), dtype=self.tdtype, **dev)
+        self.v_ins = torch.empty((L, max_seqs, Hkv, d), dtype=self.tdtype, **dev)
+        self.q_rot, self.k_rot, self.out = self.q_rots[0], self.k_rots[0], self.outs[0]
+        self.q_in, self.k_in, self.v_in = self.q_ins[0], self.k_ins[0], self.v_ins[0]
         self._graphs = None
         # two pinned metadata buffers so the host can fill step i+1 while step
         # i's copy (or, mapped, its kernels) still reads the other one
@@ -143,26 +176,42 @@ class PagedDecoder:
         return npv
 
     # -- a1..a4 --------------------------------------------------------------
-    def step_args(self, B, q, k, v, attn_bias=None):
+    def step_args(self, B, q, k, v, attn_bias=None, layer=0):
         self._set_device_views(B)
+        ws = self.workspace if layer % 2 == 0 else self.workspace2
         return binding.make_step_args(
-            q, k, v, self.q_rot[:B], self.k_rot[:B], self.k_cache, self.v_cache,
-            self.positions, self.slots, self.seq_lens, self.tables,
-            self.scale, self.rope_base, self.num_parts, self.workspace, self.out[:B],
+            q, k, v, self.q_rots[layer, :B], self.k_rots[layer, :B], self.k_caches[layer],
+            self.v_caches[layer], self.positions, self.slots, self.seq_lens, self.tables,
+            self.scale, self.rope_base, self.num_parts, ws, self.outs[layer, :B],
             attn_bias, self.flags, self.err)
 
+    def layer_args(self, B, q, k, v, attn_bias=None):
+        """``StepArgs`` of every layer (``q [L,B,Hq,d]``, ``k, v [L,B,Hkv,d]``)."""
+        return binding.layer_args_array(
+            [self.step_args(B, q[l], k[l], v[l], attn_bias, l) for l in range(self.n_layers)])
+
+    def _launch(self, B, q, k, v, attn_bias, stream):
+        if self.n_layers == 1:
+            if q.dim() == 4:
+                q, k, v = q[0], k[0], v[0]
+            binding.decode_step_args(self.step_args(B, q, k, v, attn_bias), stream)
+        else:
+            binding.decode_step_layers(self.layer_args(B, q, k, v, attn_bias), stream)
+
     def step(self, seq_ids, q, k, v, attn_bias=None, stream=None):
-        """One decode step for the listed sequences; returns ``out[:B]`` (device)."""
+        """One decode step for the listed sequences; returns ``out[:B]`` (device;
+        with several layers, ``outs[:, :B]``).  q/k/v are ``[B,H,d]`` for one
+        layer or ``[L,B,H,d]``."""
         torch = self.torch
         B = len(seq_ids)
         self.prepare(seq_ids, stream)
-        binding.decode_step_args(self.step_args(B, q, k, v, attn_bias), stream)
+        self._launch(B, q, k, v, attn_bias, stream)
         if self._pending is not None:
             ev = torch.cuda.Event()
             ev.record(stream if stream is not None else torch.cuda.current_stream(self.device))
             self._pending["event"] = ev
             self._pending = None
-        return self.out[:B]
+        return self.out[:B] if self.n_layers == 1 else self.outs[:, :B]
 
     # -- CUDA graph of the whole device step ("neurogrid releases" v0.8.0) ---
     def capture(self, B, attn_bias=None):
@@ -180,12 +229,19 @@ class PagedDecoder:
         for h in self._host:
             if self.metadata == "mapped":
                 self._meta_cur = h["raw"]
-            args = self.step_args(B, self.q_in[:B], self.k_in[:B], self.v_in[:B], attn_bias)
+            if self.n_layers == 1:
+                args = self.step_args(B, self.q_in[:B], self.k_in[:B], self.v_in[:B], attn_bias)
+            else:
+                args = self.layer_args(B, self.q_ins[:, :B], self.k_ins[:, :B],
+                                       self.v_ins[:, :B], attn_bias)
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 if self.metadata == "copy":
                     self._meta_dev[:nbytes].copy_(h["raw"][:nbytes], non_blocking=True)
-                binding.decode_step_args(args, stream)
+                if self.n_layers == 1:
+                    binding.decode_step_args(args, stream)
+                else:
+                    binding.decode_step_layers(args, stream)
             graphs.append(g)
             all_args.append(args)
         torch.cuda.current_stream(self.device).wait_stream(stream)
@@ -204,7 +260,7 @@ class PagedDecoder:
         ev = torch.cuda.Event()
         ev.record(torch.cuda.current_stream(self.device))
         self._host[turn]["event"] = ev
-        return self.out[:B]
+        return self.out[:B] if self.n_layers == 1 else self.outs[:, :B]
 
     def device_errors(self):
         """Reads and clears the device error flag (a D2H copy: not for the hot loop)."""

@@ -158,3 +158,18 @@ def test_cpp_allocator_rejects_bad_input(host_lib):
     with pytest.raises(binding.UnknownSequence):
         a.seq_slots(1, 0, 1)
     assert a.seq_len(s) == 3 and a.num_free() == 7
+
+
+def test_pool_blocks_from_budget(host_lib):
+    """Blocks that fit a byte budget: K and V, 16 tokens, every KV head and
+    layer per block (floor)."""
+    from paged_kv_decode_10_gb300 import binding
+    per_block = 32 * 2 * 8 * 16 * 128 * 2          # 32 layers, bf16, Hkv 8, d 128
+    assert binding.pool_blocks(per_block * 1000, 32, 8, 128, binding.BF16) == 1000
+    assert binding.pool_blocks(per_block * 1000 - 1, 32, 8, 128, binding.BF16) == 999
+    assert binding.pool_blocks(per_block - 1, 32, 8, 128, binding.BF16) == 0
+    assert binding.pool_blocks(4 * 2 * 2 * 16 * 64 * 4 * 7, 4, 2, 64, binding.F32) == 7
+    # a quarter of 280 GB for a 32-layer, 8-KV-head, d=128 bf16 model
+    assert binding.pool_blocks(70 * 10**9, 32, 8, 128, binding.BF16) == 70 * 10**9 // per_block
+    with pytest.raises(binding.PkvError):
+        binding.pool_blocks(1 << 30, 0, 8, 128, binding.BF16)
