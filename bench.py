@@ -62,6 +62,9 @@ def parse_args():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-flush", action="store_true")
+    ap.add_argument("--comparator", action="store_true",
+                    help="also time the dense right-padded batch (assemble/extract rebatch "
+                         "and a decode step over the padded rows) on the final state")
     ap.add_argument("--layers", type=int, default=1,
                     help="layers per step, each with its own KV pool under the same block "
                          "tables (one graph per step)")
@@ -498,6 +501,81 @@ def run_gpu(args, rank, world):
     return result, dec, ids, tokens, oracle_state, meta0, w
 
 
+def run_dense_comparator(args, dec, ids, w, peak):
+    """The dense right-padded batch that paging replaces, on the same rows and
+    lengths as the paged run's final state: the decode step over the padded
+    rows (gap masked, read all the same) and one rebatch (every row extracted
+    to a snapshot, then assembled again), each timed on the device after an L2
+    flush.  Paging's rebatch is a host block-table edit with no device copy."""
+    import torch
+    from paged_kv_decode_10_gb300 import binding, dense, workloads
+    device = dec.device
+    B = len(ids)
+    elem = 2 if w.dtype == "bf16" else 4
+    lens = [dec.alloc.seq_len(s) for s in ids]
+    P = max(lens)
+    cap = (P + 1 + 15) // 16 * 16
+    db = dense.DenseBatch(w.Hq, w.Hkv, w.d, w.dtype, B, cap, device, num_parts=dec.num_parts,
+                          flags=dec.flags)
+    gen = torch.Generator(device=device).manual_seed(77)
+    snaps = []
+    for L in lens:
+        k, v = db.new_snapshot(L)
+        k.normal_(generator=gen)
+        v.normal_(generator=gen)
+        snaps.append((k, v))
+    ks, vs = [s[0] for s in snaps], [s[1] for s in snaps]
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush_buf = torch.ones(max(4 * l2, 512 << 20) // 8, dtype=torch.int64, device=device)
+    stream = torch.cuda.current_stream(device)
+    reps = max(3, min(args.steps, 20))
+
+    def timed(fn):
+        ms = []
+        for _ in range(reps + 1):
+            flush_buf.sum()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ms.append(a.elapsed_time(b))
+        return statistics.mean(ms[1:]) * 1e3
+
+    db.assemble(ks, vs, lens)      # sets up the gap mask and the tables once
+    # the timed rebatch is the device copy alone (the mask is rebuilt on the
+    # host per rebatch and is not counted)
+    assemble_us = timed(lambda: binding.dense_assemble(ks, vs, lens, P, db.k, db.v, cap))
+    q, k, v = workloads.make_new_tokens(w, 0, device)
+    args_d = db.step_args(q, k, v)
+    graph = torch.cuda.CUDAGraph()
+    cap_s = torch.cuda.Stream(device)
+    cap_s.wait_stream(stream)
+    with torch.cuda.graph(graph, stream=cap_s):
+        binding.decode_step_args(args_d, cap_s)
+    stream.wait_stream(cap_s)
+    step_us = timed(graph.replay)
+    extract_us = timed(lambda: db.extract(list(range(B)), ks, vs))
+    assert db.device_errors() == 0
+    tok_bytes = w.Hkv * w.d * 2 * elem                     # K and V of one token
+    dense_attn = attn_bytes([P + 1] * B, w.Hq, w.Hkv, w.d, elem)
+    live = sum(lens)
+    rebatch_bytes = 4 * live * tok_bytes + sum(P - L for L in lens) * tok_bytes
+    return {"rows": B, "padded_len": P, "live_tokens": live, "padded_tokens": B * P,
+            "step_kernels_us": round(step_us, 3),
+            "step_attn_bytes": int(dense_attn),
+            "step_useful_bytes": int(attn_bytes([L + 1 for L in lens], w.Hq, w.Hkv, w.d, elem)),
+            "assemble_us": round(assemble_us, 3), "extract_us": round(extract_us, 3),
+            "rebatch_us": round(assemble_us + extract_us, 3),
+            # extract reads and writes every live token; assemble does the same and
+            # writes the zero gap
+            "rebatch_device_bytes": int(rebatch_bytes),
+            "rebatch_gbs": round(rebatch_bytes / ((assemble_us + extract_us) * 1e-6) / 1e9, 2),
+            "paged_rebatch_device_bytes": 0,
+            "note": "dense step = RoPE/append + attention over the padded rows (gap masked); "
+                    "rebatch = extract every row + assemble every row (one join/leave event)"}
+
+
 def prefill_summary(log, w, elem, peak):
     """Joiners' prefix KV writes of a churn run: tokens per call and the
     achieved bandwidth of pkv_prefill_kv (reads raw k and v, writes both into
@@ -660,6 +738,9 @@ def main():
             result["e2e"] = run_e2e(args, dec, ids, tokens, w)
         if not args.no_cpu and oracle_state is not None and world == 1:
             result["cpu_baseline"] = cpu_baseline(w, oracle_state, meta0, args.cpu_seconds)
+        if args.comparator and args.layers == 1:
+            result["dense_comparator"] = run_dense_comparator(args, dec, ids, w,
+                                                              result["roofline"]["peak"])
         print(json.dumps(result), flush=True)
     if world > 1:
         torch.distributed.barrier()

@@ -346,6 +346,35 @@ int pkv_decode_step(const pkv_step_args *args, void *stream);
  */
 int pkv_decode_step_layers(const pkv_step_args *layers, int32_t n_layers, void *stream);
 
+/*
+ * The dense right-padded batch that paging replaces, kept as a comparator
+ * (helexa issue 121: slice 1 assemble_batch, slice 3a extract_row).  All KV
+ * buffers use the block layout [blocks, Hkv, 16, d] (dtype): a snapshot is one
+ * sequence's tokens [0, len) in ceil(len/16) blocks; a dense batch of B rows
+ * and cap tokens per row (cap a multiple of 16) is B*cap/16 blocks, row b owning
+ * blocks [b*cap/16, (b+1)*cap/16), so the attention call reads it as a pool
+ * with block table row b = b*cap/16 + j and an additive -inf bias on the gap.
+ * k_snaps, v_snaps: host arrays of device pointers.  Buffers must be large
+ * enough for the tokens named; nothing else is checked on the device.
+ * Hkv * d * sizeof(dtype) must be at most 16 KB.
+ *
+ * pkv_dense_assemble: dense row b = snapshot b's tokens [0, lens[b]) followed by
+ * zeros up to padded_len (lens[b] <= padded_len <= cap); tokens from
+ * padded_len on are left for the decode columns.
+ * pkv_dense_extract: for each i, snapshot i = dense row rows[i]'s prefix
+ * [0, prefix_lens[i]) followed by its decode columns [padded_len,
+ * padded_len + steps) (the gap is dropped).
+ */
+int pkv_dense_assemble(const void *const *k_snaps, const void *const *v_snaps,
+                       const int32_t *lens, int32_t B, int32_t padded_len, void *k_dense,
+                       void *v_dense, int32_t cap, int32_t Hkv, int32_t d, int32_t dtype,
+                       void *stream);
+int pkv_dense_extract(const void *k_dense, const void *v_dense, int32_t cap,
+                      const int32_t *rows, const int32_t *prefix_lens, int32_t n_rows,
+                      int32_t padded_len, int32_t steps, void *const *k_snaps,
+                      void *const *v_snaps, int32_t Hkv, int32_t d, int32_t dtype,
+                      void *stream);
+
 /* The address under which kernels read the page-locked host buffer at
  * host_ptr (allocated pinned, or registered with the mapped flag), so that the
  * per-step metadata of pkv_decode_step can stay in host memory and be read by

@@ -111,6 +111,12 @@ SIGNATURES = {
     "pkv_decode_step": (ctypes.c_int, [ctypes.POINTER(StepArgs), _vp]),
     "pkv_mapped_pointer": (ctypes.c_int, [_vp, ctypes.POINTER(_vp)]),
     "pkv_decode_step_layers": (ctypes.c_int, [ctypes.POINTER(StepArgs), _c_i32, _vp]),
+    "pkv_dense_assemble": (ctypes.c_int, [ctypes.POINTER(_vp), ctypes.POINTER(_vp), _p_i32,
+                                          _c_i32, _c_i32, _vp, _vp, _c_i32, _c_i32, _c_i32,
+                                          _c_i32, _vp]),
+    "pkv_dense_extract": (ctypes.c_int, [_vp, _vp, _c_i32, _p_i32, _p_i32, _c_i32, _c_i32,
+                                         _c_i32, ctypes.POINTER(_vp), ctypes.POINTER(_vp),
+                                         _c_i32, _c_i32, _c_i32, _vp]),
     "pkv_decode_step_host": (ctypes.c_int, [ctypes.POINTER(StepArgs),
                                             ctypes.POINTER(StepHostIO), _vp]),
 }
@@ -465,6 +471,40 @@ def decode_step_layers(layers, stream=None):
     ``layers`` is a list of ``StepArgs`` or an array from ``layer_args_array``."""
     arr = layers if isinstance(layers, ctypes.Array) else layer_args_array(layers)
     _check(load().pkv_decode_step_layers(arr, len(arr), _stream(stream)))
+
+
+def _ptr_array(tensors):
+    arr = (_vp * max(len(tensors), 1))()
+    for i, t in enumerate(tensors):
+        arr[i] = _ptr(t)
+    return arr
+
+
+def dense_assemble(k_snaps, v_snaps, lens, padded_len, k_dense, v_dense, cap, stream=None):
+    """Right-padded dense batch from per-sequence snapshots (``pkv_dense_assemble``).
+    Snapshots and the dense caches use the block layout ``[blocks, Hkv, 16, d]``;
+    the dense batch has ``cap`` tokens per row."""
+    lens = np.ascontiguousarray(lens, dtype=np.int32)
+    Hkv, d = k_dense.shape[1], k_dense.shape[3]
+    _check(load().pkv_dense_assemble(_ptr_array(k_snaps), _ptr_array(v_snaps),
+                                     _np_ptr(lens, ctypes.c_int32), len(lens), int(padded_len),
+                                     _ptr(k_dense), _ptr(v_dense), int(cap), Hkv, d,
+                                     dtype_code(k_dense), _stream(stream)))
+
+
+def dense_extract(k_dense, v_dense, cap, rows, prefix_lens, padded_len, steps, k_snaps, v_snaps,
+                  stream=None):
+    """Rows of a dense batch back into snapshots: prefix plus decode columns
+    (``pkv_dense_extract``)."""
+    rows = np.ascontiguousarray(rows, dtype=np.int32)
+    prefix_lens = np.ascontiguousarray(prefix_lens, dtype=np.int32)
+    Hkv, d = k_dense.shape[1], k_dense.shape[3]
+    _check(load().pkv_dense_extract(_ptr(k_dense), _ptr(v_dense), int(cap),
+                                    _np_ptr(rows, ctypes.c_int32),
+                                    _np_ptr(prefix_lens, ctypes.c_int32), len(rows),
+                                    int(padded_len), int(steps), _ptr_array(k_snaps),
+                                    _ptr_array(v_snaps), Hkv, d, dtype_code(k_dense),
+                                    _stream(stream)))
 
 
 def pool_blocks(budget_bytes, n_layers, Hkv, d, dtype):

@@ -464,3 +464,25 @@ def test_prefill_equals_token_by_token_decode_appends(dtype):
     untouched = np.ones(nb, bool)
     untouched[a.seq_blocks(sid)] = False
     np.testing.assert_array_equal(kc[untouched], kc0[untouched])
+
+
+def test_dense_assemble_extract_hand_example_and_round_trip():
+    """Two rows of lengths 2 and 4 padded to 4: row 0's gap is columns 2..3; a
+    decode column at 4 belongs to both rows; extracting drops the gap."""
+    from oracle.dense import assemble_batch, extract_row, gap_bias
+    a = np.arange(2 * 1 * 2, dtype=float).reshape(2, 1, 2) + 1
+    b = np.arange(4 * 1 * 2, dtype=float).reshape(4, 1, 2) + 100
+    dense = assemble_batch([a, b], 4, 8)
+    assert dense.shape == (2, 8, 1, 2)
+    np.testing.assert_array_equal(dense[0, :2], a)
+    np.testing.assert_array_equal(dense[0, 2:], 0)
+    np.testing.assert_array_equal(dense[1, :4], b)
+    bias = gap_bias([2, 4], 4, 8)
+    assert bias[0].tolist() == [0, 0, -np.inf, -np.inf, 0, 0, 0, 0]
+    assert bias[1].tolist() == [0] * 8
+    dense[:, 4] = [[[7, 8]], [[9, 10]]]           # one lockstep decode column
+    np.testing.assert_array_equal(extract_row(dense, 0, 2, 4, 1),
+                                  np.concatenate([a, [[[7, 8]]]]))
+    np.testing.assert_array_equal(extract_row(dense, 1, 4, 4, 1),
+                                  np.concatenate([b, [[[9, 10]]]]))
+    np.testing.assert_array_equal(extract_row(assemble_batch([a, b], 4, 8), 0, 2, 4, 0), a)
