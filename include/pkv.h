@@ -242,7 +242,7 @@ int pkv_prefill_kv(const void *k, const void *v, const int32_t *positions,
  * workspace must not overlap on the GPU.
  *
  * Supported: dtype PKV_BF16 or PKV_F32; d in {64, 128}; Hq/Hkv in {1,2,4,8};
- * B <= 65536.  q_rot [B,Hq,d]; out [B,Hq,d] (device, dtype).
+ * B <= 65536.  q_rot [B,Hq,d] (16-byte aligned); out [B,Hq,d] (device, dtype).
  * num_parts <= 0 selects pkv_attn_default_parts for the current device;
  * at most 4096 parts.
  */

@@ -253,9 +253,10 @@ int attn_launch(const void *q_rot, const void *k_cache, const void *v_cache, int
   PKV_REQUIRE((reinterpret_cast<uintptr_t>(k_cache) & 15) == 0 &&
                   (reinterpret_cast<uintptr_t>(v_cache) & 15) == 0,
               PKV_ERR_INVALID_ARG, "caches must be 16-byte aligned");
-  PKV_REQUIRE((reinterpret_cast<uintptr_t>(q_rot) & 3) == 0 &&
+  // q_rot rows are bulk-copied into shared memory: 16-byte alignment
+  PKV_REQUIRE((reinterpret_cast<uintptr_t>(q_rot) & 15) == 0 &&
                   (reinterpret_cast<uintptr_t>(workspace) & 255) == 0,
-              PKV_ERR_INVALID_ARG, "q_rot must be 4-byte and workspace 256-byte aligned");
+              PKV_ERR_INVALID_ARG, "q_rot must be 16-byte and workspace 256-byte aligned");
   const int G = Hq / Hkv;
   if (num_parts <= 0) {
     rc = default_parts(d, dtype, flags, G, &num_parts);

@@ -74,13 +74,16 @@ struct AttnParams {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr long long kWaitLimitCycles = 1ll << 31;   // about one second
 
-// Pages of row b, or 0 for an invalid length (which also sets *bad).
-__device__ __forceinline__ int row_pages(const int32_t *seq_lens, int b, int bt_stride,
-                                         bool has_bias, int bias_stride, bool *bad) {
-  const int L = seq_lens[b];
+// Pages of a row of length L, or 0 for an invalid length (which also sets *bad).
+__device__ __forceinline__ int pages_of_len(int L, int bt_stride, bool has_bias, int bias_stride,
+                                            bool *bad) {
   const bool ok = L >= 0 && L <= bt_stride * kBlockTokens && (!has_bias || L <= bias_stride);
   *bad = !ok;
   return ok ? (L + kBlockTokens - 1) / kBlockTokens : 0;
+}
+__device__ __forceinline__ int row_pages(const int32_t *seq_lens, int b, int bt_stride,
+                                         bool has_bias, int bias_stride, bool *bad) {
+  return pages_of_len(seq_lens[b], bt_stride, has_bias, bias_stride, bad);
 }
 
 // floor(a / b) for a >= 0, b > 0 (the compiler's 64-bit division measured
@@ -306,18 +309,6 @@ struct UnitCursor {
   long long off;    // first global page of unit (b, g)
 };
 
-__device__ __forceinline__ void next_unit(UnitCursor &u, const AttnParams &p) {
-  u.off += u.n;
-  if (++u.g < p.Hkv) return;
-  u.g = 0;
-  bool bad;
-  for (++u.b; u.b < p.B; ++u.b) {
-    u.n = row_pages(p.seq_lens, u.b, p.bt_stride, p.bias != nullptr, p.bias_stride, &bad);
-    if (u.n > 0) return;
-  }
-  u.n = 0;
-}
-
 // Compile-time geometry of one kernel variant.
 template <typename T, int D, int NW, int NS>
 struct Geo {
@@ -339,7 +330,15 @@ struct Geo {
   static constexpr int kOffBad = kOffBars + 2 * NS * 8;
   static constexpr int kOffScan = kOffBad + NS * 4;
   static constexpr int kOffMisc = kOffScan + (kThreads / 32) * 4;
-  static constexpr int kSmemBytes = kOffMisc + 32 + 1024;            // + alignment slack
+  // segment slots: the producer hands each unit segment to the consumers as a
+  // 64-byte header (row, KV head, pages, length, page range, first page) and
+  // the unit's query rows (up to 8 heads), bulk-copied from global memory
+  static constexpr int kSegSlots = 4;
+  static constexpr int kSegQBytes = 8 * D * kElem;
+  static constexpr int kSegBytes = 64 + kSegQBytes;
+  static constexpr int kOffSeg = (kOffMisc + 32 + 127) / 128 * 128;
+  static constexpr int kOffSegBars = kOffSeg + kSegSlots * kSegBytes;
+  static constexpr int kSmemBytes = kOffSegBars + 2 * kSegSlots * 8 + 1024;   // + alignment slack
   static_assert(kSubs >= 1 && D * kElem % 128 == 0, "row must be whole 128-B lines");
   static_assert(NS % NW == 0, "a stage must always feed the same consumer warp");
 };
@@ -819,6 +818,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
   float *abuf_all = reinterpret_cast<float *>(smem + Q::kOffABuf);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + Q::kOffBars);
   uint64_t *empty = full + NS;
+  uint64_t *segfull = reinterpret_cast<uint64_t *>(smem + Q::kOffSegBars);
+  uint64_t *segempty = segfull + Q::kSegSlots;
   volatile int *stage_bad = reinterpret_cast<volatile int *>(smem + Q::kOffBad);
   int *scan = reinterpret_cast<int *>(smem + Q::kOffScan);
   volatile int *misc = reinterpret_cast<volatile int *>(smem + Q::kOffMisc);  // b0, rowoff0, abort
@@ -836,6 +837,10 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < Q::kSegSlots; ++s) {
+      mbar_init(&segfull[s], 1);
+      mbar_init(&segempty[s], NW);   // one arrival per consumer warp
     }
     misc[0] = -1;
     misc[1] = 0;
@@ -910,33 +915,106 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
     return;
   }
 
-  UnitCursor u0;
-  {
-    u0.b = misc[0];
-    const long long rowoff = misc[1];
-    bool bad;
-    u0.n = row_pages(p.seq_lens, u0.b, p.bt_stride, has_bias, p.bias_stride, &bad);
-    u0.g = static_cast<int>(div_floor(start - rowoff * p.Hkv, u0.n));
-    u0.off = rowoff * p.Hkv + static_cast<long long>(u0.g) * u0.n;
-  }
-
   if (warp == NW) {
     // ======================= producer warp =======================
+    // Walks the part's unit segments.  For each it hands the consumers a
+    // segment slot (header + the unit's query rows, bulk-copied) and streams
+    // the pages into the ring.  Row lengths of the part's first 64 rows and the
+    // next segment's first block ids are read ahead, so a unit boundary costs
+    // no dependent global read.
     constexpr int kBatch = NS >= 8 ? 4 : (NS >= 2 ? NS / 2 : 1);
     const uint64_t l2_stream = l2_policy_evict_first();
-    UnitCursor u = u0;
+    const int b0 = misc[0];
+    const int rl0 = b0 + lane < p.B ? p.seq_lens[b0 + lane] : 0;
+    const int rl1 = b0 + 32 + lane < p.B ? p.seq_lens[b0 + 32 + lane] : 0;
+    auto row_len = [&](int b) {   // b is warp-uniform
+      const int r = b - b0;
+      if (r < 32) return __shfl_sync(0xffffffffu, rl0, r);
+      if (r < 64) return __shfl_sync(0xffffffffu, rl1, r - 32);
+      return p.seq_lens[b];
+    };
+    auto advance = [&](UnitCursor &c) {   // next_unit with the read-ahead lengths
+      c.off += c.n;
+      if (++c.g < p.Hkv) return;
+      c.g = 0;
+      bool bad;
+      for (++c.b; c.b < p.B; ++c.b) {
+        c.n = pages_of_len(row_len(c.b), p.bt_stride, has_bias, p.bias_stride, &bad);
+        if (c.n > 0) return;
+      }
+      c.n = 0;
+    };
+    UnitCursor u;
+    {
+      const long long rowoff = misc[1];
+      bool bad;
+      u.b = b0;
+      u.n = pages_of_len(row_len(b0), p.bt_stride, has_bias, p.bias_stride, &bad);
+      u.g = static_cast<int>(div_floor(start - rowoff * p.Hkv, u.n));
+      u.off = rowoff * p.Hkv + static_cast<long long>(u.g) * u.n;
+    }
+    const uint32_t qbytes = static_cast<uint32_t>(p.G * D * sizeof(T));
     long long cur = start;
-    int x = 0;
-    bool aborted = false;
+    int x = 0, k = 0;
+    bool aborted = false, waited = FUSE;
+    int j0 = static_cast<int>(cur - u.off);
+    int j1 = static_cast<int>(min(static_cast<long long>(u.n), end - u.off));
+    int ids = (j0 + lane < j1) ? p.block_tables[static_cast<size_t>(u.b) * p.bt_stride + j0 + lane]
+                               : -1;
     while (cur < end && !aborted) {
-      const int j0 = static_cast<int>(cur - u.off);
-      const int j1 = static_cast<int>(min(static_cast<long long>(u.n), end - u.off));
       const int32_t *bt = p.block_tables + static_cast<size_t>(u.b) * p.bt_stride;
-      int ids = (j0 + lane < j1) ? bt[j0 + lane] : -1;
+      // read ahead: the next segment's unit and its first 32 block ids
+      const bool more = cur + (j1 - j0) < end;
+      UnitCursor nx = u;
+      int nj1 = 0, nids = -1;
+      if (more) {
+        advance(nx);
+        nj1 = static_cast<int>(min(static_cast<long long>(nx.n), end - nx.off));
+        nids = lane < nj1 ? p.block_tables[static_cast<size_t>(nx.b) * p.bt_stride + lane] : -1;
+      }
+      const int L = row_len(u.b);
       FusedAppend<T, D> app;
       if constexpr (FUSE) {
         if (j1 == u.n) app.fetch(p, u.b, u.g, lane);   // this part owns the last page
       }
+      bool sent = false;
+      // the segment slot: header, then the query rows (after the first batch
+      // of pages, so the first pages are on their way before any wait)
+      auto send_segment = [&]() {
+        if (lane == 0) {
+          const int slot = k % Q::kSegSlots;
+          const uint32_t sph = static_cast<uint32_t>(k / Q::kSegSlots) & 1u;
+          bool dead = misc[2] != 0;
+          if (!dead && !mbar_wait_bounded(&segempty[slot], sph ^ 1u, kWaitLimitCycles)) {
+            misc[2] = 1;
+            dead = true;
+            set_dev_err(p.err, PKV_DEVERR_TIMEOUT);
+          }
+          unsigned char *sp = smem + Q::kOffSeg + slot * Q::kSegBytes;
+          int *h = reinterpret_cast<int *>(sp);
+          h[0] = u.b;
+          h[1] = u.g;
+          h[2] = u.n;
+          h[3] = L;
+          h[4] = j0;
+          h[5] = j1;
+          *reinterpret_cast<long long *>(h + 6) = u.off;
+          if (!FUSE && !dead) {
+            if (!waited) {
+              pdl_wait();   // the query rows come from the kernel before this one
+              waited = true;
+            }
+            mbar_arrive_expect_tx(&segfull[slot], qbytes);
+            bulk_copy_g2s(smem_u32(sp + 64),
+                          static_cast<const T *>(p.q) +
+                              (static_cast<size_t>(u.b) * p.Hq + u.g * p.G) * D,
+                          qbytes, &segfull[slot]);
+          } else {
+            mbar_arrive(&segfull[slot]);
+          }
+        }
+        __syncwarp();
+      };
       for (int jb = j0; jb < j1 && !aborted; jb += 32) {
         const int cur_ids = ids;
         ids = (jb + 32 + lane < j1) ? bt[jb + 32 + lane] : -1;
@@ -985,17 +1063,33 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
             }
           }
           __syncwarp();
+          if (!sent) {
+            send_segment();
+            sent = true;
+          }
         }
         aborted = __shfl_sync(0xffffffffu, misc[2], 0) != 0;
       }
+      if (!sent) send_segment();   // (only when aborted before the first batch)
       x += j1 - j0;
       cur += j1 - j0;
-      if (cur < end) next_unit(u, p);
+      ++k;
+      if (more) {
+        u = nx;
+        j0 = 0;
+        j1 = nj1;
+        ids = nids;
+      }
     }
     if (aborted && lane == 0) {
       // never expected: let any copy still in flight land before the CTA exits
       for (int xx = max(0, x - NS); xx < x; ++xx)
         mbar_wait_bounded(&full[xx % NS], static_cast<uint32_t>(xx / NS) & 1u, kWaitLimitCycles);
+      if (k > 0) {
+        const int s = (k - 1) % Q::kSegSlots;
+        mbar_wait_bounded(&segfull[s], static_cast<uint32_t>((k - 1) / Q::kSegSlots) & 1u,
+                          kWaitLimitCycles);
+      }
     }
     return;
   }
@@ -1010,13 +1104,36 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
 
   int pend_u[2], pend_c[2], pend_n[2], pend_b[2], pend_g[2];   // at most two (see below)
   int npend = 0;
-  UnitCursor u = u0;
   long long cur = start;
-  int x = 0;
-  while (cur < end) {
-    const int j0 = static_cast<int>(cur - u.off);
-    const int j1 = static_cast<int>(min(static_cast<long long>(u.n), end - u.off));
-    const int L = p.seq_lens[u.b];
+  int x = 0, k = 0;
+  // One consumer thread waits for each segment slot; the others read it after
+  // the consumer barrier that ends the previous segment, so every consumer
+  // sees the same header and the same stop decision (misc[6]).
+  auto wait_segment = [&](int kk) {
+    const int slot = kk % Q::kSegSlots;
+    const uint32_t sph = static_cast<uint32_t>(kk / Q::kSegSlots) & 1u;
+    bool ok = misc[2] == 0;
+    if (ok && !mbar_wait_bounded(&segfull[slot], sph, kWaitLimitCycles)) {
+      misc[2] = 1;
+      set_dev_err(p.err, PKV_DEVERR_TIMEOUT);
+      ok = false;
+    }
+    misc[6] = ok ? 0 : 1;
+  };
+  if (tid == 0) wait_segment(0);
+  asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
+  while (misc[6] == 0) {
+    const int slot = k % Q::kSegSlots;
+    const unsigned char *sp = smem + Q::kOffSeg + slot * Q::kSegBytes;
+    const int *hdr = reinterpret_cast<const int *>(sp);
+    UnitCursor u;
+    u.b = hdr[0];
+    u.g = hdr[1];
+    u.n = hdr[2];
+    const int L = hdr[3];
+    const int j0 = hdr[4], j1 = hdr[5];
+    u.off = *reinterpret_cast<const long long *>(hdr + 6);
+    const T *qslot = reinterpret_cast<const T *>(sp + 64);
     // ---- this warp's pages of the segment ----
     if constexpr (KIND == 0) {
       MmaState<D> s;
@@ -1027,9 +1144,10 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
         // qs sits in the reduction buffer: nobody stashes before all have read
         asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
       } else {
-        pdl_wait();   // q_rot comes from the kernel before this one
-        mma_begin<T, D>(s, p, u.b, u.g, lane);
+        mma_begin_smem<D>(s, reinterpret_cast<const __nv_bfloat16 *>(qslot), p.G, lane);
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&segempty[slot]);
       int j = j0 + ((warp - x % NW) + NW) % NW;
       for (; j < j1; j += NW) {
         const int xx = x + (j - j0);
@@ -1058,9 +1176,10 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
         simt_begin_smem<T, D, G>(s, qs, p.G, p.scale_log2, lane);
         asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
       } else {
-        pdl_wait();   // q_rot comes from the kernel before this one
-        simt_begin<T, D, G>(s, p, u.b, u.g, lane);
+        simt_begin_smem<T, D, G>(s, qslot, p.G, p.scale_log2, lane);
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&segempty[slot]);
       int j = j0 + ((warp - x % NW) + NW) % NW;
       for (; j < j1; j += NW) {
         const int xx = x + (j - j0);
@@ -1150,10 +1269,16 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
       pend_g[npend] = u.g;
       ++npend;
     }
-    asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
     x += j1 - j0;
     cur += j1 - j0;
-    if (cur < end) next_unit(u, p);
+    ++k;
+    if (tid == 0) {
+      if (cur < end)
+        wait_segment(k);
+      else
+        misc[6] = 1;
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
   }
   if (npend == 0) return;
   // ---- a4 in the epilogue: the last part to finish a merge group merges it,
