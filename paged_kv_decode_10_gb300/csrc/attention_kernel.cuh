@@ -260,12 +260,12 @@ __device__ __forceinline__ void merge_job_column(const MergeJob J, int G, int D,
   }
   float lse = -INFINITY;
   if (den > 0.f) {
-    const float inv = 1.f / den;
+    const float inv = __frcp_rn(den);
     acc.x *= inv;
     acc.y *= inv;
     acc.z *= inv;
     acc.w *= inv;
-    lse = M + log2f(den);
+    lse = M + lg2(den);
   }
   if (J.o_grp) {
     *(reinterpret_cast<float4 *>(J.o_grp + (J.grp_slot * G + h) * D) + d4) = acc;
@@ -999,6 +999,10 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
           h[4] = j0;
           h[5] = j1;
           *reinterpret_cast<long long *>(h + 6) = u.off;
+          // parts spanned by the unit (two 64-bit divisions, off the consumers' path)
+          const int cf = part_of(u.off, P, C);
+          h[8] = cf;
+          h[9] = part_of(u.off + u.n - 1, P, C) - cf + 1;
           if (!FUSE && !dead) {
             if (!waited) {
               pdl_wait();   // the query rows come from the kernel before this one
@@ -1133,6 +1137,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
     const int L = hdr[3];
     const int j0 = hdr[4], j1 = hdr[5];
     u.off = *reinterpret_cast<const long long *>(hdr + 6);
+    const int c_first = hdr[8], nseg = hdr[9];
     const T *qslot = reinterpret_cast<const T *>(sp + 64);
     // ---- this warp's pages of the segment ----
     if constexpr (KIND == 0) {
@@ -1204,42 +1209,34 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
     // ---- combine the consumer warps' states for this segment ----
     asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
     const int u_idx = u.b * p.Hkv + u.g;
-    const int c_first = part_of(u.off, P, C);
-    const int c_last = part_of(u.off + u.n - 1, P, C);
-    const int nseg = c_last - c_first + 1;
     const int gq = p.G;
-    // per-head rescale factors of the NW warp states, once (G threads); each
-    // output element is then NW fused multiply-adds
-    float *fac = pbuf_all;   // [NW][8] factors, then 1/l [8], lse [8]
-    if (tid < gq) {
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < NW; ++w) M = fmaxf(M, red_m[w * Q::kHeadsPad + tid]);
-      float L = 0.f;
-#pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        const float f = M == -INFINITY ? 0.f : ex2(red_m[w * Q::kHeadsPad + tid] - M);
-        fac[w * Q::kHeadsPad + tid] = f;
-        L += f * red_l[w * Q::kHeadsPad + tid];
-      }
-      fac[NW * Q::kHeadsPad + tid] = L > 0.f ? 1.f / L : 0.f;
-      fac[NW * Q::kHeadsPad + 8 + tid] = L > 0.f ? M + log2f(L) : -INFINITY;
-    }
-    asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
+    // each output float4 combines the NW warp states of its head; the head's
+    // rescale factors are recomputed by every thread that needs them (a few
+    // shared loads and NW ex2), which costs less than a separate pass and a
+    // barrier
     for (int e4 = tid; e4 < gq * (D / 4); e4 += kConsumers) {
       const int h = e4 / (D / 4), d4 = e4 - h * (D / 4);
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) M = fmaxf(M, red_m[w * Q::kHeadsPad + h]);
+      float f[NW];
+      float den = 0.f;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        f[w] = M == -INFINITY ? 0.f : ex2(red_m[w * Q::kHeadsPad + h] - M);
+        den += f[w] * red_l[w * Q::kHeadsPad + h];
+      }
       float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int w = 0; w < NW; ++w) {
-        const float f = fac[w * Q::kHeadsPad + h];
         const float4 a =
             *reinterpret_cast<const float4 *>(red_acc + (w * Q::kHeadsPad + h) * D + 4 * d4);
-        o.x = fmaf(f, a.x, o.x);
-        o.y = fmaf(f, a.y, o.y);
-        o.z = fmaf(f, a.z, o.z);
-        o.w = fmaf(f, a.w, o.w);
+        o.x = fmaf(f[w], a.x, o.x);
+        o.y = fmaf(f[w], a.y, o.y);
+        o.z = fmaf(f[w], a.z, o.z);
+        o.w = fmaf(f[w], a.w, o.w);
       }
-      const float inv = fac[NW * Q::kHeadsPad + h];
+      const float inv = den > 0.f ? __frcp_rn(den) : 0.f;
       o.x *= inv;
       o.y *= inv;
       o.z *= inv;
@@ -1251,7 +1248,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
       } else {
         const size_t idx = static_cast<size_t>(u_idx) + blockIdx.x;
         *reinterpret_cast<float4 *>(p.o_part + (idx * gq + h) * D + 4 * d4) = o;
-        if (d4 == 0) p.lse_part[idx * gq + h] = fac[NW * Q::kHeadsPad + 8 + h];
+        if (d4 == 0) p.lse_part[idx * gq + h] = den > 0.f ? M + lg2(den) : -INFINITY;
       }
     }
     if (tid == 0 && j0 == 0) {
@@ -1262,12 +1259,20 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
       // only the first and last segment of a part can belong to a unit split
       // across parts: remember it and merge after streaming, so merges never
       // stall the consumer warps while the producer keeps the ring full
-      pend_u[npend] = u_idx;
-      pend_c[npend] = c_first;
-      pend_n[npend] = nseg;
-      pend_b[npend] = u.b;
-      pend_g[npend] = u.g;
-      ++npend;
+      const int q = npend++;   // constant indices keep these in registers
+      if (q == 0) {
+        pend_u[0] = u_idx;
+        pend_c[0] = c_first;
+        pend_n[0] = nseg;
+        pend_b[0] = u.b;
+        pend_g[0] = u.g;
+      } else {
+        pend_u[1] = u_idx;
+        pend_c[1] = c_first;
+        pend_n[1] = nseg;
+        pend_b[1] = u.b;
+        pend_g[1] = u.g;
+      }
     }
     x += j1 - j0;
     cur += j1 - j0;
@@ -1291,8 +1296,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
   int first_g[2], ngroups[2];
 #pragma unroll
   for (int q = 0; q < 2; ++q) {
-    const int qq = q < npend ? q : 0;
-    const int u_idx = pend_u[qq], c_first = pend_c[qq], nseg = pend_n[qq];
+    const int u_idx = q < npend ? pend_u[q] : pend_u[0];
+    const int c_first = q < npend ? pend_c[q] : pend_c[0];
+    const int nseg = q < npend ? pend_n[q] : pend_n[0];
     const int grp = (static_cast<int>(blockIdx.x) - c_first) / kMergeGroup;
     first_g[q] = c_first + grp * kMergeGroup;
     ngroups[q] = (nseg + kMergeGroup - 1) / kMergeGroup;
@@ -1308,7 +1314,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
     J.o_grp = ngroups[q] > 1 ? p.o_group : nullptr;
     J.lse_grp = p.lse_group;
     J.grp_slot = J.slot0;
-    J.out = static_cast<T *>(p.out) + (static_cast<size_t>(pend_b[qq]) * p.Hq + pend_g[qq] * p.G) * D;
+    const int bq = q < npend ? pend_b[q] : pend_b[0], gq2 = q < npend ? pend_g[q] : pend_g[0];
+    J.out = static_cast<T *>(p.out) + (static_cast<size_t>(bq) * p.Hq + gq2 * p.G) * D;
   }
   if (tid == 0) {
     fence_acq_rel_gpu();   // release this part's partials
@@ -1361,10 +1368,11 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
     MergeJob &J = job[q];
     J.o = p.o_group;
     J.lse = p.lse_group;
-    J.slot0 = static_cast<size_t>(pend_u[q < npend ? q : 0]) + pend_c[q < npend ? q : 0];
+    J.slot0 = static_cast<size_t>(q < npend ? pend_u[q] : pend_u[0]) +
+              (q < npend ? pend_c[q] : pend_c[0]);
     J.n = ngroups[q];
     J.stride = kMergeGroup;
-    J.c0 = pend_c[q < npend ? q : 0];
+    J.c0 = q < npend ? pend_c[q] : pend_c[0];
     J.level = 2;
     J.o_grp = nullptr;
   }

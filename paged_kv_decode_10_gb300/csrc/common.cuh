@@ -55,6 +55,13 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// fast base-2 logarithm (PTX lg2.approx; relative error ~2^-22)
+__device__ __forceinline__ float lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
