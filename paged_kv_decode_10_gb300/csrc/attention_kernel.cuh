@@ -59,6 +59,7 @@ struct AttnParams {
   int B, Hq, Hkv, G;
   int num_blocks, num_parts;
   int fuse_merge;           // 1: the last part of a unit merges it (a4 in the epilogue)
+  int seg_cost;             // pages of work a unit boundary is worth to the partition
   float scale_log2;         // softmax scale * log2(e)
   // whole-step kernels only (a1 + a2 fused in): the step's new tokens, where
   // they go, and where their rotated copies are reported
@@ -857,10 +858,15 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
   const int nthreads = Q::kThreads;
   const int chunk = (p.B + nthreads - 1) / nthreads;
   const int r0 = min(p.B, tid * chunk), r1 = min(p.B, r0 + chunk);
+  // The partition balances pages plus seg_cost per unit: a unit of n pages
+  // spans n + seg_cost positions, the first seg_cost of them holding no page
+  // (a part that starts a unit pays for the boundary with fewer pages).
+  const int A = p.seg_cost;
+  auto upos = [A](int n) { return n > 0 ? n + A : 0; };
   int mysum = 0;
   for (int b = r0; b < r1; ++b) {
     bool bad;
-    mysum += row_pages(p.seq_lens, b, p.bt_stride, has_bias, p.bias_stride, &bad);
+    mysum += upos(row_pages(p.seq_lens, b, p.bt_stride, has_bias, p.bias_stride, &bad));
     if (bad && blockIdx.x == 0) set_dev_err(p.err, PKV_DEVERR_BAD_LEN);
   }
   int incl = mysum;
@@ -885,7 +891,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
     long long acc = excl;
     for (int b = r0; b < r1; ++b) {
       bool bad;
-      const int n = row_pages(p.seq_lens, b, p.bt_stride, has_bias, p.bias_stride, &bad);
+      const int n = upos(row_pages(p.seq_lens, b, p.bt_stride, has_bias, p.bias_stride, &bad));
       if (start < (acc + n) * p.Hkv) {
         misc[0] = b;
         misc[1] = static_cast<int>(acc);
@@ -904,7 +910,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
     }
   }
   if (blockIdx.x == 0 && tid == 0) {
-    // total page count, for the merge to tell empty parts (C > P) from real ones
+    // total position count, for the merge to tell empty parts (C > P) from real ones
     p.meta[2 * p.B * p.Hkv] = static_cast<int32_t>(P & 0xffffffffll);
     p.meta[2 * p.B * p.Hkv + 1] = static_cast<int32_t>(P >> 32);
   }
@@ -933,8 +939,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
       if (r < 64) return __shfl_sync(0xffffffffu, rl1, r - 32);
       return p.seq_lens[b];
     };
-    auto advance = [&](UnitCursor &c) {   // next_unit with the read-ahead lengths
-      c.off += c.n;
+    auto advance = [&](UnitCursor &c) {   // the next unit, with the read-ahead lengths
+      c.off += c.n + A;
       if (++c.g < p.Hkv) return;
       c.g = 0;
       bool bad;
@@ -950,26 +956,36 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
       bool bad;
       u.b = b0;
       u.n = pages_of_len(row_len(b0), p.bt_stride, has_bias, p.bias_stride, &bad);
-      u.g = static_cast<int>(div_floor(start - rowoff * p.Hkv, u.n));
-      u.off = rowoff * p.Hkv + static_cast<long long>(u.g) * u.n;
+      u.g = static_cast<int>(div_floor(start - rowoff * p.Hkv, u.n + A));
+      u.off = rowoff * p.Hkv + static_cast<long long>(u.g) * (u.n + A);   // first position
     }
     const uint32_t qbytes = static_cast<uint32_t>(p.G * D * sizeof(T));
-    long long cur = start;
     int x = 0, k = 0;
     bool aborted = false, waited = FUSE;
-    int j0 = static_cast<int>(cur - u.off);
-    int j1 = static_cast<int>(min(static_cast<long long>(u.n), end - u.off));
+    // pages [j0, j1) of unit u lie in this part's positions [start, end); the
+    // unit's pages sit at positions off + A .. off + A + n - 1.  Only a part
+    // that lies inside one unit's first A positions has no page at all.
+    int j0 = static_cast<int>(max(0ll, start - u.off - A));
+    int j1 = static_cast<int>(min(static_cast<long long>(u.n), end - u.off - A));
+    bool last = false;
+    if (j1 <= j0) {   // no page: tell the consumers and stop
+      j0 = j1 = 0;
+      last = true;
+    }
     int ids = (j0 + lane < j1) ? p.block_tables[static_cast<size_t>(u.b) * p.bt_stride + j0 + lane]
                                : -1;
-    while (cur < end && !aborted) {
+    while (!aborted) {
       const int32_t *bt = p.block_tables + static_cast<size_t>(u.b) * p.bt_stride;
-      // read ahead: the next segment's unit and its first 32 block ids
-      const bool more = cur + (j1 - j0) < end;
+      // read ahead: the next unit (if the part reaches its pages) and its
+      // first 32 block ids
+      const long long noff = u.off + u.n + A;
+      const bool more = !last && end > noff + A;
+      last = !more;
       UnitCursor nx = u;
       int nj1 = 0, nids = -1;
       if (more) {
         advance(nx);
-        nj1 = static_cast<int>(min(static_cast<long long>(nx.n), end - nx.off));
+        nj1 = static_cast<int>(min(static_cast<long long>(nx.n), end - nx.off - A));
         nids = lane < nj1 ? p.block_tables[static_cast<size_t>(nx.b) * p.bt_stride + lane] : -1;
       }
       const int L = row_len(u.b);
@@ -999,10 +1015,12 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
           h[4] = j0;
           h[5] = j1;
           *reinterpret_cast<long long *>(h + 6) = u.off;
-          // parts spanned by the unit (two 64-bit divisions, off the consumers' path)
-          const int cf = part_of(u.off, P, C);
+          // parts spanned by the unit's pages (two 64-bit divisions, off the
+          // consumers' path), and whether this is the part's last segment
+          const int cf = part_of(u.off + A, P, C);
           h[8] = cf;
-          h[9] = part_of(u.off + u.n - 1, P, C) - cf + 1;
+          h[9] = part_of(u.off + A + u.n - 1, P, C) - cf + 1;
+          h[10] = last ? 1 : 0;
           if (!FUSE && !dead) {
             if (!waited) {
               pdl_wait();   // the query rows come from the kernel before this one
@@ -1074,16 +1092,14 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
         }
         aborted = __shfl_sync(0xffffffffu, misc[2], 0) != 0;
       }
-      if (!sent) send_segment();   // (only when aborted before the first batch)
+      if (!sent) send_segment();   // (a part with no page, or aborted before a batch)
       x += j1 - j0;
-      cur += j1 - j0;
       ++k;
-      if (more) {
-        u = nx;
-        j0 = 0;
-        j1 = nj1;
-        ids = nids;
-      }
+      if (!more) break;
+      u = nx;
+      j0 = 0;
+      j1 = nj1;
+      ids = nids;
     }
     if (aborted && lane == 0) {
       // never expected: let any copy still in flight land before the CTA exits
@@ -1108,7 +1124,6 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
 
   int pend_u[2], pend_c[2], pend_n[2], pend_b[2], pend_g[2];   // at most two (see below)
   int npend = 0;
-  long long cur = start;
   int x = 0, k = 0;
   // One consumer thread waits for each segment slot; the others read it after
   // the consumer barrier that ends the previous segment, so every consumer
@@ -1138,6 +1153,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
     const int j0 = hdr[4], j1 = hdr[5];
     u.off = *reinterpret_cast<const long long *>(hdr + 6);
     const int c_first = hdr[8], nseg = hdr[9];
+    const bool seg_last = hdr[10] != 0;
+    if (j1 <= j0) break;   // a part without pages (every consumer read the same header)
     const T *qslot = reinterpret_cast<const T *>(sp + 64);
     // ---- this warp's pages of the segment ----
     if constexpr (KIND == 0) {
@@ -1275,10 +1292,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
       }
     }
     x += j1 - j0;
-    cur += j1 - j0;
     ++k;
     if (tid == 0) {
-      if (cur < end)
+      if (!seg_last)
         wait_segment(k);
       else
         misc[6] = 1;
