@@ -223,10 +223,13 @@ int pkv_prefill_kv(const void *k, const void *v, const int32_t *positions,
  * value at an excluded token must still be finite).  A row with no tokens, or
  * whose tokens are all excluded, outputs zeros.
  *
- * Partition: the pages of all (row, KV head) units, in row-major order, form
- * one list of P pages; part c of num_parts owns pages
- * [floor(c*P/num_parts), floor((c+1)*P/num_parts)) and runs as one CTA.  A
- * unit whose pages lie in one part is written to `out` directly.  Every other
+ * Partition: the (row, KV head) units, in row-major order, are laid end to
+ * end as positions: a unit of n pages takes n + A positions, the first A
+ * without a page (A, the cost of a unit boundary in pages: 4 at d = 64, 2 at
+ * d = 128).  With P positions in all, part c of num_parts owns positions
+ * [floor(c*P/num_parts), floor((c+1)*P/num_parts)) and the pages in them, and
+ * runs as one CTA, so parts balance pages plus unit boundaries.  A unit whose
+ * pages lie in one part is written to `out` directly.  Every other
  * unit leaves one float32 (o, lse) partial per part it touches in `workspace`;
  * the LSE merge (M = max lse; out = sum exp(lse_s - M) o_s / sum exp(lse_s - M))
  * then combines them.  By default the merge runs in the epilogue of
