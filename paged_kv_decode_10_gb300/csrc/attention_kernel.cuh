@@ -804,7 +804,7 @@ __device__ __forceinline__ void simt_stash(SimtState<T, D, G> &s, float *red_acc
 // FUSE: whole-step kernel -- also rotates the step's q/k and appends k/v
 // (a1 + a2), so a decode step is one launch.
 template <typename T, int D, int NW, int NS, int KIND, int G, bool FUSE>
-__global__ void __launch_bounds__((NW + 1) * 32, 1)
+__global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
     attn_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v,
                       const __grid_constant__ AttnParams p) {

@@ -490,3 +490,11 @@ def test_mapped_metadata_churn_eager_and_graph():
         assert torch.equal(dec.k_cache, decs[0][0].k_cache)
         assert torch.equal(dec.v_cache, decs[0][0].v_cache)
         assert dec.device_errors() == 0
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_tensor_core_variants_keep_two_ctas_per_sm(d):
+    """The bf16 tensor-core kernels are sized (registers, shared memory) for two
+    resident CTAs per SM; the default partition is SMs x 2 parts."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert binding.default_parts(d, binding.BF16) == 2 * sms
