@@ -339,7 +339,10 @@ struct Geo {
   static constexpr int kSegBytes = 64 + kSegQBytes;
   static constexpr int kOffSeg = (kOffMisc + 32 + 127) / 128 * 128;
   static constexpr int kOffSegBars = kOffSeg + kSegSlots * kSegBytes;
-  static constexpr int kSmemBytes = kOffSegBars + 2 * kSegSlots * 8 + 1024;   // + alignment slack
+  // row lengths of the first kLensCache rows, as the prologue read them
+  static constexpr int kLensCache = 256;
+  static constexpr int kOffLens = kOffSegBars + 2 * kSegSlots * 8;
+  static constexpr int kSmemBytes = kOffLens + kLensCache * 4 + 1024;   // + alignment slack
   static_assert(kSubs >= 1 && D * kElem % 128 == 0, "row must be whole 128-B lines");
   static_assert(NS % NW == 0, "a stage must always feed the same consumer warp");
 };
@@ -823,6 +826,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
   uint64_t *segempty = segfull + Q::kSegSlots;
   volatile int *stage_bad = reinterpret_cast<volatile int *>(smem + Q::kOffBad);
   int *scan = reinterpret_cast<int *>(smem + Q::kOffScan);
+  int *lens_s = reinterpret_cast<int *>(smem + Q::kOffLens);
   volatile int *misc = reinterpret_cast<volatile int *>(smem + Q::kOffMisc);  // b0, rowoff0, abort
 
   const int tid = threadIdx.x;
@@ -866,7 +870,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
   int mysum = 0;
   for (int b = r0; b < r1; ++b) {
     bool bad;
-    mysum += upos(row_pages(p.seq_lens, b, p.bt_stride, has_bias, p.bias_stride, &bad));
+    const int len = p.seq_lens[b];
+    if (b < Q::kLensCache) lens_s[b] = len;   // kept for the row search and the producer
+    mysum += upos(pages_of_len(len, p.bt_stride, has_bias, p.bias_stride, &bad));
     if (bad && blockIdx.x == 0) set_dev_err(p.err, PKV_DEVERR_BAD_LEN);
   }
   int incl = mysum;
@@ -891,7 +897,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
     long long acc = excl;
     for (int b = r0; b < r1; ++b) {
       bool bad;
-      const int n = upos(row_pages(p.seq_lens, b, p.bt_stride, has_bias, p.bias_stride, &bad));
+      const int len = b < Q::kLensCache ? lens_s[b] : p.seq_lens[b];   // own rows: written above
+      const int n = upos(pages_of_len(len, p.bt_stride, has_bias, p.bias_stride, &bad));
       if (start < (acc + n) * p.Hkv) {
         misc[0] = b;
         misc[1] = static_cast<int>(acc);
@@ -902,9 +909,10 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
   }
   // rows with no token (or an invalid length) output zeros; part c clears rows
   // c, c + C, ...
-  for (int b = blockIdx.x; b < p.B; b += C) {
+  for (int b = blockIdx.x; b < p.B; b += C) {   // (after the barrier above: lens_s is complete)
     bool bad;
-    if (row_pages(p.seq_lens, b, p.bt_stride, has_bias, p.bias_stride, &bad) == 0) {
+    const int len = b < Q::kLensCache ? lens_s[b] : p.seq_lens[b];
+    if (pages_of_len(len, p.bt_stride, has_bias, p.bias_stride, &bad) == 0) {
       T *o = static_cast<T *>(p.out) + static_cast<size_t>(b) * p.Hq * D;
       for (int e = tid; e < p.Hq * D; e += nthreads) o[e] = from_f32<T>(0.f);
     }
@@ -931,9 +939,12 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
     constexpr int kBatch = NS >= 8 ? 4 : (NS >= 2 ? NS / 2 : 1);
     const uint64_t l2_stream = l2_policy_evict_first();
     const int b0 = misc[0];
-    const int rl0 = b0 + lane < p.B ? p.seq_lens[b0 + lane] : 0;
-    const int rl1 = b0 + 32 + lane < p.B ? p.seq_lens[b0 + 32 + lane] : 0;
+    // row lengths: the prologue's copy for the first rows, read ahead beyond
+    const int rl0 = b0 + lane < p.B && b0 + lane >= Q::kLensCache ? p.seq_lens[b0 + lane] : 0;
+    const int rl1 =
+        b0 + 32 + lane < p.B && b0 + 32 + lane >= Q::kLensCache ? p.seq_lens[b0 + 32 + lane] : 0;
     auto row_len = [&](int b) {   // b is warp-uniform
+      if (b < Q::kLensCache) return lens_s[b];
       const int r = b - b0;
       if (r < 32) return __shfl_sync(0xffffffffu, rl0, r);
       if (r < 64) return __shfl_sync(0xffffffffu, rl1, r - 32);
