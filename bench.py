@@ -94,18 +94,26 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload, kernel_hash):
+def profiled_traffic(workload, kernel_hash, algorithmic_now):
     """DRAM bytes per launch of the split kernel from the committed ncu summary,
-    only if it was taken on the current kernel source."""
+    only if it was taken on the current kernel source.  The capture is an
+    earlier launch of the same workload (its rows are a few tokens shorter), so
+    its DRAM bytes are scaled by the ratio of algorithmic bytes; returns
+    (bytes, note) or (None, reason)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f).get(workload)
     except Exception:
-        return None
+        return None, "no profiles/traffic.json"
     if not rec or rec.get("kernel_hash") != kernel_hash:
-        return None
-    return rec.get("dram_bytes_per_launch")
+        return None, "no ncu capture of the current kernel source"
+    dram, alg = rec.get("dram_bytes_per_launch"), rec.get("algorithmic_bytes_per_launch")
+    if not dram or not alg:
+        return None, "incomplete capture record"
+    return int(round(dram * algorithmic_now / alg)), (
+        f"ncu capture of an earlier launch: {dram} DRAM bytes for {alg} algorithmic bytes "
+        f"(ratio {dram / alg:.4f}), scaled to this launch")
 
 
 def attn_bytes(lens_after, Hq, Hkv, d, elem):
@@ -447,7 +455,8 @@ def run_gpu(args, rank, world):
 
     peak, peak_kind = measured_peak()
     khash = kernel_source_hash()
-    traffic = profiled_traffic(args.workload, khash)
+    traffic, traffic_note = profiled_traffic(args.workload, khash,
+                                             attn_bytes(last_lens, w.Hq, w.Hkv, w.d, elem))
     result = {
         "metric": "paged decode-attn achieved HBM GB/s (% of GB300 peak); batched decode steps/s",
         "value": round(value, 2),
@@ -485,7 +494,7 @@ def run_gpu(args, rank, world):
         "roofline": {"bound": "hbm", "kernel": "attn_split_kernel (a3 + fused a4), timed alone",
                      "achieved": round(attn_gbs, 2), "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": round(attn_gbs / peak, 4),
-                     "traffic": traffic,
+                     "traffic": traffic, "traffic_note": traffic_note,
                      "algorithmic_bytes_per_launch": int(attn_b),
                      "mean_launch_us": round(1e3 * statistics.mean(attn_ms), 3),
                      "kernel_hash": khash},
