@@ -142,10 +142,11 @@ int pkv_pool_blocks(uint64_t budget_bytes, int32_t n_layers, int32_t Hkv, int32_
 int pkv_alloc_dump(const pkv_alloc *a, int32_t *free_stack, int32_t cap, int32_t *n);
 
 /* Device calls.  Tensors are device memory, except that the integer index
- * arrays (positions, slot_mapping, seq_lens, block_tables) may instead be
- * page-locked host memory at its mapped address (pkv_mapped_pointer): the
- * kernels then read them in place over the CPU-GPU link, and the host must not
- * rewrite them until those kernels have finished.  All calls are asynchronous
+ * arrays (positions, slot_mapping, seq_lens, block_tables) -- and the new q, k,
+ * v of pkv_decode_step -- may instead be page-locked host memory at its mapped
+ * address (pkv_mapped_pointer): the kernels then read them in place over the
+ * CPU-GPU link, and the host must not rewrite them until those kernels have
+ * finished.  All calls are asynchronous
  * on `stream` (a cudaStream_t; NULL = the legacy default stream). */
 
 /* ======================================================================== */
@@ -321,8 +322,9 @@ typedef struct pkv_step_args {
 } pkv_step_args;
 
 /* All pointers in *args are device pointers or host memory the GPU can read
- * (pinned / mapped; positions, slot_mapping, seq_lens and block_tables may live
- * there so that a step needs no host-to-device copy); asynchronous on stream.
+ * (pinned / mapped: q, k, v, positions, slot_mapping, seq_lens and block_tables
+ * may live there so that a step needs no host-to-device copy; the kernels read
+ * them in place); asynchronous on stream.
  * Runs pkv_rope_append, then pkv_decode_attn_split launched as a programmatic
  * dependent (its prologue overlaps the RoPE kernel), and pkv_lse_merge when
  * flags has PKV_ATTN_SEPARATE_MERGE.  With PKV_STEP_FUSED the whole step is
@@ -388,6 +390,9 @@ int pkv_dense_extract(const void *k_dense, const void *v_dense, int32_t cap,
 int pkv_mapped_pointer(const void *host_ptr, void **device_ptr);
 
 /* Host-side buffers for pkv_decode_step_host (pinned memory recommended). */
+#define PKV_HOST_IN_PLACE 1   /* pkv_step_host_io.flags: the kernels read the host
+                                 inputs in place instead of copies of them */
+
 typedef struct pkv_step_host_io {
   const void *q, *k, *v;             /* [B,Hq,d], [B,Hkv,d], [B,Hkv,d] */
   const int32_t *positions;
@@ -395,13 +400,20 @@ typedef struct pkv_step_host_io {
   const int32_t *seq_lens;
   const int32_t *block_tables;       /* [B*bt_stride] */
   void *out;                         /* [B,Hq,d] */
+  int32_t flags;                     /* 0 or PKV_HOST_IN_PLACE */
 } pkv_step_host_io;
 
 /*
  * End-to-end step from host memory: copies the host inputs into the device
  * buffers named by *dev (q, k, v, positions, slot_mapping, seq_lens,
  * block_tables), runs pkv_decode_step, copies dev->out back to host->out and
- * waits for the stream.  Returns after the result is in host memory.
+ * waits for the stream.  Returns after the result is in host memory.  With
+ * PKV_HOST_IN_PLACE the inputs must be page-locked host memory; the step's
+ * kernels read them over the CPU-GPU link at their mapped addresses (no
+ * staging copies; dev's input pointers are not used) and only the output is
+ * copied back.  The mapped address of each host buffer is looked up once per
+ * device and remembered (a buffer freed and re-registered at the same address
+ * must keep its mapping).
  */
 int pkv_decode_step_host(const pkv_step_args *dev, const pkv_step_host_io *host,
                          void *stream);

@@ -65,7 +65,7 @@ class StepHostIO(ctypes.Structure):
     _fields_ = [
         ("q", _vp), ("k", _vp), ("v", _vp),
         ("positions", _vp), ("slot_mapping", _vp), ("seq_lens", _vp),
-        ("block_tables", _vp), ("out", _vp),
+        ("block_tables", _vp), ("out", _vp), ("flags", _c_i32),
     ]
 
 
@@ -122,6 +122,7 @@ SIGNATURES = {
 }
 
 _LIB = None
+ABI_VERSION = 2   # pkv_abi_version() of the library this binding describes
 
 
 def library_path():
@@ -143,6 +144,9 @@ def load():
         fn = getattr(lib, name)
         fn.restype = res
         fn.argtypes = args
+    if lib.pkv_abi_version() != ABI_VERSION:
+        raise RuntimeError(f"{path} has ABI version {lib.pkv_abi_version()}, this binding "
+                           f"expects {ABI_VERSION}: rebuild it")
     _LIB = lib
     return lib
 
@@ -215,6 +219,23 @@ class BlockAllocator:
                                           _np_ptr(lens, ctypes.c_int32),
                                           _np_ptr(tables, ctypes.c_int32), int(bt_stride)))
         return pos, slots, lens, tables
+
+    def step_runner(self, seq_ids, bt_stride, out):
+        """A no-argument callable that runs ``prepare_step`` for these sequence ids
+        into the arrays ``out`` (positions, slot_mapping, seq_lens, block_tables),
+        with every pointer converted once (a serving loop calls it every step)."""
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int32)
+        pos, slots, lens, tables = out
+        fn, h, B, bt = self._lib.pkv_prepare_step, self._h, len(ids), int(bt_stride)
+        ptrs = (_np_ptr(ids, ctypes.c_int32), _np_ptr(pos, ctypes.c_int32),
+                _np_ptr(slots, ctypes.c_int64), _np_ptr(lens, ctypes.c_int32),
+                _np_ptr(tables, ctypes.c_int32))
+        keep = (ids, out)
+
+        def run():
+            _check(fn(h, ptrs[0], B, ptrs[1], ptrs[2], ptrs[3], ptrs[4], bt))
+            return keep[1]
+        return run
 
     def seq_len(self, seq_id):
         n = ctypes.c_int32()
@@ -431,10 +452,10 @@ def make_step_args(q, k, v, q_rot, k_rot, k_cache, v_cache, positions, slot_mapp
                    block_tables, scale, rope_base, num_parts, workspace, out, attn_bias=None,
                    flags=0, err=None):
     """Fills the ``pkv_step_args`` struct.  All tensors are on the device except
-    that positions, slot_mapping, seq_lens and block_tables may be pinned host
-    tensors, which the kernels then read in place."""
+    that q, k, v, positions, slot_mapping, seq_lens and block_tables may be pinned
+    host tensors, which the kernels then read in place."""
     a = StepArgs()
-    a.q, a.k, a.v = _ptr(q), _ptr(k), _ptr(v)
+    a.q, a.k, a.v = _meta_ptr(q), _meta_ptr(k), _meta_ptr(v)
     a.q_rot, a.k_rot = _ptr(q_rot), _ptr(k_rot)
     a.k_cache, a.v_cache = _ptr(k_cache), _ptr(v_cache)
     a.num_blocks = k_cache.shape[0]
@@ -521,9 +542,14 @@ def decode_step_host(args, host_io, stream=None):
                                        _stream(stream)))
 
 
-def host_io(q, k, v, positions, slot_mapping, seq_lens, block_tables, out):
-    """``pkv_step_host_io`` over host (CPU, ideally pinned) torch tensors."""
+HOST_IN_PLACE = 1
+
+
+def host_io(q, k, v, positions, slot_mapping, seq_lens, block_tables, out, flags=0):
+    """``pkv_step_host_io`` over host (CPU, ideally pinned; pinned for
+    ``HOST_IN_PLACE``) torch tensors."""
     io = StepHostIO()
+    io.flags = int(flags)
     for name, t in (("q", q), ("k", k), ("v", v), ("positions", positions),
                     ("slot_mapping", slot_mapping), ("seq_lens", seq_lens),
                     ("block_tables", block_tables), ("out", out)):

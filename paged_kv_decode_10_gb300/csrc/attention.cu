@@ -127,6 +127,34 @@ int get_tmap(const void *base, long long rows, int D, int dtype, CUtensorMap *ou
   return PKV_OK;
 }
 
+// Device addresses of page-locked host buffers, remembered per (device, host
+// pointer): a step from host buffers looks up the same buffers every time.
+int mapped_address(const void *host, void **dev_ptr) {
+  struct Entry {
+    const void *host;
+    void *dev;
+    int device;
+  };
+  static std::mutex mu;
+  static Entry cache[32];
+  static int used = 0, next = 0;
+  int device = 0;
+  PKV_CUDA_CHECK(cudaGetDevice(&device));
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+      if (cache[i].host == host && cache[i].device == device) {
+        *dev_ptr = cache[i].dev;
+        return PKV_OK;
+      }
+  }
+  PKV_CUDA_CHECK(cudaHostGetDevicePointer(dev_ptr, const_cast<void *>(host), 0));
+  std::lock_guard<std::mutex> lock(mu);
+  const int slot = used < 32 ? used++ : (next++ % 32);
+  cache[slot] = Entry{host, *dev_ptr, device};
+  return PKV_OK;
+}
+
 bool pick_variant(int dtype, int D, int G, int flags, AttnVariant *v) {
   if (dtype == PKV_BF16 && !(flags & PKV_ATTN_SIMT)) return attn_variant_mma(D, v);
   if (dtype == PKV_BF16) return attn_variant_simt_bf16(D, G, v);
@@ -482,6 +510,28 @@ extern "C" int pkv_decode_step_host(const pkv_step_args *dev, const pkv_step_hos
   const size_t el = dtype_size(dev->dtype);
   const size_t B = static_cast<size_t>(dev->B);
   const size_t qb = B * dev->Hq * dev->d * el, kb = B * dev->Hkv * dev->d * el;
+  if (host->flags & PKV_HOST_IN_PLACE) {
+    pkv_step_args a = *dev;
+    void *m[7];
+    const void *h[7] = {host->q, host->k, host->v, host->positions, host->slot_mapping,
+                        host->seq_lens, host->block_tables};
+    for (int i = 0; i < 7; ++i) {
+      const int rc = mapped_address(h[i], &m[i]);
+      if (rc != PKV_OK) return rc;
+    }
+    a.q = m[0];
+    a.k = m[1];
+    a.v = m[2];
+    a.positions = static_cast<const int32_t *>(m[3]);
+    a.slot_mapping = static_cast<const int64_t *>(m[4]);
+    a.seq_lens = static_cast<const int32_t *>(m[5]);
+    a.block_tables = static_cast<const int32_t *>(m[6]);
+    const int rc = pkv_decode_step(&a, stream);
+    if (rc != PKV_OK) return rc;
+    PKV_CUDA_CHECK(cudaMemcpyAsync(host->out, dev->out, qb, cudaMemcpyDeviceToHost, s));
+    PKV_CUDA_CHECK(cudaStreamSynchronize(s));
+    return PKV_OK;
+  }
   PKV_CUDA_CHECK(cudaMemcpyAsync(const_cast<void *>(dev->q), host->q, qb, cudaMemcpyHostToDevice, s));
   PKV_CUDA_CHECK(cudaMemcpyAsync(const_cast<void *>(dev->k), host->k, kb, cudaMemcpyHostToDevice, s));
   PKV_CUDA_CHECK(cudaMemcpyAsync(const_cast<void *>(dev->v), host->v, kb, cudaMemcpyHostToDevice, s));

@@ -1427,11 +1427,14 @@ struct AttnLauncher {
   static cudaError_t launch_impl(const CUtensorMap &tk, const CUtensorMap &tv,
                                  const AttnParams &p, cudaStream_t s) {
     auto kern = attn_split_kernel<T, D, NW, NS, KIND, G, FUSE>;
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Q::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
+    static std::atomic<unsigned long long> attrs_set{0};
+    cudaError_t e = set_attributes_once(attrs_set, [&] {
+      cudaError_t r =
+          cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Q::kSmemBytes);
+      if (r != cudaSuccess) return r;
+      return cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  cudaSharedmemCarveoutMaxShared);
+    });
     if (e != cudaSuccess) return e;
     // launched as a programmatic dependent: the prologue (row scan, barrier
     // set-up, block-id prefetch, TMA of pages that do not hold this step's

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <cmath>
 
 #include "pkv.h"
@@ -30,6 +31,21 @@ constexpr int kBlockTokens = PKV_BLOCK_SIZE;
 
 inline size_t dtype_size(int dtype) { return dtype == PKV_BF16 ? 2 : 4; }
 inline bool dtype_ok(int dtype) { return dtype == PKV_BF16 || dtype == PKV_F32; }
+
+// Runs `set` (a kernel's cudaFuncSetAttribute calls) once per device: the
+// attributes persist for the process, and a launch then costs no extra driver
+// calls.  `done` is one flag word per kernel (bit = device ordinal).
+template <typename F>
+inline cudaError_t set_attributes_once(std::atomic<unsigned long long> &done, F &&set) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  e = set();
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 // ---- conversions ----------------------------------------------------------
 __device__ __forceinline__ float to_f32(float x) { return x; }

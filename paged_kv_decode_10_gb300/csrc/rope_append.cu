@@ -191,9 +191,12 @@ void launch_rope(int B, int threads, size_t smem, cudaStream_t s, const void *q,
   if (!dependent) {
     // same L1/shared split as the attention kernel that follows, so the SMs
     // need no reconfiguration between the two launches of a step
-    cudaFuncSetAttribute(rope_kernel<T, VEC, APPEND, false>,
-                         cudaFuncAttributePreferredSharedMemoryCarveout,
-                         cudaSharedmemCarveoutMaxShared);
+    static std::atomic<unsigned long long> attrs_set{0};
+    set_attributes_once(attrs_set, [] {
+      return cudaFuncSetAttribute(rope_kernel<T, VEC, APPEND, false>,
+                                  cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  cudaSharedmemCarveoutMaxShared);
+    });
     rope_kernel<T, VEC, APPEND, false><<<B, threads, smem, s>>>(
         static_cast<const T *>(q), static_cast<const T *>(k), static_cast<const T *>(v),
         static_cast<T *>(q_out), static_cast<T *>(k_out), positions, slots,
@@ -201,8 +204,11 @@ void launch_rope(int B, int threads, size_t smem, cudaStream_t s, const void *q,
     return;
   }
   auto kern = rope_kernel<T, VEC, APPEND, true>;
-  cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                       cudaSharedmemCarveoutMaxShared);
+  static std::atomic<unsigned long long> attrs_set{0};
+  set_attributes_once(attrs_set, [&] {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                cudaSharedmemCarveoutMaxShared);
+  });
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(B);
   cfg.blockDim = dim3(threads);

@@ -262,6 +262,64 @@ class PagedDecoder:
         self._host[turn]["event"] = ev
         return self.out[:B] if self.n_layers == 1 else self.outs[:, :B]
 
+    # -- end to end from pinned host buffers ------------------------------------
+    def capture_host(self, B, attn_bias=None):
+        """Captures, for batch size B, one CUDA graph per pinned metadata buffer
+        whose kernels read the step's new q/k/v in place from the pinned host
+        buffers ``q_host, k_host, v_host`` (over the CPU-GPU link, no staging
+        copy) and which ends with a device-to-host copy of the output into the
+        pinned ``out_host``.  ``host_step`` then costs a0 on the host, one graph
+        launch and one wait."""
+        torch = self.torch
+        if self.n_layers != 1:
+            raise ValueError("capture_host is a single-layer step")
+        pin = dict(dtype=self.tdtype, pin_memory=True)
+        self.q_host = torch.empty((B, self.Hq, self.d), **pin)
+        self.k_host = torch.empty((B, self.Hkv, self.d), **pin)
+        self.v_host = torch.empty((B, self.Hkv, self.d), **pin)
+        self.out_host = torch.empty((B, self.Hq, self.d), **pin)
+        binding.default_parts(self.d, binding.F32 if self.dtype == "f32" else binding.BF16,
+                              self.flags)   # sets kernel attributes outside capture
+        nbytes = _metadata_layout(B, self.bt_stride)[-1]
+        stream = torch.cuda.Stream(self.device)
+        stream.wait_stream(torch.cuda.current_stream(self.device))
+        graphs, all_args = [], []
+        for h in self._host:
+            if self.metadata == "mapped":
+                self._meta_cur = h["raw"]
+            args = self.step_args(B, self.q_host, self.k_host, self.v_host, attn_bias)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                if self.metadata == "copy":
+                    self._meta_dev[:nbytes].copy_(h["raw"][:nbytes], non_blocking=True)
+                binding.decode_step_args(args, stream)
+                self.out_host.copy_(self.out[:B], non_blocking=True)
+            graphs.append(g)
+            all_args.append(args)
+        torch.cuda.current_stream(self.device).wait_stream(stream)
+        self._host_graphs = (B, graphs, all_args)
+
+    def host_step(self, seq_ids):
+        """One step end to end: the caller has written the step's q/k/v into
+        ``q_host/k_host/v_host``; runs a0, replays the captured step and waits;
+        returns ``out_host`` (pinned host memory)."""
+        torch = self.torch
+        B, graphs, _ = self._host_graphs
+        if len(seq_ids) != B:
+            raise ValueError("batch size differs from the captured one")
+        self.prepare_host(seq_ids)
+        turn = self._turn
+        self._turn ^= 1
+        if self.metadata == "mapped":
+            self._meta_cur = self._host[turn]["raw"]
+            self._set_device_views(B)
+        graphs[turn].replay()
+        ev = torch.cuda.Event()
+        ev.record(torch.cuda.current_stream(self.device))
+        self._host[turn]["event"] = ev
+        ev.synchronize()
+        return self.out_host
+
     def device_errors(self):
         """Reads and clears the device error flag (a D2H copy: not for the hot loop)."""
         val = int(self.err.item())

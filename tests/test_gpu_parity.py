@@ -261,8 +261,11 @@ def test_device_error_flags_instead_of_faults():
     assert torch.all(out[0] == 0)
 
 
-def test_host_entry_point_matches_device_path():
-    """pkv_decode_step_host (host buffers in, host result out) equals the device call."""
+@pytest.mark.parametrize("flags", [0, 1])
+def test_host_entry_point_matches_device_path(flags):
+    """pkv_decode_step_host (host buffers in, host result out) equals the device
+    call, with staging copies (0) or with the kernels reading the pinned inputs
+    in place (PKV_HOST_IN_PLACE)."""
     w = workloads.make_workload("decode16")
     caches = workloads.make_caches(w, "cpu")
     tokens = workloads.make_new_tokens(w, 0, "cpu")
@@ -279,7 +282,8 @@ def test_host_entry_point_matches_device_path():
     args = dec.step_args(w.B, dq, dk, dv)
     out_h = torch.empty_like(q).pin_memory()
     pinned = [torch.from_numpy(np.ascontiguousarray(x)).pin_memory() for x in (pos, slots, lens, tables)]
-    io = binding.host_io(q.pin_memory(), k.pin_memory(), v.pin_memory(), *pinned, out_h)
+    io = binding.host_io(q.pin_memory(), k.pin_memory(), v.pin_memory(), *pinned, out_h,
+                         flags=flags)
     binding.decode_step_host(args, io)
     assert torch.equal(out_h, ref["out"])
 
@@ -498,3 +502,33 @@ def test_tensor_core_variants_keep_two_ctas_per_sm(d):
     resident CTAs per SM; the default partition is SMs x 2 parts."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     assert binding.default_parts(d, binding.BF16) == 2 * sms
+
+
+@pytest.mark.parametrize("metadata", ["mapped", "copy"])
+def test_host_step_reads_inputs_in_place(metadata):
+    """The end-to-end host step (q/k/v read in place from pinned host buffers,
+    output copied back inside the graph) gives the device step's outputs."""
+    w = workloads.make_workload("decode16")
+    d = dev()
+    caches = workloads.make_caches(w, "cpu")
+    bt = w.max_blocks_per_seq(extra_tokens=8)
+    decs = []
+    for mode in ("copy", metadata):
+        dec = engine.PagedDecoder(w.num_blocks, w.Hq, w.Hkv, w.d, w.dtype, w.B, bt,
+                                  initial_free=w.free_order, device=d,
+                                  k_cache=caches[0].to(d), v_cache=caches[1].to(d),
+                                  metadata=mode)
+        decs.append((dec, [dec.join(int(L)) for L in w.seq_lens]))
+    (ref, ids_r), (host, ids_h) = decs
+    host.capture_host(w.B)
+    for step in range(4):
+        q, k, v = workloads.make_new_tokens(w, step, "cpu")
+        out_r = ref.step(ids_r, q.to(d), k.to(d), v.to(d)).cpu()
+        host.q_host.copy_(q)
+        host.k_host.copy_(k)
+        host.v_host.copy_(v)
+        out_h = host.host_step(ids_h).clone()
+        assert torch.equal(out_r, out_h), step
+    torch.cuda.synchronize()
+    assert torch.equal(ref.k_cache, host.k_cache) and torch.equal(ref.v_cache, host.v_cache)
+    assert ref.device_errors() == 0 and host.device_errors() == 0

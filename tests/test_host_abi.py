@@ -27,7 +27,7 @@ def test_library_exports_every_declared_function(host_lib):
     for name in names:
         assert hasattr(host_lib, name), name
         assert name in binding.SIGNATURES, name
-    assert host_lib.pkv_abi_version() == 1
+    assert host_lib.pkv_abi_version() == 2
 
 
 def _run_trace(alloc_cls, errors):
@@ -173,3 +173,22 @@ def test_pool_blocks_from_budget(host_lib):
     assert binding.pool_blocks(70 * 10**9, 32, 8, 128, binding.BF16) == 70 * 10**9 // per_block
     with pytest.raises(binding.PkvError):
         binding.pool_blocks(1 << 30, 0, 8, 128, binding.BF16)
+
+
+def test_step_runner_matches_prepare_step(host_lib):
+    """The precomputed-pointer allocator step gives prepare_step's outputs and state."""
+    from paged_kv_decode_10_gb300 import binding
+    order = np.random.default_rng(5).permutation(64).astype(np.int32)
+    a = binding.BlockAllocator(64, 4, 16, order)
+    b = binding.BlockAllocator(64, 4, 16, order)
+    ids_a = [a.join(L) for L in (3, 16, 40)]
+    ids_b = [b.join(L) for L in (3, 16, 40)]
+    out = (np.empty(3, np.int32), np.empty(3, np.int64), np.empty(3, np.int32),
+           np.empty((3, 16), np.int32))
+    run = b.step_runner(ids_b, 16, out)
+    for _ in range(20):
+        ref = a.prepare_step(ids_a, 16)
+        got = run()
+        for x, y in zip(ref, got):
+            np.testing.assert_array_equal(x, y)
+    assert a.free_stack() == b.free_stack()
