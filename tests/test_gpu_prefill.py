@@ -149,3 +149,26 @@ def test_joiners_prefilled_then_decoded_match_oracle(dtype, d, hq, hkv):
         rk, rv = ref["k_cache"], ref["v_cache"]
         assert_out_close(f64(out), ref["out"], dtype, f"step {step}")
     assert dec.device_errors() == 0
+
+
+def test_prefill_skips_negative_slots_and_flags_bad_ones():
+    """A negative slot writes nothing; a slot past the pool sets PKV_DEVERR_BAD_SLOT
+    and is skipped; every other token is still written."""
+    D = dev()
+    nb, hkv, d = 8, 2, 64
+    kc = torch.zeros((nb, hkv, 16, d), dtype=torch.bfloat16, device=D)
+    vc = torch.zeros_like(kc)
+    g = torch.Generator().manual_seed(1)
+    k = torch.randn((4, hkv, d), generator=g).to(torch.bfloat16).to(D)
+    v = torch.randn((4, hkv, d), generator=g).to(torch.bfloat16).to(D)
+    pos = torch.tensor([0, 1, 2, 3], dtype=torch.int32, device=D)
+    slots = torch.tensor([5, -1, nb * 16 + 3, 17], dtype=torch.int64, device=D)
+    err = torch.zeros(1, dtype=torch.int32, device=D)
+    binding.prefill_kv(k, v, pos, slots, kc, vc, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & binding.DEVERR_BAD_SLOT
+    written = torch.zeros((nb, 16), dtype=torch.bool)
+    written[0, 5] = written[1, 1] = True
+    got = vc.transpose(1, 2).reshape(nb, 16, hkv, d).cpu()
+    assert torch.equal(got[0, 5], v[0].cpu()) and torch.equal(got[1, 1], v[3].cpu())
+    assert not got[~written].any()
