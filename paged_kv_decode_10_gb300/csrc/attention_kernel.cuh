@@ -9,17 +9,21 @@
 // h / G.
 //
 // How it runs on GB300:
-//  * Work list.  The pages of every (row, KV head) unit, row-major, form one
-//    list of P pages.  CTA c (one per part, grid = num_parts) owns the page
-//    range [c*P/C, (c+1)*P/C): every CTA streams the same number of bytes to
-//    within one 16-token page, whatever the length mix.  A unit split across
-//    CTAs leaves one (o, lse) partial per CTA; the LSE merge kernel combines
-//    them.  A unit inside one CTA is written to the output directly.
-//  * Producer warp.  Walks the CTA's pages, prefetches block ids 32 at a time
-//    and issues 2-D TMA tensor loads (128-byte swizzle) of each 16-token K and
-//    V page into a ring of NS shared-memory stages, each guarded by a
-//    full/empty mbarrier pair.  Every K/V byte is read from HBM once, because a
-//    CTA holds all G query heads of its KV head.
+//  * Work list.  The (row, KV head) units, row-major, are laid end to end as
+//    positions: a unit of n pages takes n + A positions (A = seg_cost, the
+//    cost of a unit boundary in pages).  CTA c (one per part, grid =
+//    num_parts) owns positions [c*P/C, (c+1)*P/C) and the pages in them, so
+//    every CTA gets the same pages-plus-boundaries work whatever the length
+//    mix.  A unit split across CTAs leaves one (o, lse) partial per CTA, merged
+//    in the epilogue by the last CTA to finish it (or by the LSE merge kernel);
+//    a unit inside one CTA is written to the output directly.
+//  * Producer warp.  Walks the CTA's unit segments, hands each to the
+//    consumers through a shared-memory slot (a header and the unit's query
+//    rows, bulk-copied), reads block ids 32 at a time (the next segment's
+//    ahead) and issues 2-D TMA tensor loads (128-byte swizzle, L2
+//    evict-first) of each 16-token K and V page into a ring of NS stages, each
+//    guarded by a full/empty mbarrier pair.  Every K/V byte is read from HBM
+//    once, because a CTA holds all G query heads of its KV head.
 //  * Consumer warps.  Page x of the range goes to consumer warp x % NW.  Each
 //    warp keeps its own online-softmax state (running max m, sum l,
 //    accumulator) for the G heads and, at the end of each unit segment, the
