@@ -88,10 +88,16 @@ def measured_peak():
 
 
 def kernel_source_hash():
+    """Hash of the kernel sources' code: line comments and blank lines are left
+    out, so an edit that only touches comments keeps the ncu records valid."""
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            for line in f:
+                code = line.split("//", 1)[0].strip()
+                if code:
+                    h.update(code.encode())
+                    h.update(b"\n")
     return h.hexdigest()[:16]
 
 
