@@ -123,6 +123,20 @@ def profiled_traffic(workload, kernel_hash, algorithmic_now):
         f"(ratio {dram / alg:.4f}), scaled to this launch")
 
 
+def aggregate_replicas(local_s, local_bytes, world, device=None):
+    """N replicas (one process per GPU, no exchange on the data path): the job's
+    time is the slowest rank's, its work the sum of every rank's bytes."""
+    if world == 1:
+        return local_s, local_bytes
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([local_s], dtype=torch.float64, device=device)
+    b = torch.tensor([float(local_bytes)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(b.item())
+
+
 def attn_bytes(lens_after, Hq, Hkv, d, elem):
     """Algorithmic bytes of one attention pass (a3+a4): every cached K and V
     element once, q in, out written, block-table entries and seq_lens read."""
@@ -409,10 +423,6 @@ def run_gpu(args, rank, world):
     clocks = sampler.stop()
     step_ms = [a.elapsed_time(b) for a, b in evs]
     total_s = sum(step_ms) / 1e3
-    if world > 1:
-        t = torch.tensor([total_s], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_s = float(t.item())
 
     # The dominant kernel (split-KV attention with its fused merge) timed alone
     # on the final step's state, in the step's launch configuration, and the
@@ -455,7 +465,7 @@ def run_gpu(args, rank, world):
     bytes_steps = [args.layers * attn_bytes(la, w.Hq, w.Hkv, w.d, elem) for la in lens_after]
     kv_only = [args.layers * int(np.asarray(la, np.int64).sum()) * w.Hkv * w.d * 2 * elem
                for la in lens_after]
-    total_bytes = sum(bytes_steps) * world
+    total_s, total_bytes = aggregate_replicas(total_s, sum(bytes_steps), world, device)
     value = total_bytes / total_s / 1e9
     attn_b = attn_bytes(last_lens, w.Hq, w.Hkv, w.d, elem)
     attn_gbs = attn_b / (statistics.mean(attn_ms) / 1e3) / 1e9
