@@ -532,3 +532,28 @@ def test_host_step_reads_inputs_in_place(metadata):
     torch.cuda.synchronize()
     assert torch.equal(ref.k_cache, host.k_cache) and torch.equal(ref.v_cache, host.v_cache)
     assert ref.device_errors() == 0 and host.device_errors() == 0
+
+
+def _random_case(seed):
+    r = np.random.default_rng(1000 + seed)
+    hkv = int(r.choice([1, 2, 4, 8]))
+    g = int(r.choice([1, 2, 4, 8]))
+    d = int(r.choice([64, 128]))
+    dtype = "f32" if r.random() < 0.25 else "bf16"
+    B = int(r.integers(1, 24))
+    # short rows (0, 1, page edges) next to long ones: the partition then cuts
+    # parts inside a unit's boundary positions, and many parts span no page
+    pool = [0, 1, 15, 16, 17, 31, 32, 33, int(r.integers(34, 300)), int(r.integers(300, 900))]
+    lens = [int(r.choice(pool)) for _ in range(B)]
+    parts = int(r.choice([1, 5, 37, 152, 304, 1000, 4096]))
+    return lens, g * hkv, hkv, d, dtype, parts
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_shapes_and_partitions_match_oracle(seed):
+    """Random batches (ragged, with empty and one-token rows), head groupings,
+    head sizes, dtypes and partition counts: every step matches the oracle."""
+    lens, hq, hkv, d, dtype, parts = _random_case(seed)
+    w = workloads.custom_workload(f"rand{seed}", lens, hq, hkv, d, dtype, seed=seed)
+    res = gpu_single_step(w, num_parts=parts)
+    _check_full_step(w, res)
