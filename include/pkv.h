@@ -418,6 +418,22 @@ typedef struct pkv_step_host_io {
 int pkv_decode_step_host(const pkv_step_args *dev, const pkv_step_host_io *host,
                          void *stream);
 
+/*
+ * The work of pkv_decode_step_host(dev, host) -- staging copies or in-place
+ * reads per host->flags, the step's kernels, the copy of the output back --
+ * captured once as a CUDA graph for these exact buffers (their addresses are
+ * fixed in it: each launch reads whatever the host last wrote there, typically
+ * pkv_prepare_step's outputs and the new q/k/v).  A serving loop then pays one
+ * graph launch per step instead of every launch and copy.  *out owns the graph
+ * (free with pkv_step_graph_destroy).  Nothing runs at creation.
+ */
+typedef struct pkv_step_graph pkv_step_graph;
+int pkv_step_graph_create(const pkv_step_args *dev, const pkv_step_host_io *host,
+                          pkv_step_graph **out);
+/* Launches the captured step on stream and waits for it (host->out is then set). */
+int pkv_step_graph_launch(pkv_step_graph *g, void *stream);
+void pkv_step_graph_destroy(pkv_step_graph *g);
+
 #ifdef __cplusplus
 }
 #endif

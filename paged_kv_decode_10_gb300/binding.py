@@ -119,6 +119,10 @@ SIGNATURES = {
                                          _c_i32, _c_i32, _c_i32, _vp]),
     "pkv_decode_step_host": (ctypes.c_int, [ctypes.POINTER(StepArgs),
                                             ctypes.POINTER(StepHostIO), _vp]),
+    "pkv_step_graph_create": (ctypes.c_int, [ctypes.POINTER(StepArgs),
+                                             ctypes.POINTER(StepHostIO), ctypes.POINTER(_vp)]),
+    "pkv_step_graph_launch": (ctypes.c_int, [_vp, _vp]),
+    "pkv_step_graph_destroy": (None, [_vp]),
 }
 
 _LIB = None
@@ -543,6 +547,33 @@ def decode_step_host(args, host_io, stream=None):
 
 
 HOST_IN_PLACE = 1
+
+
+class StepGraph:
+    """``pkv_step_graph``: the host step for fixed buffers captured once;
+    ``launch()`` runs one step and waits for its output in host memory."""
+
+    def __init__(self, args, io):
+        self._lib = load()
+        self._keep = (args, io)
+        h = _vp()
+        _check(self._lib.pkv_step_graph_create(ctypes.byref(args), ctypes.byref(io),
+                                               ctypes.byref(h)))
+        self._h = h
+
+    def launch(self, stream=None):
+        _check(self._lib.pkv_step_graph_launch(self._h, _stream(stream)))
+
+    def close(self):
+        if self._h:
+            self._lib.pkv_step_graph_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def host_io(q, k, v, positions, slot_mapping, seq_lens, block_tables, out, flags=0):

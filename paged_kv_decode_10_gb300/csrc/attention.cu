@@ -11,6 +11,7 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <new>
 
 #include "attention_kernel.cuh"
 
@@ -497,16 +498,18 @@ extern "C" int pkv_mapped_pointer(const void *host_ptr, void **device_ptr) {
   return PKV_OK;
 }
 
-extern "C" int pkv_decode_step_host(const pkv_step_args *dev, const pkv_step_host_io *host,
-                                    void *stream) {
-  clear_error();
+namespace {
+
+// Everything pkv_decode_step_host does except the final wait: the inputs
+// copied to the device (or, in place, the kernels pointed at their mapped
+// addresses), the step, and the output copied back.
+int enqueue_host_step(const pkv_step_args *dev, const pkv_step_host_io *host, cudaStream_t s) {
   PKV_REQUIRE(dev && host, PKV_ERR_INVALID_ARG, "NULL argument");
   PKV_REQUIRE(host->q && host->k && host->v && host->positions && host->slot_mapping &&
                   host->seq_lens && host->block_tables && host->out,
               PKV_ERR_INVALID_ARG, "NULL host buffer");
   const int rc0 = check_shapes(dev->B, dev->Hq, dev->Hkv, dev->d, dev->dtype);
   if (rc0 != PKV_OK) return rc0;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t el = dtype_size(dev->dtype);
   const size_t B = static_cast<size_t>(dev->B);
   const size_t qb = B * dev->Hq * dev->d * el, kb = B * dev->Hkv * dev->d * el;
@@ -526,26 +529,97 @@ extern "C" int pkv_decode_step_host(const pkv_step_args *dev, const pkv_step_hos
     a.slot_mapping = static_cast<const int64_t *>(m[4]);
     a.seq_lens = static_cast<const int32_t *>(m[5]);
     a.block_tables = static_cast<const int32_t *>(m[6]);
-    const int rc = pkv_decode_step(&a, stream);
+    const int rc = pkv_decode_step(&a, s);
     if (rc != PKV_OK) return rc;
-    PKV_CUDA_CHECK(cudaMemcpyAsync(host->out, dev->out, qb, cudaMemcpyDeviceToHost, s));
-    PKV_CUDA_CHECK(cudaStreamSynchronize(s));
-    return PKV_OK;
+  } else {
+    PKV_CUDA_CHECK(cudaMemcpyAsync(const_cast<void *>(dev->q), host->q, qb, cudaMemcpyHostToDevice, s));
+    PKV_CUDA_CHECK(cudaMemcpyAsync(const_cast<void *>(dev->k), host->k, kb, cudaMemcpyHostToDevice, s));
+    PKV_CUDA_CHECK(cudaMemcpyAsync(const_cast<void *>(dev->v), host->v, kb, cudaMemcpyHostToDevice, s));
+    PKV_CUDA_CHECK(cudaMemcpyAsync(const_cast<int32_t *>(dev->positions), host->positions,
+                                   B * sizeof(int32_t), cudaMemcpyHostToDevice, s));
+    PKV_CUDA_CHECK(cudaMemcpyAsync(const_cast<int64_t *>(dev->slot_mapping), host->slot_mapping,
+                                   B * sizeof(int64_t), cudaMemcpyHostToDevice, s));
+    PKV_CUDA_CHECK(cudaMemcpyAsync(const_cast<int32_t *>(dev->seq_lens), host->seq_lens,
+                                   B * sizeof(int32_t), cudaMemcpyHostToDevice, s));
+    PKV_CUDA_CHECK(cudaMemcpyAsync(const_cast<int32_t *>(dev->block_tables), host->block_tables,
+                                   B * dev->bt_stride * sizeof(int32_t), cudaMemcpyHostToDevice, s));
+    const int rc = pkv_decode_step(dev, s);
+    if (rc != PKV_OK) return rc;
   }
-  PKV_CUDA_CHECK(cudaMemcpyAsync(const_cast<void *>(dev->q), host->q, qb, cudaMemcpyHostToDevice, s));
-  PKV_CUDA_CHECK(cudaMemcpyAsync(const_cast<void *>(dev->k), host->k, kb, cudaMemcpyHostToDevice, s));
-  PKV_CUDA_CHECK(cudaMemcpyAsync(const_cast<void *>(dev->v), host->v, kb, cudaMemcpyHostToDevice, s));
-  PKV_CUDA_CHECK(cudaMemcpyAsync(const_cast<int32_t *>(dev->positions), host->positions,
-                                 B * sizeof(int32_t), cudaMemcpyHostToDevice, s));
-  PKV_CUDA_CHECK(cudaMemcpyAsync(const_cast<int64_t *>(dev->slot_mapping), host->slot_mapping,
-                                 B * sizeof(int64_t), cudaMemcpyHostToDevice, s));
-  PKV_CUDA_CHECK(cudaMemcpyAsync(const_cast<int32_t *>(dev->seq_lens), host->seq_lens,
-                                 B * sizeof(int32_t), cudaMemcpyHostToDevice, s));
-  PKV_CUDA_CHECK(cudaMemcpyAsync(const_cast<int32_t *>(dev->block_tables), host->block_tables,
-                                 B * dev->bt_stride * sizeof(int32_t), cudaMemcpyHostToDevice, s));
-  const int rc = pkv_decode_step(dev, stream);
-  if (rc != PKV_OK) return rc;
   PKV_CUDA_CHECK(cudaMemcpyAsync(host->out, dev->out, qb, cudaMemcpyDeviceToHost, s));
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" int pkv_decode_step_host(const pkv_step_args *dev, const pkv_step_host_io *host,
+                                    void *stream) {
+  clear_error();
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int rc = enqueue_host_step(dev, host, s);
+  if (rc != PKV_OK) return rc;
   PKV_CUDA_CHECK(cudaStreamSynchronize(s));
   return PKV_OK;
+}
+
+struct pkv_step_graph {
+  cudaGraphExec_t exec;
+};
+
+extern "C" int pkv_step_graph_create(const pkv_step_args *dev, const pkv_step_host_io *host,
+                                     pkv_step_graph **out) {
+  clear_error();
+  PKV_REQUIRE(dev && host && out, PKV_ERR_INVALID_ARG, "NULL argument");
+  *out = nullptr;
+  // resolve what the step would look up on its first call, outside the capture
+  pkv_step_args a = *dev;
+  if (a.num_parts <= 0 && a.B > 0) {
+    int rc = check_shapes(a.B, a.Hq, a.Hkv, a.d, a.dtype);
+    if (rc != PKV_OK) return rc;
+    rc = default_parts(a.d, a.dtype, a.flags, a.Hq / a.Hkv, &a.num_parts);
+    if (rc != PKV_OK) return rc;
+  }
+  cudaStream_t cs;
+  PKV_CUDA_CHECK(cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking));
+  cudaGraph_t graph = nullptr;
+  cudaError_t e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+  int rc = PKV_OK;
+  if (e == cudaSuccess) {
+    rc = enqueue_host_step(&a, host, cs);
+    const cudaError_t e2 = cudaStreamEndCapture(cs, &graph);   // ends the capture either way
+    if (rc == PKV_OK && e2 != cudaSuccess) e = e2;
+  }
+  cudaStreamDestroy(cs);
+  if (rc != PKV_OK) {
+    if (graph) cudaGraphDestroy(graph);
+    return rc;
+  }
+  PKV_REQUIRE(e == cudaSuccess, PKV_ERR_CUDA, "step capture failed: %s", cudaGetErrorString(e));
+  cudaGraphExec_t exec = nullptr;
+  e = cudaGraphInstantiate(&exec, graph, 0);
+  cudaGraphDestroy(graph);
+  PKV_REQUIRE(e == cudaSuccess, PKV_ERR_CUDA, "graph instantiation failed: %s",
+              cudaGetErrorString(e));
+  pkv_step_graph *g = new (std::nothrow) pkv_step_graph{exec};
+  if (!g) {
+    cudaGraphExecDestroy(exec);
+    return fail(PKV_ERR_CUDA, "out of host memory");
+  }
+  *out = g;
+  return PKV_OK;
+}
+
+extern "C" int pkv_step_graph_launch(pkv_step_graph *g, void *stream) {
+  clear_error();
+  PKV_REQUIRE(g, PKV_ERR_INVALID_ARG, "NULL graph");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  PKV_CUDA_CHECK(cudaGraphLaunch(g->exec, s));
+  PKV_CUDA_CHECK(cudaStreamSynchronize(s));
+  return PKV_OK;
+}
+
+extern "C" void pkv_step_graph_destroy(pkv_step_graph *g) {
+  if (!g) return;
+  cudaGraphExecDestroy(g->exec);
+  delete g;
 }

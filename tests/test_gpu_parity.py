@@ -557,3 +557,54 @@ def test_random_shapes_and_partitions_match_oracle(seed):
     w = workloads.custom_workload(f"rand{seed}", lens, hq, hkv, d, dtype, seed=seed)
     res = gpu_single_step(w, num_parts=parts)
     _check_full_step(w, res)
+
+
+@pytest.mark.parametrize("flags", [0, 1])
+def test_step_graph_matches_host_step(flags):
+    """The captured host step (pkv_step_graph) run over several steps gives the
+    per-call host step's outputs and caches, with staging copies or in place."""
+    w = workloads.make_workload("decode16")
+    d = dev()
+    caches = workloads.make_caches(w, "cpu")
+    bt = w.max_blocks_per_seq(extra_tokens=8)
+    runs = []
+    for use_graph in (False, True):
+        dec = engine.PagedDecoder(w.num_blocks, w.Hq, w.Hkv, w.d, w.dtype, w.B, bt,
+                                  initial_free=w.free_order, device=d,
+                                  k_cache=caches[0].to(d), v_cache=caches[1].to(d))
+        ids = [dec.join(int(L)) for L in w.seq_lens]
+        q0, k0, v0 = workloads.make_new_tokens(w, 0, "cpu")
+        qh, kh, vh = q0.pin_memory(), k0.pin_memory(), v0.pin_memory()
+        meta_h = (torch.empty(w.B, dtype=torch.int32).pin_memory(),
+                  torch.empty(w.B, dtype=torch.int64).pin_memory(),
+                  torch.empty(w.B, dtype=torch.int32).pin_memory(),
+                  torch.empty((w.B, bt), dtype=torch.int32).pin_memory())
+        meta_d = [torch.empty_like(m, device=d) for m in meta_h]
+        dq, dk, dv = (torch.empty_like(t, device=d) for t in (q0, k0, v0))
+        out_h = torch.empty_like(q0).pin_memory()
+        args = binding.make_step_args(dq, dk, dv, dec.q_rot[:w.B], dec.k_rot[:w.B], dec.k_cache,
+                                      dec.v_cache, *meta_d, dec.scale, dec.rope_base,
+                                      dec.num_parts, dec.workspace, dec.out[:w.B], err=dec.err)
+        io = binding.host_io(qh, kh, vh, *meta_h, out_h, flags=flags)
+        graph = binding.StepGraph(args, io) if use_graph else None
+        prepare = dec.alloc.step_runner(ids, bt, tuple(m.numpy() for m in meta_h))
+        outs = []
+        for step in range(4):
+            q, k, v = workloads.make_new_tokens(w, step, "cpu")
+            qh.copy_(q)
+            kh.copy_(k)
+            vh.copy_(v)
+            prepare()
+            if use_graph:
+                graph.launch()
+            else:
+                binding.decode_step_host(args, io)
+            outs.append(out_h.clone())
+        if graph is not None:
+            graph.close()
+        torch.cuda.synchronize()
+        runs.append((outs, dec.k_cache.clone(), dec.v_cache.clone(), dec.device_errors()))
+    (o1, k1, v1, e1), (o2, k2, v2, e2) = runs
+    for a, b in zip(o1, o2):
+        assert torch.equal(a, b)
+    assert torch.equal(k1, k2) and torch.equal(v1, v2) and e1 == 0 and e2 == 0
