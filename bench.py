@@ -271,8 +271,9 @@ def setup(w, device, parts, flags, steps_total, metadata, n_layers=1):
     pool_bytes = w.num_blocks * w.Hkv * 16 * w.d * (2 if w.dtype == "bf16" else 4)
     gen_dev = "cpu" if pool_bytes < (1 << 30) else device
     k_cache, v_cache = workloads.make_caches(w, gen_dev)
-    # room for the timed steps plus the three end-to-end runs (up to 3 x 53 steps)
-    bt = w.max_blocks_per_seq(extra_tokens=steps_total + 64 + 3 * 53)
+    # room for the timed steps, the three end-to-end runs (up to 3 x 53 steps)
+    # and a wall-clock pass over a churn plan (up to 64 steps)
+    bt = w.max_blocks_per_seq(extra_tokens=steps_total + 64 + 3 * 53 + 64)
     if n_layers > 1:
         # every layer's pool starts as a copy of the same synthetic cache
         kd, vd = k_cache.to(device), v_cache.to(device)
@@ -337,11 +338,12 @@ def run_gpu(args, rank, world):
         pre_slot = torch.empty(max_t, dtype=torch.int64).pin_memory()
         pre_done = [None]
 
-    def churn(s):
+    def churn(s, timed=True):
         """Continuous batching: before step s >= 1 the planned rows leave and new
         rows join in their places (host allocator; no KV moves), and the joiners'
         prefix KV is written into their new blocks by the prefill kernel
-        (pkv_seq_slots + pkv_prefill_kv, timed on its own after an L2 flush)."""
+        (pkv_seq_slots + pkv_prefill_kv, timed on its own after an L2 flush
+        unless `timed` is off)."""
         if not w.churn or s == 0:
             return
         leave, prefixes = w.churn[(s - 1) % len(w.churn)]
@@ -359,7 +361,8 @@ def run_gpu(args, rank, world):
             dec.alloc.seq_slots(ids[row], 0, int(pre), out=(pos_np[n:n + int(pre)],
                                                             slot_np[n:n + int(pre)]))
             n += int(pre)
-        flush()
+        if timed:
+            flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for layer in range(dec.n_layers):
@@ -368,7 +371,8 @@ def run_gpu(args, rank, world):
                                err=dec.err, stream=stream)
         e1.record(stream)
         pre_done[0] = e1
-        prefill_log.append((s, n * dec.n_layers, e0, e1))
+        if timed:
+            prefill_log.append((s, n * dec.n_layers, e0, e1))
 
     # warm-up: eager steps through the C ABI (one pkv_decode_step call each)
     meta0 = None
@@ -410,6 +414,7 @@ def run_gpu(args, rank, world):
     for i in range(K):
         churn(W + GW + i)
         stage(W + GW + i)
+        dec.wait_host_buffer()   # the replay two steps back still reads it
         t0 = time.perf_counter()
         lens_after.append(np.array(dec.prepare_host(ids)[2]))
         t_host += time.perf_counter() - t0
@@ -461,6 +466,38 @@ def run_gpu(args, rank, world):
     attn_ms = time_graph(attn_graph)
     kern_ms = time_graph(kern_graph)
     last_lens = lens_after[-1]
+
+    # churn plans: one more pass over the plan timed by the wall clock, host work
+    # included (join/leave, the joiners' prefill, a0, graph launch), no flush
+    wall = None
+    if w.churn and world == 1:
+        n_wall = len(w.churn)
+        s0 = W + GW + K + 1
+        phase = [0.0] * 4     # churn + prefill enqueue, input staging, a0, graph launch
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(n_wall):
+            ta = time.perf_counter()
+            churn(s0 + i, timed=False)
+            tb = time.perf_counter()
+            stage((s0 + i) % len(tokens))
+            tc = time.perf_counter()
+            dec.prepare_host(ids)
+            td = time.perf_counter()
+            dec.replay_step()
+            te = time.perf_counter()
+            for j, dt in enumerate((tb - ta, tc - tb, td - tc, te - td)):
+                phase[j] += dt
+        torch.cuda.synchronize()
+        wall_s = time.perf_counter() - t0
+        us = lambda x: round(1e6 * x / n_wall, 1)
+        wall = {"steps": n_wall, "steps_per_s": round(n_wall / wall_s, 1),
+                "ms_per_step": round(1e3 * wall_s / n_wall, 4),
+                "host_us_per_step": {"join_leave_prefill": us(phase[0]), "stage_inputs": us(phase[1]),
+                                     "a0": us(phase[2]), "graph_launch": us(phase[3])},
+                "includes": "host join/leave, joiners' prefix KV (pkv_prefill_kv), a0, "
+                            "one graph launch per step; no L2 flush; the host phases include "
+                            "waits for the GPU to release pinned buffers"}
 
     bytes_steps = [args.layers * attn_bytes(la, w.Hq, w.Hkv, w.d, elem) for la in lens_after]
     kv_only = [args.layers * int(np.asarray(la, np.int64).sum()) * w.Hkv * w.d * 2 * elem
@@ -518,6 +555,7 @@ def run_gpu(args, rank, world):
                      "kernel_hash": khash},
         "host_a0_us_per_step": round(1e6 * t_host / K, 2),
         "host_churn_us_per_step": round(1e6 * statistics.mean(churn_s), 2) if churn_s else None,
+        "churn_wall_clock": wall,
         "step_kernels_us": round(1e3 * statistics.mean(kern_ms), 3),
         "prefill": prefill_summary([x[1:] for x in prefill_log if x[0] >= W + GW], w, elem,
                                    peak),
@@ -623,8 +661,8 @@ def run_e2e(args, dec, ids, tokens, w):
     """Same metric end to end through the C ABI from pinned host buffers: each
     timed step runs the host allocator (a0) and one launch of the captured host
     step (pkv_step_graph: the kernels read q/k/v and the step metadata in place
-    over the CPU-GPU link -- the host-to-device transfer of the inputs happens
-    inside them -- then the output is copied back to host memory), and waits.
+    over the CPU-GPU link and write the output in place into host memory -- the
+    host-to-device and device-to-host transfers happen inside them), and waits.
     For context the same steps are also timed through pkv_decode_step_host
     without the graph, and with a cudaMemcpyAsync of every input."""
     import torch
@@ -693,7 +731,7 @@ def run_e2e(args, dec, ids, tokens, w):
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "steps": n, "ms_per_step": round(1e3 * secs / n, 4),
             "path": "pkv_step_graph_launch: a0 + one graph (kernels reading the pinned inputs "
-                    "over the CPU-GPU link, D2H copy of the output) + stream wait",
+                    "and writing the pinned output over the CPU-GPU link) + stream wait",
             "without_graph": {"value": round(gbs_p, 2), "unit": "GB/s",
                               "ms_per_step": round(ms_p, 4),
                               "path": "pkv_decode_step_host, PKV_HOST_IN_PLACE"},

@@ -246,7 +246,8 @@ int pkv_prefill_kv(const void *k, const void *v, const int32_t *positions,
  * workspace must not overlap on the GPU.
  *
  * Supported: dtype PKV_BF16 or PKV_F32; d in {64, 128}; Hq/Hkv in {1,2,4,8};
- * B <= 65536.  q_rot [B,Hq,d] (16-byte aligned); out [B,Hq,d] (device, dtype).
+ * B <= 65536.  q_rot [B,Hq,d] (16-byte aligned); out [B,Hq,d] (device, dtype,
+ * 16-byte aligned).
  * num_parts <= 0 selects pkv_attn_default_parts for the current device;
  * at most 4096 parts.
  */
@@ -321,10 +322,11 @@ typedef struct pkv_step_args {
   int32_t *dev_err_flag;             /* nullable */
 } pkv_step_args;
 
-/* All pointers in *args are device pointers or host memory the GPU can read
+/* All pointers in *args are device pointers or host memory the GPU can reach
  * (pinned / mapped: q, k, v, positions, slot_mapping, seq_lens and block_tables
- * may live there so that a step needs no host-to-device copy; the kernels read
- * them in place); asynchronous on stream.
+ * may live there so that a step needs no host-to-device copy -- the kernels read
+ * them in place -- and out so that it needs no copy back; give the mapped
+ * address, pkv_mapped_pointer); asynchronous on stream.
  * Runs pkv_rope_append, then pkv_decode_attn_split launched as a programmatic
  * dependent (its prologue overlaps the RoPE kernel), and pkv_lse_merge when
  * flags has PKV_ATTN_SEPARATE_MERGE.  With PKV_STEP_FUSED the whole step is
@@ -391,7 +393,8 @@ int pkv_mapped_pointer(const void *host_ptr, void **device_ptr);
 
 /* Host-side buffers for pkv_decode_step_host (pinned memory recommended). */
 #define PKV_HOST_IN_PLACE 1   /* pkv_step_host_io.flags: the kernels read the host
-                                 inputs in place instead of copies of them */
+                                 inputs and write the host output in place
+                                 instead of going through device copies */
 
 typedef struct pkv_step_host_io {
   const void *q, *k, *v;             /* [B,Hq,d], [B,Hkv,d], [B,Hkv,d] */
@@ -408,10 +411,10 @@ typedef struct pkv_step_host_io {
  * buffers named by *dev (q, k, v, positions, slot_mapping, seq_lens,
  * block_tables), runs pkv_decode_step, copies dev->out back to host->out and
  * waits for the stream.  Returns after the result is in host memory.  With
- * PKV_HOST_IN_PLACE the inputs must be page-locked host memory; the step's
- * kernels read them over the CPU-GPU link at their mapped addresses (no
- * staging copies; dev's input pointers are not used) and only the output is
- * copied back.  The mapped address of each host buffer is looked up once per
+ * PKV_HOST_IN_PLACE the inputs and host->out must be page-locked host memory;
+ * the step's kernels read the inputs and write the result over the CPU-GPU
+ * link at their mapped addresses (no staging or result copies; dev's input
+ * pointers and dev->out are not used).  The mapped address of each host buffer is looked up once per
  * device and remembered (a buffer freed and re-registered at the same address
  * must keep its mapping).
  */

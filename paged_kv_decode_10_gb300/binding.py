@@ -457,7 +457,8 @@ def make_step_args(q, k, v, q_rot, k_rot, k_cache, v_cache, positions, slot_mapp
                    flags=0, err=None):
     """Fills the ``pkv_step_args`` struct.  All tensors are on the device except
     that q, k, v, positions, slot_mapping, seq_lens and block_tables may be pinned
-    host tensors, which the kernels then read in place."""
+    host tensors, which the kernels then read in place, and out may be a pinned
+    host tensor, which the kernels then write in place."""
     a = StepArgs()
     a.q, a.k, a.v = _meta_ptr(q), _meta_ptr(k), _meta_ptr(v)
     a.q_rot, a.k_rot = _ptr(q_rot), _ptr(k_rot)
@@ -473,7 +474,7 @@ def make_step_args(q, k, v, q_rot, k_rot, k_cache, v_cache, positions, slot_mapp
     a.scale, a.rope_base = float(scale), float(rope_base)
     a.dtype, a.flags, a.num_parts = dtype_code(q), int(flags), int(num_parts)
     a.workspace, a.workspace_bytes = _ptr(workspace), workspace.numel()
-    a.out = _ptr(out)
+    a.out = _meta_ptr(out)
     a.dev_err_flag = _ptr(err)
     return a
 

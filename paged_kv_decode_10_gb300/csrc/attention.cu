@@ -286,6 +286,9 @@ int attn_launch(const void *q_rot, const void *k_cache, const void *v_cache, int
   PKV_REQUIRE((reinterpret_cast<uintptr_t>(q_rot) & 15) == 0 &&
                   (reinterpret_cast<uintptr_t>(workspace) & 255) == 0,
               PKV_ERR_INVALID_ARG, "q_rot must be 16-byte and workspace 256-byte aligned");
+  // output rows are written with vector stores
+  PKV_REQUIRE((reinterpret_cast<uintptr_t>(out) & 15) == 0, PKV_ERR_INVALID_ARG,
+              "out must be 16-byte aligned");
   const int G = Hq / Hkv;
   if (num_parts <= 0) {
     rc = default_parts(d, dtype, flags, G, &num_parts);
@@ -501,8 +504,9 @@ extern "C" int pkv_mapped_pointer(const void *host_ptr, void **device_ptr) {
 namespace {
 
 // Everything pkv_decode_step_host does except the final wait: the inputs
-// copied to the device (or, in place, the kernels pointed at their mapped
-// addresses), the step, and the output copied back.
+// copied to the device, the step and the output copied back; or, in place, the
+// step's kernels pointed at the mapped addresses of the host inputs and of the
+// host output.
 int enqueue_host_step(const pkv_step_args *dev, const pkv_step_host_io *host, cudaStream_t s) {
   PKV_REQUIRE(dev && host, PKV_ERR_INVALID_ARG, "NULL argument");
   PKV_REQUIRE(host->q && host->k && host->v && host->positions && host->slot_mapping &&
@@ -514,11 +518,12 @@ int enqueue_host_step(const pkv_step_args *dev, const pkv_step_host_io *host, cu
   const size_t B = static_cast<size_t>(dev->B);
   const size_t qb = B * dev->Hq * dev->d * el, kb = B * dev->Hkv * dev->d * el;
   if (host->flags & PKV_HOST_IN_PLACE) {
+    // inputs read and the result written in place over the CPU-GPU link
     pkv_step_args a = *dev;
-    void *m[7];
-    const void *h[7] = {host->q, host->k, host->v, host->positions, host->slot_mapping,
-                        host->seq_lens, host->block_tables};
-    for (int i = 0; i < 7; ++i) {
+    void *m[8];
+    const void *h[8] = {host->q, host->k, host->v, host->positions, host->slot_mapping,
+                        host->seq_lens, host->block_tables, host->out};
+    for (int i = 0; i < 8; ++i) {
       const int rc = mapped_address(h[i], &m[i]);
       if (rc != PKV_OK) return rc;
     }
@@ -529,23 +534,22 @@ int enqueue_host_step(const pkv_step_args *dev, const pkv_step_host_io *host, cu
     a.slot_mapping = static_cast<const int64_t *>(m[4]);
     a.seq_lens = static_cast<const int32_t *>(m[5]);
     a.block_tables = static_cast<const int32_t *>(m[6]);
-    const int rc = pkv_decode_step(&a, s);
-    if (rc != PKV_OK) return rc;
-  } else {
-    PKV_CUDA_CHECK(cudaMemcpyAsync(const_cast<void *>(dev->q), host->q, qb, cudaMemcpyHostToDevice, s));
-    PKV_CUDA_CHECK(cudaMemcpyAsync(const_cast<void *>(dev->k), host->k, kb, cudaMemcpyHostToDevice, s));
-    PKV_CUDA_CHECK(cudaMemcpyAsync(const_cast<void *>(dev->v), host->v, kb, cudaMemcpyHostToDevice, s));
-    PKV_CUDA_CHECK(cudaMemcpyAsync(const_cast<int32_t *>(dev->positions), host->positions,
-                                   B * sizeof(int32_t), cudaMemcpyHostToDevice, s));
-    PKV_CUDA_CHECK(cudaMemcpyAsync(const_cast<int64_t *>(dev->slot_mapping), host->slot_mapping,
-                                   B * sizeof(int64_t), cudaMemcpyHostToDevice, s));
-    PKV_CUDA_CHECK(cudaMemcpyAsync(const_cast<int32_t *>(dev->seq_lens), host->seq_lens,
-                                   B * sizeof(int32_t), cudaMemcpyHostToDevice, s));
-    PKV_CUDA_CHECK(cudaMemcpyAsync(const_cast<int32_t *>(dev->block_tables), host->block_tables,
-                                   B * dev->bt_stride * sizeof(int32_t), cudaMemcpyHostToDevice, s));
-    const int rc = pkv_decode_step(dev, s);
-    if (rc != PKV_OK) return rc;
+    a.out = m[7];
+    return pkv_decode_step(&a, s);
   }
+  PKV_CUDA_CHECK(cudaMemcpyAsync(const_cast<void *>(dev->q), host->q, qb, cudaMemcpyHostToDevice, s));
+  PKV_CUDA_CHECK(cudaMemcpyAsync(const_cast<void *>(dev->k), host->k, kb, cudaMemcpyHostToDevice, s));
+  PKV_CUDA_CHECK(cudaMemcpyAsync(const_cast<void *>(dev->v), host->v, kb, cudaMemcpyHostToDevice, s));
+  PKV_CUDA_CHECK(cudaMemcpyAsync(const_cast<int32_t *>(dev->positions), host->positions,
+                                 B * sizeof(int32_t), cudaMemcpyHostToDevice, s));
+  PKV_CUDA_CHECK(cudaMemcpyAsync(const_cast<int64_t *>(dev->slot_mapping), host->slot_mapping,
+                                 B * sizeof(int64_t), cudaMemcpyHostToDevice, s));
+  PKV_CUDA_CHECK(cudaMemcpyAsync(const_cast<int32_t *>(dev->seq_lens), host->seq_lens,
+                                 B * sizeof(int32_t), cudaMemcpyHostToDevice, s));
+  PKV_CUDA_CHECK(cudaMemcpyAsync(const_cast<int32_t *>(dev->block_tables), host->block_tables,
+                                 B * dev->bt_stride * sizeof(int32_t), cudaMemcpyHostToDevice, s));
+  const int rc = pkv_decode_step(dev, s);
+  if (rc != PKV_OK) return rc;
   PKV_CUDA_CHECK(cudaMemcpyAsync(host->out, dev->out, qb, cudaMemcpyDeviceToHost, s));
   return PKV_OK;
 }

@@ -26,6 +26,8 @@ continuous-batching PR.
 """
 import math
 
+import numpy as np
+
 from . import binding
 
 
@@ -109,22 +111,31 @@ class PagedDecoder:
         self._graphs = None
         # two pinned metadata buffers so the host can fill step i+1 while step
         # i's copy (or, mapped, its kernels) still reads the other one
-        self._host = [dict(raw=torch.empty(cap, dtype=torch.uint8, pin_memory=True), event=None)
-                      for _ in range(2)]
+        self._host = [dict(raw=torch.empty(cap, dtype=torch.uint8, pin_memory=True), event=None,
+                           runner=None) for _ in range(2)]
         self._turn = 0
         self._pending = None
         self.last_metadata = None
+        self._view_cache = {}
         self._meta_cur = self._meta_dev if metadata == "copy" else self._host[0]["raw"]
         self._set_device_views(max_seqs)
 
     # -- packed metadata views ----------------------------------------------
     def _views(self, raw, B):
+        """Typed views of one packed metadata buffer for batch size B (made once
+        per buffer and B: the buffers live as long as the decoder)."""
+        key = (raw.data_ptr(), B)
+        hit = self._view_cache.get(key)
+        if hit is not None:
+            return hit
         torch = self.torch
         o_slots, o_pos, o_lens, o_tab, end = _metadata_layout(B, self.bt_stride)
-        return (raw[o_pos:o_pos + 4 * B].view(torch.int32),
-                raw[o_slots:o_slots + 8 * B].view(torch.int64),
-                raw[o_lens:o_lens + 4 * B].view(torch.int32),
-                raw[o_tab:end].view(torch.int32).view(B, self.bt_stride)), end
+        views = ((raw[o_pos:o_pos + 4 * B].view(torch.int32),
+                  raw[o_slots:o_slots + 8 * B].view(torch.int64),
+                  raw[o_lens:o_lens + 4 * B].view(torch.int32),
+                  raw[o_tab:end].view(torch.int32).view(B, self.bt_stride)), end)
+        self._view_cache[key] = views
+        return views
 
     def _set_device_views(self, B):
         """positions/slots/seq_lens/tables: the views the kernels read (device
@@ -140,15 +151,28 @@ class PagedDecoder:
         self.alloc.leave(seq_id)
 
     # -- a0 ----------------------------------------------------------------
-    def prepare_host(self, seq_ids):
-        """a0 into the pinned buffer that the next copy (or replay) reads."""
+    def wait_host_buffer(self):
+        """Blocks until the GPU no longer reads the pinned metadata buffer that
+        the next ``prepare_host`` fills (the step two launches back)."""
         h = self._host[self._turn]
         if h["event"] is not None:
             h["event"].synchronize()
+            h["event"] = None
+
+    def prepare_host(self, seq_ids):
+        """a0 into the pinned buffer that the next copy (or replay) reads."""
+        self.wait_host_buffer()
+        h = self._host[self._turn]
         B = len(seq_ids)
-        views, _ = self._views(h["raw"], B)
-        npv = tuple(t.numpy() for t in views)
-        self.alloc.prepare_step(seq_ids, self.bt_stride, out=npv)
+        run = h["runner"]
+        if run is None or run[0] != B:
+            views, _ = self._views(h["raw"], B)
+            npv = tuple(t.numpy() for t in views)
+            ids = np.empty(B, np.int32)
+            run = h["runner"] = (B, ids, npv, self.alloc.step_runner(ids, self.bt_stride, npv))
+        _, ids, npv, fn = run
+        ids[:] = seq_ids
+        fn()
         self.last_metadata = npv
         return npv
 
@@ -176,14 +200,14 @@ class PagedDecoder:
         return npv
 
     # -- a1..a4 --------------------------------------------------------------
-    def step_args(self, B, q, k, v, attn_bias=None, layer=0):
+    def step_args(self, B, q, k, v, attn_bias=None, layer=0, out=None):
         self._set_device_views(B)
         ws = self.workspace if layer % 2 == 0 else self.workspace2
         return binding.make_step_args(
             q, k, v, self.q_rots[layer, :B], self.k_rots[layer, :B], self.k_caches[layer],
             self.v_caches[layer], self.positions, self.slots, self.seq_lens, self.tables,
-            self.scale, self.rope_base, self.num_parts, ws, self.outs[layer, :B],
-            attn_bias, self.flags, self.err)
+            self.scale, self.rope_base, self.num_parts, ws,
+            self.outs[layer, :B] if out is None else out, attn_bias, self.flags, self.err)
 
     def layer_args(self, B, q, k, v, attn_bias=None):
         """``StepArgs`` of every layer (``q [L,B,Hq,d]``, ``k, v [L,B,Hkv,d]``)."""
@@ -267,9 +291,9 @@ class PagedDecoder:
         """Captures, for batch size B, one CUDA graph per pinned metadata buffer
         whose kernels read the step's new q/k/v in place from the pinned host
         buffers ``q_host, k_host, v_host`` (over the CPU-GPU link, no staging
-        copy) and which ends with a device-to-host copy of the output into the
-        pinned ``out_host``.  ``host_step`` then costs a0 on the host, one graph
-        launch and one wait."""
+        copy) and write the output in place into the pinned ``out_host`` (no
+        copy back).  ``host_step`` then costs a0 on the host, one graph launch
+        and one wait."""
         torch = self.torch
         if self.n_layers != 1:
             raise ValueError("capture_host is a single-layer step")
@@ -287,13 +311,13 @@ class PagedDecoder:
         for h in self._host:
             if self.metadata == "mapped":
                 self._meta_cur = h["raw"]
-            args = self.step_args(B, self.q_host, self.k_host, self.v_host, attn_bias)
+            args = self.step_args(B, self.q_host, self.k_host, self.v_host, attn_bias,
+                                  out=self.out_host)
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 if self.metadata == "copy":
                     self._meta_dev[:nbytes].copy_(h["raw"][:nbytes], non_blocking=True)
                 binding.decode_step_args(args, stream)
-                self.out_host.copy_(self.out[:B], non_blocking=True)
             graphs.append(g)
             all_args.append(args)
         torch.cuda.current_stream(self.device).wait_stream(stream)
