@@ -334,43 +334,44 @@ def run_gpu(args, rank, world):
         gen = torch.Generator(device=device).manual_seed(1000 + w.seed)
         pre_k = torch.randn((max_t, w.Hkv, w.d), generator=gen, device=device).to(dec.tdtype)
         pre_v = torch.randn((max_t, w.Hkv, w.d), generator=gen, device=device).to(dec.tdtype)
-        pre_pos = torch.empty(max_t, dtype=torch.int32).pin_memory()
-        pre_slot = torch.empty(max_t, dtype=torch.int64).pin_memory()
-        pre_done = [None]
+        # two pinned (positions, slots) buffers, so that filling one never waits
+        # for the prefill that still reads the other
+        pre_bufs = []
+        for _ in range(2):
+            pos_t = torch.empty(max_t, dtype=torch.int32).pin_memory()
+            slot_t = torch.empty(max_t, dtype=torch.int64).pin_memory()
+            pre_bufs.append(dict(pos=pos_t, slot=slot_t, np=(pos_t.numpy(), slot_t.numpy()),
+                                 done=None))
 
     def churn(s, timed=True):
         """Continuous batching: before step s >= 1 the planned rows leave and new
         rows join in their places (host allocator; no KV moves), and the joiners'
         prefix KV is written into their new blocks by the prefill kernel
-        (pkv_seq_slots + pkv_prefill_kv, timed on its own after an L2 flush
-        unless `timed` is off)."""
+        (pkv_seqs_join's prefix slots + pkv_prefill_kv, timed on its own after an
+        L2 flush unless `timed` is off)."""
         if not w.churn or s == 0:
             return
         leave, prefixes = w.churn[(s - 1) % len(w.churn)]
+        buf = pre_bufs[s % 2]
+        if buf["done"] is not None:
+            buf["done"].synchronize()   # the prefill two churns back reads these arrays
         t0 = time.perf_counter()
-        for row in leave:
-            dec.leave(ids[row])
-        for row, pre in zip(leave, prefixes):
-            ids[row] = dec.join(int(pre))
+        dec.alloc.leave_many([ids[row] for row in leave])
+        joined = dec.alloc.join_many(prefixes, buf["np"])
+        for row, sid in zip(leave, joined):
+            ids[row] = int(sid)
         churn_s.append(time.perf_counter() - t0)
-        if pre_done[0] is not None:
-            pre_done[0].synchronize()   # the last prefill still reads the pinned arrays
-        n = 0
-        pos_np, slot_np = pre_pos.numpy(), pre_slot.numpy()
-        for row, pre in zip(leave, prefixes):
-            dec.alloc.seq_slots(ids[row], 0, int(pre), out=(pos_np[n:n + int(pre)],
-                                                            slot_np[n:n + int(pre)]))
-            n += int(pre)
+        n = int(np.sum(prefixes))
         if timed:
             flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for layer in range(dec.n_layers):
-            binding.prefill_kv(pre_k[:n], pre_v[:n], pre_pos[:n], pre_slot[:n],
+            binding.prefill_kv(pre_k[:n], pre_v[:n], buf["pos"][:n], buf["slot"][:n],
                                dec.k_caches[layer], dec.v_caches[layer], base=dec.rope_base,
                                err=dec.err, stream=stream)
         e1.record(stream)
-        pre_done[0] = e1
+        buf["done"] = e1
         if timed:
             prefill_log.append((s, n * dec.n_layers, e0, e1))
 

@@ -108,6 +108,20 @@ void pkv_alloc_destroy(pkv_alloc *a);
 int pkv_seq_join(pkv_alloc *a, int32_t prefix_len, int32_t *seq_id);
 int pkv_seq_leave(pkv_alloc *a, int32_t seq_id);
 
+/* Several joins in one call (one host call per step for a serving loop that
+ * admits many sequences): the same as pkv_seq_join(prefix_lens[i]) for i = 0..n-1
+ * in order, into seq_ids[i].  If positions and slot_mapping are given they receive,
+ * packed one sequence after another, the positions and cache slots of every
+ * joiner's prefix tokens [0, prefix_lens[i]) (sum(prefix_lens) entries, as
+ * pkv_seq_slots gives them): the input of pkv_prefill_kv.  All or nothing: if
+ * the sequence ids, the pool or a table cannot take every joiner, nothing
+ * changes (PKV_ERR_OUT_OF_BLOCKS when the pool is short). */
+int pkv_seqs_join(pkv_alloc *a, const int32_t *prefix_lens, int32_t n, int32_t *seq_ids,
+                  int32_t *positions, int64_t *slot_mapping);
+/* Several leaves in one call: pkv_seq_leave(seq_ids[i]) for i = 0..n-1 in order.
+ * All or nothing: every id must be live and listed once, else nothing changes. */
+int pkv_seqs_leave(pkv_alloc *a, const int32_t *seq_ids, int32_t n);
+
 /*
  * Host part of one decode step for the B listed (distinct, live) sequences.
  * Outputs (host arrays, row b = seq_ids[b]):

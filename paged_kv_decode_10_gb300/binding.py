@@ -78,6 +78,8 @@ SIGNATURES = {
     "pkv_alloc_destroy": (None, [_vp]),
     "pkv_seq_join": (ctypes.c_int, [_vp, _c_i32, _p_i32]),
     "pkv_seq_leave": (ctypes.c_int, [_vp, _c_i32]),
+    "pkv_seqs_join": (ctypes.c_int, [_vp, _p_i32, _c_i32, _p_i32, _p_i32, _p_i64]),
+    "pkv_seqs_leave": (ctypes.c_int, [_vp, _p_i32, _c_i32]),
     "pkv_prepare_step": (ctypes.c_int, [_vp, _p_i32, _c_i32, _p_i32, _p_i64, _p_i32, _p_i32,
                                         _c_i32]),
     "pkv_seq_len": (ctypes.c_int, [_vp, _c_i32, _p_i32]),
@@ -126,7 +128,7 @@ SIGNATURES = {
 }
 
 _LIB = None
-ABI_VERSION = 2   # pkv_abi_version() of the library this binding describes
+ABI_VERSION = 3   # pkv_abi_version() of the library this binding describes
 
 
 def library_path():
@@ -207,6 +209,28 @@ class BlockAllocator:
 
     def leave(self, seq_id):
         _check(self._lib.pkv_seq_leave(self._h, int(seq_id)))
+
+    def join_many(self, prefix_lens, slots_out=None):
+        """Joins one sequence per prefix length in one call (``pkv_seqs_join``);
+        returns their ids.  ``slots_out = (positions, slot_mapping)``, arrays of at
+        least sum(prefix_lens) entries, also receives every joiner's prefix
+        positions and cache slots, packed in order."""
+        lens = np.ascontiguousarray(prefix_lens, dtype=np.int32)
+        ids = np.empty(len(lens), np.int32)
+        pos = slots = None
+        if slots_out is not None:
+            pos, slots = slots_out
+            if len(pos) < lens.sum() or len(slots) < lens.sum():
+                raise PkvError(ERR_INVALID_ARG, "slots_out too short for the prefixes")
+            pos, slots = _np_ptr(pos, ctypes.c_int32), _np_ptr(slots, ctypes.c_int64)
+        _check(self._lib.pkv_seqs_join(self._h, _np_ptr(lens, ctypes.c_int32), len(lens),
+                                       _np_ptr(ids, ctypes.c_int32), pos, slots))
+        return ids
+
+    def leave_many(self, seq_ids):
+        """Retires the listed sequences in one call (``pkv_seqs_leave``)."""
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int32)
+        _check(self._lib.pkv_seqs_leave(self._h, _np_ptr(ids, ctypes.c_int32), len(ids)))
 
     def prepare_step(self, seq_ids, bt_stride, out=None):
         """Returns ``positions, slot_mapping, seq_lens, block_tables`` (numpy).

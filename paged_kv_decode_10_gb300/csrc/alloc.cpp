@@ -183,6 +183,64 @@ extern "C" int pkv_prepare_step(pkv_alloc *a, const int32_t *seq_ids, int32_t B,
   return PKV_OK;
 }
 
+extern "C" int pkv_seqs_join(pkv_alloc *a, const int32_t *prefix_lens, int32_t n,
+                             int32_t *seq_ids, int32_t *positions, int64_t *slot_mapping) {
+  pkv::clear_error();
+  PKV_REQUIRE(a && n >= 0, PKV_ERR_INVALID_ARG, "NULL allocator or n < 0");
+  if (n == 0) return PKV_OK;
+  PKV_REQUIRE(prefix_lens && seq_ids, PKV_ERR_INVALID_ARG, "NULL argument");
+  PKV_REQUIRE(!positions == !slot_mapping, PKV_ERR_INVALID_ARG,
+              "give both positions and slot_mapping, or neither");
+  // validate the whole batch before changing anything
+  PKV_REQUIRE(static_cast<size_t>(n) <= a->free_ids.size(), PKV_ERR_INVALID_ARG,
+              "%d joins but only %zu free sequence ids", n, a->free_ids.size());
+  int64_t need = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t L = prefix_lens[i];
+    PKV_REQUIRE(L >= 0, PKV_ERR_INVALID_ARG, "joiner %d: prefix_len %d < 0", i, L);
+    PKV_REQUIRE(blocks_for(L) <= a->max_blocks_per_seq, PKV_ERR_INVALID_ARG,
+                "joiner %d: prefix of %d tokens needs %lld blocks > max_blocks_per_seq %d", i,
+                L, (long long)blocks_for(L), a->max_blocks_per_seq);
+    need += blocks_for(L);
+  }
+  PKV_REQUIRE(need <= static_cast<int64_t>(a->free_stack.size()), PKV_ERR_OUT_OF_BLOCKS,
+              "joins need %lld blocks, %zu free", (long long)need, a->free_stack.size());
+  int64_t k = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    const int rc = pkv_seq_join(a, prefix_lens[i], &seq_ids[i]);   // cannot fail now
+    if (rc != PKV_OK) return rc;
+    if (!positions) continue;
+    const int32_t *t = a->table(seq_ids[i]);
+    for (int32_t p = 0; p < prefix_lens[i]; ++p, ++k) {
+      positions[k] = p;
+      slot_mapping[k] = static_cast<int64_t>(t[p / kBlock]) * kBlock + p % kBlock;
+    }
+  }
+  return PKV_OK;
+}
+
+extern "C" int pkv_seqs_leave(pkv_alloc *a, const int32_t *seq_ids, int32_t n) {
+  pkv::clear_error();
+  PKV_REQUIRE(a && n >= 0, PKV_ERR_INVALID_ARG, "NULL allocator or n < 0");
+  if (n == 0) return PKV_OK;
+  PKV_REQUIRE(seq_ids, PKV_ERR_INVALID_ARG, "NULL seq_ids");
+  if (++a->epoch == 0) {
+    std::fill(a->stamp.begin(), a->stamp.end(), 0u);
+    a->epoch = 1;
+  }
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t s = seq_ids[i];
+    PKV_REQUIRE(a->is_live(s), PKV_ERR_UNKNOWN_SEQ, "sequence %d is not live", s);
+    PKV_REQUIRE(a->stamp[s] != a->epoch, PKV_ERR_INVALID_ARG, "sequence %d listed twice", s);
+    a->stamp[s] = a->epoch;
+  }
+  for (int32_t i = 0; i < n; ++i) {
+    const int rc = pkv_seq_leave(a, seq_ids[i]);
+    if (rc != PKV_OK) return rc;
+  }
+  return PKV_OK;
+}
+
 extern "C" int pkv_seq_len(const pkv_alloc *a, int32_t seq_id, int32_t *len) {
   pkv::clear_error();
   PKV_REQUIRE(a && len, PKV_ERR_INVALID_ARG, "NULL argument");

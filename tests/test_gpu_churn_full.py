@@ -1,8 +1,9 @@
 """churn256 at full size (B=256, 32/8 heads, d=128, bf16) in the launch
 configuration the benchmark times: the default partition, step metadata read
 in place from pinned host memory, one CUDA graph replay per step, and before
-every step after the first 26 rows leave and 26 join with a prefix whose KV
-pkv_prefill_kv writes into their new blocks.
+every step after the first 26 rows leave and 26 join (one pkv_seqs_leave and one
+pkv_seqs_join call, which also gives the joiners' prefix slots) with a prefix
+whose KV pkv_prefill_kv writes into their new blocks.
 
 The oracle cannot redo a 256-row step at this size in seconds, so it checks
 sampled rows one by one: each sampled row replays its own history in float64
@@ -83,22 +84,25 @@ def test_churn256_graph_steps_match_oracle_on_sampled_rows():
     for s in range(STEPS):
         if s:
             leave, prefixes = w.churn[s - 1]
+            dec.alloc.leave_many([ids[row] for row in leave])
             for row in leave:
-                dec.leave(ids[row])
                 model.leave(ids[row])
-            pos_l, slot_l, pre_k, pre_v = [], [], [], []
-            for row, pre in zip(leave, prefixes):
+            total = int(np.sum(prefixes))
+            pos_all = np.empty(total, np.int32)
+            slot_all = np.empty(total, np.int64)
+            joined = dec.alloc.join_many(prefixes, (pos_all, slot_all))
+            pre_k, pre_v = [], []
+            k_off = 0
+            for row, pre, sid in zip(leave, prefixes, joined):
                 row, pre = int(row), int(pre)
-                ids[row] = dec.join(pre)
+                ids[row] = int(sid)
                 assert ids[row] == model.join(pre)
-                p, sl = dec.alloc.seq_slots(ids[row], 0, pre)
                 mp, msl = model.seq_slots(ids[row], 0, pre)
-                np.testing.assert_array_equal(p, mp)
-                np.testing.assert_array_equal(sl, msl)
+                np.testing.assert_array_equal(pos_all[k_off:k_off + pre], mp)
+                np.testing.assert_array_equal(slot_all[k_off:k_off + pre], msl)
+                k_off += pre
                 kr = torch.randn((pre, w.Hkv, w.d), generator=gen).to(torch.bfloat16)
                 vr = torch.randn((pre, w.Hkv, w.d), generator=gen).to(torch.bfloat16)
-                pos_l.append(p)
-                slot_l.append(sl)
                 pre_k.append(kr)
                 pre_v.append(vr)
                 if row in hist:
@@ -108,8 +112,7 @@ def test_churn256_graph_steps_match_oracle_on_sampled_rows():
                                         base=w.rope_base, dtype=w.dtype)
                     hist[row] = dict(k=_token_major(kc, pre), v=_token_major(vc, pre))
             binding.prefill_kv(torch.cat(pre_k).to(D), torch.cat(pre_v).to(D),
-                               torch.from_numpy(np.concatenate(pos_l)).to(D),
-                               torch.from_numpy(np.concatenate(slot_l)).to(D),
+                               torch.from_numpy(pos_all).to(D), torch.from_numpy(slot_all).to(D),
                                dec.k_cache, dec.v_cache, base=w.rope_base, err=dec.err)
         q, k, v = workloads.make_new_tokens(w, s, "cpu")
         dec.q_in[:w.B].copy_(q)

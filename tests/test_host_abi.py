@@ -27,7 +27,7 @@ def test_library_exports_every_declared_function(host_lib):
     for name in names:
         assert hasattr(host_lib, name), name
         assert name in binding.SIGNATURES, name
-    assert host_lib.pkv_abi_version() == 2
+    assert host_lib.pkv_abi_version() == 3
 
 
 def _run_trace(alloc_cls, errors):
@@ -192,3 +192,81 @@ def test_step_runner_matches_prepare_step(host_lib):
         for x, y in zip(ref, got):
             np.testing.assert_array_equal(x, y)
     assert a.free_stack() == b.free_stack()
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_batched_join_leave_equal_single_calls_in_order(host_lib, seed):
+    """pkv_seqs_join / pkv_seqs_leave against the allocator model doing the same
+    joins and leaves one at a time: same ids, prefix slots, tables and free
+    stack (bit-exact); a batch that cannot be taken whole changes nothing."""
+    from paged_kv_decode_10_gb300 import binding
+    r = np.random.default_rng(100 + seed)
+    nb, max_seqs, bt = 300, 20, 30
+    order = r.permutation(nb).astype(np.int32)
+    cpp = binding.BlockAllocator(nb, max_seqs, bt, order)
+    model = BlockAllocatorModel(nb, max_seqs=max_seqs, max_blocks_per_seq=bt,
+                                initial_free=order)
+    live = []
+
+    def same_state():
+        assert cpp.free_stack() == model.free
+        for s in live:
+            assert cpp.seq_blocks(s) == model.seq_blocks(s)
+            assert cpp.seq_len(s) == model.seq_len(s)
+
+    for _ in range(60):
+        if live and r.random() < 0.5:
+            k = int(r.integers(1, len(live) + 1))
+            leave = [live[i] for i in r.choice(len(live), size=k, replace=False)]
+            cpp.leave_many(leave)
+            for s in leave:
+                model.leave(s)
+                live.remove(s)
+        n = int(r.integers(0, max_seqs - len(live) + 1))
+        prefixes = r.integers(0, 120, size=n).astype(np.int32)
+        need = int(sum(-(-int(p) // 16) for p in prefixes))
+        pos = np.full(int(prefixes.sum()) + 3, -7, np.int32)
+        slots = np.full(int(prefixes.sum()) + 3, -7, np.int64)
+        if need > model.num_free():
+            before = cpp.free_stack()
+            with pytest.raises(binding.OutOfBlocks):
+                cpp.join_many(prefixes, (pos, slots))
+            assert cpp.free_stack() == before and (pos == -7).all()
+            same_state()
+            continue
+        ids = cpp.join_many(prefixes, (pos, slots))
+        k = 0
+        for sid, p in zip(ids, prefixes):
+            assert sid == model.join(int(p))
+            live.append(int(sid))
+            mp, ms = model.seq_slots(int(sid), 0, int(p))
+            np.testing.assert_array_equal(pos[k:k + p], mp)
+            np.testing.assert_array_equal(slots[k:k + p], ms)
+            k += int(p)
+        assert (pos[k:] == -7).all()
+        same_state()
+        if live:   # a step so that lengths and tables move between batches
+            ids_s = [s for s in live if model.seq_len(s) < (bt - 1) * 16]
+            try:
+                ref = model.prepare_step(ids_s, bt)
+            except OutOfBlocks:
+                continue
+            for a_, b_ in zip(ref, cpp.prepare_step(ids_s, bt)):
+                np.testing.assert_array_equal(a_, b_)
+    # leave: an unknown or repeated id rejects the whole batch
+    if len(live) >= 2:
+        before = cpp.free_stack()
+        with pytest.raises(binding.PkvError):
+            cpp.leave_many([live[0], live[0]])
+        with pytest.raises(binding.UnknownSequence):
+            cpp.leave_many([live[1], max_seqs + 5])
+        assert cpp.free_stack() == before
+        same_state()
+    # join: more joiners than free ids, or a prefix longer than a table, changes nothing
+    before = cpp.free_stack()
+    with pytest.raises(binding.PkvError):
+        cpp.join_many([0] * (max_seqs - len(live) + 1))
+    with pytest.raises(binding.PkvError):
+        cpp.join_many([1, bt * 16 + 1])
+    assert cpp.free_stack() == before
+    same_state()
