@@ -42,6 +42,7 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0   # GB300 HBM3e, nominal (context beside the measured peak)
 KERNEL_SOURCES = ["paged_kv_decode_10_gb300/csrc/attention_kernel.cuh",
                   "paged_kv_decode_10_gb300/csrc/attention_mma.cu",
                   "paged_kv_decode_10_gb300/csrc/attention_simt_bf16.cu",
@@ -157,17 +158,25 @@ class ClockSampler:
         self.index = index
         self.proc = None
         self.lines = []
+        self.first = 0
 
     def start(self):
+        """Starts sampling every 10 ms and returns once the first sample is in
+        (so that the samples after ``start`` fall inside the region that follows)."""
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
+                 "--format=csv,noheader,nounits", "-lms", "10"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except Exception:
             self.proc = None
+            return
+        t_end = time.perf_counter() + 5.0
+        while not self.lines and time.perf_counter() < t_end:
+            time.sleep(0.005)
+        self.first = len(self.lines)
 
     def _read(self):
         for line in self.proc.stdout:
@@ -176,6 +185,7 @@ class ClockSampler:
     def stop(self):
         if self.proc is None:
             return None
+        self.lines = self.lines[self.first:] or self.lines[-1:]
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -426,7 +436,6 @@ def run_gpu(args, rank, world):
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    clocks = sampler.stop()
     step_ms = [a.elapsed_time(b) for a, b in evs]
     total_s = sum(step_ms) / 1e3
 
@@ -466,6 +475,7 @@ def run_gpu(args, rank, world):
 
     attn_ms = time_graph(attn_graph)
     kern_ms = time_graph(kern_graph)
+    clocks = sampler.stop()   # sampled over the timed steps and the two timings above
     last_lens = lens_after[-1]
 
     # churn plans: one more pass over the plan timed by the wall clock, host work
@@ -553,6 +563,9 @@ def run_gpu(args, rank, world):
                      "traffic": traffic, "traffic_note": traffic_note,
                      "algorithmic_bytes_per_launch": int(attn_b),
                      "mean_launch_us": round(1e3 * statistics.mean(attn_ms), 3),
+                     "median_launch_us": round(1e3 * statistics.median(attn_ms), 3),
+                     "nominal_peak": NOMINAL_HBM_GBS,
+                     "frac_of_nominal": round(attn_gbs / NOMINAL_HBM_GBS, 4),
                      "kernel_hash": khash},
         "host_a0_us_per_step": round(1e6 * t_host / K, 2),
         "host_churn_us_per_step": round(1e6 * statistics.mean(churn_s), 2) if churn_s else None,

@@ -81,8 +81,8 @@ int pkv_abi_version(void);
 /* a0: host block allocator                                                  */
 /* ======================================================================== */
 /*
- * Policy ("neurogrid releases" v0.7.0: O(1) alloc/free, per-sequence block
- * tables; v0.8.0: kv_len = position + 1):
+ * Policy ("neurogrid releases" v0.7.0: constant-time block allocation and
+ * release, one block table per sequence; v0.8.0: kv_len = position + 1):
  *  - The free list is a stack, seeded bottom-to-top with `initial_free` (a
  *    permutation of 0..num_blocks-1; NULL = 0,1,2,...).  Pop takes the top.
  *  - join pops ceil(prefix_len/16) blocks in table order and takes the

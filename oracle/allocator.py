@@ -2,9 +2,9 @@
 
 Test infrastructure only (see the package docstring).
 
-The neurogrid v0.7.0 release names "Block Allocator: O(1) alloc/free,
-per-sequence block tables" with blocks of 16 tokens allocated on demand, and the
-v0.8.0 release computes ``kv_len = position + 1``.  The pages fix no policy
+The neurogrid v0.7.0 release describes a block allocator with constant-time
+allocation and release, a block table per sequence and 16-token blocks taken on
+demand; the v0.8.0 release computes ``kv_len = position + 1``.  The pages fix no policy
 beyond that; the policy below is our plainest reading and is what the C++
 allocator must reproduce bit for bit:
 

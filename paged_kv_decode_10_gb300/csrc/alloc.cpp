@@ -1,8 +1,9 @@
 // Host block allocator for the paged KV cache.
 //
-// "neurogrid releases" v0.7.0, Paged KV Cache: the cache is allocated in fixed
-// 16-token blocks on demand; "Block Allocator: O(1) alloc/free, per-sequence
-// block tables".  v0.8.0: kv_len = position + 1.  The policy (LIFO free stack,
+// "neurogrid releases" v0.7.0, Paged KV Cache: the cache grows in fixed
+// 16-token blocks taken on demand, a block allocator hands blocks out and takes
+// them back in constant time, and every sequence has its own block table.
+// v0.8.0: kv_len = position + 1.  The policy (LIFO free stack,
 // smallest free sequence id on join, lazy block at position % 16 == 0, atomic
 // failure) is stated in pkv.h.
 #include <algorithm>
