@@ -1,25 +1,35 @@
 """Benchmark of the continuous-batching decode step over a paged KV cache.
 
-One step = a0 host allocator (positions, slots, seq_lens, block tables) + one
-H2D copy of that metadata + a1 RoPE + a2 append + a3 split-KV paged attention
-+ a4 LSE merge, on one stream, for every row of the workload.  Steps are
-consecutive decode steps (every row grows by one token per step).
+One step = a0 host allocator (positions, slots, seq_lens, block tables, into a
+pinned buffer the kernels read in place; ``--metadata copy`` adds an H2D copy
+instead) + a1 RoPE + a2 append + a3 split-KV paged attention with a4 (LSE
+merge) fused into its epilogue, for every row of the workload, replayed as one
+CUDA graph.  Steps are consecutive decode steps (every row grows by one token
+per step); churn workloads also move rows out and in between steps.
 
 Default workload: ``decode16`` (B=16, L ~ U[128, 2048], 32 query / 8 KV heads,
-d=64, bf16).  Its KV (~36 MB) fits in L2, so L2 is flushed (a 2x-L2 buffer is
-written) before every timed step and only the step itself sits between the
-CUDA events.
+d=64, bf16).  Its KV (~36 MB) fits in L2, so before every timed step a buffer
+of 4x the L2 size is read (evicting the KV without dirty write-backs) and only
+the step itself sits between the CUDA events.
 
 Printed JSON line (rank 0):
-  value        whole-job KV throughput: algorithmic attention bytes of all steps
-               / device time of all steps (a0 copy + a1..a4), GB/s
-  attn_gbs     the same bytes / time of a3+a4 only
-  steps_per_s  decode steps per second (device time)
-  roofline     the split-attention kernel (a3): algorithmic bytes per launch /
-               mean launch time, against the measured HBM copy peak
-  e2e          the same metric through ``pkv_decode_step_host`` (host buffers;
-               H2D of q/k/v + metadata and D2H of the output inside the timing)
-  cpu_baseline the float64 oracle timed on this host on a bounded sample
+  value            whole-job throughput: algorithmic attention bytes of all
+                   steps / device time of all steps, GB/s
+  steps_per_s      decode steps per second (device time)
+  roofline         the attention kernel (a3 + fused a4) timed alone after the
+                   same flush: algorithmic bytes per launch / mean launch time
+                   against the measured HBM copy peak, with the ncu DRAM bytes
+                   of the same kernel source (``profiles/traffic.json``)
+  step_kernels_us  the step's kernels (RoPE/append + attention) without the host
+  host_a0_us_per_step  the host allocator per step
+  e2e              the same metric through the C ABI's captured host step
+                   (pkv_step_graph_launch: a0, inputs read and output written
+                   in place in pinned host memory, stream wait), wall clock
+  cpu_baseline     the float64 oracle timed on this host on a bounded sample
+  clocks           nvidia-smi SM clock samples over the timed regions
+  prefill, churn_wall_clock  (churn workloads) the joiners' prefix KV writes,
+                   and one pass over the churn plan timed by the wall clock
+  dense_comparator (``--comparator``) the right-padded batch paging replaces
 
 ``--impl reference`` times the float64 oracle (the only reference this method
 has) on the host cores for the same workload and metric.
