@@ -27,7 +27,9 @@
  *  - The library never allocates device memory.  The caller owns every device
  *    buffer and the CUDA stream.  Device calls are asynchronous on `stream`
  *    (a cudaStream_t passed as void*, NULL = legacy default stream), make no
- *    device-to-host copy and check cudaGetLastError after each launch.
+ *    device-to-host copy (the host-step calls at the end of this header are
+ *    the exception: they return the result in host memory) and check
+ *    cudaGetLastError after each launch.
  *  - Every tensor is dense and row-major in the layout stated.  dtype is
  *    PKV_F32 or PKV_BF16 and applies to q, k, v, the caches and the output.
  *  - dev_err_flag (nullable, device int32): kernels that meet an out-of-range

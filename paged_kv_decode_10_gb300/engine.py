@@ -16,11 +16,12 @@ With ``n_layers > 1`` every layer has its own K/V pool ("neurogrid releases"
 v0.7.0: per-layer caches) indexed by the same block tables; a step runs the
 layers in order through ``pkv_decode_step_layers`` (each layer's kernels
 overlap the previous layer's tail) and one graph holds all of them.
-``pool_blocks_for_vram`` sizes the pool from the free device memory (v0.7.0:
-blocks from available VRAM, 25% budget).
+``pool_blocks_for_vram`` sizes the pool from the free device memory (v0.7.0
+sizes it from a quarter of the free VRAM).
 
 Joins and leaves only edit the allocator's block tables ("neurogrid releases"
-v0.7.0: on-demand blocks, O(1) alloc/free); no KV is moved when the batch
+v0.7.0: blocks taken on demand, constant-time allocation and release); no KV
+is moved when the batch
 changes, which is what replaces the extract/re-assemble rebatch of the helexa
 continuous-batching PR.
 """
