@@ -94,19 +94,3 @@ def prefill_kv(k, v, positions, slot_mapping, k_cache, v_cache, *, base, dtype,
         k_cache[blk, :, row, :] = round_to(rope_rotate_half(k[t], positions[t], base), dtype)
         v_cache[blk, :, row, :] = v[t]
     return k_cache, v_cache
-
-
-def attend_rows(q_rot, k_cache, v_cache, block_tables, seq_lens, rows, *, scale,
-                attn_bias=None, block_size=16):
-    """Float64 attention outputs (not rounded) for selected batch ``rows``.
-
-    Used to check sampled rows of large workloads one by one: ``q_rot`` and the
-    caches are the post-RoPE, post-append state computed by this oracle.
-    """
-    res = {}
-    for b in rows:
-        bias = None if attn_bias is None else attn_bias[b]
-        o, _ = decode_attention_row(q_rot[b], k_cache, v_cache, block_tables[b],
-                                    int(seq_lens[b]), scale, bias, block_size)
-        res[b] = o
-    return res
