@@ -2,8 +2,8 @@
 
 TEST INFRASTRUCTURE ONLY.  This package is a plain, slow, float64 CPU
 restatement of what the decode step computes.  Only the test suite, the smoke
-check in ``__graft_entry__`` and the CPU-baseline leg of ``bench.py`` may import
-it.  The product path (the CUDA library and its Python binding) never imports,
+check in ``__graft_entry__`` and the CPU legs of ``bench.py`` (``cpu_baseline``
+and ``--impl reference``) may import it.  The product path (the CUDA library and its Python binding) never imports,
 links or executes anything in here, and this package imports nothing from the
 product: the two share no code, tables or constants.
 
@@ -27,5 +27,10 @@ Modules
                block table (parity pinned by the tests in
                ``tests/test_oracle_pins.py``).
 ``allocator``  model of the host block allocator (LIFO free stack).
-``step``       one whole decode step: RoPE, slot append, attention.
+``step``       one whole decode step (RoPE, slot append, attention) and the
+               joiners' prefix write (RoPE of each prefix key, slot write).
+``dense``      the right-padded dense batch: assemble, extract a row, gap mask.
+
+Every function is pinned by tests in ``tests/test_oracle_pins.py`` against
+closed forms, hand-worked values, library routines or brute force.
 """
