@@ -3,9 +3,10 @@
 TEST INFRASTRUCTURE ONLY.  This package is a plain, slow, float64 CPU
 restatement of what the decode step computes.  Only the test suite, the smoke
 check in ``__graft_entry__`` and the CPU legs of ``bench.py`` (``cpu_baseline``
-and ``--impl reference``) may import it.  The product path (the CUDA library and its Python binding) never imports,
-links or executes anything in here, and this package imports nothing from the
-product: the two share no code, tables or constants.
+and ``--impl reference``) may import it.  The product path (the CUDA library
+and its Python binding) never imports, links or executes anything in here, and
+this package imports nothing from the product: the two share no code, tables or
+constants.
 
 Sources (the three web pages the method is taken from):
 
