@@ -7,6 +7,7 @@ or call :func:`build`.  Set ``PKV_PTXAS_VERBOSE=1`` to print register and
 shared-memory use of every kernel.
 """
 import concurrent.futures as cf
+import fcntl
 import os
 import shutil
 import subprocess
@@ -52,15 +53,29 @@ def _compile(src, verbose):
     return obj, (res.stdout + res.stderr) if verbose else ""
 
 
+def _fresh():
+    if not os.path.exists(LIB):
+        return False
+    return os.path.getmtime(LIB) >= max(os.path.getmtime(p) for p in _deps())
+
+
 def build(force=False, verbose=None):
-    """Compile and link the library; returns its path."""
+    """Compile and link the library; returns its path.  Processes that build at
+    the same time (one per rank) take turns on a lock file; a process that
+    finds the library fresh once it holds the lock does nothing."""
     if verbose is None:
         verbose = os.environ.get("PKV_PTXAS_VERBOSE") == "1"
     os.makedirs(os.path.join(BUILD, "obj"), exist_ok=True)
-    if not force and os.path.exists(LIB):
-        newest = max(os.path.getmtime(p) for p in _deps())
-        if os.path.getmtime(LIB) >= newest:
+    if not force and _fresh():
+        return LIB
+    with open(os.path.join(BUILD, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        if not force and _fresh():
             return LIB
+        return _build_locked(verbose)
+
+
+def _build_locked(verbose):
     srcs = _sources()
     with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
         results = list(ex.map(lambda s: _compile(s, verbose), srcs))
@@ -69,7 +84,7 @@ def build(force=False, verbose=None):
             if log:
                 sys.stderr.write(log)
     objs = [o for o, _ in results]
-    tmp = LIB + ".tmp"
+    tmp = f"{LIB}.tmp{os.getpid()}"
     cmd = [_nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
