@@ -171,7 +171,18 @@ def _check(rc):
 # --------------------------------------------------------------------------
 # host allocator
 # --------------------------------------------------------------------------
-def _np_ptr(a, ctype):
+_NP_OF = {ctypes.c_int32: np.int32, ctypes.c_int64: np.int64}
+
+
+def _np_ptr(a, ctype, min_len=0):
+    """Pointer to a numpy array the library reads or fills: the dtype must be
+    the C type's, the array C-contiguous and at least ``min_len`` long (the C
+    side writes through the pointer without knowing the array)."""
+    if not isinstance(a, np.ndarray) or a.dtype != _NP_OF[ctype]:
+        raise PkvError(ERR_INVALID_ARG, f"expected a numpy {np.dtype(_NP_OF[ctype])} array, "
+                                        f"got {getattr(a, 'dtype', type(a))}")
+    if not a.flags.c_contiguous or a.size < min_len:
+        raise PkvError(ERR_INVALID_ARG, f"array must be C-contiguous with >= {min_len} entries")
     return a.ctypes.data_as(ctypes.POINTER(ctype))
 
 
@@ -219,10 +230,9 @@ class BlockAllocator:
         ids = np.empty(len(lens), np.int32)
         pos = slots = None
         if slots_out is not None:
-            pos, slots = slots_out
-            if len(pos) < lens.sum() or len(slots) < lens.sum():
-                raise PkvError(ERR_INVALID_ARG, "slots_out too short for the prefixes")
-            pos, slots = _np_ptr(pos, ctypes.c_int32), _np_ptr(slots, ctypes.c_int64)
+            n = int(lens.astype(np.int64).sum())
+            pos = _np_ptr(slots_out[0], ctypes.c_int32, n)
+            slots = _np_ptr(slots_out[1], ctypes.c_int64, n)
         _check(self._lib.pkv_seqs_join(self._h, _np_ptr(lens, ctypes.c_int32), len(lens),
                                        _np_ptr(ids, ctypes.c_int32), pos, slots))
         return ids
@@ -242,10 +252,11 @@ class BlockAllocator:
                    np.empty((B, bt_stride), np.int32))
         pos, slots, lens, tables = out
         _check(self._lib.pkv_prepare_step(self._h, _np_ptr(ids, ctypes.c_int32), B,
-                                          _np_ptr(pos, ctypes.c_int32),
-                                          _np_ptr(slots, ctypes.c_int64),
-                                          _np_ptr(lens, ctypes.c_int32),
-                                          _np_ptr(tables, ctypes.c_int32), int(bt_stride)))
+                                          _np_ptr(pos, ctypes.c_int32, B),
+                                          _np_ptr(slots, ctypes.c_int64, B),
+                                          _np_ptr(lens, ctypes.c_int32, B),
+                                          _np_ptr(tables, ctypes.c_int32, B * int(bt_stride)),
+                                          int(bt_stride)))
         return pos, slots, lens, tables
 
     def step_runner(self, seq_ids, bt_stride, out):
@@ -255,9 +266,9 @@ class BlockAllocator:
         ids = np.ascontiguousarray(seq_ids, dtype=np.int32)
         pos, slots, lens, tables = out
         fn, h, B, bt = self._lib.pkv_prepare_step, self._h, len(ids), int(bt_stride)
-        ptrs = (_np_ptr(ids, ctypes.c_int32), _np_ptr(pos, ctypes.c_int32),
-                _np_ptr(slots, ctypes.c_int64), _np_ptr(lens, ctypes.c_int32),
-                _np_ptr(tables, ctypes.c_int32))
+        ptrs = (_np_ptr(ids, ctypes.c_int32), _np_ptr(pos, ctypes.c_int32, B),
+                _np_ptr(slots, ctypes.c_int64, B), _np_ptr(lens, ctypes.c_int32, B),
+                _np_ptr(tables, ctypes.c_int32, B * bt))
         keep = (ids, out)
 
         def run():
@@ -285,8 +296,8 @@ class BlockAllocator:
             out = (np.empty(count, np.int32), np.empty(count, np.int64))
         pos, slots = out
         _check(self._lib.pkv_seq_slots(self._h, int(seq_id), int(start), int(count),
-                                       _np_ptr(pos, ctypes.c_int32),
-                                       _np_ptr(slots, ctypes.c_int64)))
+                                       _np_ptr(pos, ctypes.c_int32, int(count)),
+                                       _np_ptr(slots, ctypes.c_int64, int(count))))
         return pos, slots
 
     def num_free(self):
@@ -535,6 +546,8 @@ def dense_assemble(k_snaps, v_snaps, lens, padded_len, k_dense, v_dense, cap, st
     Snapshots and the dense caches use the block layout ``[blocks, Hkv, 16, d]``;
     the dense batch has ``cap`` tokens per row."""
     lens = np.ascontiguousarray(lens, dtype=np.int32)
+    if not len(k_snaps) == len(v_snaps) == len(lens):
+        raise PkvError(ERR_INVALID_ARG, "one K and one V snapshot per length")
     Hkv, d = k_dense.shape[1], k_dense.shape[3]
     _check(load().pkv_dense_assemble(_ptr_array(k_snaps), _ptr_array(v_snaps),
                                      _np_ptr(lens, ctypes.c_int32), len(lens), int(padded_len),
@@ -548,6 +561,8 @@ def dense_extract(k_dense, v_dense, cap, rows, prefix_lens, padded_len, steps, k
     (``pkv_dense_extract``)."""
     rows = np.ascontiguousarray(rows, dtype=np.int32)
     prefix_lens = np.ascontiguousarray(prefix_lens, dtype=np.int32)
+    if not len(prefix_lens) == len(k_snaps) == len(v_snaps) == len(rows):
+        raise PkvError(ERR_INVALID_ARG, "one prefix length and K/V snapshot per row")
     Hkv, d = k_dense.shape[1], k_dense.shape[3]
     _check(load().pkv_dense_extract(_ptr(k_dense), _ptr(v_dense), int(cap),
                                     _np_ptr(rows, ctypes.c_int32),

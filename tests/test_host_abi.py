@@ -270,3 +270,23 @@ def test_batched_join_leave_equal_single_calls_in_order(host_lib, seed):
         cpp.join_many([1, bt * 16 + 1])
     assert cpp.free_stack() == before
     same_state()
+
+
+def test_binding_rejects_arrays_the_library_would_misread(host_lib):
+    """Output arrays of the wrong dtype, layout or length are refused before the
+    C side writes through them."""
+    from paged_kv_decode_10_gb300 import binding
+    a = binding.BlockAllocator(64, 4, 8)
+    sid = a.join(20)
+    with pytest.raises(binding.PkvError):
+        a.seq_slots(sid, 0, 20, out=(np.empty(20, np.int64), np.empty(20, np.int64)))
+    with pytest.raises(binding.PkvError):
+        a.seq_slots(sid, 0, 20, out=(np.empty(20, np.int32), np.empty(19, np.int64)))
+    with pytest.raises(binding.PkvError):
+        a.join_many([5, 7], (np.empty(12, np.int32), np.empty(11, np.int64)))
+    with pytest.raises(binding.PkvError):
+        a.prepare_step([sid], 8, out=(np.empty(1, np.int32), np.empty(1, np.int64),
+                                      np.empty(1, np.int32), np.empty((1, 16), np.int32)[:, ::2]))
+    assert a.num_free() == 64 - 2          # nothing above changed the allocator
+    pos, slots = a.seq_slots(sid, 0, 20)
+    assert pos.tolist() == list(range(20))
