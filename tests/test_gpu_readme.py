@@ -1,4 +1,4 @@
-"""The Python example in README.md runs as written on the GPU."""
+"""The Python usage example of the repository's readme runs as written on the GPU."""
 import os
 import re
 
@@ -14,7 +14,7 @@ def test_readme_example_runs():
     blocks = re.findall(r"```python\n(.*?)```", text, flags=re.S)
     assert blocks, "README has no python example"
     scope = {}
-    exec(compile(blocks[0], "README.md example", "exec"), scope)
+    exec(compile(blocks[0], "readme example", "exec"), scope)
     out, B = scope["out"], scope["B"]
     assert tuple(out.shape) == (B, 32, 128)
     assert bool(out.float().isfinite().all())
