@@ -348,6 +348,73 @@ def test_step_keys_are_stored_post_rope():
     assert abs(lhs - rhs) < 1e-5
 
 
+def _complex_rotate(x, pos, base=10000.0):
+    """Rotate head vectors ``x[..., d]`` at ``pos`` by complex multiplication:
+    pair (x[i], x[i + d/2]) is the number x[i] + i x[i + d/2] times e^{i theta_i}."""
+    d = x.shape[-1]
+    half = d // 2
+    theta = pos / base ** (2.0 * np.arange(half) / d)
+    z = (x[..., :half] + 1j * x[..., half:]) * np.exp(1j * theta)
+    return np.concatenate([z.real, z.imag], axis=-1)
+
+
+def _torch_round(x, dtype):
+    t = torch.from_numpy(np.ascontiguousarray(x))
+    return t.to(torch.bfloat16 if dtype == "bf16" else torch.float32).double().numpy()
+
+
+@pytest.mark.parametrize("dtype,L,hq,hkv,d", [("bf16", 37, 8, 2, 64), ("bf16", 300, 32, 8, 128),
+                                              ("f32", 21, 4, 2, 64)])
+def test_step_rotates_the_query_at_its_position(dtype, L, hq, hkv, d):
+    """helexa issue 121, slice 1 (per-row cos/sin at each row's position,
+    rotate-half): the step rotates the new query at ``positions[b]`` -- the
+    row's cached length, one less than ``seq_lens[b]`` -- rounds it once to the
+    storage type and scores the gathered keys with it.  Built without the
+    oracle: the rotation by complex multiplication, the rounding by torch's
+    cast, the attention by torch's float64 SDPA over a contiguous cache (an
+    identity block table).  The mistakes this must catch (the query rotated at
+    seq_lens, not rotated, or scored without its rounding) are shown to move
+    the output by many units of the storage type's last place."""
+    r = np.random.default_rng(1000 + L)
+    nblk = -(-(L + 1) // 16)
+    # cached keys are post-RoPE values, drawn directly; values on the grid of T
+    k_cache = _torch_round(r.standard_normal((nblk, hkv, 16, d)), dtype)
+    v_cache = _torch_round(r.standard_normal((nblk, hkv, 16, d)), dtype)
+    # a large query makes the softmax sharp, so that the rounding of the
+    # rotated query shows in the output
+    q = _torch_round(r.standard_normal((1, hq, d)) * 6.0, dtype)
+    knew = _torch_round(r.standard_normal((1, hkv, d)), dtype)
+    vnew = _torch_round(r.standard_normal((1, hkv, d)), dtype)
+    pos, scale = L, 1 / math.sqrt(d)
+    res = decode_step(q, knew, vnew, [pos], [pos], [L + 1], np.arange(nblk)[None, :],
+                      k_cache, v_cache, scale=scale, base=10000.0, dtype=dtype)
+
+    def reference(q_pos, round_q=True, rotate=True):
+        qr = _complex_rotate(q[0], q_pos) if rotate else q[0]
+        qr = _torch_round(qr, dtype) if round_q else qr
+        kr = _torch_round(_complex_rotate(knew[0], pos), dtype)
+        K = k_cache.transpose(1, 0, 2, 3).reshape(hkv, nblk * 16, d).copy()
+        V = v_cache.transpose(1, 0, 2, 3).reshape(hkv, nblk * 16, d).copy()
+        K[:, pos], V[:, pos] = kr, vnew[0]
+        G = hq // hkv
+        o = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(qr)[:, None, :],
+            torch.from_numpy(K[:, :L + 1]).repeat_interleave(G, dim=0),
+            torch.from_numpy(V[:, :L + 1]).repeat_interleave(G, dim=0), scale=scale)[:, 0]
+        return qr, _torch_round(o.numpy(), dtype)
+
+    q_ref, out_ref = reference(pos)
+    np.testing.assert_array_equal(res["q_rot"][0], q_ref)
+    ulp = np.maximum(np.abs(out_ref), 2.0 ** -20) * (2.0 ** -7 if dtype == "bf16" else 2.0 ** -23)
+    assert (np.abs(res["out"][0] - out_ref) <= ulp).all()
+    # each plausible mistake moves the output well past that tolerance
+    wrong = [reference(pos + 1)[1], reference(pos, rotate=False)[1]]
+    if dtype == "bf16":
+        wrong.append(reference(pos, round_q=False)[1])
+    for w in wrong:
+        assert (np.abs(w - out_ref) > 4 * ulp).any()
+
+
 # --------------------------------------------------------------------------
 # allocator model against the hand-derived trace
 # --------------------------------------------------------------------------
