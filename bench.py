@@ -7,10 +7,13 @@ merge) fused into its epilogue, for every row of the workload, replayed as one
 CUDA graph.  Steps are consecutive decode steps (every row grows by one token
 per step); churn workloads also move rows out and in between steps.
 
-Default workload: ``decode16`` (B=16, L ~ U[128, 2048], 32 query / 8 KV heads,
-d=64, bf16).  Its KV (~36 MB) fits in L2, so before every timed step a buffer
-of 4x the L2 size is read (evicting the KV without dirty write-backs) and only
-the step itself sits between the CUDA events.
+Default workload: ``churn256`` (B=256, L ~ lognormal(median 2048, sigma 0.5)
+clipped to [512, 8192], 32 query / 8 KV heads, d=128, bf16; before every step
+26 rows leave and 26 join with prefixes of 256-1024 tokens, whose KV the
+prefill kernel writes).  A step reads ~2.4 GB of KV, far more than L2; a
+buffer of 4x the L2 size is still read before every timed step (evicting the
+KV without dirty write-backs) and only the step itself sits between the CUDA
+events.  ``--workload decode16`` (or any other workload name) selects another.
 
 Printed JSON line (rank 0):
   value            whole-job throughput: algorithmic attention bytes of all
@@ -20,13 +23,16 @@ Printed JSON line (rank 0):
                    same flush: algorithmic bytes per launch / mean launch time
                    against the measured HBM copy peak, with the ncu DRAM bytes
                    of the same kernel source (``profiles/traffic.json``)
+  rooflines        the same for the workloads named by ``--also`` (default
+                   ragged64 and long131k), each set up and timed in this run
   step_kernels_us  the step's kernels (RoPE/append + attention) without the host
   host_a0_us_per_step  the host allocator per step
   e2e              the same metric through the C ABI's captured host step
                    (pkv_step_graph_launch: a0, inputs read and output written
                    in place in pinned host memory, stream wait), wall clock
-  cpu_baseline     the float64 oracle timed on this host on a bounded sample
-  clocks           nvidia-smi SM clock samples over the timed regions
+  cpu_baseline     the float64 oracle on this host's cores, wall clock, over a
+                   sample of the final step's (row, KV head) units
+  clocks           nvidia-smi SM clock samples taken inside the timed regions
   prefill, churn_wall_clock  (churn workloads) the joiners' prefix KV writes,
                    and one pass over the churn plan timed by the wall clock
   dense_comparator (``--comparator``) the right-padded batch paging replaces
@@ -67,7 +73,10 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
-    ap.add_argument("--workload", default="decode16")
+    ap.add_argument("--workload", default="churn256")
+    ap.add_argument("--also", default="ragged64,long131k",
+                    help="other workloads whose attention kernel is timed alone in the same "
+                         "run (comma-separated; empty for none)")
     ap.add_argument("--flags", type=int, default=0, help="1 = CUDA-core attention consumer")
     ap.add_argument("--parts", type=int, default=0, help="attention partition (0 = default)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -159,7 +168,9 @@ def attn_bytes(lens_after, Hq, Hkv, d, elem):
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+    """nvidia-smi samples of SM clock and throttle reasons, kept for the timed
+    regions only: ``window()`` brackets a region, and a sample counts when it
+    arrives inside one (or within 20 ms after its end)."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -167,12 +178,11 @@ class ClockSampler:
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.lines = []
-        self.first = 0
+        self.lines = []          # (arrival time, line)
+        self.windows = []
 
     def start(self):
-        """Starts sampling every 10 ms and returns once the first sample is in
-        (so that the samples after ``start`` fall inside the region that follows)."""
+        """Starts sampling every 10 ms and returns once the first sample is in."""
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
@@ -186,25 +196,38 @@ class ClockSampler:
         t_end = time.perf_counter() + 5.0
         while not self.lines and time.perf_counter() < t_end:
             time.sleep(0.005)
-        self.first = len(self.lines)
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    class _Window:
+        def __init__(self, owner):
+            self.owner = owner
+
+        def __enter__(self):
+            self.t0 = time.perf_counter()
+
+        def __exit__(self, *exc):
+            self.owner.windows.append((self.t0, time.perf_counter() + 0.02))
+
+    def window(self):
+        return self._Window(self)
 
     def stop(self):
         if self.proc is None:
             return None
-        self.lines = self.lines[self.first:] or self.lines[-1:]
+        time.sleep(0.03)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
         self.thread.join(timeout=2)
+        inside = [ln for t, ln in self.lines if any(a <= t <= b for a, b in self.windows)]
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in inside:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 8:
                 continue
@@ -216,63 +239,140 @@ class ClockSampler:
             for n, v in zip(names, parts[4:8]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
+        timed_s = sum(b - a - 0.02 for a, b in self.windows)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0,
+                    "timed_region_s": round(timed_s, 3)}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "timed_region_s": round(timed_s, 3)}
 
 
 # ---------------------------------------------------------------------------
 # oracle on the host (cpu baseline and the reference arm)
 # ---------------------------------------------------------------------------
-def _oracle_row_job(job):
-    """Runs inside a spawned worker: one row of the step through the oracle."""
+# The sample is a set of (row, KV head) units of one decode step.  Their raw
+# inputs (the storage type's bits: q rows of the group, the new k and v, the
+# row's K/V pages of that head) sit in one shared-memory block; spawned
+# workers, one per host core, each run the float64 oracle's decode step on one
+# unit at a time.  A pass over the sample is timed by the wall clock.
+_WORKER = None
+
+
+def _oracle_worker_init(shm_name, spec):
+    global _WORKER
+    from multiprocessing import shared_memory
+    _WORKER = (shared_memory.SharedMemory(name=shm_name), spec)
+
+
+def _upcast(raw, dtype):
+    """Storage-type values (bf16 as its 16-bit pattern, or float32) to float64."""
+    if dtype == "bf16":
+        return (raw.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return raw.astype(np.float64)
+
+
+def _oracle_unit_job(i):
+    """Runs inside a worker: unit i through the oracle's decode step."""
     from oracle.step import decode_step
-    q, k, v, pos, slot, lens, n, kc, vc, scale, dtype = job
-    t0 = time.perf_counter()
-    decode_step(q, k, v, pos, [slot], lens, np.arange(n)[None, :], kc, vc, scale=scale,
-                base=10000.0, dtype=dtype)
-    return time.perf_counter() - t0
+    shm, (dtype, G, d, scale, base, table) = _WORKER
+    elem = np.uint16 if dtype == "bf16" else np.float32
+    buf = np.ndarray((shm.size // np.dtype(elem).itemsize,), dtype=elem, buffer=shm.buf)
+    off, n, pos, L = (int(x) for x in table[i])
+    page = 16 * d
+    q = _upcast(buf[off:off + G * d], dtype).reshape(1, G, d)
+    k = _upcast(buf[off + G * d:off + (G + 1) * d], dtype).reshape(1, 1, d)
+    v = _upcast(buf[off + (G + 1) * d:off + (G + 2) * d], dtype).reshape(1, 1, d)
+    o = off + (G + 2) * d
+    kc = _upcast(buf[o:o + n * page], dtype).reshape(n, 1, 16, d)
+    vc = _upcast(buf[o + n * page:o + 2 * n * page], dtype).reshape(n, 1, 16, d)
+    decode_step(q, k, v, [pos], [pos], [L], np.arange(n)[None, :], kc, vc, scale=scale,
+                base=base, dtype=dtype)
+    return i
 
 
-def oracle_jobs(w, caches, tokens, meta, rows):
+def _raw(t, dtype):
+    """A CPU tensor's values as the numpy array the workers read."""
     import torch
-    pos, slots, lens, tables = meta
-    jobs, nbytes = [], 0
-    elem = 2 if w.dtype == "bf16" else 4
-    for b in rows:
-        n = -(-int(lens[b]) // 16)
-        blocks = torch.from_numpy(tables[b, :n].astype(np.int64))
-        kc = caches[0][blocks].double().numpy()
-        vc = caches[1][blocks].double().numpy()
-        j = int(pos[b]) // 16
-        jobs.append(tuple(t[b:b + 1].double().numpy() for t in tokens) +
-                    (pos[b:b + 1], j * 16 + int(slots[b]) % 16, lens[b:b + 1], n, kc, vc,
-                     w.scale, w.dtype))
-        nbytes += attn_bytes([lens[b]], w.Hq, w.Hkv, w.d, elem)
-    return jobs, nbytes
+    t = t.contiguous()
+    return t.view(torch.int16).numpy().view(np.uint16) if dtype == "bf16" else t.numpy()
 
 
-def oracle_pool(cores):
-    import multiprocessing as mp
-    env_keys = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
-    saved = {k: os.environ.get(k) for k in env_keys}
-    for k in env_keys:
-        os.environ[k] = "1"
-    pool = mp.get_context("spawn").Pool(cores)
-    for k, v in saved.items():
-        if v is None:
-            os.environ.pop(k, None)
-        else:
-            os.environ[k] = v
-    return pool
+class OracleSample:
+    """The (row, KV head) units of ``rows`` in one decode step, packed into shared
+    memory.  ``pages(b)`` returns the K and V pages ``[n, Hkv, 16, d]`` of row
+    b's first n blocks as CPU tensors; ``tokens`` are the step's new q/k/v; ``meta``
+    its (positions, slots, seq_lens, block_tables)."""
+
+    def __init__(self, w, rows, tokens, meta, pages):
+        from multiprocessing import shared_memory
+        self.w, self.rows = w, list(rows)
+        pos, _, lens, _ = meta
+        G, d = w.group, w.d
+        q, k, v = (t.cpu() for t in tokens)
+        units, chunks, off = [], [], 0
+        for b in self.rows:
+            n = -(-int(lens[b]) // 16)
+            kp, vp = pages(b, n)
+            for g in range(w.Hkv):
+                parts = [q[b, g * G:(g + 1) * G], k[b, g], v[b, g], kp[:, g], vp[:, g]]
+                flat = [_raw(x, w.dtype).reshape(-1) for x in parts]
+                units.append((off, n, int(pos[b]), int(lens[b])))
+                chunks.append(flat)
+                off += sum(len(x) for x in flat)
+        itemsize = 2 if w.dtype == "bf16" else 4
+        self.shm = shared_memory.SharedMemory(create=True, size=max(off * itemsize, 16))
+        buf = np.ndarray((off,), dtype=np.uint16 if w.dtype == "bf16" else np.float32,
+                         buffer=self.shm.buf)
+        for (o, _, _, _), flat in zip(units, chunks):
+            for x in flat:
+                buf[o:o + len(x)] = x
+                o += len(x)
+        del buf
+        self.table = np.array(units, np.int64)
+        # longest units first, so the pass does not end on one long unit
+        self.order = [int(i) for i in np.argsort(-self.table[:, 1], kind="stable")]
+        elem = 2 if w.dtype == "bf16" else 4
+        self.nbytes = attn_bytes([lens[b] for b in self.rows], w.Hq, w.Hkv, w.d, elem)
+
+    def pool(self, cores):
+        import multiprocessing as mp
+        env_keys = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+        saved = {k: os.environ.get(k) for k in env_keys}
+        for k in env_keys:
+            os.environ[k] = "1"
+        try:
+            spec = (self.w.dtype, self.w.group, self.w.d, self.w.scale, self.w.rope_base,
+                    self.table)
+            return mp.get_context("spawn").Pool(cores, initializer=_oracle_worker_init,
+                                                initargs=(self.shm.name, spec))
+        finally:
+            for k, val in saved.items():
+                if val is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = val
+
+    def run_pass(self, pool):
+        """One pass over every unit; returns its wall-clock seconds."""
+        t0 = time.perf_counter()
+        pool.map(_oracle_unit_job, self.order, chunksize=1)
+        return time.perf_counter() - t0
+
+    def close(self):
+        self.shm.close()
+        self.shm.unlink()
+
+    def describe(self):
+        every = self.rows[1] - self.rows[0] if len(self.rows) > 1 else 1
+        return (f"the {len(self.table)} (row, KV head) units of {len(self.rows)} of the "
+                f"{self.w.B} rows (every {every}th row from row 0) of one {self.w.name} decode "
+                f"step; float64 numpy oracle, one spawned single-threaded worker per host core, "
+                f"one unit per task, wall clock")
 
 
-def run_oracle_sample(pool, cores, jobs, nbytes):
-    """Returns (GB/s, compute seconds per core, rows)."""
-    secs = pool.map(_oracle_row_job, jobs, chunksize=1)
-    per_core = sum(secs) / cores
-    return nbytes / per_core / 1e9, per_core, len(jobs)
+def sample_rows(w, target_rows=32):
+    step = max(1, w.B // target_rows)
+    return list(range(0, w.B, step))
 
 
 def host_cores():
@@ -318,7 +418,68 @@ def setup(w, device, parts, flags, steps_total, metadata, n_layers=1):
     return dec, ids, tokens, (k_cache, v_cache) if gen_dev == "cpu" else None
 
 
-def run_gpu(args, rank, world):
+def time_graph_launches(g, K, flush, stream, sampler):
+    """K replays of graph g, each after an L2 flush, between CUDA events on
+    ``stream``; returns the milliseconds of each."""
+    import torch
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    with sampler.window():
+        for i in range(K):
+            flush()
+            ev[i][0].record(stream)
+            g.replay()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    return [e[0].elapsed_time(e[1]) for e in ev]
+
+
+def attention_roofline(name, args, device, flush, stream, sampler, peak):
+    """The attention kernel (a3 + fused a4) alone on another workload, in the
+    bench's launch configuration: every row joined, a few eager decode steps,
+    then K graph launches of the attention call on the final step's state, each
+    after an L2 flush; also the step's kernels (RoPE/append + attention)."""
+    import torch
+    from paged_kv_decode_10_gb300 import binding, workloads
+    w = workloads.make_workload(name)
+    n_eager = 4
+    dec, ids, tokens, _ = setup(w, device, args.parts, args.flags, n_eager, args.metadata)
+    for s in range(n_eager):
+        dec.step(ids, *tokens[s])
+    torch.cuda.synchronize()
+    B = len(ids)
+    lens = np.array(dec.last_metadata[2])
+    step_args = dec.step_args(B, *tokens[n_eager - 1])   # re-running the last step is idempotent
+    cap = torch.cuda.Stream(device)
+    cap.wait_stream(stream)
+    attn_graph, kern_graph = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(attn_graph, stream=cap):
+        binding.decode_attention(dec.q_rot[:B], dec.k_cache, dec.v_cache, dec.tables,
+                                 dec.seq_lens, scale=dec.scale, num_parts=dec.num_parts,
+                                 workspace=dec.workspace, out=dec.out[:B], flags=dec.flags,
+                                 err=dec.err, stream=cap)
+    with torch.cuda.graph(kern_graph, stream=cap):
+        binding.decode_step_args(step_args, cap)
+    stream.wait_stream(cap)
+    attn_ms = time_graph_launches(attn_graph, args.steps, flush, stream, sampler)
+    kern_ms = time_graph_launches(kern_graph, args.steps, flush, stream, sampler)
+    assert dec.device_errors() == 0, f"device error flag set during the {name} timing"
+    elem = 2 if w.dtype == "bf16" else 4
+    ab = attn_bytes(lens, w.Hq, w.Hkv, w.d, elem)
+    gbs = ab / (statistics.mean(attn_ms) / 1e3) / 1e9
+    traffic, note = profiled_traffic(name, kernel_source_hash(), ab)
+    return {"workload": name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.d,
+            "mean_kv_len": float(np.mean(lens)), "num_parts": dec.num_parts,
+            "bound": "hbm", "kernel": "attn_split_kernel (a3 + fused a4), timed alone",
+            "achieved": round(gbs, 2), "peak": peak, "unit": "GB/s", "frac": round(gbs / peak, 4),
+            "traffic": traffic, "traffic_note": note, "algorithmic_bytes_per_launch": int(ab),
+            "mean_launch_us": round(1e3 * statistics.mean(attn_ms), 3),
+            "median_launch_us": round(1e3 * statistics.median(attn_ms), 3),
+            "frac_of_nominal": round(gbs / NOMINAL_HBM_GBS, 4),
+            "step_kernels_us": round(1e3 * statistics.mean(kern_ms), 3),
+            "steps_per_s": round(1e3 / statistics.mean(kern_ms), 1)}
+
+
+def run_gpu(args, rank, world, want_cpu=False):
     import torch
     from paged_kv_decode_10_gb300 import binding, workloads
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -326,8 +487,8 @@ def run_gpu(args, rank, world):
     torch.cuda.set_device(device)
     w = workloads.make_workload(args.workload)
     W, K, GW = args.warmup, args.steps, 2
-    dec, ids, tokens, cpu_caches = setup(w, device, args.parts, args.flags, W + GW + K + 1,
-                                          args.metadata, args.layers)
+    dec, ids, tokens, _ = setup(w, device, args.parts, args.flags, W + GW + K + 1,
+                                args.metadata, args.layers)
     assert dec.bt_stride * 16 >= int(w.seq_lens.max()) + W + GW + K + 64
     B = len(ids)
     elem = 2 if w.dtype == "bf16" else 4
@@ -341,10 +502,6 @@ def run_gpu(args, rank, world):
     def flush():
         if not args.no_flush:
             flush_buf.sum()
-
-    oracle_state = None
-    if not args.no_cpu and rank == 0 and cpu_caches is not None:
-        oracle_state = (cpu_caches, [(t[0] if args.layers > 1 else t).cpu() for t in tokens[0]])
 
     churn_s = []
     prefill_log = []     # (tokens, start event, end event) per churn step
@@ -396,13 +553,10 @@ def run_gpu(args, rank, world):
             prefill_log.append((s, n * dec.n_layers, e0, e1))
 
     # warm-up: eager steps through the C ABI (one pkv_decode_step call each)
-    meta0 = None
     for s in range(W):
         churn(s)
         q, k, v = tokens[s]
         dec.step(ids, q, k, v)
-        if s == 0:
-            meta0 = [np.array(x) for x in dec.last_metadata]
     # the timed step: one CUDA graph (metadata H2D + rope/append + attention)
     dec.capture(B)
 
@@ -432,18 +586,19 @@ def run_gpu(args, rank, world):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     t_host = 0.0
-    for i in range(K):
-        churn(W + GW + i)
-        stage(W + GW + i)
-        dec.wait_host_buffer()   # the replay two steps back still reads it
-        t0 = time.perf_counter()
-        lens_after.append(np.array(dec.prepare_host(ids)[2]))
-        t_host += time.perf_counter() - t0
-        flush()   # still running on the GPU when the replay below is enqueued
-        evs[i][0].record(stream)
-        dec.replay_step()
-        evs[i][1].record(stream)
-    torch.cuda.synchronize()
+    with sampler.window():
+        for i in range(K):
+            churn(W + GW + i)
+            stage(W + GW + i)
+            dec.wait_host_buffer()   # the replay two steps back still reads it
+            t0 = time.perf_counter()
+            lens_after.append(np.array(dec.prepare_host(ids)[2]))
+            t_host += time.perf_counter() - t0
+            flush()   # still running on the GPU when the replay below is enqueued
+            evs[i][0].record(stream)
+            dec.replay_step()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     step_ms = [a.elapsed_time(b) for a, b in evs]
@@ -474,19 +629,26 @@ def run_gpu(args, rank, world):
     stream.wait_stream(cap)
 
     def time_graph(g):
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
-        for i in range(K):
-            flush()
-            ev[i][0].record(stream)
-            g.replay()
-            ev[i][1].record(stream)
-        torch.cuda.synchronize()
-        return [e[0].elapsed_time(e[1]) for e in ev]
+        return time_graph_launches(g, K, flush, stream, sampler)
 
     attn_ms = time_graph(attn_graph)
     kern_ms = time_graph(kern_graph)
-    clocks = sampler.stop()   # sampled over the timed steps and the two timings above
     last_lens = lens_after[-1]
+
+    # the oracle's sample: rows of the final timed step, their pages copied to
+    # the host before the state moves on
+    sample = None
+    if want_cpu:
+        meta = [np.array(x) for x in dec.last_metadata]
+        last_tok = tokens[W + GW + K - 1]
+        if args.layers > 1:
+            last_tok = tuple(t[0] for t in last_tok)
+
+        def pages(b, n):
+            idx = torch.from_numpy(meta[3][b, :n].astype(np.int64)).to(device)
+            return dec.k_cache[idx].cpu(), dec.v_cache[idx].cpu()
+
+        sample = OracleSample(w, sample_rows(w), last_tok, meta, pages)
 
     # churn plans: one more pass over the plan timed by the wall clock, host work
     # included (join/leave, the joiners' prefill, a0, graph launch), no flush
@@ -520,6 +682,12 @@ def run_gpu(args, rank, world):
                             "one graph launch per step; no L2 flush; the host phases include "
                             "waits for the GPU to release pinned buffers"}
 
+    peak, peak_kind = measured_peak()
+    rooflines = {}
+    for name in [x for x in args.also.split(",") if x and x != w.name]:
+        rooflines[name] = attention_roofline(name, args, device, flush, stream, sampler, peak)
+    clocks = sampler.stop()
+
     bytes_steps = [args.layers * attn_bytes(la, w.Hq, w.Hkv, w.d, elem) for la in lens_after]
     kv_only = [args.layers * int(np.asarray(la, np.int64).sum()) * w.Hkv * w.d * 2 * elem
                for la in lens_after]
@@ -529,7 +697,6 @@ def run_gpu(args, rank, world):
     attn_gbs = attn_b / (statistics.mean(attn_ms) / 1e3) / 1e9
     assert dec.device_errors() == 0, "device error flag set during the bench"
 
-    peak, peak_kind = measured_peak()
     khash = kernel_source_hash()
     traffic, traffic_note = profiled_traffic(args.workload, khash,
                                              attn_bytes(last_lens, w.Hq, w.Hkv, w.d, elem))
@@ -585,9 +752,10 @@ def run_gpu(args, rank, world):
                                    peak),
         "gpu_launches": K * args.layers * ((1 if args.flags & 4 else 2) +
                                            (1 if args.flags & 2 else 0)),
+        "rooflines": rooflines or None,
         "clocks": clocks,
     }
-    return result, dec, ids, tokens, oracle_state, meta0, w
+    return result, dec, ids, tokens, sample, w
 
 
 def run_dense_comparator(args, dec, ids, w, peak):
@@ -763,68 +931,63 @@ def run_e2e(args, dec, ids, tokens, w):
                             "path": "pkv_decode_step_host with one cudaMemcpyAsync per input"}}
 
 
-def cpu_baseline(w, oracle_state, meta0, budget_s):
-    cores = min(16, host_cores())
-    caches, toks = oracle_state
-    pool = oracle_pool(cores)
+def cpu_baseline(sample, budget_s):
+    """The float64 oracle on this host's cores over the sample, wall clock: one
+    untimed pass (worker start-up), then passes until ``budget_s`` is used."""
+    cores = host_cores()
+    pool = sample.pool(cores)
     try:
-        rows = list(range(w.B))
-        jobs, nbytes = oracle_jobs(w, caches, toks, meta0, rows)
-        gbs, per_core, nrows = run_oracle_sample(pool, cores, jobs, nbytes)
-        # repeat whole passes until the budget is used (bounded)
-        reps = 1
+        sample.run_pass(pool)
+        secs, passes = 0.0, 0
         t_end = time.perf_counter() + budget_s
-        total_per_core = per_core
-        while time.perf_counter() < t_end and reps < 50:
-            _, pc, _ = run_oracle_sample(pool, cores, jobs, nbytes)
-            total_per_core += pc
-            reps += 1
-        gbs = reps * nbytes / total_per_core / 1e9
+        while passes < 1 or (time.perf_counter() < t_end and passes < 50):
+            secs += sample.run_pass(pool)
+            passes += 1
     finally:
         pool.close()
         pool.join()
+        sample.close()
+    gbs = passes * sample.nbytes / secs / 1e9
     return {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"{reps} pass(es) over all {nrows} rows of the first step (float64 "
-                      f"numpy oracle, one spawned single-threaded worker per core; "
-                      f"time = summed worker compute seconds / cores)"}
+            "sample": f"{passes} timed pass(es) over " + sample.describe(),
+            "sample_bytes": int(sample.nbytes),
+            "ms_per_pass": round(1e3 * secs / passes, 2)}
 
 
 # ---------------------------------------------------------------------------
 # reference arm: the oracle on the host cores
 # ---------------------------------------------------------------------------
 def run_reference(args, rank, world):
-    import torch
     from oracle.allocator import BlockAllocatorModel
     from paged_kv_decode_10_gb300 import workloads
     if rank != 0:
         return None
     w = workloads.make_workload(args.workload)
-    caches = workloads.make_caches(w, "cpu")
-    toks = workloads.make_new_tokens(w, 0, "cpu")
     bt = w.max_blocks_per_seq()
     model = BlockAllocatorModel(w.num_blocks, max_seqs=w.B, max_blocks_per_seq=bt,
                                 initial_free=w.free_order)
     mids = [model.join(int(L)) for L in w.seq_lens]
     meta = model.prepare_step(mids, bt)
-    cores = min(16, host_cores())
-    pool = oracle_pool(cores)
+    rows = sample_rows(w)
+    tokens = workloads.make_new_tokens(w, 0, "cpu")
+
+    def pages(b, n):   # the sampled rows' pages, drawn N(0,1) row by row
+        shape = (n, w.Hkv, 16, w.d)
+        return (workloads.normal(shape, w.dtype, w.seed * 7919 + 2 * b + 1),
+                workloads.normal(shape, w.dtype, w.seed * 7919 + 2 * b + 2))
+
+    sample = OracleSample(w, rows, tokens, meta, pages)
+    cores = host_cores()
+    pool = sample.pool(cores)
     try:
-        jobs, nbytes = oracle_jobs(w, caches, toks, meta, range(w.B))
-        # each bench step is one row of the workload (rows taken in turn)
-        per_row = [(j, attn_bytes([meta[2][b]], w.Hq, w.Hkv, w.d,
-                                  2 if w.dtype == "bf16" else 4)) for b, j in enumerate(jobs)]
-        for i in range(args.warmup):
-            run_oracle_sample(pool, cores, [per_row[i % w.B][0]], per_row[i % w.B][1])
-        secs, total = 0.0, 0
-        for i in range(args.steps):
-            job, nb = per_row[i % w.B]
-            _, per_core, _ = run_oracle_sample(pool, 1, [job], nb)
-            secs += per_core
-            total += nb
+        for _ in range(max(1, args.warmup)):
+            sample.run_pass(pool)
+        secs = sum(sample.run_pass(pool) for _ in range(args.steps))
     finally:
         pool.close()
         pool.join()
-    value = total / secs / 1e9
+        sample.close()
+    value = args.steps * sample.nbytes / secs / 1e9
     return {"impl": "reference", "metric": "paged decode-attn achieved HBM GB/s (% of GB300 "
             "peak); batched decode steps/s", "value": round(value, 4), "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -832,11 +995,11 @@ def run_reference(args, rank, world):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
                        "head_dim": w.d, "block_size": 16},
-            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
                              "kind": "oracle",
-                             "sample": "one row of the workload's first decode step per bench "
-                                       "step, rows in turn (float64 numpy oracle, single "
-                                       "thread)"},
+                             "sample": "each bench step is one pass over " + sample.describe()
+                             + " (pages of the sampled rows drawn N(0,1))",
+                             "sample_bytes": int(sample.nbytes)},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
@@ -857,12 +1020,13 @@ def main():
             backend="nccl", init_method="env://")
     from paged_kv_decode_10_gb300 import build
     build.build()
-    result, dec, ids, tokens, oracle_state, meta0, w = run_gpu(args, rank, world)
+    want_cpu = not args.no_cpu and rank == 0 and world == 1
+    result, dec, ids, tokens, sample, w = run_gpu(args, rank, world, want_cpu)
     if rank == 0:
         if not args.no_e2e and args.layers == 1:
             result["e2e"] = run_e2e(args, dec, ids, tokens, w)
-        if not args.no_cpu and oracle_state is not None and world == 1:
-            result["cpu_baseline"] = cpu_baseline(w, oracle_state, meta0, args.cpu_seconds)
+        if sample is not None:
+            result["cpu_baseline"] = cpu_baseline(sample, args.cpu_seconds)
         if args.comparator and args.layers == 1:
             result["dense_comparator"] = run_dense_comparator(args, dec, ids, w,
                                                               result["roofline"]["peak"])
