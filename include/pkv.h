@@ -73,6 +73,12 @@ extern "C" {
                                      merging them in the split kernel's epilogue */
 #define PKV_STEP_FUSED 4          /* pkv_decode_step: run a1+a2 inside the attention kernel
                                      (one launch per step) instead of as their own kernel */
+#define PKV_ATTN_SHORT_WAITS 8    /* diagnostic: every wait inside the attention kernel gives
+                                     up after ~64 SM clocks instead of ~1 s, so the timeout
+                                     path can be exercised (PKV_DEVERR_TIMEOUT is set, the
+                                     output is incomplete, every copy the kernel issued still
+                                     lands before it exits); the workspace must be zero-filled
+                                     again before its next use */
 
 /* Message for the calling thread's last failed call ("" if none). */
 const char *pkv_last_error(void);
@@ -250,8 +256,13 @@ int pkv_prefill_kv(const void *k, const void *v, const int32_t *positions,
  * unit leaves one float32 (o, lse) partial per part it touches in `workspace`;
  * the LSE merge (M = max lse; out = sum exp(lse_s - M) o_s / sum exp(lse_s - M))
  * then combines them.  By default the merge runs in the epilogue of
- * pkv_decode_attn_split (the last part to finish a unit merges it), so `out`
- * is complete when the call's kernel ends.  With PKV_ATTN_SEPARATE_MERGE the
+ * pkv_decode_attn_split, so `out` is complete when the call's kernel ends:
+ * the last H parts of a unit to finish each merge a slice of its output
+ * columns (H <= 32, at least 8 float4 columns each).  H > 1 only when the
+ * grid fits on the GPU at once (num_parts <= the resident CTAs, which the
+ * default partition always does): the kernel is then launched cooperatively,
+ * so the helpers may wait for each other; otherwise the last part to finish
+ * merges the unit alone.  With PKV_ATTN_SEPARATE_MERGE the
  * split kernel stops at the partials and pkv_lse_merge must follow with the
  * same arguments.  pkv_lse_merge may also be called after a fused call: it
  * recomputes the same merge from the partials left in the workspace.
@@ -264,10 +275,13 @@ int pkv_prefill_kv(const void *k, const void *v, const int32_t *positions,
  * Supported: dtype PKV_BF16 or PKV_F32; d in {64, 128}; Hq/Hkv in {1,2,4,8};
  * B <= 65536.  q_rot [B,Hq,d] (16-byte aligned); out [B,Hq,d] (device, dtype,
  * 16-byte aligned).
- * num_parts <= 0 selects pkv_attn_default_parts for the current device;
- * at most 4096 parts.
+ * num_parts <= 0 selects pkv_attn_default_parts(d, Hq, Hkv, dtype, flags) for the
+ * current device (every SM holding as many CTAs as fit: the kernel variant,
+ * and so the count, depends on the head dimension, the group size Hq/Hkv, the
+ * dtype and PKV_ATTN_SIMT); at most 4096 parts.
  */
-int pkv_attn_default_parts(int32_t d, int32_t dtype, int32_t flags, int32_t *num_parts);
+int pkv_attn_default_parts(int32_t d, int32_t Hq, int32_t Hkv, int32_t dtype, int32_t flags,
+                           int32_t *num_parts);
 int pkv_attn_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t d,
                              int32_t num_parts, size_t *bytes);
 

@@ -19,6 +19,7 @@ BLOCK_SIZE = 16
 DEVERR_BAD_BLOCK, DEVERR_BAD_SLOT, DEVERR_BAD_LEN, DEVERR_TIMEOUT = 1, 2, 4, 8
 ATTN_SIMT = 1
 ATTN_SEPARATE_MERGE = 2
+ATTN_SHORT_WAITS = 8
 STEP_FUSED = 4
 
 _c_i32 = ctypes.c_int32
@@ -97,7 +98,7 @@ SIGNATURES = {
                                   _c_i32, _vp, _vp]),
     "pkv_prefill_kv": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_i32, _c_i32, _c_i32,
                                       _c_i32, ctypes.c_float, _c_i32, _vp, _vp]),
-    "pkv_attn_default_parts": (ctypes.c_int, [_c_i32, _c_i32, _c_i32, _p_i32]),
+    "pkv_attn_default_parts": (ctypes.c_int, [_c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _p_i32]),
     "pkv_attn_workspace_bytes": (ctypes.c_int, [_c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
                                                 ctypes.POINTER(_size_t)]),
     "pkv_decode_attn_split": (ctypes.c_int, [_vp, _vp, _vp, _c_i32, _vp, _c_i32, _vp, _vp,
@@ -128,7 +129,7 @@ SIGNATURES = {
 }
 
 _LIB = None
-ABI_VERSION = 3   # pkv_abi_version() of the library this binding describes
+ABI_VERSION = 4   # pkv_abi_version() of the library this binding describes
 
 
 def library_path():
@@ -410,9 +411,9 @@ def append(k_rot, v, slot_mapping, k_cache, v_cache, err=None, stream=None):
                              _ptr(err), _stream(stream)))
 
 
-def default_parts(d, dtype, flags=0):
+def default_parts(d, dtype, flags=0, Hq=32, Hkv=8):
     n = ctypes.c_int32()
-    _check(load().pkv_attn_default_parts(d, dtype, flags, ctypes.byref(n)))
+    _check(load().pkv_attn_default_parts(d, Hq, Hkv, dtype, flags, ctypes.byref(n)))
     return n.value
 
 
@@ -474,7 +475,7 @@ def decode_attention(q_rot, k_cache, v_cache, block_tables, seq_lens, scale, num
     B, Hq, d = q_rot.shape
     Hkv = k_cache.shape[1]
     if num_parts is None:
-        num_parts = default_parts(d, dtype_code(q_rot), flags)
+        num_parts = default_parts(d, dtype_code(q_rot), flags, Hq, Hkv)
     if workspace is None:
         workspace = alloc_workspace(B, Hq, Hkv, d, num_parts, q_rot.device)
     if out is None:

@@ -13,49 +13,50 @@
 #include <mutex>
 #include <new>
 
+#include "attention_host.h"
 #include "attention_kernel.cuh"
 
 namespace pkv {
 namespace {
 
 constexpr int kMaxB = 65536;
-// the fused merge keeps up to ceil((num_parts + 1) / 16) group weights per head
-// in the CTA's reduction buffer (2048 floats at d = 64)
 constexpr int kMaxParts = 4096;
+// PKV_ATTN_SHORT_WAITS: every wait gives up after this many SM clocks
+constexpr long long kShortWaitCycles = 64;
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct Workspace {
-  int32_t *counters;       // [U + C]
-  int32_t *unit_counters;  // [U]
+  int32_t *counters;       // [U] partials written, per unit
+  int32_t *done;           // [U] merge helpers finished, per unit
   int32_t *meta;           // [U x 2 + 2]
   float *lse, *o;          // [(U + C) x G], [(U + C) x G x D]
-  float *lse2, *o2;        // the same shapes, merged groups
   size_t bytes;
+  size_t counter_bytes;    // the leading counters and done regions
 };
 
-// [counters][unit_counters][meta][lse][o][lse2][o2], each region 256-byte aligned
+// [counters][done][meta][lse][o], each region 256-byte aligned.  Unit u's
+// partial from part c sits at slot u + c (slots of different units never
+// coincide: a later unit's parts start no earlier than the previous unit's
+// last part).
 Workspace workspace_layout(void *base, int B, int Hq, int Hkv, int D, int C) {
   const size_t U = static_cast<size_t>(B) * Hkv;
   const size_t G = static_cast<size_t>(Hq / Hkv);
   const size_t S = U + static_cast<size_t>(C);
-  const size_t sizes[7] = {align256(S * sizeof(int32_t)), align256(U * sizeof(int32_t)),
+  const size_t sizes[5] = {align256(U * sizeof(int32_t)), align256(U * sizeof(int32_t)),
                            align256((U * 2 + 2) * sizeof(int32_t)),
-                           align256(S * G * sizeof(float)),
-                           align256(S * G * static_cast<size_t>(D) * sizeof(float)),
                            align256(S * G * sizeof(float)),
                            align256(S * G * static_cast<size_t>(D) * sizeof(float))};
   char *p = static_cast<char *>(base);
-  char *r[7];
+  char *r[5];
   size_t off = 0;
-  for (int i = 0; i < 7; ++i) {
+  for (int i = 0; i < 5; ++i) {
     r[i] = p + off;
     off += sizes[i];
   }
   return Workspace{reinterpret_cast<int32_t *>(r[0]), reinterpret_cast<int32_t *>(r[1]),
                    reinterpret_cast<int32_t *>(r[2]), reinterpret_cast<float *>(r[3]),
-                   reinterpret_cast<float *>(r[4]), reinterpret_cast<float *>(r[5]),
-                   reinterpret_cast<float *>(r[6]), off};
+                   reinterpret_cast<float *>(r[4]), off, sizes[0] + sizes[1]};
 }
 
 // ---- cuTensorMapEncodeTiled through the runtime's driver entry point ------
@@ -174,18 +175,51 @@ int check_shapes(int B, int Hq, int Hkv, int D, int dtype) {
   return PKV_OK;
 }
 
-int default_parts(int D, int dtype, int flags, int G, int *parts) {
-  AttnVariant v;
-  PKV_REQUIRE(pick_variant(dtype, D, G, flags, &v), PKV_ERR_UNSUPPORTED, "no kernel variant");
-  int dev = 0, sms = 0, occ = 0;
+// CTAs of a variant that are resident at once on the current device (SMs x
+// blocks per SM), remembered per (device, variant).
+int resident_ctas(const AttnVariant &v, int *ctas) {
+  struct Entry {
+    int device;
+    cudaError_t (*occupancy)(int *);
+    int ctas;
+  };
+  static std::mutex mu;
+  static Entry cache[64];
+  static int used = 0;
+  int dev = 0;
   PKV_CUDA_CHECK(cudaGetDevice(&dev));
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+      if (cache[i].device == dev && cache[i].occupancy == v.occupancy) {
+        *ctas = cache[i].ctas;
+        return PKV_OK;
+      }
+  }
+  int sms = 0, occ = 0;
   PKV_CUDA_CHECK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
   PKV_CUDA_CHECK(v.occupancy(&occ));
   PKV_REQUIRE(occ > 0, PKV_ERR_CUDA, "attention kernel cannot be resident (smem %d)",
               v.smem_bytes);
-  *parts = sms * occ;
+  std::lock_guard<std::mutex> lock(mu);
+  if (used < 64) cache[used++] = Entry{dev, v.occupancy, sms * occ};
+  *ctas = sms * occ;
   return PKV_OK;
 }
+
+}  // namespace
+
+int default_parts(int D, int dtype, int flags, int G, int *parts) {
+  AttnVariant v;
+  PKV_REQUIRE(pick_variant(dtype, D, G, flags, &v), PKV_ERR_UNSUPPORTED, "no kernel variant");
+  return resident_ctas(v, parts);
+}
+
+size_t workspace_counter_bytes(int B, int Hq, int Hkv, int D, int C) {
+  return workspace_layout(nullptr, B, Hq, Hkv, D, C).counter_bytes;
+}
+
+namespace {
 
 // ---- a4: LSE merge ----------------------------------------------------------
 template <typename T>
@@ -231,14 +265,14 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const float *__restrict_
 
 using namespace pkv;
 
-extern "C" int pkv_attn_default_parts(int32_t d, int32_t dtype, int32_t flags,
-                                      int32_t *num_parts) {
+extern "C" int pkv_attn_default_parts(int32_t d, int32_t Hq, int32_t Hkv, int32_t dtype,
+                                      int32_t flags, int32_t *num_parts) {
   clear_error();
   PKV_REQUIRE(num_parts, PKV_ERR_INVALID_ARG, "num_parts is NULL");
-  PKV_REQUIRE(dtype_ok(dtype), PKV_ERR_UNSUPPORTED, "dtype %d", dtype);
-  PKV_REQUIRE(d == 64 || d == 128, PKV_ERR_UNSUPPORTED, "head_dim %d", d);
+  int rc = check_shapes(1, Hq, Hkv, d, dtype);
+  if (rc != PKV_OK) return rc;
   int parts = 0;
-  const int rc = default_parts(d, dtype, flags, 8, &parts);
+  rc = default_parts(d, dtype, flags, Hq / Hkv, &parts);
   if (rc != PKV_OK) return rc;
   *num_parts = parts;
   return PKV_OK;
@@ -316,10 +350,16 @@ int attn_launch(const void *q_rot, const void *k_cache, const void *v_cache, int
   p.lse_part = ws.lse;
   p.meta = ws.meta;
   p.counters = ws.counters;
-  p.unit_counters = ws.unit_counters;
-  p.o_group = ws.o2;
-  p.lse_group = ws.lse2;
+  p.done = ws.done;
   p.fuse_merge = (flags & PKV_ATTN_SEPARATE_MERGE) ? 0 : 1;
+  // A grid that fits on the GPU at once is launched cooperatively, which
+  // guarantees that every CTA is resident; only then may the merge of a unit
+  // be shared by several parts that wait for each other.
+  int resident = 0;
+  rc = resident_ctas(v, &resident);
+  if (rc != PKV_OK) return rc;
+  p.max_helpers = num_parts <= resident ? kMaxHelpers : 1;
+  p.wait_limit = (flags & PKV_ATTN_SHORT_WAITS) ? kShortWaitCycles : kWaitLimitCycles;
   // a unit boundary (segment combine, pipeline drain) costs a CTA about as
   // long as streaming this many pages (measured on GB300: ~0.7 us against
   // ~0.17 us per 2 KB-row page at d=64 and ~0.33 us per page at d=128)

@@ -53,18 +53,18 @@ struct AttnParams {
   float *o_part;            // [(U + C), G, D]
   float *lse_part;          // [(U + C), G]
   int32_t *meta;            // [U, 2]: first part, number of parts spanned; then P (int64)
-  int32_t *counters;        // [U + C] finished-part counters per merge group (kept at 0)
-  int32_t *unit_counters;   // [U] finished-group counters per unit (kept at 0)
-  float *o_group;           // [(U + C), G, D] merged groups of a unit's partials
-  float *lse_group;         // [(U + C), G]
+  int32_t *counters;        // [U] parts of a split unit that have written their partial
+  int32_t *done;            // [U] merge helpers of a unit that are done (both kept at 0)
   void *out;                // [B, Hq, D]
   int32_t *err;
   int bt_stride, bias_stride;
   int B, Hq, Hkv, G;
   int num_blocks, num_parts;
-  int fuse_merge;           // 1: the last part of a unit merges it (a4 in the epilogue)
+  int fuse_merge;           // 1: the parts of a unit merge it (a4 in the epilogue)
+  int max_helpers;          // parts that may share one unit's merge (1 unless co-resident)
   int seg_cost;             // pages of work a unit boundary is worth to the partition
   float scale_log2;         // softmax scale * log2(e)
+  long long wait_limit;     // SM clocks after which a pipeline or merge wait gives up
   // whole-step kernels only (a1 + a2 fused in): the step's new tokens, where
   // they go, and where their rotated copies are reported
   const void *q_new, *k_new, *v_new;   // [B,Hq,D], [B,Hkv,D], [B,Hkv,D]
@@ -78,6 +78,12 @@ struct AttnParams {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr long long kWaitLimitCycles = 1ll << 31;   // about one second
+// a merge helper takes at least this many float4 columns of a unit's output
+constexpr int kHelperMinCols = 8;
+constexpr int kMaxHelpers = 32;
+// units split over fewer parts are merged by their last part alone (its loads
+// of all partials fit in one round trip; helpers would only add a wait)
+constexpr int kHelperMinSplit = 8;
 
 // Pages of a row of length L, or 0 for an invalid length (which also sets *bad).
 __device__ __forceinline__ int pages_of_len(int L, int bt_stride, bool has_bias, int bias_stride,
@@ -101,15 +107,15 @@ __device__ __forceinline__ int part_of(long long x, long long P, int C) {
   return static_cast<int>(div_floor((x + 1) * C - 1, P));
 }
 
-// The fused merge combines a unit's partials in groups of kMergeGroup parts
-// (the last part of a group to finish merges the group), then the last group
-// merger combines the group results: no CTA ever merges more than
-// max(kMergeGroup, groups) partials, whatever the split count.
-constexpr int kMergeGroup = 16;
-
 // A part owns no page when C > P and its page range is empty.
 __device__ __forceinline__ bool part_empty(long long c, long long P, int C) {
   return div_floor(P * c, C) == div_floor(P * (c + 1), C);
+}
+
+// The same, kept out of line: callers test C > P first, and the 64-bit
+// divisions must not be evaluated speculatively on the common path.
+static __device__ __noinline__ bool part_empty_slow(long long c, long long P, int C) {
+  return part_empty(c, P, C);
 }
 
 // Parts c0 .. c0+n-1 that own at least one page (all of them when C <= P).
@@ -122,18 +128,6 @@ static __device__ __noinline__ int count_real_parts(int c0, int n, long long P, 
 }
 __device__ __forceinline__ int real_parts(int c0, int n, long long P, int C) {
   return C <= P ? n : count_real_parts(c0, n, P, C);
-}
-
-// Merge groups of a unit spanning parts c0 .. c0+nseg-1 that own a page.
-static __device__ __noinline__ int count_real_groups(int c0, int nseg, long long P, int C) {
-  const int ng = (nseg + kMergeGroup - 1) / kMergeGroup;
-  int r = 0;
-  for (int k = 0; k < ng; ++k)
-    r += count_real_parts(c0 + k * kMergeGroup, min(kMergeGroup, nseg - k * kMergeGroup), P, C) > 0;
-  return r;
-}
-__device__ __forceinline__ int real_groups(int c0, int nseg, long long P, int C) {
-  return C <= P ? (nseg + kMergeGroup - 1) / kMergeGroup : count_real_groups(c0, nseg, P, C);
 }
 
 // a4, the LSE merge of one float4 column (head h, dims 4*d4 .. 4*d4+3) over the
@@ -192,105 +186,158 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16 *dst, float4
   *reinterpret_cast<uint2 *>(dst) = w;
 }
 
-// One merge of the fused a4: the partials i < n stored at slots
-// slot0 + i*stride of (o, lse).  Level 1 merges up to kMergeGroup partials of
-// consecutive parts c0 + i; level 2 merges the group results of a unit whose
-// parts c0 .. c0+nseg-1 formed several groups.  The result goes to the group
-// buffers at grp_slot (a level-1 merge of a multi-group unit) or to the unit's
-// output rows.
-struct MergeJob {
-  const float *o, *lse;
-  size_t slot0;
-  int n, stride;
-  int c0, nseg, level;
-  float *o_grp, *lse_grp;   // non-null: write the merged group here
-  size_t grp_slot;
-  void *out;                // else: the unit's [G, D] output rows
+// The fused a4.  Every part of a unit split over n parts writes its (o, lse)
+// partial and adds one to the unit's counter.  The last H parts to arrive are
+// the unit's merge helpers: helper r waits until the counter reaches n, then
+// merges float4 columns [r*NC/H, (r+1)*NC/H) of the unit's output (NC = G*D/4)
+// over all n partials.  With H > 1 the merge of a long unit is spread over H
+// CTAs and each thread issues the loads of its few partials at once, so it
+// costs about one L2 round trip after the last partial lands.  Helpers wait on
+// other CTAs of the grid, so H > 1 only when the launch makes every CTA
+// co-resident (a cooperative launch); otherwise H = 1, the last part alone.
+__device__ __forceinline__ int merge_helpers(int n, int ncols, int max_helpers) {
+  return max(1, min(n, min(max_helpers, ncols / kHelperMinCols)));
+}
+
+// Online combination of partials (base-2 lse) into (M, den, acc): acc and den
+// are sums of 2^(lse_s - M) o_s and 2^(lse_s - M).
+struct MergeAcc {
+  float M, den;
+  float4 acc;
 };
 
-// Partial i of job J does not exist: its part (level 1), or every part of its
-// group (level 2), owns no page (only possible when C > P).
-static __device__ __noinline__ bool merge_skip_slow(const MergeJob &J, int i, long long P, int C) {
-  if (J.level == 1) return part_empty(J.c0 + i, P, C);
-  return count_real_parts(J.c0 + i * kMergeGroup, min(kMergeGroup, J.nseg - i * kMergeGroup), P,
-                          C) == 0;
-}
-__device__ __forceinline__ bool merge_skip(const MergeJob &J, int i, long long P, int C) {
-  return C > P && merge_skip_slow(J, i, P, C);
+template <int K>
+__device__ __forceinline__ void merge_acc_add(MergeAcc &a, const float (&l)[K],
+                                              const float4 (&v)[K]) {
+  float m = a.M;
+#pragma unroll
+  for (int u = 0; u < K; ++u) m = fmaxf(m, l[u]);
+  if (m == -INFINITY) return;
+  const float r = ex2(a.M - m);   // 0 while nothing was accumulated
+  a.den *= r;
+  a.acc.x *= r;
+  a.acc.y *= r;
+  a.acc.z *= r;
+  a.acc.w *= r;
+#pragma unroll
+  for (int u = 0; u < K; ++u) {
+    const float w = ex2(l[u] - m);
+    if (w != 0.f) {
+      a.den += w;
+      a.acc.x = fmaf(w, v[u].x, a.acc.x);
+      a.acc.y = fmaf(w, v[u].y, a.acc.y);
+      a.acc.z = fmaf(w, v[u].z, a.acc.z);
+      a.acc.w = fmaf(w, v[u].w, a.acc.w);
+    }
+  }
+  a.M = m;
 }
 
-// The merge of one float4 column (head h, dims 4*d4 .. 4*d4+3) of job J by one
-// thread.  The lse and o loads of K partials are issued together, so a merge of
-// n <= K partials costs one L2 round trip; longer ones rescale a running
-// maximum chunk by chunk.  Loads bypass L1: other CTAs wrote the partials.
-template <typename T, int K>
-__device__ __forceinline__ void merge_job_column(const MergeJob J, int G, int D, int h, int d4,
-                                                 long long P, int C) {
-  float M = -INFINITY, den = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s0 = 0; s0 < J.n; s0 += K) {
+// Partials i = j, j + R, j + 2R, ... < nseg of unit u_idx (part cf + i, slot
+// u_idx + cf + i; parts that own no page have none), float4 column `col`.
+// The loads of up to 8 partials go out together.  Loads bypass L1: other CTAs
+// of this grid wrote the partials.
+__device__ __forceinline__ MergeAcc merge_partials(const float *o, const float *lse, int u_idx,
+                                                   int cf, int nseg, int j, int R, int col,
+                                                   int G, int D, long long P, int C) {
+  const int h = col / (D / 4), d4 = col - h * (D / 4);
+  MergeAcc a{-INFINITY, 0.f, make_float4(0.f, 0.f, 0.f, 0.f)};
+  constexpr int K = 8;
+  for (int i0 = j; i0 < nseg; i0 += K * R) {
     float l[K];
     float4 v[K];
 #pragma unroll
-    for (int u = 0; u < K; ++u) {
-      const int s = s0 + u;
-      const bool on = s < J.n && !merge_skip(J, s, P, C);
-      const size_t slot = J.slot0 + static_cast<size_t>(s) * J.stride;
-      l[u] = on ? __ldcg(J.lse + slot * G + h) : -INFINITY;
-      v[u] = on ? __ldcg(reinterpret_cast<const float4 *>(J.o + (slot * G + h) * D) + d4)
+    for (int t = 0; t < K; ++t) {
+      const int i = i0 + t * R;
+      const bool on = i < nseg && !(C > P && part_empty_slow(cf + i, P, C));
+      const size_t slot = static_cast<size_t>(u_idx) + cf + i;
+      l[t] = on ? __ldcg(lse + slot * G + h) : -INFINITY;
+      v[t] = on ? __ldcg(reinterpret_cast<const float4 *>(o + (slot * G + h) * D) + d4)
                 : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    float m = M;
-#pragma unroll
-    for (int u = 0; u < K; ++u) m = fmaxf(m, l[u]);
-    if (m == -INFINITY) continue;
-    const float r = ex2(M - m);   // 0 while nothing was accumulated
-    den *= r;
-    acc.x *= r;
-    acc.y *= r;
-    acc.z *= r;
-    acc.w *= r;
-#pragma unroll
-    for (int u = 0; u < K; ++u) {
-      const float w = ex2(l[u] - m);
-      if (w != 0.f) {
-        den += w;
-        acc.x = fmaf(w, v[u].x, acc.x);
-        acc.y = fmaf(w, v[u].y, acc.y);
-        acc.z = fmaf(w, v[u].z, acc.z);
-        acc.w = fmaf(w, v[u].w, acc.w);
+    merge_acc_add<K>(a, l, v);
+  }
+  return a;
+}
+
+template <typename T>
+__device__ __forceinline__ void merge_store(T *out_rows, int col, int D, const MergeAcc &a) {
+  const int h = col / (D / 4), d4 = col - h * (D / 4);
+  float4 o = a.acc;
+  if (a.den > 0.f) {
+    const float inv = __frcp_rn(a.den);
+    o.x *= inv;
+    o.y *= inv;
+    o.z *= inv;
+    o.w *= inv;
+  } else {
+    o = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  store4<T>(out_rows + h * D + 4 * d4, o);
+}
+
+// Helper r of H: columns [r*NC/H, (r+1)*NC/H) of unit u_idx (parts cf ..
+// cf+nseg-1) merged into out_rows [G, D] by the NTHR consumer threads.  When
+// the slice has fewer columns than threads, R = NTHR / cols threads share a
+// column (each takes every R-th partial) and combine through `scratch`
+// (NTHR * 6 floats of shared memory; all NTHR threads must call this).
+template <typename T, int NTHR>
+__device__ __forceinline__ void merge_slice(const AttnParams &p, int u_idx, int cf, int nseg,
+                                            long long P, int C, int r, int H, int D, T *out_rows,
+                                            float *scratch, int tid) {
+  const int NC = p.G * (D / 4);
+  const int col0 = r * NC / H, cols = (r + 1) * NC / H - col0;
+  const int R = max(1, NTHR / cols);
+  if (R == 1) {
+    for (int c = tid; c < cols; c += NTHR)
+      merge_store<T>(out_rows, col0 + c, D,
+                     merge_partials(p.o_part, p.lse_part, u_idx, cf, nseg, 0, 1, col0 + c, p.G, D,
+                                    P, C));
+    return;
+  }
+  MergeAcc a{-INFINITY, 0.f, make_float4(0.f, 0.f, 0.f, 0.f)};
+  if (tid < cols * R)
+    a = merge_partials(p.o_part, p.lse_part, u_idx, cf, nseg, tid / cols, R, col0 + tid % cols,
+                       p.G, D, P, C);
+  float *e = scratch + tid * 6;
+  e[0] = a.M;
+  e[1] = a.den;
+  e[2] = a.acc.x;
+  e[3] = a.acc.y;
+  e[4] = a.acc.z;
+  e[5] = a.acc.w;
+  asm volatile("bar.sync 1, %0;" ::"r"(NTHR) : "memory");
+  if (tid < cols) {
+    // combine the R subset results: rescale each to the largest M
+    float m = -INFINITY;
+    for (int q = 0; q < R; ++q) m = fmaxf(m, scratch[(tid + q * cols) * 6]);
+    MergeAcc t{m, 0.f, make_float4(0.f, 0.f, 0.f, 0.f)};
+    if (m != -INFINITY) {
+      for (int q = 0; q < R; ++q) {
+        const float *f = scratch + (tid + q * cols) * 6;
+        const float w = ex2(f[0] - m);   // 0 for a subset that saw nothing
+        t.den = fmaf(w, f[1], t.den);
+        t.acc.x = fmaf(w, f[2], t.acc.x);
+        t.acc.y = fmaf(w, f[3], t.acc.y);
+        t.acc.z = fmaf(w, f[4], t.acc.z);
+        t.acc.w = fmaf(w, f[5], t.acc.w);
       }
     }
-    M = m;
-  }
-  float lse = -INFINITY;
-  if (den > 0.f) {
-    const float inv = __frcp_rn(den);
-    acc.x *= inv;
-    acc.y *= inv;
-    acc.z *= inv;
-    acc.w *= inv;
-    lse = M + lg2(den);
-  }
-  if (J.o_grp) {
-    *(reinterpret_cast<float4 *>(J.o_grp + (J.grp_slot * G + h) * D) + d4) = acc;
-    if (d4 == 0) J.lse_grp[J.grp_slot * G + h] = lse;
-  } else {
-    store4<T>(static_cast<T *>(J.out) + h * D + 4 * d4, acc);
+    merge_store<T>(out_rows, col0 + tid, D, t);
   }
 }
 
-// The jobs' columns spread over the nthr consumer threads: with two jobs of a
-// small unit every thread has one column, and all loads are in flight at once.
-template <typename T>
-__device__ __forceinline__ void merge_jobs(const MergeJob J0, const MergeJob J1, int njobs,
-                                           int G, int D, long long P, int C, int tid, int nthr) {
-  const int cols = G * (D / 4);
-  for (int item = tid; item < njobs * cols; item += nthr) {
-    const int q = item >= cols ? 1 : 0;
-    const int col = item - q * cols;
-    const int h = col / (D / 4), d4 = col - h * (D / 4);
-    merge_job_column<T, 8>(q ? J1 : J0, G, D, h, d4, P, C);
+// Waits until *counter >= target (acquire); gives up after ~limit SM clocks.
+__device__ __forceinline__ bool wait_count(const int32_t *counter, int target, long long limit) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
+  if (v >= target) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    __nanosleep(32);
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
+    if (v >= target) return true;
+    if (clock64() - t0 > limit) return false;
   }
 }
 
@@ -307,6 +354,32 @@ __device__ __forceinline__ int atom_add_relaxed_gpu(int32_t *p, int v) {
                : "l"(p), "r"(v)
                : "memory");
   return old;
+}
+
+__device__ __forceinline__ void fence_sc_cta() { asm volatile("fence.sc.cta;" ::: "memory"); }
+
+// Waits (bounded) for the last phase armed on every ring stage and segment
+// slot, the only phases that can still have a copy in flight.
+template <int NS, int SLOTS>
+__device__ __noinline__ void drain_copies(uint64_t *full, uint64_t *segfull, const int *stage_pg,
+                                          const int *slot_seg, int lane) {
+  for (int s = lane; s < NS; s += 32)
+    if (stage_pg[s] >= 0)
+      mbar_wait_bounded(&full[s], static_cast<uint32_t>(stage_pg[s] / NS) & 1u, kWaitLimitCycles);
+  for (int s = lane; s < SLOTS; s += 32)
+    if (slot_seg[s] >= 0)
+      mbar_wait_bounded(&segfull[s], static_cast<uint32_t>(slot_seg[s] / SLOTS) & 1u,
+                        kWaitLimitCycles);
+}
+
+// A consumer thread gives up: it records the abort and, if the producer warp
+// has already finished (and so will not drain), drains the copies itself.
+template <int NS, int SLOTS>
+__device__ __noinline__ void consumer_abort(volatile int *misc, uint64_t *full, uint64_t *segfull,
+                                            const int *stage_pg, const int *slot_seg) {
+  misc[2] = 1;
+  fence_sc_cta();
+  if (misc[3] != 0) drain_copies<NS, SLOTS>(full, segfull, stage_pg, slot_seg, 0);
 }
 
 struct UnitCursor {
@@ -334,14 +407,17 @@ struct Geo {
   static constexpr int kOffBars = kOffABuf + NW * kHeadsPad * 4;      // 8-aligned
   static constexpr int kOffBad = kOffBars + 2 * NS * 8;
   static constexpr int kOffScan = kOffBad + NS * 4;
-  static constexpr int kOffMisc = kOffScan + (kThreads / 32) * 4;
+  static constexpr int kOffMisc = kOffScan + (kThreads / 32) * 4;   // 16 ints
   // segment slots: the producer hands each unit segment to the consumers as a
   // 64-byte header (row, KV head, pages, length, page range, first page) and
   // the unit's query rows (up to 8 heads), bulk-copied from global memory
   static constexpr int kSegSlots = 4;
   static constexpr int kSegQBytes = 8 * D * kElem;
   static constexpr int kSegBytes = 64 + kSegQBytes;
-  static constexpr int kOffSeg = (kOffMisc + 32 + 127) / 128 * 128;
+  // per ring stage and per segment slot: the last page / segment the producer
+  // arrived on it for (its pending phase, which an aborting CTA drains)
+  static constexpr int kOffPg = kOffMisc + 64;
+  static constexpr int kOffSeg = (kOffPg + (NS + kSegSlots) * 4 + 127) / 128 * 128;
   static constexpr int kOffSegBars = kOffSeg + kSegSlots * kSegBytes;
   // row lengths of the first kLensCache rows, as the prologue read them
   static constexpr int kLensCache = 256;
@@ -832,6 +908,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
   int *scan = reinterpret_cast<int *>(smem + Q::kOffScan);
   int *lens_s = reinterpret_cast<int *>(smem + Q::kOffLens);
   volatile int *misc = reinterpret_cast<volatile int *>(smem + Q::kOffMisc);  // b0, rowoff0, abort
+  int *stage_pg = reinterpret_cast<int *>(smem + Q::kOffPg);   // [NS], then [kSegSlots]
+  int *slot_seg = stage_pg + NS;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -853,7 +931,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
     }
     misc[0] = -1;
     misc[1] = 0;
-    misc[2] = 0;
+    misc[2] = 0;   // a wait gave up: stop
+    misc[3] = 0;   // the producer warp has issued its last copy
+    for (int s = 0; s < NS + Q::kSegSlots; ++s) stage_pg[s] = -1;
     fence_barrier_init();
     fence_proxy_async_smem();
   }
@@ -1016,38 +1096,44 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
           const int slot = k % Q::kSegSlots;
           const uint32_t sph = static_cast<uint32_t>(k / Q::kSegSlots) & 1u;
           bool dead = misc[2] != 0;
-          if (!dead && !mbar_wait_bounded(&segempty[slot], sph ^ 1u, kWaitLimitCycles)) {
+          if (!dead && !mbar_wait_bounded(&segempty[slot], sph ^ 1u, p.wait_limit)) {
             misc[2] = 1;
             dead = true;
             set_dev_err(p.err, PKV_DEVERR_TIMEOUT);
           }
-          unsigned char *sp = smem + Q::kOffSeg + slot * Q::kSegBytes;
-          int *h = reinterpret_cast<int *>(sp);
-          h[0] = u.b;
-          h[1] = u.g;
-          h[2] = u.n;
-          h[3] = L;
-          h[4] = j0;
-          h[5] = j1;
-          *reinterpret_cast<long long *>(h + 6) = u.off;
-          // parts spanned by the unit's pages (two 64-bit divisions, off the
-          // consumers' path), and whether this is the part's last segment
-          const int cf = part_of(u.off + A, P, C);
-          h[8] = cf;
-          h[9] = part_of(u.off + A + u.n - 1, P, C) - cf + 1;
-          h[10] = last ? 1 : 0;
-          if (!FUSE && !dead) {
-            if (!waited) {
-              pdl_wait();   // the query rows come from the kernel before this one
-              waited = true;
+          // once anything has given up, nothing more is handed over (the
+          // consumers stop too), so no barrier gets an arrival for a phase the
+          // other side never finished
+          if (!dead) {
+            unsigned char *sp = smem + Q::kOffSeg + slot * Q::kSegBytes;
+            int *h = reinterpret_cast<int *>(sp);
+            h[0] = u.b;
+            h[1] = u.g;
+            h[2] = u.n;
+            h[3] = L;
+            h[4] = j0;
+            h[5] = j1;
+            *reinterpret_cast<long long *>(h + 6) = u.off;
+            // parts spanned by the unit's pages (two 64-bit divisions, off the
+            // consumers' path), and whether this is the part's last segment
+            const int cf = part_of(u.off + A, P, C);
+            h[8] = cf;
+            h[9] = part_of(u.off + A + u.n - 1, P, C) - cf + 1;
+            h[10] = last ? 1 : 0;
+            if (!FUSE) {
+              if (!waited) {
+                pdl_wait();   // the query rows come from the kernel before this one
+                waited = true;
+              }
+              mbar_arrive_expect_tx(&segfull[slot], qbytes);
+              bulk_copy_g2s(smem_u32(sp + 64),
+                            static_cast<const T *>(p.q) +
+                                (static_cast<size_t>(u.b) * p.Hq + u.g * p.G) * D,
+                            qbytes, &segfull[slot]);
+            } else {
+              mbar_arrive(&segfull[slot]);
             }
-            mbar_arrive_expect_tx(&segfull[slot], qbytes);
-            bulk_copy_g2s(smem_u32(sp + 64),
-                          static_cast<const T *>(p.q) +
-                              (static_cast<size_t>(u.b) * p.Hq + u.g * p.G) * D,
-                          qbytes, &segfull[slot]);
-          } else {
-            mbar_arrive(&segfull[slot]);
+            slot_seg[slot] = k;
           }
         }
         __syncwarp();
@@ -1072,13 +1158,16 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
             const int st = xx % NS;
             const uint32_t ph = static_cast<uint32_t>(xx / NS) & 1u;
             bool dead = misc[2] != 0;
-            if (!dead && !mbar_wait_bounded(&empty[st], ph ^ 1u, kWaitLimitCycles)) {
+            if (!dead && !mbar_wait_bounded(&empty[st], ph ^ 1u, p.wait_limit)) {
               misc[2] = 1;
               dead = true;
               set_dev_err(p.err, PKV_DEVERR_TIMEOUT);
             }
             const bool ok = !dead && blk >= 0 && blk < p.num_blocks;
-            stage_bad[st] = ok ? 0 : 1;
+            if (!dead) {
+              stage_bad[st] = ok ? 0 : 1;
+              stage_pg[st] = xx;
+            }
             if (ok) {
               // the last page of a unit holds the token appended by the kernel
               // before this one: wait for that grid before reading it
@@ -1094,8 +1183,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
                 tma_load_2d_hint(vdst + sub * Q::kSubBytes, &tmap_v, sub * Q::kSubCols, y,
                                  &full[st], l2_stream);
               }
-            } else {
-              if (!dead) set_dev_err(p.err, PKV_DEVERR_BAD_BLOCK);
+            } else if (!dead) {
+              set_dev_err(p.err, PKV_DEVERR_BAD_BLOCK);
               mbar_arrive(&full[st]);
             }
           }
@@ -1116,16 +1205,20 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
       j1 = nj1;
       ids = nids;
     }
-    if (aborted && lane == 0) {
-      // never expected: let any copy still in flight land before the CTA exits
-      for (int xx = max(0, x - NS); xx < x; ++xx)
-        mbar_wait_bounded(&full[xx % NS], static_cast<uint32_t>(xx / NS) & 1u, kWaitLimitCycles);
-      if (k > 0) {
-        const int s = (k - 1) % Q::kSegSlots;
-        mbar_wait_bounded(&segfull[s], static_cast<uint32_t>((k - 1) / Q::kSegSlots) & 1u,
-                          kWaitLimitCycles);
-      }
+    // Every copy this warp issued must land before the CTA exits.  Normally
+    // the consumers wait for all of them anyway; consumers that gave up a
+    // wait may not.  The producer marks itself finished, then looks for an
+    // abort; a consumer that aborts marks that, then looks for a finished
+    // producer (store, sequentially consistent fence, load on both sides): at
+    // least one of them sees the other and drains.
+    __syncwarp();
+    if (lane == 0) {
+      fence_sc_cta();   // this warp's stage and slot records before the mark
+      misc[3] = 1;
+      fence_sc_cta();
     }
+    if (__shfl_sync(0xffffffffu, misc[2], 0) != 0)
+      drain_copies<NS, Q::kSegSlots>(full, segfull, stage_pg, slot_seg, lane);
     return;
   }
 
@@ -1147,8 +1240,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
     const int slot = kk % Q::kSegSlots;
     const uint32_t sph = static_cast<uint32_t>(kk / Q::kSegSlots) & 1u;
     bool ok = misc[2] == 0;
-    if (ok && !mbar_wait_bounded(&segfull[slot], sph, kWaitLimitCycles)) {
-      misc[2] = 1;
+    if (ok && !mbar_wait_bounded(&segfull[slot], sph, p.wait_limit)) {
+      consumer_abort<NS, Q::kSegSlots>(misc, full, segfull, stage_pg, slot_seg);
       set_dev_err(p.err, PKV_DEVERR_TIMEOUT);
       ok = false;
     }
@@ -1191,8 +1284,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
         const int st = xx % NS;
         const uint32_t ph = static_cast<uint32_t>(xx / NS) & 1u;
         bool ready = !misc[2];
-        if (ready && !mbar_wait_bounded(&full[st], ph, kWaitLimitCycles)) {
-          misc[2] = 1;
+        if (ready && !mbar_wait_bounded(&full[st], ph, p.wait_limit)) {
+          consumer_abort<NS, Q::kSegSlots>(misc, full, segfull, stage_pg, slot_seg);
           set_dev_err(p.err, PKV_DEVERR_TIMEOUT);
           ready = false;
         }
@@ -1202,7 +1295,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
                       j * kBlockTokens, lane);
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st]);
+        // a stage is handed back only after its page was seen to land
+        if (lane == 0 && ready) mbar_arrive(&empty[st]);
       }
       mma_stash<D>(s, my_acc, my_m, my_l, lane);
     } else {
@@ -1223,8 +1317,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
         const int st = xx % NS;
         const uint32_t ph = static_cast<uint32_t>(xx / NS) & 1u;
         bool ready = !misc[2];
-        if (ready && !mbar_wait_bounded(&full[st], ph, kWaitLimitCycles)) {
-          misc[2] = 1;
+        if (ready && !mbar_wait_bounded(&full[st], ph, p.wait_limit)) {
+          consumer_abort<NS, Q::kSegSlots>(misc, full, segfull, stage_pg, slot_seg);
           set_dev_err(p.err, PKV_DEVERR_TIMEOUT);
           ready = false;
         }
@@ -1234,7 +1328,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
                              u.b, j * kBlockTokens, lane, pbuf, abuf);
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st]);
+        if (lane == 0 && ready) mbar_arrive(&empty[st]);
       }
       simt_stash<T, D, G>(s, my_acc, my_m, my_l, lane);
     }
@@ -1317,98 +1411,83 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
     asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
   }
   if (npend == 0) return;
-  // ---- a4 in the epilogue: the last part to finish a merge group merges it,
-  // the last group merger of a unit merges the groups (threadfence-reduction
-  // pattern; every counter is reset by the CTA that consumes it).  Both
-  // pending units go through each phase together, so the counters cost one
-  // round trip and the merges one or two more. ----
+  // ---- a4 in the epilogue.  Both pending units (a part's first and last
+  // segment) report at once: one release fence, both counter increments in
+  // flight, one acquire fence.  A part among the last H of a unit to arrive
+  // is one of its merge helpers (see merge_slice); helpers that are not the
+  // last to arrive wait for the rest.  Then every slice this part merges goes
+  // out in one pass. ----
   // (the segment loop ended with a consumer barrier: all partials are written)
-  MergeJob job[2];
-  int first_g[2], ngroups[2];
-#pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const int u_idx = q < npend ? pend_u[q] : pend_u[0];
-    const int c_first = q < npend ? pend_c[q] : pend_c[0];
-    const int nseg = q < npend ? pend_n[q] : pend_n[0];
-    const int grp = (static_cast<int>(blockIdx.x) - c_first) / kMergeGroup;
-    first_g[q] = c_first + grp * kMergeGroup;
-    ngroups[q] = (nseg + kMergeGroup - 1) / kMergeGroup;
-    MergeJob &J = job[q];
-    J.o = p.o_part;
-    J.lse = p.lse_part;
-    J.slot0 = static_cast<size_t>(u_idx) + first_g[q];
-    J.n = min(kMergeGroup, nseg - grp * kMergeGroup);
-    J.stride = 1;
-    J.c0 = first_g[q];
-    J.nseg = nseg;
-    J.level = 1;
-    J.o_grp = ngroups[q] > 1 ? p.o_group : nullptr;
-    J.lse_grp = p.lse_group;
-    J.grp_slot = J.slot0;
-    const int bq = q < npend ? pend_b[q] : pend_b[0], gq2 = q < npend ? pend_g[q] : pend_g[0];
-    J.out = static_cast<T *>(p.out) + (static_cast<size_t>(bq) * p.Hq + gq2 * p.G) * D;
-  }
+  volatile int *roles = misc + 8;   // per pending unit: helper index (-1: none), H
   if (tid == 0) {
     fence_acq_rel_gpu();   // release this part's partials
     int prev[2];
 #pragma unroll
     for (int q = 0; q < 2; ++q)
-      if (q < npend) prev[q] = atom_add_relaxed_gpu(&p.counters[pend_u[q] + first_g[q]], 1);
-    fence_acq_rel_gpu();   // acquire the other parts' partials
-    int last = 0;
+      if (q < npend) prev[q] = atom_add_relaxed_gpu(&p.counters[pend_u[q]], 1);
+    fence_acq_rel_gpu();   // acquire the partials of the parts that arrived before
 #pragma unroll
-    for (int q = 0; q < 2; ++q)
-      if (q < npend && prev[q] == real_parts(first_g[q], job[q].n, P, C) - 1) {
-        last |= 1 << q;
-        p.counters[pend_u[q] + first_g[q]] = 0;
+    for (int q = 0; q < 2; ++q) {
+      int r = -1, H = 1;
+      if (q < npend) {
+        const int n = real_parts(pend_c[q], pend_n[q], P, C);
+        H = n < kHelperMinSplit ? 1 : merge_helpers(n, p.G * (D / 4), p.max_helpers);
+        r = prev[q] - (n - H);
+        if (r >= 0 && r < H - 1 && !wait_count(&p.counters[pend_u[q]], n, p.wait_limit)) {
+          set_dev_err(p.err, PKV_DEVERR_TIMEOUT);
+          r = -1;   // (the counters stay set: the workspace must be cleared)
+        }
       }
-    misc[4] = last;
+      roles[2 * q] = r;
+      roles[2 * q + 1] = H;
+    }
   }
   asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
-  const int last1 = misc[4];
-  if (last1 == 0) return;
-  merge_jobs<T>((last1 & 1) ? job[0] : job[1], job[1], last1 == 3 ? 2 : 1, p.G, D, P, C, tid, kConsumers);
-  // level 2 for the units that have several groups
-  int multi = 0;
-#pragma unroll
-  for (int q = 0; q < 2; ++q)
-    if ((last1 >> q & 1) && ngroups[q] > 1) multi |= 1 << q;
-  if (multi == 0) return;
-  asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");   // group results written
+  const int ra = roles[0], Ha = roles[1], rb = roles[2], Hb = roles[3];
+  if (ra < 0 && rb < 0) return;   // (the same for every consumer thread)
+  float *scratch = red_acc;       // free: the segment combines are done
+  auto rows_of = [&](int q) {
+    return static_cast<T *>(p.out) +
+           (static_cast<size_t>(q ? pend_b[1] : pend_b[0]) * p.Hq + (q ? pend_g[1] : pend_g[0]) * p.G) *
+               D;
+  };
+  const int NC = p.G * (D / 4);
+  if (Ha == 1 && Hb == 1) {
+    // the last part of each unit merges all of it: the columns of both units
+    // are spread over the threads in one pass
+    const int n0 = ra >= 0 ? NC : 0, n1 = rb >= 0 ? NC : 0;
+    for (int item = tid; item < n0 + n1; item += kConsumers) {
+      const int q = item >= n0 ? 1 : 0;
+      const int col = item - q * n0;
+      merge_store<T>(rows_of(q), col, D,
+                     merge_partials(p.o_part, p.lse_part, q ? pend_u[1] : pend_u[0],
+                                    q ? pend_c[1] : pend_c[0], q ? pend_n[1] : pend_n[0], 0, 1,
+                                    col, p.G, D, P, C));
+    }
+  } else {
+    for (int q = 0; q < npend; ++q) {
+      const int r = q ? rb : ra, H = q ? Hb : Ha;
+      if (r < 0) continue;
+      merge_slice<T, kConsumers>(p, q ? pend_u[1] : pend_u[0], q ? pend_c[1] : pend_c[0],
+                                 q ? pend_n[1] : pend_n[0], P, C, r, H, D, rows_of(q), scratch,
+                                 tid);
+      asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");   // scratch reuse
+    }
+  }
   if (tid == 0) {
-    fence_acq_rel_gpu();
-    int prev[2];
+    // this part is done with the partials: the last helper of a unit to finish
+    // resets its counters for the next call
 #pragma unroll
-    for (int q = 0; q < 2; ++q)
-      if (multi >> q & 1) prev[q] = atom_add_relaxed_gpu(&p.unit_counters[pend_u[q]], 1);
-    fence_acq_rel_gpu();
-    int last = 0;
-#pragma unroll
-    for (int q = 0; q < 2; ++q)
-      if ((multi >> q & 1) && prev[q] == real_groups(pend_c[q], pend_n[q], P, C) - 1) {
-        last |= 1 << q;
-        p.unit_counters[pend_u[q]] = 0;
+    for (int q = 0; q < 2; ++q) {
+      const int r = q ? rb : ra, H = q ? Hb : Ha;
+      if (r < 0) continue;
+      const int u_idx = q ? pend_u[1] : pend_u[0];
+      if (H == 1 || atom_add_relaxed_gpu(&p.done[u_idx], 1) == H - 1) {
+        p.counters[u_idx] = 0;
+        if (H > 1) p.done[u_idx] = 0;
       }
-    misc[5] = last;
+    }
   }
-  asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
-  const int last2 = misc[5];
-  if (last2 == 0) return;
-#pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    MergeJob &J = job[q];
-    J.o = p.o_group;
-    J.lse = p.lse_group;
-    J.slot0 = static_cast<size_t>(q < npend ? pend_u[q] : pend_u[0]) +
-              (q < npend ? pend_c[q] : pend_c[0]);
-    J.n = ngroups[q];
-    J.stride = kMergeGroup;
-    J.c0 = q < npend ? pend_c[q] : pend_c[0];
-    J.level = 2;
-    J.o_grp = nullptr;
-  }
-  merge_jobs<T>((last2 & 1) ? job[0] : job[1], job[1], last2 == 3 ? 2 : 1, p.G, D, P, C, tid,
-                kConsumers);
 }
 
 // ---------------------------------------------------------------------------
@@ -1448,11 +1527,21 @@ struct AttnLauncher {
     cfg.blockDim = dim3(Q::kThreads);
     cfg.dynamicSmemBytes = Q::kSmemBytes;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    // merge helpers wait for other CTAs of the grid: a cooperative launch
+    // guarantees that all of them are resident (the host enables helpers only
+    // for grids that fit)
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (p.max_helpers > 1) {
+      attr[na].id = cudaLaunchAttributeCooperative;
+      attr[na++].val.cooperative = 1;
+    }
+    if (!FUSE) {
+      attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[na++].val.programmaticStreamSerializationAllowed = 1;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = FUSE ? 0 : 1;
+    cfg.numAttrs = na;
     e = cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

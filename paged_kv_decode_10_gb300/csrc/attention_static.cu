@@ -16,6 +16,7 @@
 // __device__ variable is not a device address).
 #include <mutex>
 
+#include "attention_host.h"
 #include "common.cuh"
 
 namespace {
@@ -60,14 +61,18 @@ extern "C" int pkv_decode_attn_static(const void *q_rot, const void *k_cache,
   PKV_REQUIRE(!(flags & PKV_ATTN_SEPARATE_MERGE), PKV_ERR_INVALID_ARG,
               "the static-scratch call always merges in the attention kernel");
   if (B == 0) return PKV_OK;
-  int rc;
+  size_t need = 0;
+  // (pkv_attn_workspace_bytes also checks the shapes, so Hq / Hkv is valid
+  // below; it needs a part count, so a default one is sized after it)
+  int rc = pkv_attn_workspace_bytes(B, Hq, Hkv, d, num_parts > 0 ? num_parts : 1, &need);
+  if (rc != PKV_OK) return rc;
   if (num_parts <= 0) {
-    rc = pkv_attn_default_parts(d, dtype, flags, &num_parts);
+    // the same default as pkv_decode_attn_split: it depends on the group size
+    rc = pkv::default_parts(d, dtype, flags, Hq / Hkv, &num_parts);
+    if (rc != PKV_OK) return rc;
+    rc = pkv_attn_workspace_bytes(B, Hq, Hkv, d, num_parts, &need);
     if (rc != PKV_OK) return rc;
   }
-  size_t need = 0;
-  rc = pkv_attn_workspace_bytes(B, Hq, Hkv, d, num_parts, &need);
-  if (rc != PKV_OK) return rc;
   PKV_REQUIRE(need <= kStaticScratchBytes, PKV_ERR_UNSUPPORTED,
               "this call needs %zu bytes of scratch, more than the %zu-byte static array "
               "(use pkv_decode_attn_split with a caller-provided workspace)",
@@ -75,9 +80,13 @@ extern "C" int pkv_decode_attn_static(const void *q_rot, const void *k_cache,
   void *scratch = nullptr;
   rc = scratch_address(&scratch);
   if (rc != PKV_OK) return rc;
-  // Earlier calls may have used another layout (other B, heads or parts), so
-  // the merge counters cannot be assumed zero: clear the bytes this call uses.
-  PKV_CUDA_CHECK(cudaMemsetAsync(scratch, 0, need, static_cast<cudaStream_t>(stream)));
+  // The kernel reads nothing of its scratch before writing it except the merge
+  // counters, which it expects at zero and leaves at zero.  An earlier call
+  // with another layout (other B, heads or parts), or one that gave up a wait,
+  // can leave non-zero words where this call's counters sit: clear them.
+  PKV_CUDA_CHECK(cudaMemsetAsync(scratch, 0, pkv::workspace_counter_bytes(B, Hq, Hkv, d,
+                                                                          num_parts),
+                                 static_cast<cudaStream_t>(stream)));
   return pkv_decode_attn_split(q_rot, k_cache, v_cache, num_blocks, block_tables, bt_stride,
                                seq_lens, attn_bias, bias_stride, B, Hq, Hkv, d, scale, num_parts,
                                scratch, need, out, dtype, flags, dev_err_flag, stream);

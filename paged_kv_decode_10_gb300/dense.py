@@ -45,7 +45,7 @@ class DenseBatch:
         self.k = torch.zeros(shape, dtype=self.tdtype, **dev)
         self.v = torch.zeros(shape, dtype=self.tdtype, **dev)
         code = binding.F32 if dtype == "f32" else binding.BF16
-        self.num_parts = num_parts or binding.default_parts(d, code, flags)
+        self.num_parts = num_parts or binding.default_parts(d, code, flags, Hq, Hkv)
         self.workspace = binding.alloc_workspace(max_rows, Hq, Hkv, d, self.num_parts, self.device)
         self.q_rot = torch.empty((max_rows, Hq, d), dtype=self.tdtype, **dev)
         self.k_rot = torch.empty((max_rows, Hkv, d), dtype=self.tdtype, **dev)

@@ -89,7 +89,7 @@ class PagedDecoder:
         self.alloc = binding.BlockAllocator(num_blocks, max_seqs, max_blocks_per_seq,
                                             initial_free)
         code = binding.F32 if dtype == "f32" else binding.BF16
-        self.num_parts = num_parts or binding.default_parts(d, code, flags)
+        self.num_parts = num_parts or binding.default_parts(d, code, flags, Hq, Hkv)
         self.workspace = binding.alloc_workspace(max_seqs, Hq, Hkv, d, self.num_parts,
                                                  self.device)
         # consecutive layers alternate between two workspaces
@@ -246,7 +246,7 @@ class PagedDecoder:
         launch."""
         torch = self.torch
         binding.default_parts(self.d, binding.F32 if self.dtype == "f32" else binding.BF16,
-                              self.flags)   # sets kernel attributes outside capture
+                              self.flags, self.Hq, self.Hkv)   # kernel attributes outside capture
         nbytes = _metadata_layout(B, self.bt_stride)[-1]
         stream = torch.cuda.Stream(self.device)
         stream.wait_stream(torch.cuda.current_stream(self.device))
@@ -304,7 +304,7 @@ class PagedDecoder:
         self.v_host = torch.empty((B, self.Hkv, self.d), **pin)
         self.out_host = torch.empty((B, self.Hq, self.d), **pin)
         binding.default_parts(self.d, binding.F32 if self.dtype == "f32" else binding.BF16,
-                              self.flags)   # sets kernel attributes outside capture
+                              self.flags, self.Hq, self.Hkv)   # kernel attributes outside capture
         nbytes = _metadata_layout(B, self.bt_stride)[-1]
         stream = torch.cuda.Stream(self.device)
         stream.wait_stream(torch.cuda.current_stream(self.device))

@@ -27,7 +27,24 @@ def test_library_exports_every_declared_function(host_lib):
     for name in names:
         assert hasattr(host_lib, name), name
         assert name in binding.SIGNATURES, name
-    assert host_lib.pkv_abi_version() == 3
+    assert host_lib.pkv_abi_version() == 4
+
+
+def test_binding_constants_match_the_header():
+    """Status codes, dtype codes, flag bits and error bits of the binding are the
+    values the header defines."""
+    from paged_kv_decode_10_gb300 import binding
+    defines = dict((m.group(1), int(m.group(2))) for m in re.finditer(
+        r"#define PKV_([A-Z0-9_]+)\s+(\d+)", open(HEADER).read()))
+    checked = 0
+    for name, value in defines.items():
+        if hasattr(binding, name):
+            assert getattr(binding, name) == value, name
+            checked += 1
+    for must in ("ATTN_SIMT", "ATTN_SEPARATE_MERGE", "STEP_FUSED", "ATTN_SHORT_WAITS",
+                 "DEVERR_TIMEOUT", "ERR_CUDA", "BF16", "HOST_IN_PLACE"):
+        assert must in defines and hasattr(binding, must), must
+    assert checked >= 18
 
 
 def _run_trace(alloc_cls, errors):

@@ -1,15 +1,19 @@
 """The attention call that allocates nothing (pkv_decode_attn_static).
 
-Callers that cannot allocate device memory use a scratch array compiled into
-the library instead of a workspace they would have to provide.  This file is
-collected last so that a run stopping at the first failure has already run
-every other test; it also passes when run alone in a fresh process.
+Some callers cannot allocate device memory at all -- code that runs under
+another runtime's memory manager, plugins that are handed only their input and
+output tensors, paths that must never reach an allocator -- so they cannot
+provide the workspace pkv_decode_attn_split needs.  pkv_decode_attn_static takes
+its scratch from an array compiled into the library instead.  These tests call
+it through the C ABI and compare it with the workspace call and with the float64
+oracle.  This file is collected last so that a run stopping at the first failure
+has already run every other test; it also passes when run alone in a fresh
+process.
 """
-import numpy as np
 import pytest
 import torch
 
-from helpers import TOL, dev, gpu_single_step
+from helpers import TOL, assert_out_close, dev, f64, gpu_single_step, oracle_metadata, oracle_rows
 from paged_kv_decode_10_gb300 import binding, workloads
 
 pytestmark = pytest.mark.gpu
@@ -38,9 +42,48 @@ def test_static_scratch_matches_workspace_call_twice(name):
         assert diff <= TOL[w.dtype], diff
 
 
+@pytest.mark.parametrize("name", ["decode16", "tiny"])
+def test_static_scratch_matches_the_oracle(name):
+    """Every row of the call without a workspace against the float64 oracle, at
+    the same tolerances as the workspace path (1e-5 float32, 2e-2 bf16)."""
+    w = workloads.make_workload(name)
+    res = gpu_single_step(w)
+    dec = res["decoder"]
+    B = w.B
+    out = torch.full_like(dec.out[:B], float("nan"))
+    binding.decode_attention_static(dec.q_rot[:B], dec.k_cache, dec.v_cache, dec.tables,
+                                    dec.seq_lens, dec.scale, out, err=dec.err)
+    torch.cuda.synchronize()
+    assert dec.device_errors() == 0
+    caches = workloads.make_caches(w, "cpu")
+    tokens = workloads.make_new_tokens(w, 0, "cpu")
+    ref = oracle_rows(w, caches, tokens, oracle_metadata(w), range(B))
+    got = f64(out)
+    for b in range(B):
+        assert_out_close(got[b], ref[b]["out"], w.dtype, f"row {b}")
+
+
+@pytest.mark.parametrize("name,hq,hkv", [("g8", 32, 4), ("g2", 16, 8), ("g1", 8, 8)])
+def test_static_default_partition_equals_workspace_default(name, hq, hkv):
+    """Left at its default, the call without a workspace picks the same
+    partition as pkv_decode_attn_split for the same group size, so the two give
+    bit-identical outputs (float32 runs on the CUDA-core consumer, whose
+    variants differ by group size)."""
+    w = workloads.custom_workload(name, [5, 300, 17, 1200, 0, 64], hq, hkv, 64, "f32", seed=31)
+    res = gpu_single_step(w)
+    dec = res["decoder"]
+    B = w.B
+    ref = binding.decode_attention(dec.q_rot[:B], dec.k_cache, dec.v_cache, dec.tables,
+                                   dec.seq_lens, dec.scale)
+    out = torch.empty_like(ref)
+    binding.decode_attention_static(dec.q_rot[:B], dec.k_cache, dec.v_cache, dec.tables,
+                                    dec.seq_lens, dec.scale, out)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+
+
 def test_static_scratch_alternating_shapes():
     """A call with another layout in between must not leave stale counters."""
-    outs = {}
     for name in ["decode16", "tiny", "decode16"]:
         w = workloads.make_workload(name)
         res = gpu_single_step(w)
