@@ -456,7 +456,7 @@ def attention_roofline(name, args, device, flush, stream, sampler, peak):
         binding.decode_attention(dec.q_rot[:B], dec.k_cache, dec.v_cache, dec.tables,
                                  dec.seq_lens, scale=dec.scale, num_parts=dec.num_parts,
                                  workspace=dec.workspace, out=dec.out[:B], flags=dec.flags,
-                                 err=dec.err, stream=cap)
+                                 err=dec.err, stream=cap, plan=dec.plan)
     with torch.cuda.graph(kern_graph, stream=cap):
         binding.decode_step_args(step_args, cap)
     stream.wait_stream(cap)
@@ -620,7 +620,7 @@ def run_gpu(args, rank, world, want_cpu=False):
         binding.decode_attention(dec.q_rot[:B], dec.k_cache, dec.v_cache, dec.tables,
                                  dec.seq_lens, scale=dec.scale, num_parts=dec.num_parts,
                                  workspace=dec.workspace, out=dec.out[:B], flags=dec.flags,
-                                 err=dec.err, stream=cap)
+                                 err=dec.err, stream=cap, plan=dec.plan)
     with torch.cuda.graph(kern_graph, stream=cap):
         if args.layers > 1:
             binding.decode_step_layers(step_args, cap)
@@ -870,19 +870,27 @@ def run_e2e(args, dec, ids, tokens, w):
               torch.empty((B, dec.bt_stride), dtype=torch.int32).pin_memory())
     dq, dk, dv = (torch.empty_like(t, device=device) for t in pinned)
     meta_d = [torch.empty_like(m, device=device) for m in meta_h]
+    # the host-planned partition, written by the host after a0 like the metadata
+    plan_h = torch.empty((dec.num_parts, binding.PLAN_INTS), dtype=torch.int32).pin_memory()
+    plan_d = torch.empty_like(plan_h, device=device)
     args_s = binding.make_step_args(
         dq, dk, dv, dec.q_rot[:B], dec.k_rot[:B], dec.k_cache, dec.v_cache, *meta_d,
         dec.scale, dec.rope_base, dec.num_parts, dec.workspace, dec.out[:B],
-        flags=dec.flags, err=dec.err)
+        flags=dec.flags, err=dec.err, plan=plan_d)
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     flush_buf = torch.ones(max(2 * l2, 256 << 20) // 8, dtype=torch.int64, device=device)
     h2d = sum(t.numel() * t.element_size() for t in pinned) + \
-        sum(t.numel() * t.element_size() for t in meta_h)
+        sum(t.numel() * t.element_size() for t in meta_h) + plan_h.numel() * 4
     d2h = out_h.numel() * out_h.element_size()
     n = max(3, min(args.steps, 50))
 
     views = tuple(m.numpy() for m in meta_h)
-    prepare = dec.alloc.step_runner(ids, dec.bt_stride, views)
+    a0 = dec.alloc.step_runner(ids, dec.bt_stride, views)
+    planner = binding.plan_runner(views[2], views[3], w.Hkv, w.d, dec.num_parts, plan_h.numpy())
+
+    def prepare():
+        a0()
+        planner()
     call, args_ref = binding.load().pkv_decode_step_host, ctypes.byref(args_s)
     stream = binding._stream()
 
@@ -901,7 +909,8 @@ def run_e2e(args, dec, ids, tokens, w):
                 nbytes += attn_bytes(views[2], w.Hq, w.Hkv, w.d, elem)
         return nbytes / secs / 1e9, 1e3 * secs / n
 
-    io_in_place = binding.host_io(*pinned, *meta_h, out_h, flags=binding.HOST_IN_PLACE)
+    io_in_place = binding.host_io(*pinned, *meta_h, out_h, flags=binding.HOST_IN_PLACE,
+                                  plan=plan_h)
     # the headline: the captured host step (pkv_step_graph), one launch per step
     graph = binding.StepGraph(args_s, io_in_place)
     launch = binding.load().pkv_step_graph_launch
@@ -918,7 +927,7 @@ def run_e2e(args, dec, ids, tokens, w):
             nbytes += attn_bytes(views[2], w.Hq, w.Hkv, w.d, elem)
     graph.close()
     gbs_p, ms_p = timed(io_in_place)
-    gbs_c, ms_c = timed(binding.host_io(*pinned, *meta_h, out_h))
+    gbs_c, ms_c = timed(binding.host_io(*pinned, *meta_h, out_h, plan=plan_h))
     return {"value": round(nbytes / secs / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "steps": n, "ms_per_step": round(1e3 * secs / n, 4),

@@ -65,6 +65,7 @@ extern "C" {
 #define PKV_DEVERR_BAD_SLOT 2   /* a slot outside [0, num_blocks * 16) */
 #define PKV_DEVERR_BAD_LEN 4    /* seq_len < 0, or longer than bt_stride*16 or bias_stride */
 #define PKV_DEVERR_TIMEOUT 8    /* an internal pipeline wait gave up (never expected) */
+#define PKV_DEVERR_BAD_PLAN 16  /* PKV_ATTN_CHECK_PLAN: the plan disagrees with the metadata */
 
 /* flags for the attention calls */
 #define PKV_ATTN_SIMT 1         /* use the CUDA-core consumer instead of mma.sync (bf16 only;
@@ -79,6 +80,9 @@ extern "C" {
                                      output is incomplete, every copy the kernel issued still
                                      lands before it exits); the workspace must be zero-filled
                                      again before its next use */
+#define PKV_ATTN_CHECK_PLAN 16    /* with a plan: also derive the partition from the metadata
+                                     in the kernel, set PKV_DEVERR_BAD_PLAN where the plan
+                                     disagrees and use the derived one there */
 
 /* Message for the calling thread's last failed call ("" if none). */
 const char *pkv_last_error(void);
@@ -321,6 +325,44 @@ int pkv_decode_attn_static(const void *q_rot, const void *k_cache, const void *v
                            int32_t num_parts, void *out, int32_t dtype, int32_t flags,
                            int32_t *dev_err_flag, void *stream);
 
+/*
+ * Host-planned partition.  Without a plan, every CTA of the attention kernel
+ * first reads all row lengths (to find where its part starts) and then the
+ * block ids of its first pages: two dependent reads before its first page
+ * load, each a round trip over the CPU-GPU link when the step's metadata is
+ * read in place from host memory.  The host that prepared the metadata (a0)
+ * can state the same partition instead: pkv_plan_parts writes one record of
+ * PKV_PLAN_INTS int32 per part, and the kernel then makes one read before it
+ * loads pages.  Record c (part c of num_parts):
+ *   [0] first row b0 of the part (-1: the part owns no position)
+ *   [1] positions of the rows before b0, per KV head (sum of n_b + A over
+ *       rows b < b0 with n_b > 0 pages; A = 4 at d = 64, 2 at d = 128)
+ *   [2] seq_lens[b0], [3] seq_lens[b0 + 1] (0 past the last row)
+ *   [4], [5] P, the total position count (int64, low word first)
+ *   [6], [7] zero
+ *   [8 + i], i < 32: block id of page j0 + i of the part's first unit segment
+ *       (j0 its first page there), -1 past the segment's last page
+ * The plan is a pure function of (seq_lens, block tables, B, Hkv, d,
+ * bt_stride, bias_stride, num_parts): it must come from the very metadata the
+ * kernel reads, and be rebuilt whenever that changes.  PKV_ATTN_CHECK_PLAN
+ * makes the kernel verify it.  Host-only; plan is [num_parts * PKV_PLAN_INTS].
+ */
+#define PKV_PLAN_INTS 40
+int pkv_plan_parts(const int32_t *seq_lens, int32_t B, int32_t Hkv, int32_t d,
+                   const int32_t *block_tables, int32_t bt_stride, int32_t bias_stride,
+                   int32_t num_parts, int32_t *plan);
+
+/* pkv_decode_attn_split with a plan from pkv_plan_parts (device or mapped
+ * pointer; num_parts must be the plan's).  Same results, bit for bit. */
+int pkv_decode_attn_planned(const void *q_rot, const void *k_cache, const void *v_cache,
+                            int32_t num_blocks, const int32_t *block_tables,
+                            int32_t bt_stride, const int32_t *seq_lens,
+                            const float *attn_bias, int32_t bias_stride, int32_t B,
+                            int32_t Hq, int32_t Hkv, int32_t d, float scale,
+                            int32_t num_parts, const int32_t *plan, void *workspace,
+                            size_t workspace_bytes, void *out, int32_t dtype, int32_t flags,
+                            int32_t *dev_err_flag, void *stream);
+
 /* bt_stride and bias_stride (0 when no bias was given) are the values passed to
  * pkv_decode_attn_split: they decide which rows are valid, exactly as there. */
 int pkv_lse_merge(const void *workspace, size_t workspace_bytes, const int32_t *seq_lens,
@@ -350,6 +392,8 @@ typedef struct pkv_step_args {
   size_t workspace_bytes;
   void *out;                         /* [B,Hq,d] */
   int32_t *dev_err_flag;             /* nullable */
+  const int32_t *plan;               /* nullable: pkv_plan_parts of this step's metadata
+                                        for num_parts parts (num_parts must then be > 0) */
 } pkv_step_args;
 
 /* All pointers in *args are device pointers or host memory the GPU can reach
@@ -434,6 +478,8 @@ typedef struct pkv_step_host_io {
   const int32_t *block_tables;       /* [B*bt_stride] */
   void *out;                         /* [B,Hq,d] */
   int32_t flags;                     /* 0 or PKV_HOST_IN_PLACE */
+  const int32_t *plan;               /* nullable: the step's plan (pkv_plan_parts), read in
+                                        place or copied to dev->plan like the metadata */
 } pkv_step_host_io;
 
 /*

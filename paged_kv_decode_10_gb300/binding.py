@@ -17,9 +17,12 @@ OK, ERR_INVALID_ARG, ERR_OUT_OF_BLOCKS, ERR_UNKNOWN_SEQ, ERR_UNSUPPORTED, ERR_CU
 F32, BF16 = 0, 1
 BLOCK_SIZE = 16
 DEVERR_BAD_BLOCK, DEVERR_BAD_SLOT, DEVERR_BAD_LEN, DEVERR_TIMEOUT = 1, 2, 4, 8
+DEVERR_BAD_PLAN = 16
+PLAN_INTS = 40
 ATTN_SIMT = 1
 ATTN_SEPARATE_MERGE = 2
 ATTN_SHORT_WAITS = 8
+ATTN_CHECK_PLAN = 16
 STEP_FUSED = 4
 
 _c_i32 = ctypes.c_int32
@@ -58,7 +61,7 @@ class StepArgs(ctypes.Structure):
         ("scale", ctypes.c_float), ("rope_base", ctypes.c_float),
         ("dtype", _c_i32), ("flags", _c_i32), ("num_parts", _c_i32),
         ("workspace", _vp), ("workspace_bytes", _size_t),
-        ("out", _vp), ("dev_err_flag", _vp),
+        ("out", _vp), ("dev_err_flag", _vp), ("plan", _vp),
     ]
 
 
@@ -66,7 +69,7 @@ class StepHostIO(ctypes.Structure):
     _fields_ = [
         ("q", _vp), ("k", _vp), ("v", _vp),
         ("positions", _vp), ("slot_mapping", _vp), ("seq_lens", _vp),
-        ("block_tables", _vp), ("out", _vp), ("flags", _c_i32),
+        ("block_tables", _vp), ("out", _vp), ("flags", _c_i32), ("plan", _vp),
     ]
 
 
@@ -109,6 +112,12 @@ SIGNATURES = {
                                               _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
                                               ctypes.c_float, _c_i32, _vp, _c_i32, _c_i32, _vp,
                                               _vp]),
+    "pkv_plan_parts": (ctypes.c_int, [_p_i32, _c_i32, _c_i32, _c_i32, _p_i32, _c_i32, _c_i32,
+                                      _c_i32, _p_i32]),
+    "pkv_decode_attn_planned": (ctypes.c_int, [_vp, _vp, _vp, _c_i32, _vp, _c_i32, _vp, _vp,
+                                               _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
+                                               ctypes.c_float, _c_i32, _vp, _vp, _size_t, _vp,
+                                               _c_i32, _c_i32, _vp, _vp]),
     "pkv_lse_merge": (ctypes.c_int, [_vp, _size_t, _vp, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
                                      _c_i32, _c_i32, _vp, _c_i32, _vp]),
     "pkv_decode_step": (ctypes.c_int, [ctypes.POINTER(StepArgs), _vp]),
@@ -129,7 +138,7 @@ SIGNATURES = {
 }
 
 _LIB = None
-ABI_VERSION = 4   # pkv_abi_version() of the library this binding describes
+ABI_VERSION = 5   # pkv_abi_version() of the library this binding describes
 
 
 def library_path():
@@ -444,6 +453,55 @@ def decode_attn_split(q_rot, k_cache, v_cache, block_tables, seq_lens, scale, nu
         dtype_code(q_rot), int(flags), _ptr(err), _stream(stream)))
 
 
+def plan_parts(seq_lens, Hkv, d, block_tables, num_parts, bias_stride=0, out=None):
+    """Host-planned partition (``pkv_plan_parts``) of numpy step metadata:
+    ``seq_lens int32 [B]``, ``block_tables int32 [B, bt_stride]``; returns (or
+    fills) ``int32 [num_parts, PLAN_INTS]``."""
+    lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    tables = np.ascontiguousarray(block_tables, dtype=np.int32)
+    B = len(lens)
+    if tables.ndim != 2 or tables.shape[0] != B:
+        raise PkvError(ERR_INVALID_ARG, "block_tables must be [B, bt_stride]")
+    if out is None:
+        out = np.empty((num_parts, PLAN_INTS), np.int32)
+    _check(load().pkv_plan_parts(_np_ptr(lens, ctypes.c_int32), B, int(Hkv), int(d),
+                                 _np_ptr(tables, ctypes.c_int32), tables.shape[1],
+                                 int(bias_stride), int(num_parts),
+                                 _np_ptr(out, ctypes.c_int32, num_parts * PLAN_INTS)))
+    return out
+
+
+def plan_runner(seq_lens, block_tables, Hkv, d, num_parts, out, bias_stride=0):
+    """A no-argument callable running ``pkv_plan_parts`` on these (fixed)
+    numpy arrays into ``out`` with every pointer converted once, for a loop
+    that re-plans every step after a0 rewrote the arrays in place."""
+    fn = load().pkv_plan_parts
+    B, bt = len(seq_lens), block_tables.shape[1]
+    ptrs = (_np_ptr(seq_lens, ctypes.c_int32, B), _np_ptr(block_tables, ctypes.c_int32, B * bt),
+            _np_ptr(out, ctypes.c_int32, num_parts * PLAN_INTS))
+    args = (ptrs[0], B, int(Hkv), int(d), ptrs[1], bt, int(bias_stride), int(num_parts), ptrs[2])
+    keep = (seq_lens, block_tables, out)
+
+    def run():
+        _check(fn(*args))
+        return keep[2]
+    return run
+
+
+def decode_attn_planned(q_rot, k_cache, v_cache, block_tables, seq_lens, scale, num_parts, plan,
+                        workspace, out, attn_bias=None, flags=0, err=None, stream=None):
+    """a3 with a host-planned partition (``plan``: device or pinned int32
+    ``[num_parts, PLAN_INTS]`` tensor from ``plan_parts``)."""
+    B, Hq, d = q_rot.shape
+    Hkv = k_cache.shape[1]
+    bias_stride = attn_bias.shape[1] if attn_bias is not None else 0
+    _check(load().pkv_decode_attn_planned(
+        _ptr(q_rot), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0], _meta_ptr(block_tables),
+        block_tables.shape[1], _meta_ptr(seq_lens), _ptr(attn_bias), bias_stride, B, Hq, Hkv, d,
+        float(scale), int(num_parts), _meta_ptr(plan), _ptr(workspace), workspace.numel(),
+        _ptr(out), dtype_code(q_rot), int(flags), _ptr(err), _stream(stream)))
+
+
 def decode_attention_static(q_rot, k_cache, v_cache, block_tables, seq_lens, scale, out,
                             num_parts=0, attn_bias=None, flags=0, err=None, stream=None):
     """a3 + fused a4 with the library's built-in scratch array instead of a
@@ -469,8 +527,10 @@ def lse_merge(workspace, seq_lens, bt_stride, B, Hq, Hkv, d, num_parts, out, bia
 
 
 def decode_attention(q_rot, k_cache, v_cache, block_tables, seq_lens, scale, num_parts=None,
-                     workspace=None, out=None, attn_bias=None, flags=0, err=None, stream=None):
-    """a3 + a4: returns ``out [B,Hq,d]``."""
+                     workspace=None, out=None, attn_bias=None, flags=0, err=None, stream=None,
+                     plan=None):
+    """a3 + a4: returns ``out [B,Hq,d]`` (with ``plan``, through the host-planned
+    partition; ``num_parts`` must then be the plan's)."""
     torch = _torch()
     B, Hq, d = q_rot.shape
     Hkv = k_cache.shape[1]
@@ -480,8 +540,12 @@ def decode_attention(q_rot, k_cache, v_cache, block_tables, seq_lens, scale, num
         workspace = alloc_workspace(B, Hq, Hkv, d, num_parts, q_rot.device)
     if out is None:
         out = torch.empty_like(q_rot)
-    decode_attn_split(q_rot, k_cache, v_cache, block_tables, seq_lens, scale, num_parts,
-                      workspace, out, attn_bias, flags, err, stream)
+    if plan is not None:
+        decode_attn_planned(q_rot, k_cache, v_cache, block_tables, seq_lens, scale, num_parts,
+                            plan, workspace, out, attn_bias, flags, err, stream)
+    else:
+        decode_attn_split(q_rot, k_cache, v_cache, block_tables, seq_lens, scale, num_parts,
+                          workspace, out, attn_bias, flags, err, stream)
     if flags & ATTN_SEPARATE_MERGE:
         lse_merge(workspace, seq_lens, block_tables.shape[1], B, Hq, Hkv, d, num_parts, out,
                   attn_bias.shape[1] if attn_bias is not None else 0, stream)
@@ -490,7 +554,7 @@ def decode_attention(q_rot, k_cache, v_cache, block_tables, seq_lens, scale, num
 
 def make_step_args(q, k, v, q_rot, k_rot, k_cache, v_cache, positions, slot_mapping, seq_lens,
                    block_tables, scale, rope_base, num_parts, workspace, out, attn_bias=None,
-                   flags=0, err=None):
+                   flags=0, err=None, plan=None):
     """Fills the ``pkv_step_args`` struct.  All tensors are on the device except
     that q, k, v, positions, slot_mapping, seq_lens and block_tables may be pinned
     host tensors, which the kernels then read in place, and out may be a pinned
@@ -512,6 +576,7 @@ def make_step_args(q, k, v, q_rot, k_rot, k_cache, v_cache, positions, slot_mapp
     a.workspace, a.workspace_bytes = _ptr(workspace), workspace.numel()
     a.out = _meta_ptr(out)
     a.dev_err_flag = _ptr(err)
+    a.plan = _meta_ptr(plan)
     return a
 
 
@@ -617,14 +682,16 @@ class StepGraph:
             pass
 
 
-def host_io(q, k, v, positions, slot_mapping, seq_lens, block_tables, out, flags=0):
+def host_io(q, k, v, positions, slot_mapping, seq_lens, block_tables, out, flags=0, plan=None):
     """``pkv_step_host_io`` over host (CPU, ideally pinned; pinned for
     ``HOST_IN_PLACE``) torch tensors."""
     io = StepHostIO()
     io.flags = int(flags)
     for name, t in (("q", q), ("k", k), ("v", v), ("positions", positions),
                     ("slot_mapping", slot_mapping), ("seq_lens", seq_lens),
-                    ("block_tables", block_tables), ("out", out)):
+                    ("block_tables", block_tables), ("out", out), ("plan", plan)):
+        if t is None and name == "plan":
+            continue
         if t.is_cuda or not t.is_contiguous():
             raise PkvError(ERR_INVALID_ARG, f"{name} must be a contiguous host tensor")
         setattr(io, name, _vp(t.data_ptr()))

@@ -300,7 +300,8 @@ int attn_launch(const void *q_rot, const void *k_cache, const void *v_cache, int
                 const float *attn_bias, int32_t bias_stride, int32_t B, int32_t Hq, int32_t Hkv,
                 int32_t d, float scale, int32_t num_parts, void *workspace,
                 size_t workspace_bytes, void *out, int32_t dtype, int32_t flags,
-                int32_t *dev_err_flag, void *stream, const pkv_step_args *step) {
+                int32_t *dev_err_flag, void *stream, const pkv_step_args *step,
+                const int32_t *plan) {
   int rc = check_shapes(B, Hq, Hkv, d, dtype);
   if (rc != PKV_OK) return rc;
   if (B == 0) return PKV_OK;
@@ -324,6 +325,10 @@ int attn_launch(const void *q_rot, const void *k_cache, const void *v_cache, int
   PKV_REQUIRE((reinterpret_cast<uintptr_t>(out) & 15) == 0, PKV_ERR_INVALID_ARG,
               "out must be 16-byte aligned");
   const int G = Hq / Hkv;
+  PKV_REQUIRE(!plan || num_parts > 0, PKV_ERR_INVALID_ARG,
+              "a plan is made for a given num_parts: pass it");
+  PKV_REQUIRE(!plan || (reinterpret_cast<uintptr_t>(plan) & 15) == 0, PKV_ERR_INVALID_ARG,
+              "plan must be 16-byte aligned");
   if (num_parts <= 0) {
     rc = default_parts(d, dtype, flags, G, &num_parts);
     if (rc != PKV_OK) return rc;
@@ -360,11 +365,10 @@ int attn_launch(const void *q_rot, const void *k_cache, const void *v_cache, int
   if (rc != PKV_OK) return rc;
   p.max_helpers = num_parts <= resident ? kMaxHelpers : 1;
   p.wait_limit = (flags & PKV_ATTN_SHORT_WAITS) ? kShortWaitCycles : kWaitLimitCycles;
-  // a unit boundary (segment combine, pipeline drain) costs a CTA about as
-  // long as streaming this many pages (measured on GB300: ~0.7 us against
-  // ~0.17 us per 2 KB-row page at d=64 and ~0.33 us per page at d=128)
-  p.seg_cost = d <= 64 ? 4 : 2;
+  p.seg_cost = seg_cost(d);
   p.out = out;
+  p.plan = plan;
+  p.check_plan = (flags & PKV_ATTN_CHECK_PLAN) ? 1 : 0;
   p.err = dev_err_flag;
   p.bt_stride = bt_stride;
   p.bias_stride = attn_bias ? bias_stride : 0;
@@ -414,7 +418,23 @@ extern "C" int pkv_decode_attn_split(const void *q_rot, const void *k_cache, con
   clear_error();
   return attn_launch(q_rot, k_cache, v_cache, num_blocks, block_tables, bt_stride, seq_lens,
                      attn_bias, bias_stride, B, Hq, Hkv, d, scale, num_parts, workspace,
-                     workspace_bytes, out, dtype, flags, dev_err_flag, stream, nullptr);
+                     workspace_bytes, out, dtype, flags, dev_err_flag, stream, nullptr, nullptr);
+}
+
+extern "C" int pkv_decode_attn_planned(const void *q_rot, const void *k_cache,
+                                       const void *v_cache, int32_t num_blocks,
+                                       const int32_t *block_tables, int32_t bt_stride,
+                                       const int32_t *seq_lens, const float *attn_bias,
+                                       int32_t bias_stride, int32_t B, int32_t Hq, int32_t Hkv,
+                                       int32_t d, float scale, int32_t num_parts,
+                                       const int32_t *plan, void *workspace,
+                                       size_t workspace_bytes, void *out, int32_t dtype,
+                                       int32_t flags, int32_t *dev_err_flag, void *stream) {
+  clear_error();
+  PKV_REQUIRE(plan, PKV_ERR_INVALID_ARG, "plan is NULL");
+  return attn_launch(q_rot, k_cache, v_cache, num_blocks, block_tables, bt_stride, seq_lens,
+                     attn_bias, bias_stride, B, Hq, Hkv, d, scale, num_parts, workspace,
+                     workspace_bytes, out, dtype, flags, dev_err_flag, stream, nullptr, plan);
 }
 
 extern "C" int pkv_lse_merge(const void *workspace, size_t workspace_bytes,
@@ -452,6 +472,8 @@ extern "C" int pkv_lse_merge(const void *workspace, size_t workspace_bytes,
 extern "C" int pkv_decode_step(const pkv_step_args *a, void *stream) {
   clear_error();
   PKV_REQUIRE(a, PKV_ERR_INVALID_ARG, "args is NULL");
+  PKV_REQUIRE(!a->plan || a->num_parts > 0, PKV_ERR_INVALID_ARG,
+              "a plan is made for a given num_parts: set args->num_parts");
   int num_parts = a->num_parts;
   if (num_parts <= 0 && a->B > 0) {
     int rc = check_shapes(a->B, a->Hq, a->Hkv, a->d, a->dtype);
@@ -465,17 +487,17 @@ extern "C" int pkv_decode_step(const pkv_step_args *a, void *stream) {
                          a->k_cache, a->v_cache, a->B, a->Hq, a->Hkv, a->d, a->num_blocks,
                          a->rope_base, a->dtype, a->dev_err_flag, stream);
     if (rc != PKV_OK) return rc;
-    rc = pkv_decode_attn_split(a->q_rot, a->k_cache, a->v_cache, a->num_blocks, a->block_tables,
-                               a->bt_stride, a->seq_lens, a->attn_bias, a->bias_stride, a->B,
-                               a->Hq, a->Hkv, a->d, a->scale, num_parts, a->workspace,
-                               a->workspace_bytes, a->out, a->dtype, a->flags, a->dev_err_flag,
-                               stream);
+    clear_error();
+    rc = attn_launch(a->q_rot, a->k_cache, a->v_cache, a->num_blocks, a->block_tables,
+                     a->bt_stride, a->seq_lens, a->attn_bias, a->bias_stride, a->B, a->Hq, a->Hkv,
+                     a->d, a->scale, num_parts, a->workspace, a->workspace_bytes, a->out,
+                     a->dtype, a->flags, a->dev_err_flag, stream, nullptr, a->plan);
   } else {
     // PKV_STEP_FUSED: the whole step in one launch
     rc = attn_launch(a->q_rot, a->k_cache, a->v_cache, a->num_blocks, a->block_tables,
                      a->bt_stride, a->seq_lens, a->attn_bias, a->bias_stride, a->B, a->Hq, a->Hkv,
                      a->d, a->scale, num_parts, a->workspace, a->workspace_bytes, a->out,
-                     a->dtype, a->flags, a->dev_err_flag, stream, a);
+                     a->dtype, a->flags, a->dev_err_flag, stream, a, a->plan);
   }
   if (rc != PKV_OK) return rc;
   if (!(a->flags & PKV_ATTN_SEPARATE_MERGE)) return PKV_OK;
@@ -492,6 +514,8 @@ extern "C" int pkv_decode_step_layers(const pkv_step_args *layers, int32_t n_lay
   for (int32_t l = 0; l < n_layers; ++l) {   // checked before anything is launched
     PKV_REQUIRE(!(layers[l].flags & PKV_STEP_FUSED), PKV_ERR_UNSUPPORTED,
                 "PKV_STEP_FUSED is a single-layer form");
+    PKV_REQUIRE(!layers[l].plan || layers[l].num_parts > 0, PKV_ERR_INVALID_ARG,
+                "a plan is made for a given num_parts: set num_parts");
     if (l > 0)
       PKV_REQUIRE(layers[l].workspace != layers[l - 1].workspace, PKV_ERR_INVALID_ARG,
                   "layers %d and %d share a workspace", l - 1, l);
@@ -518,11 +542,11 @@ extern "C" int pkv_decode_step_layers(const pkv_step_args *layers, int32_t n_lay
                                  stream);
     }
     if (rc != PKV_OK) return rc;
-    rc = pkv_decode_attn_split(a->q_rot, a->k_cache, a->v_cache, a->num_blocks, a->block_tables,
-                               a->bt_stride, a->seq_lens, a->attn_bias, a->bias_stride, a->B,
-                               a->Hq, a->Hkv, a->d, a->scale, num_parts, a->workspace,
-                               a->workspace_bytes, a->out, a->dtype, a->flags, a->dev_err_flag,
-                               stream);
+    clear_error();
+    rc = attn_launch(a->q_rot, a->k_cache, a->v_cache, a->num_blocks, a->block_tables,
+                     a->bt_stride, a->seq_lens, a->attn_bias, a->bias_stride, a->B, a->Hq, a->Hkv,
+                     a->d, a->scale, num_parts, a->workspace, a->workspace_bytes, a->out,
+                     a->dtype, a->flags, a->dev_err_flag, stream, nullptr, a->plan);
     if (rc != PKV_OK) return rc;
     if (a->flags & PKV_ATTN_SEPARATE_MERGE) {
       rc = pkv_lse_merge(a->workspace, a->workspace_bytes, a->seq_lens, a->bt_stride,
@@ -560,13 +584,15 @@ int enqueue_host_step(const pkv_step_args *dev, const pkv_step_host_io *host, cu
   if (host->flags & PKV_HOST_IN_PLACE) {
     // inputs read and the result written in place over the CPU-GPU link
     pkv_step_args a = *dev;
-    void *m[8];
-    const void *h[8] = {host->q, host->k, host->v, host->positions, host->slot_mapping,
-                        host->seq_lens, host->block_tables, host->out};
-    for (int i = 0; i < 8; ++i) {
+    void *m[9] = {};
+    const void *h[9] = {host->q, host->k, host->v, host->positions, host->slot_mapping,
+                        host->seq_lens, host->block_tables, host->out, host->plan};
+    for (int i = 0; i < 9; ++i) {
+      if (!h[i]) continue;   // (only the plan is optional)
       const int rc = mapped_address(h[i], &m[i]);
       if (rc != PKV_OK) return rc;
     }
+    a.plan = static_cast<const int32_t *>(m[8]);
     a.q = m[0];
     a.k = m[1];
     a.v = m[2];
@@ -588,7 +614,18 @@ int enqueue_host_step(const pkv_step_args *dev, const pkv_step_host_io *host, cu
                                  B * sizeof(int32_t), cudaMemcpyHostToDevice, s));
   PKV_CUDA_CHECK(cudaMemcpyAsync(const_cast<int32_t *>(dev->block_tables), host->block_tables,
                                  B * dev->bt_stride * sizeof(int32_t), cudaMemcpyHostToDevice, s));
-  const int rc = pkv_decode_step(dev, s);
+  pkv_step_args a = *dev;
+  if (host->plan) {
+    PKV_REQUIRE(dev->plan && dev->num_parts > 0, PKV_ERR_INVALID_ARG,
+                "a host plan needs dev->plan (device buffer) and dev->num_parts");
+    PKV_CUDA_CHECK(cudaMemcpyAsync(const_cast<int32_t *>(dev->plan), host->plan,
+                                   static_cast<size_t>(dev->num_parts) * PKV_PLAN_INTS *
+                                       sizeof(int32_t),
+                                   cudaMemcpyHostToDevice, s));
+  } else {
+    a.plan = nullptr;
+  }
+  const int rc = pkv_decode_step(&a, s);
   if (rc != PKV_OK) return rc;
   PKV_CUDA_CHECK(cudaMemcpyAsync(host->out, dev->out, qb, cudaMemcpyDeviceToHost, s));
   return PKV_OK;

@@ -56,6 +56,8 @@ struct AttnParams {
   int32_t *counters;        // [U] parts of a split unit that have written their partial
   int32_t *done;            // [U] merge helpers of a unit that are done (both kept at 0)
   void *out;                // [B, Hq, D]
+  const int32_t *plan;      // nullable: [C, PKV_PLAN_INTS] host-planned partition (pkv_plan_parts)
+  int check_plan;           // also derive the partition here and flag a plan that disagrees
   int32_t *err;
   int bt_stride, bias_stride;
   int B, Hq, Hkv, G;
@@ -942,73 +944,127 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
     prefetch_tmap(&tmap_v);
   }
 
-  // ---- page counts of all rows: per-thread chunk sums, block-wide scan ----
-  const int nthreads = Q::kThreads;
-  const int chunk = (p.B + nthreads - 1) / nthreads;
-  const int r0 = min(p.B, tid * chunk), r1 = min(p.B, r0 + chunk);
   // The partition balances pages plus seg_cost per unit: a unit of n pages
   // spans n + seg_cost positions, the first seg_cost of them holding no page
   // (a part that starts a unit pays for the boundary with fewer pages).
   const int A = p.seg_cost;
   auto upos = [A](int n) { return n > 0 ? n + A : 0; };
-  int mysum = 0;
-  for (int b = r0; b < r1; ++b) {
-    bool bad;
-    const int len = p.seq_lens[b];
-    if (b < Q::kLensCache) lens_s[b] = len;   // kept for the row search and the producer
-    mysum += upos(pages_of_len(len, p.bt_stride, has_bias, p.bias_stride, &bad));
-    if (bad && blockIdx.x == 0) set_dev_err(p.err, PKV_DEVERR_BAD_LEN);
+  const int nthreads = Q::kThreads;
+  // ---- host-planned partition: this part's record (one read; its block ids
+  // let the producer issue the first TMA loads without a block-table read) ----
+  const bool planned = p.plan != nullptr;
+  const int32_t *rec = planned ? p.plan + static_cast<size_t>(blockIdx.x) * PKV_PLAN_INTS : nullptr;
+  int4 rec_h = make_int4(-1, 0, 0, 0), rec_p = make_int4(0, 0, 0, 0);
+  int plan_ids = -1;
+  if (planned) {
+    rec_h = __ldcg(reinterpret_cast<const int4 *>(rec));       // row, row offset, L, next L
+    rec_p = __ldcg(reinterpret_cast<const int4 *>(rec) + 1);   // P (int64)
+    // the producer's first block ids go out in the same round trip
+    if (warp == NW) plan_ids = __ldcg(rec + 8 + lane);
   }
-  int incl = mysum;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) scan[warp] = incl;
-  __syncthreads();
-  int before = 0, total = 0;
-  for (int w = 0; w < nthreads / 32; ++w) {
-    const int t = scan[w];
-    if (w < warp) before += t;
-    total += t;
-  }
-  const long long excl = before + incl - mysum;
-  const long long P = static_cast<long long>(total) * p.Hkv;
-  const long long start = div_floor(P * blockIdx.x, C);
-  const long long end = div_floor(P * (blockIdx.x + 1), C);
-  if (start < end && mysum > 0 && start >= excl * p.Hkv && start < (excl + mysum) * p.Hkv) {
-    long long acc = excl;
+  // ---- otherwise (or to check the plan): page counts of all rows,
+  // per-thread chunk sums, block-wide scan ----
+  const bool scanned = !planned || p.check_plan;
+  long long P_dev = 0;
+  if (scanned) {
+    const int chunk = (p.B + nthreads - 1) / nthreads;
+    const int r0 = min(p.B, tid * chunk), r1 = min(p.B, r0 + chunk);
+    int mysum = 0;
     for (int b = r0; b < r1; ++b) {
       bool bad;
-      const int len = b < Q::kLensCache ? lens_s[b] : p.seq_lens[b];   // own rows: written above
-      const int n = upos(pages_of_len(len, p.bt_stride, has_bias, p.bias_stride, &bad));
-      if (start < (acc + n) * p.Hkv) {
-        misc[0] = b;
-        misc[1] = static_cast<int>(acc);
-        break;
+      const int len = p.seq_lens[b];
+      if (b < Q::kLensCache) lens_s[b] = len;   // kept for the row search and the producer
+      mysum += upos(pages_of_len(len, p.bt_stride, has_bias, p.bias_stride, &bad));
+      if (bad && blockIdx.x == 0) set_dev_err(p.err, PKV_DEVERR_BAD_LEN);
+    }
+    int incl = mysum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) scan[warp] = incl;
+    __syncthreads();
+    int before = 0, total = 0;
+    for (int w = 0; w < nthreads / 32; ++w) {
+      const int t = scan[w];
+      if (w < warp) before += t;
+      total += t;
+    }
+    const long long excl = before + incl - mysum;
+    P_dev = static_cast<long long>(total) * p.Hkv;
+    const long long s0 = div_floor(P_dev * blockIdx.x, C);
+    if (s0 < div_floor(P_dev * (blockIdx.x + 1), C) && mysum > 0 && s0 >= excl * p.Hkv &&
+        s0 < (excl + mysum) * p.Hkv) {
+      long long acc = excl;
+      for (int b = r0; b < r1; ++b) {
+        bool bad;
+        const int len = b < Q::kLensCache ? lens_s[b] : p.seq_lens[b];   // own rows: written above
+        const int n = upos(pages_of_len(len, p.bt_stride, has_bias, p.bias_stride, &bad));
+        if (s0 < (acc + n) * p.Hkv) {
+          misc[0] = b;
+          misc[1] = static_cast<int>(acc);
+          break;
+        }
+        acc += n;
       }
-      acc += n;
+    }
+    // rows with no token (or an invalid length) output zeros; part c clears
+    // rows c, c + C, ...
+    for (int b = blockIdx.x; b < p.B; b += C) {   // (after the barrier above: lens_s is complete)
+      bool bad;
+      const int len = b < Q::kLensCache ? lens_s[b] : p.seq_lens[b];
+      if (pages_of_len(len, p.bt_stride, has_bias, p.bias_stride, &bad) == 0) {
+        T *o = static_cast<T *>(p.out) + static_cast<size_t>(b) * p.Hq * D;
+        for (int e = tid; e < p.Hq * D; e += nthreads) o[e] = from_f32<T>(0.f);
+      }
     }
   }
-  // rows with no token (or an invalid length) output zeros; part c clears rows
-  // c, c + C, ...
-  for (int b = blockIdx.x; b < p.B; b += C) {   // (after the barrier above: lens_s is complete)
-    bool bad;
-    const int len = b < Q::kLensCache ? lens_s[b] : p.seq_lens[b];
-    if (pages_of_len(len, p.bt_stride, has_bias, p.bias_stride, &bad) == 0) {
-      T *o = static_cast<T *>(p.out) + static_cast<size_t>(b) * p.Hq * D;
-      for (int e = tid; e < p.Hq * D; e += nthreads) o[e] = from_f32<T>(0.f);
+  const long long P_plan =
+      static_cast<long long>(static_cast<uint32_t>(rec_p.x)) | (static_cast<long long>(rec_p.y) << 32);
+  __syncthreads();
+  // with a plan, the producer starts from it; checked plans must agree with
+  // the partition derived here (otherwise that one is used, and flagged)
+  bool use_plan = planned;
+  if (planned && p.check_plan) {
+    bool same = P_plan == P_dev;
+    if (same && div_floor(P_dev * blockIdx.x, C) < div_floor(P_dev * (blockIdx.x + 1), C)) {
+      const int b = misc[0];
+      same = b >= 0 && b == rec_h.x && misc[1] == rec_h.y && rec_h.z == p.seq_lens[b] &&
+             (b + 1 >= p.B || rec_h.w == p.seq_lens[b + 1]);
+    }
+    if (!same) {
+      use_plan = false;
+      if (tid == 0) set_dev_err(p.err, PKV_DEVERR_BAD_PLAN);
     }
   }
+  const long long P = use_plan ? P_plan : P_dev;
+  const long long start = div_floor(P * blockIdx.x, C);
+  const long long end = div_floor(P * (blockIdx.x + 1), C);
   if (blockIdx.x == 0 && tid == 0) {
     // total position count, for the merge to tell empty parts (C > P) from real ones
     p.meta[2 * p.B * p.Hkv] = static_cast<int32_t>(P & 0xffffffffll);
     p.meta[2 * p.B * p.Hkv + 1] = static_cast<int32_t>(P >> 32);
   }
-  __syncthreads();
+  // rows with no token: without the scan, the consumer warps clear them (off
+  // the producer's path)
+  if (!scanned && warp < NW) {
+    for (int b = blockIdx.x; b < p.B; b += C) {
+      bool bad;
+      if (pages_of_len(p.seq_lens[b], p.bt_stride, has_bias, p.bias_stride, &bad) == 0) {
+        T *o = static_cast<T *>(p.out) + static_cast<size_t>(b) * p.Hq * D;
+        for (int e = tid; e < p.Hq * D; e += NW * 32) o[e] = from_f32<T>(0.f);
+      }
+      if (bad && tid == 0) set_dev_err(p.err, PKV_DEVERR_BAD_LEN);
+    }
+  }
   if (start >= end) return;
-  if (misc[0] < 0) {   // the row scan found no owner of `start` (never expected)
+  if (use_plan && rec_h.x >= p.B) {   // a record naming no row: never read outside seq_lens
+    if (tid == 0) set_dev_err(p.err, PKV_DEVERR_BAD_PLAN);
+    return;
+  }
+  const int first_row = use_plan ? rec_h.x : misc[0];
+  if (first_row < 0) {   // no owner of `start` (never expected)
     if (tid == 0) set_dev_err(p.err, PKV_DEVERR_TIMEOUT);
     return;
   }
@@ -1022,13 +1078,16 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
     // no dependent global read.
     constexpr int kBatch = NS >= 8 ? 4 : (NS >= 2 ? NS / 2 : 1);
     const uint64_t l2_stream = l2_policy_evict_first();
-    const int b0 = misc[0];
-    // row lengths: the prologue's copy for the first rows, read ahead beyond
-    const int rl0 = b0 + lane < p.B && b0 + lane >= Q::kLensCache ? p.seq_lens[b0 + lane] : 0;
-    const int rl1 =
-        b0 + 32 + lane < p.B && b0 + 32 + lane >= Q::kLensCache ? p.seq_lens[b0 + 32 + lane] : 0;
+    const int b0 = first_row;
+    // row lengths: the prologue's copy for the first rows (or the plan's for
+    // rows b0 and b0 + 1), read ahead beyond
+    const int lc = scanned ? Q::kLensCache : 0;
+    const int rl0 = b0 + lane < p.B && b0 + lane >= lc ? p.seq_lens[b0 + lane] : 0;
+    const int rl1 = b0 + 32 + lane < p.B && b0 + 32 + lane >= lc ? p.seq_lens[b0 + 32 + lane] : 0;
     auto row_len = [&](int b) {   // b is warp-uniform
-      if (b < Q::kLensCache) return lens_s[b];
+      if (b < lc) return lens_s[b];
+      if (use_plan && b == b0) return rec_h.z;
+      if (use_plan && b == b0 + 1) return rec_h.w;
       const int r = b - b0;
       if (r < 32) return __shfl_sync(0xffffffffu, rl0, r);
       if (r < 64) return __shfl_sync(0xffffffffu, rl1, r - 32);
@@ -1047,7 +1106,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
     };
     UnitCursor u;
     {
-      const long long rowoff = misc[1];
+      const long long rowoff = use_plan ? rec_h.y : misc[1];
       bool bad;
       u.b = b0;
       u.n = pages_of_len(row_len(b0), p.bt_stride, has_bias, p.bias_stride, &bad);
@@ -1067,8 +1126,16 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
       j0 = j1 = 0;
       last = true;
     }
-    int ids = (j0 + lane < j1) ? p.block_tables[static_cast<size_t>(u.b) * p.bt_stride + j0 + lane]
-                               : -1;
+    // block ids of the first 32 pages: from the plan, or read from the table
+    // (and, when the plan is checked, compared with it)
+    int ids;
+    if (use_plan && !p.check_plan) {
+      ids = plan_ids;
+    } else {
+      ids = (j0 + lane < j1) ? p.block_tables[static_cast<size_t>(u.b) * p.bt_stride + j0 + lane]
+                             : -1;
+      if (use_plan && plan_ids != ids) set_dev_err(p.err, PKV_DEVERR_BAD_PLAN);
+    }
     while (!aborted) {
       const int32_t *bt = p.block_tables + static_cast<size_t>(u.b) * p.bt_stride;
       // read ahead: the next unit (if the part reaches its pages) and its

@@ -20,4 +20,4 @@ void clear_error() { g_last_error[0] = '\0'; }
 
 extern "C" const char *pkv_last_error(void) { return g_last_error; }
 
-extern "C" int pkv_abi_version(void) { return 4; }
+extern "C" int pkv_abi_version(void) { return 5; }

@@ -41,20 +41,23 @@ def pool_blocks_for_vram(n_layers, Hkv, d, dtype, fraction=0.25, device=None):
     return binding.pool_blocks(int(free * fraction), n_layers, Hkv, d, code)
 
 
-def _metadata_layout(B, bt_stride):
-    """Byte offsets of slot_mapping (int64), positions, seq_lens and block tables
-    (int32) in one packed buffer for batch size B, and its size."""
+def _metadata_layout(B, bt_stride, plan_parts=0):
+    """Byte offsets of slot_mapping (int64), positions, seq_lens, block tables
+    (int32) and the partition plan (int32 [plan_parts, PLAN_INTS], 16-byte
+    aligned) in one packed buffer for batch size B, and its size."""
     slots = 0
     pos = 8 * B
     lens = pos + 4 * B
     tables = (lens + 4 * B + 15) // 16 * 16
-    return slots, pos, lens, tables, tables + 4 * B * bt_stride
+    plan = (tables + 4 * B * bt_stride + 15) // 16 * 16
+    return slots, pos, lens, tables, plan, plan + 4 * binding.PLAN_INTS * plan_parts
 
 
 class PagedDecoder:
     def __init__(self, num_blocks, Hq, Hkv, d, dtype, max_seqs, max_blocks_per_seq,
                  initial_free=None, device="cuda", num_parts=None, rope_base=10000.0,
-                 scale=None, flags=0, k_cache=None, v_cache=None, metadata="copy", n_layers=1):
+                 scale=None, flags=0, k_cache=None, v_cache=None, metadata="copy", n_layers=1,
+                 plan=True):
         import torch
         if metadata not in ("copy", "mapped"):
             raise ValueError(f"metadata must be 'copy' or 'mapped', not {metadata!r}")
@@ -62,6 +65,9 @@ class PagedDecoder:
             raise ValueError("n_layers must be >= 1")
         self.metadata = metadata
         self.n_layers = n_layers
+        # a0 also states the attention partition (pkv_plan_parts), so the
+        # kernel starts from it instead of scanning every row length first
+        self.planned = bool(plan)
         self.torch = torch
         self.device = torch.device(device)
         self.Hq, self.Hkv, self.d = Hq, Hkv, d
@@ -96,7 +102,8 @@ class PagedDecoder:
         self.workspace2 = (binding.alloc_workspace(max_seqs, Hq, Hkv, d, self.num_parts,
                                                    self.device) if L > 1 else None)
         dev = dict(device=self.device)
-        cap = _metadata_layout(max_seqs, self.bt_stride)[-1]
+        self._plan_parts = self.num_parts if self.planned else 0
+        cap = _metadata_layout(max_seqs, self.bt_stride, self._plan_parts)[-1]
         self._meta_dev = torch.empty(cap if metadata == "copy" else 0, dtype=torch.uint8, **dev)
         # per-layer buffers [L, max_seqs, H, d]; the unsuffixed names are layer 0
         self.q_rots = torch.empty((L, max_seqs, Hq, d), dtype=self.tdtype, **dev)
@@ -130,18 +137,21 @@ class PagedDecoder:
         if hit is not None:
             return hit
         torch = self.torch
-        o_slots, o_pos, o_lens, o_tab, end = _metadata_layout(B, self.bt_stride)
+        o_slots, o_pos, o_lens, o_tab, o_plan, end = _metadata_layout(B, self.bt_stride,
+                                                                      self._plan_parts)
         views = ((raw[o_pos:o_pos + 4 * B].view(torch.int32),
                   raw[o_slots:o_slots + 8 * B].view(torch.int64),
                   raw[o_lens:o_lens + 4 * B].view(torch.int32),
-                  raw[o_tab:end].view(torch.int32).view(B, self.bt_stride)), end)
+                  raw[o_tab:o_plan].view(torch.int32)[:B * self.bt_stride].view(B, self.bt_stride),
+                  raw[o_plan:end].view(torch.int32).view(-1, binding.PLAN_INTS)
+                  if self.planned else None), end)
         self._view_cache[key] = views
         return views
 
     def _set_device_views(self, B):
         """positions/slots/seq_lens/tables: the views the kernels read (device
         tensors, or pinned host tensors when mapped)."""
-        (self.positions, self.slots, self.seq_lens, self.tables), _ = self._views(
+        (self.positions, self.slots, self.seq_lens, self.tables, self.plan), _ = self._views(
             self._meta_cur, B)
 
     # -- batch membership ----------------------------------------------------
@@ -168,12 +178,19 @@ class PagedDecoder:
         run = h["runner"]
         if run is None or run[0] != B:
             views, _ = self._views(h["raw"], B)
-            npv = tuple(t.numpy() for t in views)
+            npv = tuple(t.numpy() for t in views[:4])
             ids = np.empty(B, np.int32)
-            run = h["runner"] = (B, ids, npv, self.alloc.step_runner(ids, self.bt_stride, npv))
-        _, ids, npv, fn = run
+            planner = None
+            if self.planned:
+                planner = binding.plan_runner(npv[2], npv[3], self.Hkv, self.d, self.num_parts,
+                                              views[4].numpy())
+            run = h["runner"] = (B, ids, npv, self.alloc.step_runner(ids, self.bt_stride, npv),
+                                 planner)
+        _, ids, npv, fn, planner = run
         ids[:] = seq_ids
         fn()
+        if planner is not None:
+            planner()
         self.last_metadata = npv
         return npv
 
@@ -190,7 +207,7 @@ class PagedDecoder:
             self._pending = h   # released by the event recorded after the kernels
             self._set_device_views(B)
             return npv
-        nbytes = _metadata_layout(B, self.bt_stride)[-1]
+        nbytes = _metadata_layout(B, self.bt_stride, self._plan_parts)[-1]
         s = stream if stream is not None else torch.cuda.current_stream(self.device)
         with torch.cuda.stream(s):
             self._meta_dev[:nbytes].copy_(h["raw"][:nbytes], non_blocking=True)
@@ -208,7 +225,8 @@ class PagedDecoder:
             q, k, v, self.q_rots[layer, :B], self.k_rots[layer, :B], self.k_caches[layer],
             self.v_caches[layer], self.positions, self.slots, self.seq_lens, self.tables,
             self.scale, self.rope_base, self.num_parts, ws,
-            self.outs[layer, :B] if out is None else out, attn_bias, self.flags, self.err)
+            self.outs[layer, :B] if out is None else out, attn_bias, self.flags, self.err,
+            plan=self.plan)
 
     def layer_args(self, B, q, k, v, attn_bias=None):
         """``StepArgs`` of every layer (``q [L,B,Hq,d]``, ``k, v [L,B,Hkv,d]``)."""
@@ -247,7 +265,7 @@ class PagedDecoder:
         torch = self.torch
         binding.default_parts(self.d, binding.F32 if self.dtype == "f32" else binding.BF16,
                               self.flags, self.Hq, self.Hkv)   # kernel attributes outside capture
-        nbytes = _metadata_layout(B, self.bt_stride)[-1]
+        nbytes = _metadata_layout(B, self.bt_stride, self._plan_parts)[-1]
         stream = torch.cuda.Stream(self.device)
         stream.wait_stream(torch.cuda.current_stream(self.device))
         graphs, all_args = [], []
@@ -305,7 +323,7 @@ class PagedDecoder:
         self.out_host = torch.empty((B, self.Hq, self.d), **pin)
         binding.default_parts(self.d, binding.F32 if self.dtype == "f32" else binding.BF16,
                               self.flags, self.Hq, self.Hkv)   # kernel attributes outside capture
-        nbytes = _metadata_layout(B, self.bt_stride)[-1]
+        nbytes = _metadata_layout(B, self.bt_stride, self._plan_parts)[-1]
         stream = torch.cuda.Stream(self.device)
         stream.wait_stream(torch.cuda.current_stream(self.device))
         graphs, all_args = [], []

@@ -261,6 +261,65 @@ def test_device_error_flags_instead_of_faults():
     assert torch.all(out[0] == 0)
 
 
+@pytest.mark.parametrize("name,parts", [("tiny", None), ("tiny", 7), ("decode16", None),
+                                        ("ragged64", None), ("long131k", None),
+                                        ("ragged64", 4096), ("decode16", 1)])
+def test_planned_partition_equals_the_device_one(name, parts):
+    """Attention through the host-planned partition (pkv_plan_parts, one record
+    per part) is bit-identical to the partition the kernel derives itself; in
+    check mode the kernel derives it too and finds no disagreement."""
+    w = workloads.make_workload(name)
+    res = gpu_single_step(w, num_parts=parts)
+    dec = res["decoder"]
+    B = w.B
+    _, _, lens, tables = (np.array(x) for x in dec.last_metadata)
+    plan = torch.from_numpy(binding.plan_parts(lens, w.Hkv, w.d, tables, dec.num_parts)).to(dev())
+    args = (dec.q_rot[:B], dec.k_cache, dec.v_cache, dec.tables, dec.seq_lens, dec.scale)
+    ref = binding.decode_attention(*args, num_parts=dec.num_parts, err=dec.err)
+    got = binding.decode_attention(*args, num_parts=dec.num_parts, plan=plan, err=dec.err)
+    chk = binding.decode_attention(*args, num_parts=dec.num_parts, plan=plan, err=dec.err,
+                                   flags=binding.ATTN_CHECK_PLAN)
+    torch.cuda.synchronize()
+    assert dec.device_errors() == 0
+    assert torch.equal(got, ref) and torch.equal(chk, ref)
+    assert torch.equal(ref.cpu(), res["out"])
+
+
+def test_checked_plan_that_disagrees_is_flagged_and_not_used():
+    w = workloads.make_workload("decode16")
+    res = gpu_single_step(w)
+    dec = res["decoder"]
+    B = w.B
+    _, _, lens, tables = (np.array(x) for x in dec.last_metadata)
+    plan = binding.plan_parts(lens, w.Hkv, w.d, tables, dec.num_parts)
+    bad = plan.copy()
+    bad[5, 1] += 1            # row offset of part 5
+    bad[9, 8] = bad[9, 9]     # first block id of part 9
+    args = (dec.q_rot[:B], dec.k_cache, dec.v_cache, dec.tables, dec.seq_lens, dec.scale)
+    out = binding.decode_attention(*args, num_parts=dec.num_parts, err=dec.err,
+                                   plan=torch.from_numpy(bad).to(dev()),
+                                   flags=binding.ATTN_CHECK_PLAN)
+    torch.cuda.synchronize()
+    assert dec.device_errors() == binding.DEVERR_BAD_PLAN
+    assert torch.equal(out.cpu(), res["out"])
+
+
+def test_engine_without_plan_matches_engine_with_plan():
+    w = workloads.make_workload("ragged64")
+    res = gpu_single_step(w)
+    d = dev()
+    k_cache, v_cache = workloads.make_caches(w, "cpu")
+    q, k, v = workloads.make_new_tokens(w, 0, "cpu")
+    dec = engine.PagedDecoder(w.num_blocks, w.Hq, w.Hkv, w.d, w.dtype, w.B,
+                              w.max_blocks_per_seq(), initial_free=w.free_order, device=d,
+                              k_cache=k_cache.to(d), v_cache=v_cache.to(d), plan=False)
+    ids = [dec.join(int(L)) for L in w.seq_lens]
+    out = dec.step(ids, q.to(d), k.to(d), v.to(d))
+    torch.cuda.synchronize()
+    assert res["decoder"].planned and not dec.planned
+    assert torch.equal(out.cpu(), res["out"])
+
+
 @pytest.mark.parametrize("name,flags", [("tiny", 0), ("decode16", 0), ("decode16", 1)])
 def test_waits_that_give_up_report_a_timeout(name, flags):
     """With PKV_ATTN_SHORT_WAITS every wait inside the attention kernel gives up

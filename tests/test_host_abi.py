@@ -27,7 +27,7 @@ def test_library_exports_every_declared_function(host_lib):
     for name in names:
         assert hasattr(host_lib, name), name
         assert name in binding.SIGNATURES, name
-    assert host_lib.pkv_abi_version() == 4
+    assert host_lib.pkv_abi_version() == 5
 
 
 def test_binding_constants_match_the_header():
@@ -307,3 +307,67 @@ def test_binding_rejects_arrays_the_library_would_misread(host_lib):
     assert a.num_free() == 64 - 2          # nothing above changed the allocator
     pos, slots = a.seq_slots(sid, 0, 20)
     assert pos.tolist() == list(range(20))
+
+
+def _plan_by_enumeration(lens, Hkv, d, tables, bt_stride, bias_stride, C):
+    """The attention partition written out position by position: every unit
+    (row, KV head) of a row with n > 0 pages is A positions without a page
+    followed by its n pages, units in row-major order; part c owns positions
+    [P*c // C, P*(c+1) // C).  Record fields as pkv.h states them."""
+    A = 4 if d <= 64 else 2
+    pos = []      # (row, KV head, page or -1)
+    for b, L in enumerate(lens):
+        ok = 0 <= L <= bt_stride * 16 and (bias_stride <= 0 or L <= bias_stride)
+        n = -(-L // 16) if ok else 0
+        for g in range(Hkv if n else 0):
+            pos += [(b, g, -1)] * A + [(b, g, j) for j in range(n)]
+    P = len(pos)
+    out = np.zeros((C, 40), np.int64)
+    for c in range(C):
+        rec = [-1, 0, 0, 0, P & 0xffffffff, P >> 32, 0, 0] + [-1] * 32
+        start, end = P * c // C, P * (c + 1) // C
+        if start < end:
+            b, g, _ = pos[start]
+            pages = [j for (bb, gg, j) in pos[start:end] if (bb, gg) == (b, g) and j >= 0]
+            rec[0] = b
+            rec[1] = sum(1 for (bb, gg, _) in pos if bb < b) // Hkv
+            rec[2] = lens[b]
+            rec[3] = lens[b + 1] if b + 1 < len(lens) else 0
+            for i, j in enumerate(pages[:32]):
+                rec[8 + i] = tables[b][j]
+        out[c] = rec
+    return out
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_plan_parts_equals_the_partition_written_out(host_lib, seed):
+    """pkv_plan_parts bit-exact against the partition enumerated position by
+    position (ragged rows, empty rows, lengths the kernel rejects, a bias
+    stride, fewer and more parts than positions)."""
+    from paged_kv_decode_10_gb300 import binding
+    r = np.random.default_rng(seed)
+    B = int(r.integers(1, 14))
+    Hkv = int(r.choice([1, 2, 4, 8]))
+    d = int(r.choice([64, 128]))
+    bt = int(r.integers(2, 40))
+    lens = r.integers(0, bt * 16 + 1, size=B)
+    lens[r.random(B) < 0.15] = 0
+    if seed % 4 == 1:
+        lens[0] = bt * 16 + 5                  # longer than the table: not counted
+    bias_stride = int(r.integers(1, bt * 16)) if seed % 3 == 2 else 0
+    tables = r.integers(0, 10000, size=(B, bt)).astype(np.int32)
+    for C in (1, 3, 7, 64, 304, 1000):
+        got = binding.plan_parts(lens.astype(np.int32), Hkv, d, tables, C, bias_stride)
+        want = _plan_by_enumeration([int(x) for x in lens], Hkv, d, tables.tolist(), bt,
+                                    bias_stride, C)
+        np.testing.assert_array_equal(got.astype(np.int64), want, err_msg=f"C={C}")
+
+
+def test_plan_parts_rejects_bad_arguments(host_lib):
+    from paged_kv_decode_10_gb300 import binding
+    lens = np.array([5], np.int32)
+    tables = np.zeros((1, 1), np.int32)
+    with pytest.raises(binding.PkvError):
+        binding.plan_parts(lens, 2, 96, tables, 4)          # head_dim not built
+    with pytest.raises(binding.PkvError):
+        binding.plan_parts(lens, 0, 64, tables, 4)          # no KV head

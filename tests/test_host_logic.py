@@ -62,13 +62,15 @@ def test_metadata_layout_is_aligned_and_disjoint():
     from paged_kv_decode_10_gb300.engine import _metadata_layout
     for B in (1, 3, 16, 255, 256):
         for bt in (1, 7, 160, 8193):
-            o_slots, o_pos, o_lens, o_tab, end = _metadata_layout(B, bt)
-            spans = sorted([(o_slots, 8 * B), (o_pos, 4 * B), (o_lens, 4 * B), (o_tab, 4 * B * bt)])
-            for (a, n), (b, _) in zip(spans, spans[1:]):
-                assert a + n <= b                       # no overlap
-            assert o_slots % 8 == 0 and o_pos % 4 == 0 and o_lens % 4 == 0
-            assert o_tab % 16 == 0                      # rows start 16-byte aligned
-            assert end == o_tab + 4 * B * bt
+            for parts in (0, 1, 304):
+                o_slots, o_pos, o_lens, o_tab, o_plan, end = _metadata_layout(B, bt, parts)
+                spans = sorted([(o_slots, 8 * B), (o_pos, 4 * B), (o_lens, 4 * B),
+                                (o_tab, 4 * B * bt), (o_plan, 160 * parts)])
+                for (a, n), (b, _) in zip(spans, spans[1:]):
+                    assert a + n <= b                   # no overlap
+                assert o_slots % 8 == 0 and o_pos % 4 == 0 and o_lens % 4 == 0
+                assert o_tab % 16 == 0 and o_plan % 16 == 0   # 16-byte aligned rows / records
+                assert end == o_plan + 160 * parts
 
 
 def test_attention_byte_accounting_hand_example():
