@@ -146,6 +146,17 @@ int pkv_seqs_leave(pkv_alloc *a, const int32_t *seq_ids, int32_t n);
 int pkv_prepare_step(pkv_alloc *a, const int32_t *seq_ids, int32_t B,
                      int32_t *positions, int64_t *slot_mapping, int32_t *seq_lens,
                      int32_t *block_tables, int32_t bt_stride);
+/* The same step, for a block_tables buffer that is rewritten step after step:
+ * row_state (int32 [B*3], all -1 before the first call on a fresh buffer, then
+ * kept by the caller with that buffer) records which sequence, join and table
+ * length each row of the buffer holds, and only the entries that differ are
+ * written (a row whose sequence stayed gets just its new blocks; a row that
+ * changed sequence is rewritten and its stale entries set to -1).  The buffer
+ * then holds exactly what pkv_prepare_step would have written.  Every output
+ * and all allocator state are the same as pkv_prepare_step's. */
+int pkv_prepare_step_cached(pkv_alloc *a, const int32_t *seq_ids, int32_t B,
+                            int32_t *positions, int64_t *slot_mapping, int32_t *seq_lens,
+                            int32_t *block_tables, int32_t bt_stride, int32_t *row_state);
 
 int pkv_seq_len(const pkv_alloc *a, int32_t seq_id, int32_t *len);
 /* Copies up to cap block ids of the sequence's table into out; *n = table length. */
@@ -512,6 +523,71 @@ int pkv_step_graph_create(const pkv_step_args *dev, const pkv_step_host_io *host
 /* Launches the captured step on stream and waits for it (host->out is then set). */
 int pkv_step_graph_launch(pkv_step_graph *g, void *stream);
 void pkv_step_graph_destroy(pkv_step_graph *g);
+
+/* ======================================================================== */
+/* native serving loop: continuous batching, one host call per step          */
+/* ======================================================================== */
+/*
+ * The continuous-batching loop of helexa issue 121, slice 3b (admit joiners,
+ * prefill them, rebatch, decode every live sequence in lockstep) over the
+ * paged cache of "neurogrid releases" v0.7.0 (joining or leaving edits block
+ * tables only; no KV moves), the step replayed as one CUDA graph that reads
+ * the host-written metadata in place (v0.8.0).  A joiner takes over the row of
+ * a sequence that left, so the batch keeps its B rows and two captured graphs
+ * (one per pinned metadata buffer, used alternately) serve every step.
+ *
+ * The caller owns every buffer and keeps each alive and in place for the
+ * server's lifetime (the server allocates no device memory):
+ *  - step: pkv_decode_step's device buffers and sizes for B rows.  step.q,
+ *    step.k, step.v are the graph's input buffers.  Its metadata and plan
+ *    pointers are ignored (the server points them into meta_host); num_parts
+ *    must be > 0; attn_bias must be NULL.
+ *  - alloc: the block allocator; rows[b] (B entries) are live sequences of it,
+ *    which the server then manages (joins and leaves go through the server).
+ *  - meta_host[2]: page-locked host buffers of pkv_server_meta_bytes(B,
+ *    bt_stride, num_parts) bytes, 16-byte aligned (positions, slots, lengths,
+ *    block tables and the partition plan of a step).
+ *  - prefix_host[2]: page-locked host buffers of
+ *    pkv_server_prefix_bytes(max_prefix_tokens) bytes (joiners' prefix
+ *    positions and slots), or NULL when max_prefix_tokens is 0.
+ * Creation captures the two graphs; nothing runs.
+ */
+typedef struct pkv_server pkv_server;
+typedef struct pkv_server_desc {
+  pkv_step_args step;
+  pkv_alloc *alloc;
+  const int32_t *rows;               /* [step.B] live sequence ids, one per row */
+  void *meta_host[2];
+  void *prefix_host[2];
+  int32_t max_prefix_tokens;         /* most prefix tokens joining in one step */
+} pkv_server_desc;
+size_t pkv_server_meta_bytes(int32_t B, int32_t bt_stride, int32_t num_parts);
+size_t pkv_server_prefix_bytes(int32_t max_prefix_tokens);
+int pkv_server_create(const pkv_server_desc *desc, pkv_server **out);
+/*
+ * One step, enqueued on stream.  The sequences of rows leave_rows[0..n-1]
+ * retire and n joiners take those rows, joiner i with a prefix of
+ * prefix_lens[i] tokens whose raw keys and values are prefix_k, prefix_v
+ * (device, [sum(prefix_lens), Hkv, d], joiner after joiner): they are rotated
+ * at their positions and written into the joiners' blocks (pkv_prefill_kv).
+ * Then every row decodes one token: q, k, v (device, [B,Hq,d], [B,Hkv,d],
+ * [B,Hkv,d]; NULL or the step's own input buffers: nothing to copy) are copied
+ * into the step's input buffers, a0 (pkv_prepare_step_cached) and the plan
+ * (pkv_plan_parts) are written into a metadata buffer, and the captured step
+ * is launched: the result is in step.out when the stream gets there.  The
+ * call waits only for the step two calls back, which used the same host
+ * buffers.  Argument errors change nothing; a failure after the leaves (the
+ * pool cannot take the joiners: PKV_ERR_OUT_OF_BLOCKS) leaves the server
+ * unusable, and every later step returns PKV_ERR_INVALID_ARG.
+ */
+int pkv_server_step(pkv_server *s, const int32_t *leave_rows, const int32_t *prefix_lens,
+                    int32_t n, const void *prefix_k, const void *prefix_v, const void *q,
+                    const void *k, const void *v, void *stream);
+/* The sequence id of every row ([B]). */
+int pkv_server_rows(const pkv_server *s, int32_t *rows);
+/* Frees the server (not the caller's buffers or allocator); call after its
+ * last step has finished on the GPU. */
+void pkv_server_destroy(pkv_server *s);
 
 #ifdef __cplusplus
 }

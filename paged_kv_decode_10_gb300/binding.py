@@ -73,6 +73,13 @@ class StepHostIO(ctypes.Structure):
     ]
 
 
+class ServerDesc(ctypes.Structure):
+    _fields_ = [
+        ("step", StepArgs), ("alloc", _vp), ("rows", _vp),
+        ("meta_host", _vp * 2), ("prefix_host", _vp * 2), ("max_prefix_tokens", _c_i32),
+    ]
+
+
 # name -> (restype, argtypes); every symbol declared in include/pkv.h
 SIGNATURES = {
     "pkv_last_error": (ctypes.c_char_p, []),
@@ -86,6 +93,8 @@ SIGNATURES = {
     "pkv_seqs_leave": (ctypes.c_int, [_vp, _p_i32, _c_i32]),
     "pkv_prepare_step": (ctypes.c_int, [_vp, _p_i32, _c_i32, _p_i32, _p_i64, _p_i32, _p_i32,
                                         _c_i32]),
+    "pkv_prepare_step_cached": (ctypes.c_int, [_vp, _p_i32, _c_i32, _p_i32, _p_i64, _p_i32,
+                                               _p_i32, _c_i32, _p_i32]),
     "pkv_seq_len": (ctypes.c_int, [_vp, _c_i32, _p_i32]),
     "pkv_seq_blocks": (ctypes.c_int, [_vp, _c_i32, _p_i32, _c_i32, _p_i32]),
     "pkv_seq_slots": (ctypes.c_int, [_vp, _c_i32, _c_i32, _c_i32, _p_i32, _p_i64]),
@@ -135,6 +144,13 @@ SIGNATURES = {
                                              ctypes.POINTER(StepHostIO), ctypes.POINTER(_vp)]),
     "pkv_step_graph_launch": (ctypes.c_int, [_vp, _vp]),
     "pkv_step_graph_destroy": (None, [_vp]),
+    "pkv_server_meta_bytes": (_size_t, [_c_i32, _c_i32, _c_i32]),
+    "pkv_server_prefix_bytes": (_size_t, [_c_i32]),
+    "pkv_server_create": (ctypes.c_int, [ctypes.POINTER(ServerDesc), ctypes.POINTER(_vp)]),
+    "pkv_server_step": (ctypes.c_int, [_vp, _p_i32, _p_i32, _c_i32, _vp, _vp, _vp, _vp, _vp,
+                                       _vp]),
+    "pkv_server_rows": (ctypes.c_int, [_vp, _p_i32]),
+    "pkv_server_destroy": (None, [_vp]),
 }
 
 _LIB = None
@@ -285,6 +301,19 @@ class BlockAllocator:
             _check(fn(h, ptrs[0], B, ptrs[1], ptrs[2], ptrs[3], ptrs[4], bt))
             return keep[1]
         return run
+
+    def prepare_step_cached(self, seq_ids, bt_stride, out, row_state):
+        """``pkv_prepare_step_cached`` into ``out`` (positions, slot_mapping,
+        seq_lens, block_tables) with the caller-kept ``row_state`` (int32 [B*3])."""
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int32)
+        B = len(ids)
+        pos, slots, lens, tables = out
+        _check(self._lib.pkv_prepare_step_cached(
+            self._h, _np_ptr(ids, ctypes.c_int32), B, _np_ptr(pos, ctypes.c_int32, B),
+            _np_ptr(slots, ctypes.c_int64, B), _np_ptr(lens, ctypes.c_int32, B),
+            _np_ptr(tables, ctypes.c_int32, B * int(bt_stride)), int(bt_stride),
+            _np_ptr(row_state, ctypes.c_int32, 3 * B)))
+        return out
 
     def seq_len(self, seq_id):
         n = ctypes.c_int32()
@@ -696,3 +725,82 @@ def host_io(q, k, v, positions, slot_mapping, seq_lens, block_tables, out, flags
             raise PkvError(ERR_INVALID_ARG, f"{name} must be a contiguous host tensor")
         setattr(io, name, _vp(t.data_ptr()))
     return io
+
+
+class Server:
+    """The native serving loop (``pkv_server``) over a single-layer
+    ``engine.PagedDecoder``'s device buffers for the sequences ``rows`` (one
+    per row); joins and leaves then go through ``step``.  Holds the pinned host
+    buffers the server needs."""
+
+    def __init__(self, dec, rows, max_prefix_tokens):
+        torch = _torch()
+        lib = load()
+        B = len(rows)
+        self.B, self._lib = B, lib
+        nb = lib.pkv_server_meta_bytes(B, dec.bt_stride, dec.num_parts)
+        pb = lib.pkv_server_prefix_bytes(int(max_prefix_tokens))
+        self.meta = [torch.empty(nb, dtype=torch.uint8).pin_memory() for _ in range(2)]
+        self.prefix = [torch.empty(max(pb, 16), dtype=torch.uint8).pin_memory() for _ in range(2)]
+        self.rows_in = np.ascontiguousarray(rows, dtype=np.int32)
+        step = make_step_args(dec.q_in[:B], dec.k_in[:B], dec.v_in[:B], dec.q_rot[:B],
+                              dec.k_rot[:B], dec.k_cache, dec.v_cache, dec.positions[:B],
+                              dec.slots[:B], dec.seq_lens[:B], dec.tables[:B], dec.scale,
+                              dec.rope_base, dec.num_parts, dec.workspace, dec.out[:B],
+                              flags=dec.flags, err=dec.err)
+        self.desc = ServerDesc()
+        self.desc.step = step
+        self.desc.alloc = dec.alloc._h
+        self.desc.rows = self.rows_in.ctypes.data_as(_vp)
+        for t in range(2):
+            self.desc.meta_host[t] = _vp(self.meta[t].data_ptr())
+            self.desc.prefix_host[t] = _vp(self.prefix[t].data_ptr())
+        self.desc.max_prefix_tokens = int(max_prefix_tokens)
+        h = _vp()
+        _check(lib.pkv_server_create(ctypes.byref(self.desc), ctypes.byref(h)))
+        self._h = h
+
+    def step(self, leave_rows, prefix_lens, prefix_k=None, prefix_v=None, q=None, k=None,
+             v=None, stream=None):
+        """One step (see ``pkv_server_step``); leave_rows and prefix_lens are
+        int32 numpy arrays of the same length."""
+        lr = np.ascontiguousarray(leave_rows, dtype=np.int32)
+        pl = np.ascontiguousarray(prefix_lens, dtype=np.int32)
+        if len(lr) != len(pl):
+            raise PkvError(ERR_INVALID_ARG, "one prefix length per leaving row")
+        _check(self._lib.pkv_server_step(
+            self._h, _np_ptr(lr, ctypes.c_int32), _np_ptr(pl, ctypes.c_int32), len(lr),
+            _ptr(prefix_k), _ptr(prefix_v), _ptr(q), _ptr(k), _ptr(v), _stream(stream)))
+
+    def step_runner(self, leave_rows, prefix_lens, prefix_k=None, prefix_v=None, q=None, k=None,
+                    v=None, stream=None):
+        """A no-argument callable running this step with every argument
+        converted once (a loop that replays a planned schedule)."""
+        lr = np.ascontiguousarray(leave_rows, dtype=np.int32)
+        pl = np.ascontiguousarray(prefix_lens, dtype=np.int32)
+        if len(lr) != len(pl):
+            raise PkvError(ERR_INVALID_ARG, "one prefix length per leaving row")
+        args = (self._h, _np_ptr(lr, ctypes.c_int32), _np_ptr(pl, ctypes.c_int32), len(lr),
+                _ptr(prefix_k), _ptr(prefix_v), _ptr(q), _ptr(k), _ptr(v), _stream(stream))
+        fn, keep = self._lib.pkv_server_step, (lr, pl, prefix_k, prefix_v, q, k, v)
+
+        def run():
+            _check(fn(*args))
+            return keep
+        return run
+
+    def rows(self):
+        out = np.empty(self.B, np.int32)
+        _check(self._lib.pkv_server_rows(self._h, _np_ptr(out, ctypes.c_int32, self.B)))
+        return out
+
+    def close(self):
+        if self._h:
+            self._lib.pkv_server_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -26,6 +26,7 @@ struct pkv_alloc {
   std::vector<int32_t> lengths;          // per sequence id
   std::vector<uint8_t> live;             // per sequence id
   std::vector<uint32_t> stamp;           // per sequence id, duplicate detection
+  std::vector<int32_t> generation;       // per sequence id, joins so far (ids are reused)
   uint32_t epoch = 0;
   std::priority_queue<int32_t, std::vector<int32_t>, std::greater<int32_t>> free_ids;
 
@@ -82,6 +83,7 @@ extern "C" int pkv_alloc_create(int32_t num_blocks, int32_t block_size, int32_t 
     a->lengths.assign(max_seqs, 0);
     a->live.assign(max_seqs, 0);
     a->stamp.assign(max_seqs, 0);
+    a->generation.assign(max_seqs, 0);
     for (int32_t i = 0; i < max_seqs; ++i) a->free_ids.push(i);
   } catch (...) {
     delete a;
@@ -115,6 +117,7 @@ extern "C" int pkv_seq_join(pkv_alloc *a, int32_t prefix_len, int32_t *seq_id) {
   a->n_blocks[sid] = static_cast<int32_t>(need);
   a->lengths[sid] = prefix_len;
   a->live[sid] = 1;
+  ++a->generation[sid];
   *seq_id = sid;
   return PKV_OK;
 }
@@ -132,11 +135,14 @@ extern "C" int pkv_seq_leave(pkv_alloc *a, int32_t seq_id) {
   return PKV_OK;
 }
 
-extern "C" int pkv_prepare_step(pkv_alloc *a, const int32_t *seq_ids, int32_t B,
-                                int32_t *positions, int64_t *slot_mapping,
-                                int32_t *seq_lens, int32_t *block_tables,
-                                int32_t bt_stride) {
-  pkv::clear_error();
+namespace {
+
+// a0 for one step (pkv_prepare_step).  With row_state, block_tables is a
+// buffer an earlier call wrote with the same row_state, and only the entries
+// that differ from what it holds are written.
+int prepare_step_impl(pkv_alloc *a, const int32_t *seq_ids, int32_t B, int32_t *positions,
+                      int64_t *slot_mapping, int32_t *seq_lens, int32_t *block_tables,
+                      int32_t bt_stride, int32_t *row_state) {
   PKV_REQUIRE(a, PKV_ERR_INVALID_ARG, "NULL allocator");
   PKV_REQUIRE(B >= 0, PKV_ERR_INVALID_ARG, "B < 0");
   if (B == 0) return PKV_OK;
@@ -178,10 +184,48 @@ extern "C" int pkv_prepare_step(pkv_alloc *a, const int32_t *seq_ids, int32_t B,
     seq_lens[b] = pos + 1;
     int32_t *row = block_tables + static_cast<size_t>(b) * bt_stride;
     const int32_t n = a->n_blocks[s];
-    std::memcpy(row, t, sizeof(int32_t) * n);
-    for (int32_t j = n; j < bt_stride; ++j) row[j] = -1;
+    if (!row_state) {
+      std::memcpy(row, t, sizeof(int32_t) * n);
+      for (int32_t j = n; j < bt_stride; ++j) row[j] = -1;
+      continue;
+    }
+    // row_state[3b..3b+2]: sequence id, its join generation, entries held
+    int32_t *rs = row_state + 3 * static_cast<size_t>(b);
+    const bool same = rs[0] == s && rs[1] == a->generation[s] && rs[2] >= 0 && rs[2] <= n;
+    if (same) {
+      // the same sequence as last time in this buffer: its table only grew
+      std::memcpy(row + rs[2], t + rs[2], sizeof(int32_t) * (n - rs[2]));
+    } else {
+      std::memcpy(row, t, sizeof(int32_t) * n);
+      const int32_t held = (rs[2] >= 0 && rs[2] <= bt_stride && rs[0] >= 0) ? rs[2] : bt_stride;
+      for (int32_t j = n; j < held; ++j) row[j] = -1;
+    }
+    rs[0] = s;
+    rs[1] = a->generation[s];
+    rs[2] = n;
   }
   return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" int pkv_prepare_step(pkv_alloc *a, const int32_t *seq_ids, int32_t B,
+                                int32_t *positions, int64_t *slot_mapping,
+                                int32_t *seq_lens, int32_t *block_tables,
+                                int32_t bt_stride) {
+  pkv::clear_error();
+  return prepare_step_impl(a, seq_ids, B, positions, slot_mapping, seq_lens, block_tables,
+                           bt_stride, nullptr);
+}
+
+extern "C" int pkv_prepare_step_cached(pkv_alloc *a, const int32_t *seq_ids, int32_t B,
+                                       int32_t *positions, int64_t *slot_mapping,
+                                       int32_t *seq_lens, int32_t *block_tables,
+                                       int32_t bt_stride, int32_t *row_state) {
+  pkv::clear_error();
+  PKV_REQUIRE(row_state, PKV_ERR_INVALID_ARG, "NULL row_state");
+  return prepare_step_impl(a, seq_ids, B, positions, slot_mapping, seq_lens, block_tables,
+                           bt_stride, row_state);
 }
 
 extern "C" int pkv_seqs_join(pkv_alloc *a, const int32_t *prefix_lens, int32_t n,

@@ -371,3 +371,39 @@ def test_plan_parts_rejects_bad_arguments(host_lib):
         binding.plan_parts(lens, 2, 96, tables, 4)          # head_dim not built
     with pytest.raises(binding.PkvError):
         binding.plan_parts(lens, 0, 64, tables, 4)          # no KV head
+
+
+def test_prepare_step_cached_equals_prepare_step_under_churn(host_lib):
+    """pkv_prepare_step_cached writing into two alternating table buffers (as the
+    serving loop does) leaves every output and each buffer exactly as
+    pkv_prepare_step writes them, through joins and leaves that reuse sequence
+    ids and blocks, over many steps."""
+    from paged_kv_decode_10_gb300 import binding
+    r = np.random.default_rng(5)
+    nb, B, bt = 400, 12, 12
+    perm = r.permutation(nb).astype(np.int32)
+    full = binding.BlockAllocator(nb, 64, bt, perm)
+    cached = binding.BlockAllocator(nb, 64, bt, perm)
+    lens0 = r.integers(0, 60, size=B)
+    rows = [[a.join(int(L)) for L in lens0] for a in (full, cached)]
+    assert rows[0] == rows[1]
+    bufs = []
+    for _ in range(2):
+        out = (np.empty(B, np.int32), np.empty(B, np.int64), np.empty(B, np.int32),
+               np.full((B, bt), 7777, np.int32))          # stale garbage to begin with
+        bufs.append((out, np.full(3 * B, -1, np.int32)))
+    for step in range(60):
+        if step % 3 == 2:
+            leave = r.choice(B, size=3, replace=False)
+            prefixes = r.integers(0, 40, size=3)
+            for a, ids in zip((full, cached), rows):
+                a.leave_many([ids[i] for i in leave])
+                for i, sid in zip(leave, a.join_many(prefixes)):
+                    ids[i] = int(sid)
+            assert rows[0] == rows[1]
+        want = full.prepare_step(rows[0], bt)
+        out, state = bufs[step % 2]
+        got = cached.prepare_step_cached(rows[1], bt, out, state)
+        for g, w_ in zip(got, want):
+            np.testing.assert_array_equal(g, w_)
+        assert full.free_stack() == cached.free_stack()
