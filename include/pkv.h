@@ -352,7 +352,8 @@ int pkv_decode_attn_static(const void *q_rot, const void *k_cache, const void *v
  *   [4], [5] P, the total position count (int64, low word first)
  *   [6], [7] zero
  *   [8 + i], i < 32: block id of page j0 + i of the part's first unit segment
- *       (j0 its first page there), -1 past the segment's last page
+ *       (j0 its first page there); entries past the segment's last page are
+ *       not written (and not read)
  * The plan is a pure function of (seq_lens, block tables, B, Hkv, d,
  * bt_stride, bias_stride, num_parts): it must come from the very metadata the
  * kernel reads, and be rebuilt whenever that changes.  PKV_ATTN_CHECK_PLAN

@@ -1134,7 +1134,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
     } else {
       ids = (j0 + lane < j1) ? p.block_tables[static_cast<size_t>(u.b) * p.bt_stride + j0 + lane]
                              : -1;
-      if (use_plan && plan_ids != ids) set_dev_err(p.err, PKV_DEVERR_BAD_PLAN);
+      if (use_plan && j0 + lane < j1 && plan_ids != ids) set_dev_err(p.err, PKV_DEVERR_BAD_PLAN);
     }
     while (!aborted) {
       const int32_t *bt = p.block_tables + static_cast<size_t>(u.b) * p.bt_stride;

@@ -10,6 +10,7 @@
 // block ids.  The rule for which rows count (valid lengths) and the cost A are
 // the kernel's; the kernel can verify a plan (PKV_ATTN_CHECK_PLAN).
 #include <cstdint>
+#include <cstring>
 #include <vector>
 
 #include "attention_host.h"
@@ -46,28 +47,52 @@ extern "C" int pkv_plan_parts(const int32_t *seq_lens, int32_t B, int32_t Hkv, i
   }
   const int64_t P = rowoff[B] * Hkv;
   PKV_REQUIRE(rowoff[B] < (int64_t(1) << 31), PKV_ERR_UNSUPPORTED, "too many positions");
-  int32_t b = 0;   // the part starts advance monotonically: one walk over the rows
+  // One merged walk over the parts and the units, without divisions: part
+  // starts floor(P*c/C) advance by P/C plus a carry from the remainders, and
+  // the unit cursor (row b, KV head g, first position off) moves forward to the
+  // unit holding each start.
+  const int64_t q0 = P / C, r0 = P % C;
+  int64_t start = 0, rem = 0;
+  int32_t b = 0, g = 0;
+  while (b < B && rowoff[b + 1] == rowoff[b]) ++b;          // first row with pages
+  int64_t off = b < B ? rowoff[b] * Hkv : 0;
+  int64_t n = b < B ? rowoff[b + 1] - rowoff[b] - A : 0;     // its pages
   for (int64_t c = 0; c < C; ++c) {
+    rem += r0;
+    const int64_t end = start + q0 + (rem >= C ? 1 : 0);
+    if (rem >= C) rem -= C;
     int32_t *r = plan + c * PKV_PLAN_INTS;
-    for (int i = 0; i < PKV_PLAN_INTS; ++i) r[i] = (i >= 8) ? -1 : 0;
     r[0] = -1;
+    r[1] = r[2] = r[3] = r[6] = r[7] = 0;
     r[4] = static_cast<int32_t>(static_cast<uint64_t>(P) & 0xffffffffu);
     r[5] = static_cast<int32_t>(static_cast<uint64_t>(P) >> 32);
-    const int64_t start = P * c / C, end = P * (c + 1) / C;
-    if (start >= end) continue;
-    while (b < B && start >= rowoff[b + 1] * Hkv) ++b;   // the row whose positions hold start
-    if (b >= B) continue;                               // (not reached: start < P)
-    const int64_t n = rowoff[b + 1] - rowoff[b] - A;     // pages of row b (> 0)
-    r[0] = b;
-    r[1] = static_cast<int32_t>(rowoff[b]);
-    r[2] = seq_lens[b];
-    r[3] = b + 1 < B ? seq_lens[b + 1] : 0;
-    const int64_t g = (start - rowoff[b] * Hkv) / (n + A);   // KV head of the first unit
-    const int64_t off = rowoff[b] * Hkv + g * (n + A);       // its first position
-    const int64_t j0 = start - off - A > 0 ? start - off - A : 0;
-    const int64_t j1 = end - off - A < n ? end - off - A : n;
-    const int32_t *table = block_tables + static_cast<int64_t>(b) * bt_stride;
-    for (int64_t i = 0; i < 32 && j0 + i < j1; ++i) r[8 + i] = table[j0 + i];
+    if (start < end) {
+      while (start >= off + n + A) {   // the unit holding `start` (start < P: it exists)
+        off += n + A;
+        if (++g == Hkv) {
+          g = 0;
+          for (++b; b < B && rowoff[b + 1] == rowoff[b]; ++b) {
+          }
+          n = rowoff[b + 1] - rowoff[b] - A;
+        }
+      }
+      r[0] = b;
+      r[1] = static_cast<int32_t>(rowoff[b]);
+      r[2] = seq_lens[b];
+      r[3] = b + 1 < B ? seq_lens[b + 1] : 0;
+      const int64_t j0 = start - off - A > 0 ? start - off - A : 0;
+      const int64_t j1 = end - off - A < n ? end - off - A : n;
+      // the ids of the segment's pages; entries past its last page are left as
+      // they are (nothing reads them)
+      const int64_t m = j1 - j0 < 32 ? j1 - j0 : 32;
+      const int32_t *ids = block_tables + static_cast<int64_t>(b) * bt_stride + j0;
+      if (m == 32) {
+        for (int i = 0; i < 32; ++i) r[8 + i] = ids[i];   // (a fixed-size copy vectorises)
+      } else {
+        for (int64_t i = 0; i < m; ++i) r[8 + i] = ids[i];
+      }
+    }
+    start = end;
   }
   return PKV_OK;
 }

@@ -357,9 +357,11 @@ def test_plan_parts_equals_the_partition_written_out(host_lib, seed):
     bias_stride = int(r.integers(1, bt * 16)) if seed % 3 == 2 else 0
     tables = r.integers(0, 10000, size=(B, bt)).astype(np.int32)
     for C in (1, 3, 7, 64, 304, 1000):
-        got = binding.plan_parts(lens.astype(np.int32), Hkv, d, tables, C, bias_stride)
+        got = binding.plan_parts(lens.astype(np.int32), Hkv, d, tables, C, bias_stride,
+                                 out=np.full((C, 40), -1, np.int32))
         want = _plan_by_enumeration([int(x) for x in lens], Hkv, d, tables.tolist(), bt,
                                     bias_stride, C)
+        # (ids past a segment's last page are not written: -1 from the fill above)
         np.testing.assert_array_equal(got.astype(np.int64), want, err_msg=f"C={C}")
 
 
