@@ -285,20 +285,28 @@ class BlockAllocator:
                                           int(bt_stride)))
         return pos, slots, lens, tables
 
-    def step_runner(self, seq_ids, bt_stride, out):
+    def step_runner(self, seq_ids, bt_stride, out, row_state=None):
         """A no-argument callable that runs ``prepare_step`` for these sequence ids
         into the arrays ``out`` (positions, slot_mapping, seq_lens, block_tables),
-        with every pointer converted once (a serving loop calls it every step)."""
+        with every pointer converted once (a serving loop calls it every step).
+        With ``row_state`` (int32 [B*3], -1 before the first call) it runs
+        ``prepare_step_cached``: ``out`` must then be the same arrays every call."""
         ids = np.ascontiguousarray(seq_ids, dtype=np.int32)
         pos, slots, lens, tables = out
-        fn, h, B, bt = self._lib.pkv_prepare_step, self._h, len(ids), int(bt_stride)
+        h, B, bt = self._h, len(ids), int(bt_stride)
         ptrs = (_np_ptr(ids, ctypes.c_int32), _np_ptr(pos, ctypes.c_int32, B),
                 _np_ptr(slots, ctypes.c_int64, B), _np_ptr(lens, ctypes.c_int32, B),
                 _np_ptr(tables, ctypes.c_int32, B * bt))
-        keep = (ids, out)
+        if row_state is None:
+            fn, extra = self._lib.pkv_prepare_step, ()
+        else:
+            fn, extra = self._lib.pkv_prepare_step_cached, (_np_ptr(row_state, ctypes.c_int32,
+                                                                    3 * B),)
+        keep = (ids, out, row_state)
+        args = (h, ptrs[0], B, ptrs[1], ptrs[2], ptrs[3], ptrs[4], bt) + extra
 
         def run():
-            _check(fn(h, ptrs[0], B, ptrs[1], ptrs[2], ptrs[3], ptrs[4], bt))
+            _check(fn(*args))
             return keep[1]
         return run
 
