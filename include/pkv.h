@@ -351,7 +351,7 @@ int pkv_decode_attn_static(const void *q_rot, const void *k_cache, const void *v
  *   [2] seq_lens[b0], [3] seq_lens[b0 + 1] (0 past the last row)
  *   [4], [5] P, the total position count (int64, low word first)
  *   [6], [7] zero
- *   [8 + i], i < 32: block id of page j0 + i of the part's first unit segment
+ *   [8 + i], i < 16: block id of page j0 + i of the part's first unit segment
  *       (j0 its first page there); entries past the segment's last page are
  *       not written (and not read)
  * The plan is a pure function of (seq_lens, block tables, B, Hkv, d,
@@ -359,7 +359,7 @@ int pkv_decode_attn_static(const void *q_rot, const void *k_cache, const void *v
  * kernel reads, and be rebuilt whenever that changes.  PKV_ATTN_CHECK_PLAN
  * makes the kernel verify it.  Host-only; plan is [num_parts * PKV_PLAN_INTS].
  */
-#define PKV_PLAN_INTS 40
+#define PKV_PLAN_INTS 24
 int pkv_plan_parts(const int32_t *seq_lens, int32_t B, int32_t Hkv, int32_t d,
                    const int32_t *block_tables, int32_t bt_stride, int32_t bias_stride,
                    int32_t num_parts, int32_t *plan);

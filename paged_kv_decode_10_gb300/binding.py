@@ -18,7 +18,7 @@ F32, BF16 = 0, 1
 BLOCK_SIZE = 16
 DEVERR_BAD_BLOCK, DEVERR_BAD_SLOT, DEVERR_BAD_LEN, DEVERR_TIMEOUT = 1, 2, 4, 8
 DEVERR_BAD_PLAN = 16
-PLAN_INTS = 40
+PLAN_INTS = 24
 ATTN_SIMT = 1
 ATTN_SEPARATE_MERGE = 2
 ATTN_SHORT_WAITS = 8

@@ -80,6 +80,8 @@ struct AttnParams {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr long long kWaitLimitCycles = 1ll << 31;   // about one second
+// block ids a plan record carries (the first chunk of a part's pages)
+constexpr int kPlanIds = PKV_PLAN_INTS - 8;
 // a merge helper takes at least this many float4 columns of a unit's output
 constexpr int kHelperMinCols = 8;
 constexpr int kMaxHelpers = 32;
@@ -960,7 +962,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
     rec_h = __ldcg(reinterpret_cast<const int4 *>(rec));       // row, row offset, L, next L
     rec_p = __ldcg(reinterpret_cast<const int4 *>(rec) + 1);   // P (int64)
     // the producer's first block ids go out in the same round trip
-    if (warp == NW) plan_ids = __ldcg(rec + 8 + lane);
+    if (warp == NW && lane < kPlanIds) plan_ids = __ldcg(rec + 8 + lane);
   }
   // ---- otherwise (or to check the plan): page counts of all rows,
   // per-thread chunk sums, block-wide scan ----
@@ -1126,15 +1128,18 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
       j0 = j1 = 0;
       last = true;
     }
-    // block ids of the first 32 pages: from the plan, or read from the table
-    // (and, when the plan is checked, compared with it)
-    int ids;
+    // block ids of the first chunk of pages: the plan's first kPlanIds (the
+    // table read of the next chunk is then in flight behind them), or the first
+    // 32 read from the table (and, when the plan is checked, compared with it)
+    int ids, chunk = 32;
     if (use_plan && !p.check_plan) {
       ids = plan_ids;
+      chunk = kPlanIds;
     } else {
       ids = (j0 + lane < j1) ? p.block_tables[static_cast<size_t>(u.b) * p.bt_stride + j0 + lane]
                              : -1;
-      if (use_plan && j0 + lane < j1 && plan_ids != ids) set_dev_err(p.err, PKV_DEVERR_BAD_PLAN);
+      if (use_plan && lane < kPlanIds && j0 + lane < j1 && plan_ids != ids)
+        set_dev_err(p.err, PKV_DEVERR_BAD_PLAN);
     }
     while (!aborted) {
       const int32_t *bt = p.block_tables + static_cast<size_t>(u.b) * p.bt_stride;
@@ -1205,10 +1210,10 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
         }
         __syncwarp();
       };
-      for (int jb = j0; jb < j1 && !aborted; jb += 32) {
+      for (int jb = j0; jb < j1 && !aborted; jb += chunk, chunk = 32) {
         const int cur_ids = ids;
-        ids = (jb + 32 + lane < j1) ? bt[jb + 32 + lane] : -1;
-        const int cnt = min(32, j1 - jb);
+        ids = (jb + chunk + lane < j1) ? bt[jb + chunk + lane] : -1;
+        const int cnt = min(chunk, j1 - jb);
         // pages go out kBatch at a time, lane l < kBatch taking page i + l, so
         // the barrier waits, arrivals and TMA issues of a batch share warp
         // instructions (one page per lane-instruction costs ~600 cycles)

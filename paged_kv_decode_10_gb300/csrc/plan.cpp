@@ -84,10 +84,11 @@ extern "C" int pkv_plan_parts(const int32_t *seq_lens, int32_t B, int32_t Hkv, i
       const int64_t j1 = end - off - A < n ? end - off - A : n;
       // the ids of the segment's pages; entries past its last page are left as
       // they are (nothing reads them)
-      const int64_t m = j1 - j0 < 32 ? j1 - j0 : 32;
+      constexpr int kIds = PKV_PLAN_INTS - 8;
+      const int64_t m = j1 - j0 < kIds ? j1 - j0 : kIds;
       const int32_t *ids = block_tables + static_cast<int64_t>(b) * bt_stride + j0;
-      if (m == 32) {
-        for (int i = 0; i < 32; ++i) r[8 + i] = ids[i];   // (a fixed-size copy vectorises)
+      if (m == kIds) {
+        for (int i = 0; i < kIds; ++i) r[8 + i] = ids[i];   // (a fixed-size copy vectorises)
       } else {
         for (int64_t i = 0; i < m; ++i) r[8 + i] = ids[i];
       }

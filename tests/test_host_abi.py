@@ -322,9 +322,9 @@ def _plan_by_enumeration(lens, Hkv, d, tables, bt_stride, bias_stride, C):
         for g in range(Hkv if n else 0):
             pos += [(b, g, -1)] * A + [(b, g, j) for j in range(n)]
     P = len(pos)
-    out = np.zeros((C, 40), np.int64)
+    out = np.zeros((C, 24), np.int64)
     for c in range(C):
-        rec = [-1, 0, 0, 0, P & 0xffffffff, P >> 32, 0, 0] + [-1] * 32
+        rec = [-1, 0, 0, 0, P & 0xffffffff, P >> 32, 0, 0] + [-1] * 16
         start, end = P * c // C, P * (c + 1) // C
         if start < end:
             b, g, _ = pos[start]
@@ -333,7 +333,7 @@ def _plan_by_enumeration(lens, Hkv, d, tables, bt_stride, bias_stride, C):
             rec[1] = sum(1 for (bb, gg, _) in pos if bb < b) // Hkv
             rec[2] = lens[b]
             rec[3] = lens[b + 1] if b + 1 < len(lens) else 0
-            for i, j in enumerate(pages[:32]):
+            for i, j in enumerate(pages[:16]):
                 rec[8 + i] = tables[b][j]
         out[c] = rec
     return out
@@ -358,7 +358,7 @@ def test_plan_parts_equals_the_partition_written_out(host_lib, seed):
     tables = r.integers(0, 10000, size=(B, bt)).astype(np.int32)
     for C in (1, 3, 7, 64, 304, 1000):
         got = binding.plan_parts(lens.astype(np.int32), Hkv, d, tables, C, bias_stride,
-                                 out=np.full((C, 40), -1, np.int32))
+                                 out=np.full((C, 24), -1, np.int32))
         want = _plan_by_enumeration([int(x) for x in lens], Hkv, d, tables.tolist(), bt,
                                     bias_stride, C)
         # (ids past a segment's last page are not written: -1 from the fill above)

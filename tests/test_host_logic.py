@@ -65,12 +65,12 @@ def test_metadata_layout_is_aligned_and_disjoint():
             for parts in (0, 1, 304):
                 o_slots, o_pos, o_lens, o_tab, o_plan, end = _metadata_layout(B, bt, parts)
                 spans = sorted([(o_slots, 8 * B), (o_pos, 4 * B), (o_lens, 4 * B),
-                                (o_tab, 4 * B * bt), (o_plan, 160 * parts)])
+                                (o_tab, 4 * B * bt), (o_plan, 96 * parts)])
                 for (a, n), (b, _) in zip(spans, spans[1:]):
                     assert a + n <= b                   # no overlap
                 assert o_slots % 8 == 0 and o_pos % 4 == 0 and o_lens % 4 == 0
                 assert o_tab % 16 == 0 and o_plan % 16 == 0   # 16-byte aligned rows / records
-                assert end == o_plan + 160 * parts
+                assert end == o_plan + 96 * parts
 
 
 def test_attention_byte_accounting_hand_example():
