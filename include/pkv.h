@@ -435,7 +435,10 @@ int pkv_decode_step(const pkv_step_args *args, void *stream);
  * its attention kernel as a dependent of its RoPE/append kernel, so each
  * layer's start overlaps the previous layer's tail.  Consecutive layers must
  * not share a workspace (two alternating workspaces suffice).
- * PKV_STEP_FUSED is rejected.  Stops at the first failing layer.
+ * PKV_STEP_FUSED is rejected.  Stops at the first failing layer.  The layers'
+ * attention kernels are not launched cooperatively, so each unit's merge is
+ * done by its last part alone (the next layer's kernels may then start on SMs
+ * the previous layer has freed).
  */
 int pkv_decode_step_layers(const pkv_step_args *layers, int32_t n_layers, void *stream);
 

@@ -301,7 +301,7 @@ int attn_launch(const void *q_rot, const void *k_cache, const void *v_cache, int
                 int32_t d, float scale, int32_t num_parts, void *workspace,
                 size_t workspace_bytes, void *out, int32_t dtype, int32_t flags,
                 int32_t *dev_err_flag, void *stream, const pkv_step_args *step,
-                const int32_t *plan) {
+                const int32_t *plan, bool allow_helpers = true) {
   int rc = check_shapes(B, Hq, Hkv, d, dtype);
   if (rc != PKV_OK) return rc;
   if (B == 0) return PKV_OK;
@@ -359,11 +359,13 @@ int attn_launch(const void *q_rot, const void *k_cache, const void *v_cache, int
   p.fuse_merge = (flags & PKV_ATTN_SEPARATE_MERGE) ? 0 : 1;
   // A grid that fits on the GPU at once is launched cooperatively, which
   // guarantees that every CTA is resident; only then may the merge of a unit
-  // be shared by several parts that wait for each other.
+  // be shared by several parts that wait for each other.  (A chain of layers
+  // does without: a cooperative grid starts only once all of its CTAs fit, so
+  // the next layer could no longer start on the SMs the previous one frees.)
   int resident = 0;
   rc = resident_ctas(v, &resident);
   if (rc != PKV_OK) return rc;
-  p.max_helpers = num_parts <= resident ? kMaxHelpers : 1;
+  p.max_helpers = (allow_helpers && num_parts <= resident) ? kMaxHelpers : 1;
   p.wait_limit = (flags & PKV_ATTN_SHORT_WAITS) ? kShortWaitCycles : kWaitLimitCycles;
   p.seg_cost = seg_cost(d);
   p.out = out;
@@ -546,7 +548,8 @@ extern "C" int pkv_decode_step_layers(const pkv_step_args *layers, int32_t n_lay
     rc = attn_launch(a->q_rot, a->k_cache, a->v_cache, a->num_blocks, a->block_tables,
                      a->bt_stride, a->seq_lens, a->attn_bias, a->bias_stride, a->B, a->Hq, a->Hkv,
                      a->d, a->scale, num_parts, a->workspace, a->workspace_bytes, a->out,
-                     a->dtype, a->flags, a->dev_err_flag, stream, nullptr, a->plan);
+                     a->dtype, a->flags, a->dev_err_flag, stream, nullptr, a->plan,
+                     /*allow_helpers=*/false);
     if (rc != PKV_OK) return rc;
     if (a->flags & PKV_ATTN_SEPARATE_MERGE) {
       rc = pkv_lse_merge(a->workspace, a->workspace_bytes, a->seq_lens, a->bt_stride,
