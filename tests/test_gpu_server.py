@@ -104,3 +104,68 @@ def test_server_rejects_bad_steps():
     torch.cuda.synchronize()
     assert dec.device_errors() == 0
     server.close()
+
+
+def test_server_churn256_full_size_matches_engine():
+    """churn256 at full size (B=256, 26 leave / 26 join per step with prefixes of
+    256-1024 tokens) through the native serving loop, against the Python engine
+    replaying its captured graph (the launch configuration the full-size churn
+    test checks against the oracle): bit-identical outputs at every step and
+    identical caches and row map at the end; the last step's sampled rows also
+    against the oracle on the caches they read."""
+    w = workloads.make_workload("churn256")
+    dv = dev()
+    steps = 8
+    bt = w.max_blocks_per_seq(extra_tokens=steps + 16)
+    k0, v0 = workloads.make_caches(w, dv)
+    decs = [engine.PagedDecoder(w.num_blocks, w.Hq, w.Hkv, w.d, w.dtype, w.B, bt,
+                                initial_free=w.free_order, device=dv, k_cache=k0.clone(),
+                                v_cache=v0.clone(), metadata="mapped") for _ in range(2)]
+    del k0, v0
+    ref, srv_dec = decs
+    ids = [ref.join(int(L)) for L in w.seq_lens]
+    srv_ids = [srv_dec.join(int(L)) for L in w.seq_lens]
+    max_prefix = max(int(np.sum(p)) for _, p in w.churn[:steps])
+    server = binding.Server(srv_dec, srv_ids, max_prefix)
+    ref.capture(w.B)
+    gen = torch.Generator(device=dv).manual_seed(99)
+    pre_k = torch.randn((max_prefix, w.Hkv, w.d), generator=gen, device=dv).to(torch.bfloat16)
+    pre_v = torch.randn((max_prefix, w.Hkv, w.d), generator=gen, device=dv).to(torch.bfloat16)
+    pos_buf = np.empty(max_prefix, np.int32)
+    slot_buf = np.empty(max_prefix, np.int64)
+    for s in range(steps):
+        leave, prefixes = w.churn[s - 1] if s else (np.zeros(0, np.int64), np.zeros(0, np.int64))
+        n = int(np.sum(prefixes))
+        if s:
+            ref.alloc.leave_many([ids[i] for i in leave])
+            for i, sid in zip(leave, ref.alloc.join_many(prefixes, (pos_buf, slot_buf))):
+                ids[int(i)] = int(sid)
+            binding.prefill_kv(pre_k[:n], pre_v[:n], torch.from_numpy(pos_buf[:n]).to(dv),
+                               torch.from_numpy(slot_buf[:n]).to(dv), ref.k_cache, ref.v_cache,
+                               err=ref.err)
+        q, k, v = workloads.make_new_tokens(w, s, dv)
+        ref.q_in[:w.B].copy_(q)
+        ref.k_in[:w.B].copy_(k)
+        ref.v_in[:w.B].copy_(v)
+        ref.prepare_host(ids)
+        out_ref = ref.replay_step()
+        server.step(leave, prefixes, pre_k[:n] if n else None, pre_v[:n] if n else None, q, k, v)
+        torch.cuda.synchronize()
+        assert torch.equal(srv_dec.out[:w.B], out_ref), f"step {s}"
+    assert ref.device_errors() == 0 and srv_dec.device_errors() == 0
+    assert server.rows().tolist() == ids
+    assert torch.equal(srv_dec.k_cache, ref.k_cache) and torch.equal(srv_dec.v_cache, ref.v_cache)
+    pos, slots, seq_lens, tables = (np.array(x) for x in ref.last_metadata)
+    q64, k64, v64 = (f64(t) for t in (q, k, v))
+    got = f64(srv_dec.out[:w.B])
+    for b in (0, 1, 100, 255):
+        nblk = -(-int(seq_lens[b]) // 16)
+        blocks = torch.from_numpy(tables[b, :nblk].astype(np.int64)).to(dv)
+        j = int(pos[b]) // 16
+        res = decode_step(q64[b:b + 1], k64[b:b + 1], v64[b:b + 1], pos[b:b + 1],
+                          [j * 16 + int(slots[b]) % 16], seq_lens[b:b + 1],
+                          np.arange(nblk)[None, :], f64(ref.k_cache[blocks]),
+                          f64(ref.v_cache[blocks]), scale=w.scale, base=w.rope_base,
+                          dtype=w.dtype)
+        assert_out_close(got[b], res["out"][0], w.dtype, f"row {b}")
+    server.close()
