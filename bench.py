@@ -908,7 +908,7 @@ def prefill_summary(log, w, elem, peak):
     us = [1e3 * a.elapsed_time(b) for _, a, b in log]
     nbytes = [n * (4 * w.Hkv * w.d * elem + 12) for n in toks]
     gbs = sum(nbytes) / (sum(us) * 1e-6) / 1e9
-    return {"kernel": "rope_kernel (pkv_prefill_kv)", "calls": len(log),
+    return {"kernel": "prefill_kernel (pkv_prefill_kv)", "calls": len(log),
             "tokens_per_call": round(statistics.mean(toks), 1),
             "us_per_call": round(statistics.mean(us), 3), "achieved_gbs": round(gbs, 2),
             "frac": round(gbs / peak, 4), "l2": "flushed before every call"}

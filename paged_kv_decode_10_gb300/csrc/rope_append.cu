@@ -183,6 +183,118 @@ __global__ void append_kernel(const uint4 *__restrict__ k_rot, const uint4 *__re
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// pkv_prefill_kv: the prefix keys and values of joining sequences, many tokens
+// per CTA.  A token is served by TPT = (D/2) / E threads (E = elements per
+// 16-byte vector): thread l owns rotation pairs [l*E, l*E+E) of every KV head,
+// forms their E angles once (rope_cossin of the token's position, the same
+// table and arithmetic as the decode append, so a prefix key is bit-identical
+// to the key a decode step stores for it) and moves 16-byte vectors; it also
+// copies every TPT-th 16-byte chunk of the token's values.  Loads of four heads
+// (or eight value chunks) are issued together.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) prefill_kernel(
+    const uint4 *__restrict__ k, const uint4 *__restrict__ v, const int32_t *__restrict__ positions,
+    const int64_t *__restrict__ slots, uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+    int n_tokens, int Hkv, int64_t num_slots, int32_t *err, const RopeTurns turns) {
+  constexpr int E = 16 / static_cast<int>(sizeof(T));
+  constexpr int HALF = D / 2;
+  constexpr int TPT = HALF / E;        // threads per token
+  constexpr int VPR = D / E;           // 16-byte vectors per head row
+  constexpr int TOK = 256 / TPT;       // tokens per CTA
+  const int l = threadIdx.x % TPT;
+  const int t = blockIdx.x * TOK + threadIdx.x / TPT;
+  if (t >= n_tokens) return;
+  const int64_t slot = slots[t];
+  const uint32_t pos = static_cast<uint32_t>(positions[t]);
+  const uint4 *kt = k + static_cast<size_t>(t) * Hkv * VPR;
+  const uint4 *vt = v + static_cast<size_t>(t) * Hkv * VPR;
+  // the first heads' keys are in flight while the angles are formed
+  uint4 x[8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    if (j < Hkv) {
+      x[2 * j] = kt[j * VPR + l];
+      x[2 * j + 1] = kt[j * VPR + TPT + l];
+    }
+  float co[E], sn[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) rope_cossin(pos, turns.f[l * E + e], &co[e], &sn[e]);
+  bool write = slot >= 0;
+  if (slot >= num_slots) {
+    if (l == 0) set_dev_err(err, PKV_DEVERR_BAD_SLOT);
+    write = false;
+  }
+  const int64_t blk = slot / kBlockTokens;
+  // vector index of (block, head 0, row) in the cache viewed as 16-byte vectors
+  const size_t row0 = write ? static_cast<size_t>((blk * Hkv) * kBlockTokens +
+                                                  (slot - blk * kBlockTokens)) * VPR
+                            : 0;
+  for (int h0 = 0; h0 < Hkv; h0 += 4) {
+    if (h0 > 0) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (h0 + j < Hkv) {
+          x[2 * j] = kt[(h0 + j) * VPR + l];
+          x[2 * j + 1] = kt[(h0 + j) * VPR + TPT + l];
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (h0 + j >= Hkv) break;
+      const T *a = reinterpret_cast<const T *>(&x[2 * j]);
+      const T *b = reinterpret_cast<const T *>(&x[2 * j + 1]);
+      uint4 ya, yb;
+      T *pa = reinterpret_cast<T *>(&ya);
+      T *pb = reinterpret_cast<T *>(&yb);
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        float y1, y2;
+        rope_rotate(to_f32(a[e]), to_f32(b[e]), co[e], sn[e], &y1, &y2);
+        pa[e] = from_f32<T>(y1);
+        pb[e] = from_f32<T>(y2);
+      }
+      if (write) {
+        uint4 *dst = k_cache + row0 + static_cast<size_t>(h0 + j) * kBlockTokens * VPR;
+        dst[l] = ya;
+        dst[TPT + l] = yb;
+      }
+    }
+  }
+  // values: vector c of the token's [Hkv, D] row for c = l, l + TPT, ...
+  const int nv = Hkv * VPR;
+  for (int c0 = l; c0 < nv; c0 += 8 * TPT) {
+    uint4 w[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (c0 + j * TPT < nv) w[j] = vt[c0 + j * TPT];
+    if (write) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int c = c0 + j * TPT;
+        if (c < nv) {
+          const int h = c / VPR, r = c - h * VPR;
+          v_cache[row0 + static_cast<size_t>(h) * kBlockTokens * VPR + r] = w[j];
+        }
+      }
+    }
+  }
+}
+
+template <typename T, int D>
+int launch_prefill(const void *k, const void *v, const int32_t *positions, const int64_t *slots,
+                   void *k_cache, void *v_cache, int n_tokens, int Hkv, int64_t num_slots,
+                   int32_t *err, const RopeTurns &turns, cudaStream_t s) {
+  constexpr int TPT = (D / 2) / (16 / static_cast<int>(sizeof(T)));
+  constexpr int TOK = 256 / TPT;
+  const int grid = (n_tokens + TOK - 1) / TOK;
+  prefill_kernel<T, D><<<grid, 256, 0, s>>>(
+      static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), positions, slots,
+      static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), n_tokens, Hkv, num_slots,
+      err, turns);
+  PKV_LAUNCH_CHECK("prefill_kernel");
+  return PKV_OK;
+}
+
 template <typename T, int VEC, bool APPEND>
 void launch_rope(int B, int threads, size_t smem, cudaStream_t s, const void *q, const void *k,
                  const void *v, void *q_out, void *k_out, const int32_t *positions,
@@ -322,10 +434,32 @@ extern "C" int pkv_prefill_kv(const void *k, const void *v, const int32_t *posit
                               int32_t Hkv, int32_t d, int32_t num_blocks, float base,
                               int32_t dtype, int32_t *dev_err_flag, void *stream) {
   clear_error();
-  // the decode-step kernel with no query heads and no rotated-key report: every
-  // token's key is rotated and stored exactly as a decode append would store it
-  return rope_launch(nullptr, k, v, nullptr, nullptr, positions, slot_mapping, k_cache, v_cache, T,
-                     0, Hkv, d, num_blocks, base, dtype, dev_err_flag, stream, true, true);
+  // head sizes of the attention kernels, 16-byte aligned tensors: the prefill
+  // kernel; otherwise the decode-step kernel with no query heads and no
+  // rotated-key report.  Either way a token's key is rotated and stored exactly
+  // as a decode append would store it.
+  const bool fast = (d == 64 || d == 128) && dtype_ok(dtype) && T > 0 && Hkv > 0 && k && v &&
+                    positions && slot_mapping && k_cache && v_cache && aligned16(k) &&
+                    aligned16(v) && aligned16(k_cache) && aligned16(v_cache) && num_blocks >= 0 &&
+                    base > 0.0f;
+  if (!fast)
+    return rope_launch(nullptr, k, v, nullptr, nullptr, positions, slot_mapping, k_cache, v_cache,
+                       T, 0, Hkv, d, num_blocks, base, dtype, dev_err_flag, stream, true, true);
+  RopeTurns turns;
+  fill_rope_turns(base, d, turns.f);
+  const int64_t num_slots = static_cast<int64_t>(num_blocks) * kBlockTokens;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dtype == PKV_BF16)
+    return d == 64 ? launch_prefill<__nv_bfloat16, 64>(k, v, positions, slot_mapping, k_cache,
+                                                        v_cache, T, Hkv, num_slots, dev_err_flag,
+                                                        turns, s)
+                   : launch_prefill<__nv_bfloat16, 128>(k, v, positions, slot_mapping, k_cache,
+                                                         v_cache, T, Hkv, num_slots, dev_err_flag,
+                                                         turns, s);
+  return d == 64 ? launch_prefill<float, 64>(k, v, positions, slot_mapping, k_cache, v_cache, T,
+                                             Hkv, num_slots, dev_err_flag, turns, s)
+                 : launch_prefill<float, 128>(k, v, positions, slot_mapping, k_cache, v_cache, T,
+                                              Hkv, num_slots, dev_err_flag, turns, s);
 }
 
 extern "C" int pkv_append(const void *k_rot, const void *v, const int64_t *slot_mapping,
