@@ -20,9 +20,11 @@ Printed JSON line (rank 0):
                    steps / device time of all steps, GB/s
   steps_per_s      decode steps per second (device time)
   roofline         the attention kernel (a3 + fused a4) timed alone after the
-                   same flush: algorithmic bytes per launch / mean launch time
-                   against the measured HBM copy peak, with the ncu DRAM bytes
-                   of the same kernel source (``profiles/traffic.json``)
+                   same flush, with every input in HBM (the step's block
+                   tables, lengths and plan copied to the device):
+                   algorithmic bytes per launch / mean launch time against the
+                   measured HBM copy peak, with the ncu DRAM bytes of the same
+                   kernel source (``profiles/traffic.json``)
   rooflines        the same for the workloads named by ``--also`` (default
                    ragged64 and long131k), each set up and timed in this run
   step_kernels_us  the step's kernels (RoPE/append + attention) without the host
@@ -418,6 +420,15 @@ def setup(w, device, parts, flags, steps_total, metadata, n_layers=1):
     return dec, ids, tokens, (k_cache, v_cache) if gen_dev == "cpu" else None
 
 
+def resident_metadata(dec, device):
+    """The current step's block tables, lengths and plan as device tensors:
+    the attention kernel timed alone reads all of its inputs from HBM (the step
+    itself may read its metadata in place from pinned host memory)."""
+    def dev(t):
+        return None if t is None else (t if t.is_cuda else t.to(device))
+    return dev(dec.tables), dev(dec.seq_lens), dev(dec.plan)
+
+
 def time_graph_launches(g, K, flush, stream, sampler):
     """K replays of graph g, each after an L2 flush, between CUDA events on
     ``stream``; returns the milliseconds of each."""
@@ -452,11 +463,12 @@ def attention_roofline(name, args, device, flush, stream, sampler, peak):
     cap = torch.cuda.Stream(device)
     cap.wait_stream(stream)
     attn_graph, kern_graph = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    tables, lens_d, plan = resident_metadata(dec, device)
     with torch.cuda.graph(attn_graph, stream=cap):
-        binding.decode_attention(dec.q_rot[:B], dec.k_cache, dec.v_cache, dec.tables,
-                                 dec.seq_lens, scale=dec.scale, num_parts=dec.num_parts,
+        binding.decode_attention(dec.q_rot[:B], dec.k_cache, dec.v_cache, tables, lens_d,
+                                 scale=dec.scale, num_parts=dec.num_parts,
                                  workspace=dec.workspace, out=dec.out[:B], flags=dec.flags,
-                                 err=dec.err, stream=cap, plan=dec.plan)
+                                 err=dec.err, stream=cap, plan=plan)
     with torch.cuda.graph(kern_graph, stream=cap):
         binding.decode_step_args(step_args, cap)
     stream.wait_stream(cap)
@@ -469,7 +481,7 @@ def attention_roofline(name, args, device, flush, stream, sampler, peak):
     traffic, note = profiled_traffic(name, kernel_source_hash(), ab)
     return {"workload": name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.d,
             "mean_kv_len": float(np.mean(lens)), "num_parts": dec.num_parts,
-            "bound": "hbm", "kernel": "attn_split_kernel (a3 + fused a4), timed alone",
+            "bound": "hbm", "kernel": "attn_split_kernel (a3 + fused a4), timed alone, metadata in HBM",
             "achieved": round(gbs, 2), "peak": peak, "unit": "GB/s", "frac": round(gbs / peak, 4),
             "traffic": traffic, "traffic_note": note, "algorithmic_bytes_per_launch": int(ab),
             "mean_launch_us": round(1e3 * statistics.mean(attn_ms), 3),
@@ -616,11 +628,12 @@ def run_gpu(args, rank, world, want_cpu=False):
     cap = torch.cuda.Stream(device)
     cap.wait_stream(stream)
     attn_graph, kern_graph = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    tables, lens_d, plan = resident_metadata(dec, device)
     with torch.cuda.graph(attn_graph, stream=cap):
-        binding.decode_attention(dec.q_rot[:B], dec.k_cache, dec.v_cache, dec.tables,
-                                 dec.seq_lens, scale=dec.scale, num_parts=dec.num_parts,
+        binding.decode_attention(dec.q_rot[:B], dec.k_cache, dec.v_cache, tables, lens_d,
+                                 scale=dec.scale, num_parts=dec.num_parts,
                                  workspace=dec.workspace, out=dec.out[:B], flags=dec.flags,
-                                 err=dec.err, stream=cap, plan=dec.plan)
+                                 err=dec.err, stream=cap, plan=plan)
     with torch.cuda.graph(kern_graph, stream=cap):
         if args.layers > 1:
             binding.decode_step_layers(step_args, cap)
@@ -793,7 +806,7 @@ def run_gpu(args, rank, world, want_cpu=False):
         "attn_gbs": round(attn_gbs, 2),
         "pct_of_peak": round(100 * attn_gbs / peak, 2),
         "kv_bytes_per_step": int(statistics.mean(kv_only)),
-        "roofline": {"bound": "hbm", "kernel": "attn_split_kernel (a3 + fused a4), timed alone",
+        "roofline": {"bound": "hbm", "kernel": "attn_split_kernel (a3 + fused a4), timed alone, metadata in HBM",
                      "achieved": round(attn_gbs, 2), "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": round(attn_gbs / peak, 4),
                      "traffic": traffic, "traffic_note": traffic_note,
