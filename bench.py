@@ -390,12 +390,23 @@ def host_cores():
 def setup(w, device, parts, flags, steps_total, metadata, n_layers=1):
     import torch
     from paged_kv_decode_10_gb300 import engine, workloads
+    # room for the timed steps, the three end-to-end runs (up to 3 x 53 steps)
+    # and two wall-clock passes over a churn plan (up to 64 steps each)
+    extra_tokens = steps_total + 2 * 64 + 3 * 53 + 64
+    bt = w.max_blocks_per_seq(extra_tokens=extra_tokens)
+    # The recipe's pool holds 1.25x the blocks of the initial lengths; a long
+    # run appends extra_tokens to every row.  Blocks for those go to the bottom
+    # of the free stack (in seeded random order): the initial block tables and
+    # every block the recipe's pool can give are unchanged, and the extra ones
+    # are taken only once it runs dry.  (w is updated in place.)
+    extra = w.B * (-(-extra_tokens // 16) + 1)
+    rng = np.random.Generator(np.random.PCG64(w.seed + 7))
+    more = (w.num_blocks + rng.permutation(extra)).astype(np.int32)
+    w.free_order = np.concatenate([more, w.free_order])
+    w.num_blocks += extra
     pool_bytes = w.num_blocks * w.Hkv * 16 * w.d * (2 if w.dtype == "bf16" else 4)
     gen_dev = "cpu" if pool_bytes < (1 << 30) else device
     k_cache, v_cache = workloads.make_caches(w, gen_dev)
-    # room for the timed steps, the three end-to-end runs (up to 3 x 53 steps)
-    # and two wall-clock passes over a churn plan (up to 64 steps each)
-    bt = w.max_blocks_per_seq(extra_tokens=steps_total + 2 * 64 + 3 * 53 + 64)
     if n_layers > 1:
         # every layer's pool starts as a copy of the same synthetic cache
         kd, vd = k_cache.to(device), v_cache.to(device)
@@ -780,6 +791,8 @@ def run_gpu(args, rank, world, want_cpu=False):
         "steps": K,
         "warmup": W,
         "ms_per_step": round(total_s * 1e3 / K, 5),
+        "ms_per_step_median": round(statistics.median(step_ms), 5),
+        "ms_per_step_max": round(max(step_ms), 5),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -921,10 +934,14 @@ def prefill_summary(log, w, elem, peak):
     us = [1e3 * a.elapsed_time(b) for _, a, b in log]
     nbytes = [n * (4 * w.Hkv * w.d * elem + 12) for n in toks]
     gbs = sum(nbytes) / (sum(us) * 1e-6) / 1e9
+    med = statistics.median(us)
+    gbs_med = statistics.median(b / (t * 1e-6) / 1e9 for b, t in zip(nbytes, us))
     return {"kernel": "prefill_kernel (pkv_prefill_kv)", "calls": len(log),
             "tokens_per_call": round(statistics.mean(toks), 1),
             "us_per_call": round(statistics.mean(us), 3), "achieved_gbs": round(gbs, 2),
-            "frac": round(gbs / peak, 4), "l2": "flushed before every call"}
+            "frac": round(gbs / peak, 4), "us_median": round(med, 3), "us_max": round(max(us), 3),
+            "achieved_gbs_median": round(gbs_med, 2), "frac_median": round(gbs_med / peak, 4),
+            "l2": "flushed before every call"}
 
 
 def run_e2e(args, dec, ids, tokens, w):
