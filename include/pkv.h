@@ -83,6 +83,13 @@ extern "C" {
 #define PKV_ATTN_CHECK_PLAN 16    /* with a plan: also derive the partition from the metadata
                                      in the kernel, set PKV_DEVERR_BAD_PLAN where the plan
                                      disagrees and use the derived one there */
+#define PKV_LAYERS_MERGE_HELPERS 32 /* pkv_decode_step_layers: launch each layer's attention
+                                     kernel cooperatively, so that the merge of a unit split
+                                     over many parts is shared by its last parts as in a
+                                     single-layer call (otherwise its last part merges it
+                                     alone).  Worth it for long rows; the next layer's
+                                     attention kernel then starts only once the previous one
+                                     has left the GPU.  Ignored by the other calls. */
 
 /* Message for the calling thread's last failed call ("" if none). */
 const char *pkv_last_error(void);
@@ -436,9 +443,11 @@ int pkv_decode_step(const pkv_step_args *args, void *stream);
  * layer's start overlaps the previous layer's tail.  Consecutive layers must
  * not share a workspace (two alternating workspaces suffice).
  * PKV_STEP_FUSED is rejected.  Stops at the first failing layer.  The layers'
- * attention kernels are not launched cooperatively, so each unit's merge is
- * done by its last part alone (the next layer's kernels may then start on SMs
- * the previous layer has freed).
+ * attention kernels are not launched cooperatively unless a layer's flags have
+ * PKV_LAYERS_MERGE_HELPERS, so by default each unit's merge is done by its last
+ * part alone (the next layer's kernels may then start on SMs the previous layer
+ * has freed); with it, each layer merges like pkv_decode_step (bit-identical to
+ * one single-layer step per layer).
  */
 int pkv_decode_step_layers(const pkv_step_args *layers, int32_t n_layers, void *stream);
 

@@ -23,6 +23,7 @@ ATTN_SIMT = 1
 ATTN_SEPARATE_MERGE = 2
 ATTN_SHORT_WAITS = 8
 ATTN_CHECK_PLAN = 16
+LAYERS_MERGE_HELPERS = 32
 STEP_FUSED = 4
 
 _c_i32 = ctypes.c_int32

@@ -549,7 +549,7 @@ extern "C" int pkv_decode_step_layers(const pkv_step_args *layers, int32_t n_lay
                      a->bt_stride, a->seq_lens, a->attn_bias, a->bias_stride, a->B, a->Hq, a->Hkv,
                      a->d, a->scale, num_parts, a->workspace, a->workspace_bytes, a->out,
                      a->dtype, a->flags, a->dev_err_flag, stream, nullptr, a->plan,
-                     /*allow_helpers=*/false);
+                     /*allow_helpers=*/(a->flags & PKV_LAYERS_MERGE_HELPERS) != 0);
     if (rc != PKV_OK) return rc;
     if (a->flags & PKV_ATTN_SEPARATE_MERGE) {
       rc = pkv_lse_merge(a->workspace, a->workspace_bytes, a->seq_lens, a->bt_stride,

@@ -42,7 +42,8 @@ def test_binding_constants_match_the_header():
             assert getattr(binding, name) == value, name
             checked += 1
     for must in ("ATTN_SIMT", "ATTN_SEPARATE_MERGE", "STEP_FUSED", "ATTN_SHORT_WAITS",
-                 "DEVERR_TIMEOUT", "ERR_CUDA", "BF16", "HOST_IN_PLACE"):
+                 "DEVERR_TIMEOUT", "ERR_CUDA", "BF16", "HOST_IN_PLACE",
+                 "LAYERS_MERGE_HELPERS"):
         assert must in defines and hasattr(binding, must), must
     assert checked >= 18
 
