@@ -15,8 +15,10 @@ graph).
 With ``n_layers > 1`` every layer has its own K/V pool ("neurogrid releases"
 v0.7.0: per-layer caches) indexed by the same block tables; a step runs the
 layers in order through ``pkv_decode_step_layers`` (each layer's kernels
-overlap the previous layer's tail) and one graph holds all of them.
-``pool_blocks_for_vram`` sizes the pool from the free device memory (v0.7.0
+overlap the previous layer's tail) and one graph holds all of them.  When a
+step has long units (``long_units``) the layers are launched with
+PKV_LAYERS_MERGE_HELPERS, so that their merges are shared as in a one-layer
+step (``layer_merge_helpers`` forces either choice).  ``pool_blocks_for_vram`` sizes the pool from the free device memory (v0.7.0
 sizes it from a quarter of the free VRAM).
 
 Joins and leaves only edit the allocator's block tables ("neurogrid releases"
@@ -53,11 +55,24 @@ def _metadata_layout(B, bt_stride, plan_parts=0):
     return slots, pos, lens, tables, plan, plan + 4 * binding.PLAN_INTS * plan_parts
 
 
+def long_units(seq_lens, Hkv, d, num_parts, min_parts=8):
+    """Whether some (row, KV head) unit of a step with these lengths (after the
+    append) spans at least ``min_parts`` parts of the attention partition (a
+    unit of n pages when n * num_parts >= min_parts * P, P the position count:
+    pages plus the boundary cost of 4 pages at d = 64 and 2 at d = 128 per
+    unit).  Such units are merged by helpers in a single-layer call; in a layer
+    chain that takes PKV_LAYERS_MERGE_HELPERS."""
+    pages = (np.asarray(seq_lens, np.int64) + binding.BLOCK_SIZE - 1) // binding.BLOCK_SIZE
+    A = 4 if d <= 64 else 2
+    P = Hkv * int(np.sum(np.where(pages > 0, pages + A, 0)))
+    return P > 0 and int(pages.max()) * num_parts >= min_parts * P
+
+
 class PagedDecoder:
     def __init__(self, num_blocks, Hq, Hkv, d, dtype, max_seqs, max_blocks_per_seq,
                  initial_free=None, device="cuda", num_parts=None, rope_base=10000.0,
                  scale=None, flags=0, k_cache=None, v_cache=None, metadata="copy", n_layers=1,
-                 plan=True):
+                 plan=True, layer_merge_helpers=None):
         import torch
         if metadata not in ("copy", "mapped"):
             raise ValueError(f"metadata must be 'copy' or 'mapped', not {metadata!r}")
@@ -78,6 +93,11 @@ class PagedDecoder:
         self.rope_base = rope_base
         self.scale = 1.0 / math.sqrt(d) if scale is None else scale
         self.flags = flags
+        # layer chains: PKV_LAYERS_MERGE_HELPERS when the step has long units
+        # (None: decided by each prepare_host from the step's lengths, and a
+        # captured graph keeps the decision of the last one before capture)
+        self.layer_merge_helpers = layer_merge_helpers
+        self._helpers_now = bool(layer_merge_helpers)
         L = n_layers
         shape = (L, num_blocks, Hkv, binding.BLOCK_SIZE, d)
         # caches of every layer: [L, num_blocks, Hkv, 16, d]; a single-layer
@@ -191,6 +211,8 @@ class PagedDecoder:
         fn()
         if planner is not None:
             planner()
+        if self.n_layers > 1 and self.layer_merge_helpers is None:
+            self._helpers_now = long_units(npv[2], self.Hkv, self.d, self.num_parts)
         self.last_metadata = npv
         return npv
 
@@ -225,8 +247,13 @@ class PagedDecoder:
             q, k, v, self.q_rots[layer, :B], self.k_rots[layer, :B], self.k_caches[layer],
             self.v_caches[layer], self.positions, self.slots, self.seq_lens, self.tables,
             self.scale, self.rope_base, self.num_parts, ws,
-            self.outs[layer, :B] if out is None else out, attn_bias, self.flags, self.err,
+            self.outs[layer, :B] if out is None else out, attn_bias, self._step_flags(), self.err,
             plan=self.plan)
+
+    def _step_flags(self):
+        if self.n_layers > 1 and self._helpers_now:
+            return self.flags | binding.LAYERS_MERGE_HELPERS
+        return self.flags
 
     def layer_args(self, B, q, k, v, attn_bias=None):
         """``StepArgs`` of every layer (``q [L,B,Hq,d]``, ``k, v [L,B,Hkv,d]``)."""
@@ -268,25 +295,34 @@ class PagedDecoder:
         nbytes = _metadata_layout(B, self.bt_stride, self._plan_parts)[-1]
         stream = torch.cuda.Stream(self.device)
         stream.wait_stream(torch.cuda.current_stream(self.device))
-        graphs, all_args = [], []
-        for h in self._host:
-            if self.metadata == "mapped":
-                self._meta_cur = h["raw"]
-            if self.n_layers == 1:
-                args = self.step_args(B, self.q_in[:B], self.k_in[:B], self.v_in[:B], attn_bias)
-            else:
-                args = self.layer_args(B, self.q_ins[:, :B], self.k_ins[:, :B],
-                                       self.v_ins[:, :B], attn_bias)
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                if self.metadata == "copy":
-                    self._meta_dev[:nbytes].copy_(h["raw"][:nbytes], non_blocking=True)
+        # a layer chain that picks its merge per step gets both forms, and each
+        # replay takes the one its prepare_host chose
+        auto = self.n_layers > 1 and self.layer_merge_helpers is None
+        decided = self._helpers_now
+        graphs, all_args = {}, []
+        for helpers in ((False, True) if auto else (decided,)):
+            self._helpers_now = helpers
+            graphs[helpers] = []
+            for h in self._host:
+                if self.metadata == "mapped":
+                    self._meta_cur = h["raw"]
                 if self.n_layers == 1:
-                    binding.decode_step_args(args, stream)
+                    args = self.step_args(B, self.q_in[:B], self.k_in[:B], self.v_in[:B],
+                                          attn_bias)
                 else:
-                    binding.decode_step_layers(args, stream)
-            graphs.append(g)
-            all_args.append(args)
+                    args = self.layer_args(B, self.q_ins[:, :B], self.k_ins[:, :B],
+                                           self.v_ins[:, :B], attn_bias)
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    if self.metadata == "copy":
+                        self._meta_dev[:nbytes].copy_(h["raw"][:nbytes], non_blocking=True)
+                    if self.n_layers == 1:
+                        binding.decode_step_args(args, stream)
+                    else:
+                        binding.decode_step_layers(args, stream)
+                graphs[helpers].append(g)
+                all_args.append(args)
+        self._helpers_now = decided
         torch.cuda.current_stream(self.device).wait_stream(stream)
         self._graphs = (B, graphs, all_args)
 
@@ -299,7 +335,8 @@ class PagedDecoder:
         if self.metadata == "mapped":
             self._meta_cur = self._host[turn]["raw"]
             self._set_device_views(B)
-        graphs[turn].replay()
+        forms = graphs.get(self._helpers_now)
+        (forms if forms is not None else next(iter(graphs.values())))[turn].replay()
         ev = torch.cuda.Event()
         ev.record(torch.cuda.current_stream(self.device))
         self._host[turn]["event"] = ev

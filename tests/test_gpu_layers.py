@@ -23,27 +23,28 @@ def test_layers_equal_single_layer_decoders(name, L, metadata):
     """Every layer's output and caches equal those of a one-layer decoder fed
     the same layer's inputs (eager steps, then graph replays), over steps that
     cross a block boundary."""
-    _layers_against_single_layer(workloads.make_workload(name), L, metadata, 0, exact=True)
+    _layers_against_single_layer(workloads.make_workload(name), L, metadata, None, exact=True)
 
 
-@pytest.mark.parametrize("flags", [binding.LAYERS_MERGE_HELPERS, 0])
-def test_layers_with_long_rows(flags):
+@pytest.mark.parametrize("helpers,exact", [(None, True), (True, True), (False, False)])
+def test_layers_with_long_rows(helpers, exact):
     """Rows whose units span many parts (the first over 30 of them).  With
-    PKV_LAYERS_MERGE_HELPERS each layer's merge is shared by the unit's last
-    parts as in a single-layer step: bit-identical.  Without it the last part
-    merges alone: the same values up to the grouping of the float32 sums, so
-    within the bf16 output tolerance of the single-layer step."""
+    PKV_LAYERS_MERGE_HELPERS (which the decoder picks itself for such a step,
+    or is told to use) each layer's merge is shared by the unit's last parts as
+    in a single-layer step: bit-identical.  Without it the last part merges
+    alone: the same values up to the grouping of the float32 sums, so within
+    the bf16 output tolerance of the single-layer step."""
     w = workloads.custom_workload("longrows", [40000, 300, 5000], 32, 8, 128, "bf16", seed=23)
-    _layers_against_single_layer(w, 2, "copy", flags, exact=bool(flags))
+    _layers_against_single_layer(w, 2, "copy", helpers, exact)
 
 
-def _layers_against_single_layer(w, L, metadata, flags, exact):
+def _layers_against_single_layer(w, L, metadata, helpers, exact):
     d = dev()
     bt = w.max_blocks_per_seq(extra_tokens=32)
     k0, v0 = workloads.make_caches(w, "cpu")
     multi = engine.PagedDecoder(w.num_blocks, w.Hq, w.Hkv, w.d, w.dtype, w.B, bt,
                                 initial_free=w.free_order, device=d, n_layers=L,
-                                metadata=metadata, flags=flags,
+                                metadata=metadata, layer_merge_helpers=helpers,
                                 k_cache=torch.stack([k0] * L).to(d),
                                 v_cache=torch.stack([v0] * L).to(d))
     singles = [engine.PagedDecoder(w.num_blocks, w.Hq, w.Hkv, w.d, w.dtype, w.B, bt,

@@ -87,3 +87,19 @@ def test_roofline_peaks():
     assert bench.NOMINAL_HBM_GBS > bench.FALLBACK_HBM_GBS > 0
     peak, kind = bench.measured_peak()
     assert peak > 0 and kind in ("measured", "fallback")
+
+
+def test_long_units_rule():
+    """A unit of n pages counts as long when n * num_parts >= 8 * P (P: pages
+    plus 2 per unit at d = 128, 4 at d = 64, over every unit)."""
+    from paged_kv_decode_10_gb300.engine import long_units
+    # one 131073-token row, 4 KV heads: 8193 pages per unit, P = 4 * 8195
+    assert long_units([131073], 4, 128, 304)
+    assert not long_units([131073], 4, 128, 32)          # 8193 * 32 < 8 * 32780
+    assert long_units([131073], 4, 128, 33)              # 8193 * 33 >= 8 * 32780
+    # 64 rows of at most 4097 tokens over 304 parts: nothing spans 8 parts
+    assert not long_units([4097] * 64, 8, 128, 304)
+    # empty rows add nothing to P; an all-empty step has no long unit
+    assert not long_units([0, 0, 4096], 1, 64, 8)        # 256 * 8 < 8 * 260
+    assert long_units([0, 0, 4096], 1, 64, 9)
+    assert not long_units([0, 0], 8, 128, 304)
