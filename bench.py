@@ -27,6 +27,9 @@ Printed JSON line (rank 0):
                    kernel source (``profiles/traffic.json``)
   rooflines        the same for the workloads named by ``--also`` (default
                    ragged64 and long131k), each set up and timed in this run
+  layered          whole L-layer steps (``--layered``, default decode16 x 8,
+                   ragged64 x 4, long131k x 4): one graph per step, per-layer time
+                   and the layers' attention GB/s
   step_kernels_us  the step's kernels (RoPE/append + attention) without the host
   host_a0_us_per_step  the host allocator per step
   e2e              the same metric through the C ABI's captured host step
@@ -44,6 +47,7 @@ has) on the host cores for the same workload and metric.
 """
 import argparse
 import ctypes
+import gc
 import hashlib
 import json
 import math
@@ -78,6 +82,10 @@ def parse_args():
     ap.add_argument("--workload", default="churn256")
     ap.add_argument("--also", default="ragged64,long131k",
                     help="other workloads whose attention kernel is timed alone in the same "
+                         "run (comma-separated; empty for none)")
+    ap.add_argument("--layered", default="decode16:8,ragged64:4,long131k:4",
+                    help="workload:L pairs whose whole L-layer step (one graph, each layer's "
+                         "kernels overlapping the previous layer's tail) is timed in the same "
                          "run (comma-separated; empty for none)")
     ap.add_argument("--flags", type=int, default=0, help="1 = CUDA-core attention consumer")
     ap.add_argument("--parts", type=int, default=0, help="attention partition (0 = default)")
@@ -455,6 +463,51 @@ def time_graph_launches(g, K, flush, stream, sampler):
     return [e[0].elapsed_time(e[1]) for e in ev]
 
 
+def layered_step(name, L, args, device, flush, stream, sampler, peak):
+    """The whole step of an L-layer decoder (every layer its own pool under the
+    one set of block tables: RoPE/append and attention per layer, each layer's
+    kernels programmatic dependents of the previous layer's) as one CUDA graph,
+    timed after an L2 flush on the state after a few eager steps (metadata read
+    in place, as in the served step).  Per layer: the step time / L, and the
+    layers' algorithmic attention bytes / the step time."""
+    import torch
+    from paged_kv_decode_10_gb300 import workloads
+    w = workloads.make_workload(name)
+    n_eager = 4
+    dec, ids, tokens, _ = setup(w, device, args.parts, args.flags, n_eager, "mapped", L)
+    for s in range(n_eager):
+        dec.step(ids, *tokens[s])
+    B = len(ids)
+    q, k, v = tokens[n_eager - 1]
+    dec.q_ins[:, :B].copy_(q)
+    dec.k_ins[:, :B].copy_(k)
+    dec.v_ins[:, :B].copy_(v)
+    dec.capture(B)
+    torch.cuda.synchronize()
+    elem = 2 if w.dtype == "bf16" else 4
+    ms, nbytes = [], 0
+    with sampler.window():
+        for _ in range(args.steps):
+            dec.wait_host_buffer()
+            lens = np.array(dec.prepare_host(ids)[2])   # a0: each step appends a token
+            nbytes += L * attn_bytes(lens, w.Hq, w.Hkv, w.d, elem)
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            dec.replay_step()
+            b.record(stream)
+            ms.append((a, b))
+        torch.cuda.synchronize()
+    assert dec.device_errors() == 0, f"device error flag set during the {name} layered timing"
+    total_us = 1e3 * sum(x.elapsed_time(y) for x, y in ms)
+    step_us = total_us / len(ms)
+    gbs = nbytes / (total_us * 1e-6) / 1e9
+    return {"workload": name, "layers": L, "step_us": round(step_us, 3),
+            "us_per_layer": round(step_us / L, 3), "attention_gbs": round(gbs, 2),
+            "frac": round(gbs / peak, 4), "merge_helpers": bool(dec._helpers_now),
+            "step": "one graph: per layer RoPE/append + split-KV attention with fused merge"}
+
+
 def attention_roofline(name, args, device, flush, stream, sampler, peak):
     """The attention kernel (a3 + fused a4) alone on another workload, in the
     bench's launch configuration: every row joined, a few eager decode steps,
@@ -769,6 +822,12 @@ def run_gpu(args, rank, world, want_cpu=False):
     rooflines = {}
     for name in [x for x in args.also.split(",") if x and x != w.name]:
         rooflines[name] = attention_roofline(name, args, device, flush, stream, sampler, peak)
+    layered = {}
+    if args.layers == 1:
+        for spec in [x for x in args.layered.split(",") if x]:
+            name, L = spec.split(":")
+            layered[spec] = layered_step(name, int(L), args, device, flush, stream, sampler,
+                                         peak)
     clocks = sampler.stop()
 
     bytes_steps = [args.layers * attn_bytes(la, w.Hq, w.Hkv, w.d, elem) for la in lens_after]
@@ -844,6 +903,7 @@ def run_gpu(args, rank, world, want_cpu=False):
         "gpu_launches": K * args.layers * ((1 if args.flags & 4 else 2) +
                                            (1 if args.flags & 2 else 0)),
         "rooflines": rooflines or None,
+        "layered": layered or None,
         "clocks": clocks,
     }
     return result, dec, ids, tokens, sample, w
@@ -1139,10 +1199,16 @@ def main():
     from paged_kv_decode_10_gb300 import build
     build.build()
     want_cpu = not args.no_cpu and rank == 0 and world == 1
+    # no cyclic garbage collection while GPU work is timed: a collection in the
+    # host's enqueue path leaves the GPU idle between an event and the work it
+    # brackets (single steps of up to ~1 ms were seen)
+    gc.collect()
+    gc.disable()
     result, dec, ids, tokens, sample, w = run_gpu(args, rank, world, want_cpu)
     if rank == 0:
         if not args.no_e2e and args.layers == 1:
             result["e2e"] = run_e2e(args, dec, ids, tokens, w)
+        gc.enable()
         if sample is not None:
             result["cpu_baseline"] = cpu_baseline(sample, args.cpu_seconds)
         if args.comparator and args.layers == 1:
