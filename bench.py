@@ -50,7 +50,6 @@ import ctypes
 import gc
 import hashlib
 import json
-import math
 import os
 import statistics
 import subprocess

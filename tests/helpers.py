@@ -4,9 +4,8 @@ import numpy as np
 import torch
 
 from oracle.allocator import BlockAllocatorModel
-from oracle.numerics import round_to
 from oracle.step import decode_step
-from paged_kv_decode_10_gb300 import binding, engine, workloads
+from paged_kv_decode_10_gb300 import engine, workloads
 
 TOL = {"f32": 1e-5, "bf16": 2e-2}
 

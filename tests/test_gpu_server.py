@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 import torch
 
-from helpers import TOL, assert_out_close, dev, f64
+from helpers import assert_out_close, dev, f64
 from oracle.step import decode_step
 from paged_kv_decode_10_gb300 import binding, engine, workloads
 
