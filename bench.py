@@ -19,12 +19,15 @@ Printed JSON line (rank 0):
   value            whole-job throughput: algorithmic attention bytes of all
                    steps / device time of all steps, GB/s
   steps_per_s      decode steps per second (device time)
-  roofline         the attention kernel (a3 + fused a4) timed alone after the
-                   same flush, with every input in HBM (the step's block
-                   tables, lengths and plan copied to the device):
-                   algorithmic bytes per launch / mean launch time against the
-                   measured HBM copy peak, with the ncu DRAM bytes of the same
-                   kernel source (``profiles/traffic.json``)
+  roofline         the attention kernel (a3 + fused a4) timed alone with every
+                   input in HBM (the step's block tables, lengths and plan
+                   copied to the device): algorithmic bytes per launch / mean
+                   launch time against the measured HBM copy peak, with the ncu
+                   DRAM bytes of the same kernel source
+                   (``profiles/traffic.json``).  Launches that read more than
+                   L2 holds are not flushed (a GPU sleep before each keeps the
+                   GPU busy while the host enqueues; ``l2`` says which), and
+                   ``flushed_launch_us`` gives the same launches after a flush
   rooflines        the same for the workloads named by ``--also`` (default
                    ragged64 and long131k), each set up and timed in this run
   layered          whole L-layer steps (``--layered``, default decode16 x 8,
@@ -101,6 +104,11 @@ def parse_args():
     ap.add_argument("--metadata", default="mapped", choices=["copy", "mapped"],
                     help="per-step metadata: copied to the device, or read in place from "
                          "pinned host memory")
+    ap.add_argument("--launch-check", type=int, default=0, metavar="N",
+                    help="only set the workload up and run N launches (the attention kernel "
+                         "alone, or with --layers L whole L-layer steps), each after the GPU "
+                         "sleep that replaces the L2 flush for inputs larger than L2: the "
+                         "command an ncu capture of consecutive unflushed launches runs")
     return ap.parse_args()
 
 
@@ -447,14 +455,31 @@ def resident_metadata(dec, device):
     return dev(dec.tables), dev(dec.seq_lens), dev(dec.plan)
 
 
-def time_graph_launches(g, K, flush, stream, sampler):
-    """K replays of graph g, each after an L2 flush, between CUDA events on
-    ``stream``; returns the milliseconds of each."""
+def launch_prep(nbytes, flush, l2):
+    """What runs before each timed launch of a graph that reads ``nbytes``, and
+    how the line says so.  Inputs larger than L2 (the timing rules' second
+    option) are not flushed: a ~50 us GPU sleep keeps the GPU busy while the
+    host enqueues, and the kernel's code, parameters and metadata stay in L2 as
+    they do from one step to the next in serving (ncu on consecutive launches
+    of ragged64 and long131k: every KV byte still comes from DRAM).  Smaller
+    inputs get the L2 flush."""
+    import torch
+    if nbytes > l2:
+        return ((lambda: torch.cuda._sleep(100_000)),
+                f"not flushed: inputs of {nbytes / 1e6:.0f} MB per launch > L2 ({l2 / 1e6:.0f} MB);"
+                " a GPU sleep of ~50 us before each launch")
+    return flush, "flushed before every launch (inputs fit in L2)"
+
+
+def time_graph_launches(g, K, prep, stream, sampler):
+    """K replays of graph g, each after ``prep()`` (an L2 flush, or see
+    launch_prep), between CUDA events on ``stream``; returns the milliseconds
+    of each."""
     import torch
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     with sampler.window():
         for i in range(K):
-            flush()
+            prep()
             ev[i][0].record(stream)
             g.replay()
             ev[i][1].record(stream)
@@ -484,13 +509,18 @@ def layered_step(name, L, args, device, flush, stream, sampler, peak):
     dec.capture(B)
     torch.cuda.synchronize()
     elem = 2 if w.dtype == "bf16" else 4
+    lens = np.array(dec.last_metadata[2])
+    # by one layer's bytes: a layer's pool that fits in L2 can keep lines from
+    # the previous step (ncu: decode16's last layer read 23 of its 37 MB from DRAM)
+    prep, how = launch_prep(attn_bytes(lens, w.Hq, w.Hkv, w.d, elem), flush,
+                            torch.cuda.get_device_properties(device).L2_cache_size)
     ms, nbytes = [], 0
     with sampler.window():
         for _ in range(args.steps):
             dec.wait_host_buffer()
             lens = np.array(dec.prepare_host(ids)[2])   # a0: each step appends a token
             nbytes += L * attn_bytes(lens, w.Hq, w.Hkv, w.d, elem)
-            flush()
+            prep()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             dec.replay_step()
@@ -503,15 +533,16 @@ def layered_step(name, L, args, device, flush, stream, sampler, peak):
     gbs = nbytes / (total_us * 1e-6) / 1e9
     return {"workload": name, "layers": L, "step_us": round(step_us, 3),
             "us_per_layer": round(step_us / L, 3), "attention_gbs": round(gbs, 2),
-            "frac": round(gbs / peak, 4), "merge_helpers": bool(dec._helpers_now),
+            "frac": round(gbs / peak, 4), "merge_helpers": bool(dec._helpers_now), "l2": how,
             "step": "one graph: per layer RoPE/append + split-KV attention with fused merge"}
 
 
 def attention_roofline(name, args, device, flush, stream, sampler, peak):
     """The attention kernel (a3 + fused a4) alone on another workload, in the
     bench's launch configuration: every row joined, a few eager decode steps,
-    then K graph launches of the attention call on the final step's state, each
-    after an L2 flush; also the step's kernels (RoPE/append + attention)."""
+    then K graph launches of the attention call on the final step's state (each
+    prepared as launch_prep says, and again each after an L2 flush); also the
+    step's kernels (RoPE/append + attention)."""
     import torch
     from paged_kv_decode_10_gb300 import binding, workloads
     w = workloads.make_workload(name)
@@ -535,11 +566,14 @@ def attention_roofline(name, args, device, flush, stream, sampler, peak):
     with torch.cuda.graph(kern_graph, stream=cap):
         binding.decode_step_args(step_args, cap)
     stream.wait_stream(cap)
-    attn_ms = time_graph_launches(attn_graph, args.steps, flush, stream, sampler)
-    kern_ms = time_graph_launches(kern_graph, args.steps, flush, stream, sampler)
-    assert dec.device_errors() == 0, f"device error flag set during the {name} timing"
     elem = 2 if w.dtype == "bf16" else 4
     ab = attn_bytes(lens, w.Hq, w.Hkv, w.d, elem)
+    prep, how = launch_prep(ab, flush, torch.cuda.get_device_properties(device).L2_cache_size)
+    attn_ms = time_graph_launches(attn_graph, args.steps, prep, stream, sampler)
+    kern_ms = time_graph_launches(kern_graph, args.steps, prep, stream, sampler)
+    flushed_ms = (attn_ms if prep is flush else
+                  time_graph_launches(attn_graph, args.steps, flush, stream, sampler))
+    assert dec.device_errors() == 0, f"device error flag set during the {name} timing"
     gbs = ab / (statistics.mean(attn_ms) / 1e3) / 1e9
     traffic, note = profiled_traffic(name, kernel_source_hash(), ab)
     return {"workload": name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.d,
@@ -549,9 +583,55 @@ def attention_roofline(name, args, device, flush, stream, sampler, peak):
             "traffic": traffic, "traffic_note": note, "algorithmic_bytes_per_launch": int(ab),
             "mean_launch_us": round(1e3 * statistics.mean(attn_ms), 3),
             "median_launch_us": round(1e3 * statistics.median(attn_ms), 3),
-            "frac_of_nominal": round(gbs / NOMINAL_HBM_GBS, 4),
+            "frac_of_nominal": round(gbs / NOMINAL_HBM_GBS, 4), "l2": how,
+            **flushed_fields(ab, flushed_ms, peak),
             "step_kernels_us": round(1e3 * statistics.mean(kern_ms), 3),
             "steps_per_s": round(1e3 / statistics.mean(kern_ms), 1)}
+
+
+def flushed_fields(ab, flushed_ms, peak):
+    """The same launches each after an L2 flush (for comparison)."""
+    us = 1e3 * statistics.mean(flushed_ms)
+    return {"flushed_launch_us": round(us, 3), "flushed_frac": round(ab / (us * 1e-6) / 1e9 / peak, 4)}
+
+
+def launch_check(args):
+    """N launches each after a ~50 us GPU sleep and no L2 flush (see
+    launch_prep): the attention kernel alone on the state after four eager
+    steps, metadata in device memory, or with --layers L whole L-layer steps."""
+    import torch
+    from paged_kv_decode_10_gb300 import binding, workloads
+    device = torch.device("cuda", 0)
+    w = workloads.make_workload(args.workload)
+    dec, ids, tokens, _ = setup(w, device, args.parts, args.flags, 4, "mapped", args.layers)
+    for s in range(4):
+        dec.step(ids, *tokens[s])
+    B = len(ids)
+    if args.layers > 1:
+        q, k, v = tokens[3]
+        dec.q_ins[:, :B].copy_(q)
+        dec.k_ins[:, :B].copy_(k)
+        dec.v_ins[:, :B].copy_(v)
+        dec.capture(B)
+    tables, lens_d, plan = resident_metadata(dec, device)
+    for _ in range(args.launch_check):
+        if args.layers > 1:
+            dec.wait_host_buffer()
+            dec.prepare_host(ids)
+        torch.cuda._sleep(100_000)
+        if args.layers > 1:
+            dec.replay_step()
+        else:
+            binding.decode_attention(dec.q_rot[:B], dec.k_cache, dec.v_cache, tables, lens_d,
+                                     scale=dec.scale, num_parts=dec.num_parts,
+                                     workspace=dec.workspace, out=dec.out[:B], flags=dec.flags,
+                                     err=dec.err, plan=plan)
+    torch.cuda.synchronize()
+    assert dec.device_errors() == 0
+    elem = 2 if w.dtype == "bf16" else 4
+    print(json.dumps({"launch_check": args.launch_check, "workload": w.name,
+                      "layers": args.layers, "algorithmic_bytes_per_launch": int(attn_bytes(
+                          np.array(dec.last_metadata[2]), w.Hq, w.Hkv, w.d, elem))}))
 
 
 def run_gpu(args, rank, world, want_cpu=False):
@@ -704,12 +784,16 @@ def run_gpu(args, rank, world, want_cpu=False):
             binding.decode_step_args(step_args, cap)
     stream.wait_stream(cap)
 
-    def time_graph(g):
-        return time_graph_launches(g, K, flush, stream, sampler)
+    last_lens = lens_after[-1]
+    attn_b = attn_bytes(last_lens, w.Hq, w.Hkv, w.d, elem)
+    prep, prep_how = launch_prep(attn_b, flush, l2)
+
+    def time_graph(g, how=None):
+        return time_graph_launches(g, K, how or prep, stream, sampler)
 
     attn_ms = time_graph(attn_graph)
     kern_ms = time_graph(kern_graph)
-    last_lens = lens_after[-1]
+    flushed_ms = attn_ms if prep is flush else time_graph(attn_graph, flush)
 
     # the same step with the other metadata placement: copied to the device by
     # a copy node at the head of the graph (or, for a decoder that copies,
@@ -834,7 +918,6 @@ def run_gpu(args, rank, world, want_cpu=False):
                for la in lens_after]
     total_s, total_bytes = aggregate_replicas(total_s, sum(bytes_steps), world, device)
     value = total_bytes / total_s / 1e9
-    attn_b = attn_bytes(last_lens, w.Hq, w.Hkv, w.d, elem)
     attn_gbs = attn_b / (statistics.mean(attn_ms) / 1e3) / 1e9
     assert dec.device_errors() == 0, "device error flag set during the bench"
 
@@ -886,6 +969,7 @@ def run_gpu(args, rank, world, want_cpu=False):
                      "median_launch_us": round(1e3 * statistics.median(attn_ms), 3),
                      "nominal_peak": NOMINAL_HBM_GBS,
                      "frac_of_nominal": round(attn_gbs / NOMINAL_HBM_GBS, 4),
+                     "l2": prep_how, **flushed_fields(attn_b, flushed_ms, peak),
                      "kernel_hash": khash},
         "host_a0_us_per_step": round(1e6 * t_host / K, 2),
         "host_churn_us_per_step": round(1e6 * statistics.mean(churn_s), 2) if churn_s else None,
@@ -1197,6 +1281,9 @@ def main():
             backend="nccl", init_method="env://")
     from paged_kv_decode_10_gb300 import build
     build.build()
+    if args.launch_check:
+        launch_check(args)
+        return
     want_cpu = not args.no_cpu and rank == 0 and world == 1
     # no cyclic garbage collection while GPU work is timed: a collection in the
     # host's enqueue path leaves the GPU idle between an event and the work it
