@@ -14,9 +14,13 @@
 //    cost of a unit boundary in pages).  CTA c (one per part, grid =
 //    num_parts) owns positions [c*P/C, (c+1)*P/C) and the pages in them, so
 //    every CTA gets the same pages-plus-boundaries work whatever the length
-//    mix.  A unit split across CTAs leaves one (o, lse) partial per CTA, merged
-//    in the epilogue by the last CTA to finish it (or by the LSE merge kernel);
-//    a unit inside one CTA is written to the output directly.
+//    mix.  The host may state each CTA's start in a plan record (first row,
+//    its offset and length, the first block ids); otherwise the prologue
+//    derives it from a scan of the row lengths.  A unit split across CTAs
+//    leaves one (o, lse) partial per CTA, merged in the epilogue by the last
+//    CTA to finish it, or for long splits by the last H CTAs (merge helpers,
+//    one column slice each, under a cooperative launch), or by the LSE merge
+//    kernel; a unit inside one CTA is written to the output directly.
 //  * Producer warp.  Walks the CTA's unit segments, hands each to the
 //    consumers through a shared-memory slot (a header and the unit's query
 //    rows, bulk-copied), reads block ids 32 at a time (the next segment's
