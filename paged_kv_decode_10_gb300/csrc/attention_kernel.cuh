@@ -476,7 +476,8 @@ __device__ __forceinline__ void mma_begin(MmaState<D> &s, const AttnParams &p, i
 // One 16-token page: tokens t0 .. t0+15 of which the first `valid` count.
 template <int D>
 __device__ __forceinline__ void mma_page(MmaState<D> &s, const AttnParams &p, uint32_t ktile,
-                                         uint32_t vtile, int valid, int b, int t0, int lane) {
+                                         uint32_t vtile, int valid, int b, int t0, int lane,
+                                         bool may_bias) {
   const int r = lane >> 2, c = lane & 3;
   const int mq = lane >> 3;
   const int krow = (lane & 7) + (mq & 1) * 8, kj = mq >> 1;
@@ -496,7 +497,7 @@ __device__ __forceinline__ void mma_page(MmaState<D> &s, const AttnParams &p, ui
 #pragma unroll
   for (int e = 0; e < 4; ++e) sc[e] = (sa[e] + sb[e]) * p.scale_log2;
   // sc[0]: (token r, head 2c)  sc[1]: (r, 2c+1)  sc[2]: (r+8, 2c)  sc[3]: (r+8, 2c+1)
-  if (p.bias) {
+  if (may_bias && p.bias) {
     const float *bias = p.bias + static_cast<size_t>(b) * p.bias_stride + t0;
     if (r < valid) {
       const float x = bias[r] * kLog2e;
@@ -808,7 +809,8 @@ __device__ __forceinline__ void simt_begin(SimtState<T, D, G> &s, const AttnPara
 template <typename T, int D, int G>
 __device__ __forceinline__ void simt_page(SimtState<T, D, G> &s, const AttnParams &p,
                                           const char *ktile, const char *vtile, int valid, int b,
-                                          int t0, int lane, float *pbuf, float *abuf) {
+                                          int t0, int lane, float *pbuf, float *abuf,
+                                          bool may_bias) {
   constexpr int DPL = D / 32;
   constexpr int LPH = 32 / G;
   float sc[kBlockTokens];
@@ -826,7 +828,8 @@ __device__ __forceinline__ void simt_page(SimtState<T, D, G> &s, const AttnParam
     }
     sc[i] = reduce_scatter<G>(part, lane);
   }
-  const float *bias = p.bias ? p.bias + static_cast<size_t>(b) * p.bias_stride + t0 : nullptr;
+  const float *bias =
+      may_bias && p.bias ? p.bias + static_cast<size_t>(b) * p.bias_stride + t0 : nullptr;
   float mx = -INFINITY;
 #pragma unroll
   for (int i = 0; i < kBlockTokens; ++i) {
@@ -894,7 +897,11 @@ __device__ __forceinline__ void simt_stash(SimtState<T, D, G> &s, float *red_acc
 // KIND 1: SIMT consumer with compile-time group G.
 // FUSE: whole-step kernel -- also rotates the step's q/k and appends k/v
 // (a1 + a2), so a decode step is one launch.
-template <typename T, int D, int NW, int NS, int KIND, int G, bool FUSE>
+// PLAN: the launch has a plan that is not checked and no attention bias
+// (p.plan != nullptr, !p.check_plan, p.bias == nullptr): the row-length scan,
+// the plan check and the bias are compiled out, and the smaller kernel runs
+// faster (its instructions come cold at both ends of every CTA).
+template <typename T, int D, int NW, int NS, int KIND, int G, bool FUSE, bool PLAN>
 __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
     attn_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v,
@@ -922,7 +929,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int C = p.num_parts;
-  const bool has_bias = p.bias != nullptr;
+  const bool has_bias = !PLAN && p.bias != nullptr;
   // a kernel launched after this one as a programmatic dependent (the next
   // layer's RoPE/append) may start now; it waits for this grid before it reads
   // anything this grid produces
@@ -958,7 +965,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
   const int nthreads = Q::kThreads;
   // ---- host-planned partition: this part's record (one read; its block ids
   // let the producer issue the first TMA loads without a block-table read) ----
-  const bool planned = p.plan != nullptr;
+  const bool planned = PLAN || p.plan != nullptr;
   const int32_t *rec = planned ? p.plan + static_cast<size_t>(blockIdx.x) * PKV_PLAN_INTS : nullptr;
   int4 rec_h = make_int4(-1, 0, 0, 0), rec_p = make_int4(0, 0, 0, 0);
   int plan_ids = -1;
@@ -970,7 +977,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
   }
   // ---- otherwise (or to check the plan): page counts of all rows,
   // per-thread chunk sums, block-wide scan ----
-  const bool scanned = !planned || p.check_plan;
+  const bool scanned = !PLAN && (!planned || p.check_plan);
   long long P_dev = 0;
   if (scanned) {
     const int chunk = (p.B + nthreads - 1) / nthreads;
@@ -1032,7 +1039,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
   // with a plan, the producer starts from it; checked plans must agree with
   // the partition derived here (otherwise that one is used, and flagged)
   bool use_plan = planned;
-  if (planned && p.check_plan) {
+  if (!PLAN && planned && p.check_plan) {
     bool same = P_plan == P_dev;
     if (same && div_floor(P_dev * blockIdx.x, C) < div_floor(P_dev * (blockIdx.x + 1), C)) {
       const int b = misc[0];
@@ -1136,7 +1143,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
     // table read of the next chunk is then in flight behind them), or the first
     // 32 read from the table (and, when the plan is checked, compared with it)
     int ids, chunk = 32;
-    if (use_plan && !p.check_plan) {
+    if (PLAN || (use_plan && !p.check_plan)) {
       ids = plan_ids;
       chunk = kPlanIds;
     } else {
@@ -1368,7 +1375,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
         if (ready && !stage_bad[st]) {
           const uint32_t kt = smem_u32(smem + st * Q::kStageBytes);
           mma_page<D>(s, p, kt, kt + Q::kTileBytes, min(kBlockTokens, L - j * kBlockTokens), u.b,
-                      j * kBlockTokens, lane);
+                      j * kBlockTokens, lane, !PLAN);
         }
         __syncwarp();
         // a stage is handed back only after its page was seen to land
@@ -1401,7 +1408,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
         if (ready && !stage_bad[st]) {
           const char *kt = reinterpret_cast<const char *>(smem + st * Q::kStageBytes);
           simt_page<T, D, G>(s, p, kt, kt + Q::kTileBytes, min(kBlockTokens, L - j * kBlockTokens),
-                             u.b, j * kBlockTokens, lane, pbuf, abuf);
+                             u.b, j * kBlockTokens, lane, pbuf, abuf, !PLAN);
         }
         __syncwarp();
         if (lane == 0 && ready) mbar_arrive(&empty[st]);
@@ -1582,10 +1589,10 @@ struct AttnVariant {
 template <typename T, int D, int NW, int NS, int KIND, int G>
 struct AttnLauncher {
   using Q = Geo<T, D, NW, NS>;
-  template <bool FUSE>
+  template <bool FUSE, bool PLAN>
   static cudaError_t launch_impl(const CUtensorMap &tk, const CUtensorMap &tv,
                                  const AttnParams &p, cudaStream_t s) {
-    auto kern = attn_split_kernel<T, D, NW, NS, KIND, G, FUSE>;
+    auto kern = attn_split_kernel<T, D, NW, NS, KIND, G, FUSE, PLAN>;
     static std::atomic<unsigned long long> attrs_set{0};
     cudaError_t e = set_attributes_once(attrs_set, [&] {
       cudaError_t r =
@@ -1622,16 +1629,20 @@ struct AttnLauncher {
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }
+  // a launch with an unchecked plan and no bias runs the smaller variant
+  static bool lean(const AttnParams &p) { return p.plan && !p.check_plan && !p.bias; }
   static cudaError_t launch(const CUtensorMap &tk, const CUtensorMap &tv, const AttnParams &p,
                             cudaStream_t s) {
-    return launch_impl<false>(tk, tv, p, s);
+    return lean(p) ? launch_impl<false, true>(tk, tv, p, s)
+                   : launch_impl<false, false>(tk, tv, p, s);
   }
   static cudaError_t launch_step(const CUtensorMap &tk, const CUtensorMap &tv,
                                  const AttnParams &p, cudaStream_t s) {
-    return launch_impl<true>(tk, tv, p, s);
+    return lean(p) ? launch_impl<true, true>(tk, tv, p, s)
+                   : launch_impl<true, false>(tk, tv, p, s);
   }
   static cudaError_t occupancy(int *n) {
-    auto kern = attn_split_kernel<T, D, NW, NS, KIND, G, false>;
+    auto kern = attn_split_kernel<T, D, NW, NS, KIND, G, false, false>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Q::kSmemBytes);
     if (e != cudaSuccess) return e;
