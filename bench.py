@@ -57,7 +57,6 @@ import os
 import statistics
 import subprocess
 import sys
-import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -186,8 +185,11 @@ def attn_bytes(lens_after, Hq, Hkv, d, elem):
 
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons, kept for the timed
-    regions only: ``window()`` brackets a region, and a sample counts when it
-    arrives inside one (or within 20 ms after its end)."""
+    regions only: ``window()`` brackets a region, and a sample counts when its
+    timestamp falls inside one (or within 20 ms after its end).  nvidia-smi
+    writes to a file: no Python thread reads it while GPU work is timed (a
+    reader thread taking the interpreter lock between an event and the launch
+    it brackets left the GPU idle inside the timing)."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -195,38 +197,45 @@ class ClockSampler:
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.lines = []          # (arrival time, line)
+        self.lines = []          # (sample time, line)
         self.windows = []
 
     def start(self):
         """Starts sampling every 10 ms and returns once the first sample is in."""
+        import tempfile
         try:
+            self.fh = tempfile.NamedTemporaryFile("w+", suffix=".csv")
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu=timestamp,{self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "10"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
-            self.thread.start()
+                stdout=self.fh, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
             return
         t_end = time.perf_counter() + 5.0
-        while not self.lines and time.perf_counter() < t_end:
+        while os.path.getsize(self.fh.name) == 0 and time.perf_counter() < t_end:
             time.sleep(0.005)
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append((time.perf_counter(), line.strip()))
+    @staticmethod
+    def _parse(line):
+        """(sample time in seconds since the epoch, the fields after it)."""
+        import datetime
+        ts, _, rest = line.partition(",")
+        try:
+            t = datetime.datetime.strptime(ts.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None, rest.strip()
+        return t, rest.strip()
 
     class _Window:
         def __init__(self, owner):
             self.owner = owner
 
         def __enter__(self):
-            self.t0 = time.perf_counter()
+            self.t0 = time.time()
 
         def __exit__(self, *exc):
-            self.owner.windows.append((self.t0, time.perf_counter() + 0.02))
+            self.owner.windows.append((self.t0, time.time() + 0.02))
 
     def window(self):
         return self._Window(self)
@@ -240,8 +249,12 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-        self.thread.join(timeout=2)
-        inside = [ln for t, ln in self.lines if any(a <= t <= b for a, b in self.windows)]
+        with open(self.fh.name) as f:
+            self.lines = [self._parse(ln) for ln in f if ln.strip()]
+        self.fh.close()
+        # a sample without a readable timestamp counts (never drops a throttle)
+        inside = [ln for t, ln in self.lines
+                  if t is None or any(a <= t <= b for a, b in self.windows)]
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in inside:
