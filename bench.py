@@ -747,21 +747,26 @@ def run_gpu(args, rank, world, want_cpu=False):
     torch.cuda.synchronize()
     sampler = ClockSampler(local)
     sampler.start()
+    # K + 1 steps run in the timed loop and the first is not counted: the first
+    # step of the loop ran up to 8x slower than the rest, after a full untimed
+    # warm-up, for reasons outside the step (a GPU sleep before it did not help)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(K)]
+           for _ in range(K + 1)]
     lens_after = []
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     t_host = 0.0
     with sampler.window():
-        for i in range(K):
+        for i in range(K + 1):
             churn(W + GW + i)
             stage(W + GW + i)
             dec.wait_host_buffer()   # the replay two steps back still reads it
             t0 = time.perf_counter()
-            lens_after.append(np.array(dec.prepare_host(ids)[2]))
-            t_host += time.perf_counter() - t0
+            lens = np.array(dec.prepare_host(ids)[2])
+            if i > 0:
+                t_host += time.perf_counter() - t0
+                lens_after.append(lens)
             flush()   # still running on the GPU when the replay below is enqueued
             evs[i][0].record(stream)
             dec.replay_step()
@@ -769,7 +774,7 @@ def run_gpu(args, rank, world, want_cpu=False):
         torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    step_ms = [a.elapsed_time(b) for a, b in evs]
+    step_ms = [a.elapsed_time(b) for a, b in evs[1:]]
     total_s = sum(step_ms) / 1e3
 
     # The dominant kernel (split-KV attention with its fused merge) timed alone
@@ -841,7 +846,7 @@ def run_gpu(args, rank, world, want_cpu=False):
     sample = None
     if want_cpu:
         meta = [np.array(x) for x in dec.last_metadata]
-        last_tok = tokens[W + GW + K - 1]
+        last_tok = tokens[W + GW + K]
         if args.layers > 1:
             last_tok = tuple(t[0] for t in last_tok)
 
@@ -994,7 +999,7 @@ def run_gpu(args, rank, world, want_cpu=False):
                     + ("copied to device memory by a copy node at the head of the graph"
                        if other_mode == "copy" else "read in place from pinned host memory")
                     + ", against step_kernels_us for this run's placement"},
-        "prefill": prefill_summary([x[1:] for x in prefill_log if x[0] >= W + GW], w, elem,
+        "prefill": prefill_summary([x[1:] for x in prefill_log if x[0] > W + GW], w, elem,
                                    peak),
         "gpu_launches": K * args.layers * ((1 if args.flags & 4 else 2) +
                                            (1 if args.flags & 2 else 0)),
