@@ -372,7 +372,10 @@ int pkv_plan_parts(const int32_t *seq_lens, int32_t B, int32_t Hkv, int32_t d,
                    int32_t num_parts, int32_t *plan);
 
 /* pkv_decode_attn_split with a plan from pkv_plan_parts (device or mapped
- * pointer; num_parts must be the plan's).  Same results, bit for bit. */
+ * pointer; num_parts must be the plan's).  Same results, bit for bit.  Without
+ * PKV_ATTN_CHECK_PLAN and without attn_bias the launch runs a smaller build of
+ * the kernel (no row-length scan, plan check or bias code), which is faster:
+ * the plan is the fast path. */
 int pkv_decode_attn_planned(const void *q_rot, const void *k_cache, const void *v_cache,
                             int32_t num_blocks, const int32_t *block_tables,
                             int32_t bt_stride, const int32_t *seq_lens,
