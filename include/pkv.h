@@ -538,6 +538,16 @@ int pkv_step_graph_create(const pkv_step_args *dev, const pkv_step_host_io *host
                           pkv_step_graph **out);
 /* Launches the captured step on stream and waits for it (host->out is then set). */
 int pkv_step_graph_launch(pkv_step_graph *g, void *stream);
+/*
+ * The same launch without the wait, and the wait on its own: a loop can run
+ * the allocator step (a0, the plan) of step i+1 into a second set of metadata
+ * buffers (a second graph) while the GPU runs step i, then wait for step i's
+ * output and launch step i+1.  The metadata buffers a queued or running step
+ * reads must not be written until pkv_step_wait has returned for it.
+ */
+int pkv_step_graph_enqueue(pkv_step_graph *g, void *stream);
+/* Waits for everything queued on stream (the last enqueued step's output is then set). */
+int pkv_step_wait(void *stream);
 void pkv_step_graph_destroy(pkv_step_graph *g);
 
 /* ======================================================================== */

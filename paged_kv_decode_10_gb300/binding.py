@@ -144,6 +144,8 @@ SIGNATURES = {
     "pkv_step_graph_create": (ctypes.c_int, [ctypes.POINTER(StepArgs),
                                              ctypes.POINTER(StepHostIO), ctypes.POINTER(_vp)]),
     "pkv_step_graph_launch": (ctypes.c_int, [_vp, _vp]),
+    "pkv_step_graph_enqueue": (ctypes.c_int, [_vp, _vp]),
+    "pkv_step_wait": (ctypes.c_int, [_vp]),
     "pkv_step_graph_destroy": (None, [_vp]),
     "pkv_server_meta_bytes": (_size_t, [_c_i32, _c_i32, _c_i32]),
     "pkv_server_prefix_bytes": (_size_t, [_c_i32]),
@@ -708,6 +710,10 @@ class StepGraph:
     def launch(self, stream=None):
         _check(self._lib.pkv_step_graph_launch(self._h, _stream(stream)))
 
+    def enqueue(self, stream=None):
+        """The launch without the wait (see ``step_wait``)."""
+        _check(self._lib.pkv_step_graph_enqueue(self._h, _stream(stream)))
+
     def close(self):
         if self._h:
             self._lib.pkv_step_graph_destroy(self._h)
@@ -718,6 +724,12 @@ class StepGraph:
             self.close()
         except Exception:
             pass
+
+
+def step_wait(stream=None):
+    """``pkv_step_wait``: everything queued on the stream (the last enqueued
+    step's output is then in host memory)."""
+    _check(load().pkv_step_wait(_stream(stream)))
 
 
 def host_io(q, k, v, positions, slot_mapping, seq_lens, block_tables, out, flags=0, plan=None):

@@ -702,6 +702,19 @@ extern "C" int pkv_step_graph_launch(pkv_step_graph *g, void *stream) {
   return PKV_OK;
 }
 
+extern "C" int pkv_step_graph_enqueue(pkv_step_graph *g, void *stream) {
+  clear_error();
+  PKV_REQUIRE(g, PKV_ERR_INVALID_ARG, "NULL graph");
+  PKV_CUDA_CHECK(cudaGraphLaunch(g->exec, static_cast<cudaStream_t>(stream)));
+  return PKV_OK;
+}
+
+extern "C" int pkv_step_wait(void *stream) {
+  clear_error();
+  PKV_CUDA_CHECK(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+  return PKV_OK;
+}
+
 extern "C" void pkv_step_graph_destroy(pkv_step_graph *g) {
   if (!g) return;
   cudaGraphExecDestroy(g->exec);

@@ -720,3 +720,68 @@ def test_step_graph_matches_host_step(flags):
     for a, b in zip(o1, o2):
         assert torch.equal(a, b)
     assert torch.equal(k1, k2) and torch.equal(v1, v2) and e1 == 0 and e2 == 0
+
+
+@pytest.mark.parametrize("flags", [0, 1])
+def test_step_graph_pipelined_matches_sequential(flags):
+    """Two captured host steps over two sets of pinned buffers, launched with
+    pkv_step_graph_enqueue while the host prepares the next set (each set's
+    allocator step keeps its own cached row state, two steps stale), give the
+    outputs and caches of one graph launched and waited for step by step."""
+    w = workloads.make_workload("decode16")
+    d = dev()
+    caches = workloads.make_caches(w, "cpu")
+    S = 5
+    bt = w.max_blocks_per_seq(extra_tokens=S + 2)
+    runs = []
+    for pipelined in (False, True):
+        dec = engine.PagedDecoder(w.num_blocks, w.Hq, w.Hkv, w.d, w.dtype, w.B, bt,
+                                  initial_free=w.free_order, device=d,
+                                  k_cache=caches[0].to(d), v_cache=caches[1].to(d))
+        ids = [dec.join(int(L)) for L in w.seq_lens]
+        q0, k0, v0 = workloads.make_new_tokens(w, 0, "cpu")
+        dq, dk, dv = (torch.empty_like(t, device=d) for t in (q0, k0, v0))
+        meta_d = [torch.empty(w.B, dtype=torch.int32, device=d),
+                  torch.empty(w.B, dtype=torch.int64, device=d),
+                  torch.empty(w.B, dtype=torch.int32, device=d),
+                  torch.empty((w.B, bt), dtype=torch.int32, device=d)]
+        args = binding.make_step_args(dq, dk, dv, dec.q_rot[:w.B], dec.k_rot[:w.B], dec.k_cache,
+                                      dec.v_cache, *meta_d, dec.scale, dec.rope_base,
+                                      dec.num_parts, dec.workspace, dec.out[:w.B], err=dec.err)
+        sets = []
+        for _ in range(2 if pipelined else 1):
+            qkv = tuple(t.pin_memory() for t in (q0, k0, v0))
+            meta_h = (torch.empty(w.B, dtype=torch.int32).pin_memory(),
+                      torch.empty(w.B, dtype=torch.int64).pin_memory(),
+                      torch.empty(w.B, dtype=torch.int32).pin_memory(),
+                      torch.empty((w.B, bt), dtype=torch.int32).pin_memory())
+            out_h = torch.empty_like(q0).pin_memory()
+            io = binding.host_io(*qkv, *meta_h, out_h, flags=flags)
+            prepare = dec.alloc.step_runner(ids, bt, tuple(m.numpy() for m in meta_h),
+                                            row_state=np.full(3 * w.B, -1, np.int32))
+            sets.append((qkv, out_h, prepare, binding.StepGraph(args, io), io))
+        outs = [None] * S
+        for step in range(S):
+            qkv, out_h, prepare, graph, _ = sets[step % len(sets)]
+            for dst, src in zip(qkv, workloads.make_new_tokens(w, step, "cpu")):
+                dst.copy_(src)
+            prepare()
+            if pipelined:
+                if step > 0:
+                    binding.step_wait()
+                    outs[step - 1] = sets[(step - 1) % 2][1].clone()
+                graph.enqueue()
+            else:
+                graph.launch()
+                outs[step] = out_h.clone()
+        if pipelined:
+            binding.step_wait()
+            outs[S - 1] = sets[(S - 1) % 2][1].clone()
+        for s in sets:
+            s[3].close()
+        torch.cuda.synchronize()
+        runs.append((outs, dec.k_cache.clone(), dec.v_cache.clone(), dec.device_errors()))
+    (o1, k1, v1, e1), (o2, k2, v2, e2) = runs
+    for step, (a, b) in enumerate(zip(o1, o2)):
+        assert torch.equal(a, b), step
+    assert torch.equal(k1, k2) and torch.equal(v1, v2) and e1 == 0 and e2 == 0
