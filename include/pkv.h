@@ -539,15 +539,18 @@ int pkv_step_graph_create(const pkv_step_args *dev, const pkv_step_host_io *host
 /* Launches the captured step on stream and waits for it (host->out is then set). */
 int pkv_step_graph_launch(pkv_step_graph *g, void *stream);
 /*
- * The same launch without the wait, and the wait on its own: a loop can run
- * the allocator step (a0, the plan) of step i+1 into a second set of metadata
- * buffers (a second graph) while the GPU runs step i, then wait for step i's
- * output and launch step i+1.  The metadata buffers a queued or running step
- * reads must not be written until pkv_step_wait has returned for it.
+ * The same launch without the wait, and the wait on its own.  Each graph
+ * records its own completion event after every enqueue, so a loop over two
+ * graphs (two sets of host buffers) keeps the GPU busy: prepare step i into
+ * set i%2 (a0, the plan, the new q/k/v), enqueue its graph, then wait for the
+ * graph of step i-1 and read its output while the GPU runs step i.  Host
+ * buffers a queued or running launch reads or writes must not be touched until
+ * pkv_step_graph_wait has returned for that graph.
  */
 int pkv_step_graph_enqueue(pkv_step_graph *g, void *stream);
-/* Waits for everything queued on stream (the last enqueued step's output is then set). */
-int pkv_step_wait(void *stream);
+/* Waits for the last pkv_step_graph_enqueue of g (host->out is then set);
+ * returns at once if g was never enqueued. */
+int pkv_step_graph_wait(pkv_step_graph *g);
 void pkv_step_graph_destroy(pkv_step_graph *g);
 
 /* ======================================================================== */

@@ -145,7 +145,7 @@ SIGNATURES = {
                                              ctypes.POINTER(StepHostIO), ctypes.POINTER(_vp)]),
     "pkv_step_graph_launch": (ctypes.c_int, [_vp, _vp]),
     "pkv_step_graph_enqueue": (ctypes.c_int, [_vp, _vp]),
-    "pkv_step_wait": (ctypes.c_int, [_vp]),
+    "pkv_step_graph_wait": (ctypes.c_int, [_vp]),
     "pkv_step_graph_destroy": (None, [_vp]),
     "pkv_server_meta_bytes": (_size_t, [_c_i32, _c_i32, _c_i32]),
     "pkv_server_prefix_bytes": (_size_t, [_c_i32]),
@@ -711,8 +711,12 @@ class StepGraph:
         _check(self._lib.pkv_step_graph_launch(self._h, _stream(stream)))
 
     def enqueue(self, stream=None):
-        """The launch without the wait (see ``step_wait``)."""
+        """The launch without the wait (``wait`` waits for the last one)."""
         _check(self._lib.pkv_step_graph_enqueue(self._h, _stream(stream)))
+
+    def wait(self):
+        """Waits for this graph's last ``enqueue`` (its output is then set)."""
+        _check(self._lib.pkv_step_graph_wait(self._h))
 
     def close(self):
         if self._h:
@@ -724,12 +728,6 @@ class StepGraph:
             self.close()
         except Exception:
             pass
-
-
-def step_wait(stream=None):
-    """``pkv_step_wait``: everything queued on the stream (the last enqueued
-    step's output is then in host memory)."""
-    _check(load().pkv_step_wait(_stream(stream)))
 
 
 def host_io(q, k, v, positions, slot_mapping, seq_lens, block_tables, out, flags=0, plan=None):

@@ -17,4 +17,8 @@ int default_parts(int D, int dtype, int flags, int G, int *parts);
 // counters (the only bytes a call expects to find zero).
 size_t workspace_counter_bytes(int B, int Hq, int Hkv, int D, int C);
 
+// Shape rules every attention call checks (dtype, head size, B, the group
+// size Hq / Hkv); PKV_OK or the error, with the message set.
+int check_shapes(int B, int Hq, int Hkv, int D, int dtype);
+
 }  // namespace pkv

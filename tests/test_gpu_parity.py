@@ -724,10 +724,11 @@ def test_step_graph_matches_host_step(flags):
 
 @pytest.mark.parametrize("flags", [0, 1])
 def test_step_graph_pipelined_matches_sequential(flags):
-    """Two captured host steps over two sets of pinned buffers, launched with
-    pkv_step_graph_enqueue while the host prepares the next set (each set's
-    allocator step keeps its own cached row state, two steps stale), give the
-    outputs and caches of one graph launched and waited for step by step."""
+    """Two captured host steps over two sets of pinned buffers, each step
+    enqueued behind the running one and the running one then waited for with
+    pkv_step_graph_wait (each set's allocator step keeps its own cached row
+    state, two steps stale), give the outputs and caches of one graph launched
+    and waited for step by step."""
     w = workloads.make_workload("decode16")
     d = dev()
     caches = workloads.make_caches(w, "cpu")
@@ -767,15 +768,16 @@ def test_step_graph_pipelined_matches_sequential(flags):
                 dst.copy_(src)
             prepare()
             if pipelined:
+                graph.enqueue()                 # queued behind step - 1
                 if step > 0:
-                    binding.step_wait()
-                    outs[step - 1] = sets[(step - 1) % 2][1].clone()
-                graph.enqueue()
+                    prev = sets[(step - 1) % 2]
+                    prev[3].wait()
+                    outs[step - 1] = prev[1].clone()
             else:
                 graph.launch()
                 outs[step] = out_h.clone()
         if pipelined:
-            binding.step_wait()
+            sets[(S - 1) % 2][3].wait()
             outs[S - 1] = sets[(S - 1) % 2][1].clone()
         for s in sets:
             s[3].close()
