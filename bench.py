@@ -421,9 +421,9 @@ def host_cores():
 def setup(w, device, parts, flags, steps_total, metadata, n_layers=1):
     import torch
     from paged_kv_decode_10_gb300 import engine, workloads
-    # room for the timed steps, the five end-to-end runs (up to 53 steps each)
+    # room for the timed steps, the six end-to-end runs (up to 53 steps each)
     # and two wall-clock passes over a churn plan (up to 64 steps each)
-    extra_tokens = steps_total + 2 * 64 + 5 * 53 + 64
+    extra_tokens = steps_total + 2 * 64 + 6 * 53 + 64
     bt = w.max_blocks_per_seq(extra_tokens=extra_tokens)
     # The recipe's pool holds 1.25x the blocks of the initial lengths; a long
     # run appends extra_tokens to every row.  Blocks for those go to the bottom
@@ -1166,11 +1166,11 @@ def run_e2e(args, dec, ids, tokens, w):
                 nbytes += attn_bytes(views[2], w.Hq, w.Hkv, w.d, elem)
         return nbytes / secs / 1e9, 1e3 * secs / n
 
-    def host_step(io, planned):
+    def host_step(io, planned, extra_flags=0):
         a = binding.make_step_args(
             dq, dk, dv, dec.q_rot[:B], dec.k_rot[:B], dec.k_cache, dec.v_cache, *meta_d,
             dec.scale, dec.rope_base, dec.num_parts, dec.workspace, dec.out[:B],
-            flags=dec.flags, err=dec.err, plan=plan_d if planned else None)
+            flags=dec.flags | extra_flags, err=dec.err, plan=plan_d if planned else None)
         refs = (ctypes.byref(a), ctypes.byref(io))
         return (lambda: binding._check(call(refs[0], refs[1], stream))), (a, io)
 
@@ -1181,7 +1181,7 @@ def run_e2e(args, dec, ids, tokens, w):
         g = binding.StepGraph(keep[0], io)
         return (lambda: binding._check(launch(g._h, stream))), g
 
-    def pipelined(planned):
+    def pipelined(planned, extra_flags=0):
         """The captured host step with the host's allocator work (a0 + plan) of
         step i+1 running while the GPU runs step i: two graphs over two sets of
         pinned metadata, plan and output buffers, used in turn.  Per step:
@@ -1202,7 +1202,7 @@ def run_e2e(args, dec, ids, tokens, w):
         for meta, plan, out, vw, alloc_step, plan_step in sets:
             io = binding.host_io(*pinned, *meta, out, flags=binding.HOST_IN_PLACE,
                                  plan=plan if planned else None)
-            a, _ = host_step(io, planned)[1]
+            a, _ = host_step(io, planned, extra_flags)[1]
             graphs.append(binding.StepGraph(a, io))
             preps.append((lambda s0=alloc_step, s1=plan_step: (s0(), s1()))
                          if planned else alloc_step)
@@ -1240,6 +1240,11 @@ def run_e2e(args, dec, ids, tokens, w):
         g.close()
     best = min(results, key=lambda k: results[k][1])
     gbs_pipe, ms_pipe = pipelined(best)
+    # the same loop with the whole step in one kernel (PKV_STEP_FUSED): each
+    # part rotates its own units' queries and the owners of the rows' last
+    # pages append, instead of one RoPE/append kernel reading every q/k/v first
+    fused = not (dec.flags & binding.STEP_FUSED) and args.layers == 1
+    gbs_fz, ms_fz = pipelined(best, binding.STEP_FUSED) if fused else (None, None)
     io_in_place = binding.host_io(*pinned, *meta_h, out_h, flags=binding.HOST_IN_PLACE,
                                   plan=plan_h if best else None)
     gbs_p, ms_p = timed(host_step(io_in_place, best)[0], prepare_planned if best else a0)
@@ -1256,9 +1261,13 @@ def run_e2e(args, dec, ids, tokens, w):
                  "the GPU runs step i, " + plan_word(best))
     # A launch that reads more than L2 leaves nothing in it for the next step:
     # the pipelined loop (no flush between steps) is then the end-to-end figure.
+    fz_path = pipe_path + ", PKV_STEP_FUSED (one kernel per step)"
+    fz_faster = fused and ms_fz < ms_pipe
     big = attn_bytes(views[2], w.Hq, w.Hkv, w.d, elem) > l2
-    head = (gbs_pipe, ms_pipe, pipe_path) if big else (gbs, ms, seq_path)
-    tail = (gbs, ms, seq_path) if big else (gbs_pipe, ms_pipe, pipe_path +
+    pipe_best = (gbs_fz, ms_fz, fz_path) if fz_faster else (gbs_pipe, ms_pipe, pipe_path)
+    pipe_other = (gbs_pipe, ms_pipe, pipe_path) if fz_faster else (gbs_fz, ms_fz, fz_path)
+    head = pipe_best if big else (gbs, ms, seq_path)
+    tail = (gbs, ms, seq_path) if big else (pipe_best[0], pipe_best[1], pipe_best[2] +
                                             " (no L2 flush between steps: inputs fit in L2)")
     return {"value": round(head[0], 2), "unit": "GB/s",
             "h2d_bytes_per_step": int(h2d - (0 if best else plan_h.numel() * 4)),
@@ -1267,6 +1276,9 @@ def run_e2e(args, dec, ids, tokens, w):
             "sequential" if big else "pipelined": {
                 "value": round(tail[0], 2), "unit": "GB/s", "ms_per_step": round(tail[1], 4),
                 "path": tail[2]},
+            "pipelined_other_step_form": None if not fused else {
+                "value": round(pipe_other[0], 2), "unit": "GB/s",
+                "ms_per_step": round(pipe_other[1], 4), "path": pipe_other[2]},
             "other_partition": {"value": round(other[0], 2), "unit": "GB/s",
                                 "ms_per_step": round(other[1], 4), "path": plan_word(not best)},
             "without_graph": {"value": round(gbs_p, 2), "unit": "GB/s",

@@ -722,13 +722,15 @@ def test_step_graph_matches_host_step(flags):
     assert torch.equal(k1, k2) and torch.equal(v1, v2) and e1 == 0 and e2 == 0
 
 
-@pytest.mark.parametrize("flags", [0, 1])
-def test_step_graph_pipelined_matches_sequential(flags):
+@pytest.mark.parametrize("flags,fused", [(0, False), (1, False), (1, True)])
+def test_step_graph_pipelined_matches_sequential(flags, fused):
     """Two captured host steps over two sets of pinned buffers, each step
     enqueued behind the running one and the running one then waited for with
     pkv_step_graph_wait (each set's allocator step keeps its own cached row
     state, two steps stale), give the outputs and caches of one graph launched
-    and waited for step by step."""
+    and waited for step by step; with PKV_STEP_FUSED in the pipelined graphs
+    only (the whole step in one kernel, reading q/k/v in place), bit for bit
+    too."""
     w = workloads.make_workload("decode16")
     d = dev()
     caches = workloads.make_caches(w, "cpu")
@@ -748,7 +750,8 @@ def test_step_graph_pipelined_matches_sequential(flags):
                   torch.empty((w.B, bt), dtype=torch.int32, device=d)]
         args = binding.make_step_args(dq, dk, dv, dec.q_rot[:w.B], dec.k_rot[:w.B], dec.k_cache,
                                       dec.v_cache, *meta_d, dec.scale, dec.rope_base,
-                                      dec.num_parts, dec.workspace, dec.out[:w.B], err=dec.err)
+                                      dec.num_parts, dec.workspace, dec.out[:w.B], err=dec.err,
+                                      flags=binding.STEP_FUSED if fused and pipelined else 0)
         sets = []
         for _ in range(2 if pipelined else 1):
             qkv = tuple(t.pin_memory() for t in (q0, k0, v0))
