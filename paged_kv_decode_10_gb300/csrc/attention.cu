@@ -359,6 +359,8 @@ int attn_launch(const void *q_rot, const void *k_cache, const void *v_cache, int
                     step->slot_mapping,
                 PKV_ERR_INVALID_ARG, "NULL step argument");
     PKV_REQUIRE(step->rope_base > 0.0f, PKV_ERR_INVALID_ARG, "rope base must be positive");
+    PKV_REQUIRE((reinterpret_cast<uintptr_t>(step->q) & 15) == 0, PKV_ERR_INVALID_ARG,
+                "the whole-step kernel reads q in 16-byte pieces: q must be 16-byte aligned");
     p.q_new = step->q;
     p.k_new = step->k;
     p.v_new = step->v;

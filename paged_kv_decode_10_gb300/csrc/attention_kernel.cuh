@@ -643,28 +643,18 @@ __device__ __forceinline__ void simt_load_row(const char *tile, int row, int lan
 }
 
 // ---- whole-step kernels: a1 + a2 inside the attention kernel ---------------
-// Rotated queries of unit (b, g) built by the consumer threads into shared
-// memory qs [G][D] (storage type T, rounded once as pkv_rope does); the part
-// that owns the unit's first page also reports them in q_rot_out.  Every load
-// (position, both halves of each pair) is issued before any is used, and each
-// thread forms the angles of its own pairs, so this costs one memory round
-// trip and one barrier.
+// Rotated queries of unit (b, g), built by the consumer threads in place in
+// shared memory qs [G][D]: the producer put the raw rows and the row's
+// position there ahead of the segment (loaded one segment early), so this
+// costs no global round trip, only the angles and one barrier.  Storage type
+// T, rounded once as pkv_rope does; the part that owns the unit's first page
+// also reports the rotated rows in q_rot_out.
 template <typename T, int D, int NTHR>
-__device__ __forceinline__ void fused_rotate_q(const AttnParams &p, int b, int g, bool report,
-                                               T *qs, int tid) {
+__device__ __forceinline__ void fused_rotate_q(const AttnParams &p, int b, int g, uint32_t pos,
+                                               bool report, T *qs, int tid) {
   constexpr int half = D / 2;
   constexpr int KM = (8 * half + NTHR - 1) / NTHR;   // pairs per thread (G <= 8)
   const int npairs = p.G * half;
-  const T *q = static_cast<const T *>(p.q_new) + (static_cast<size_t>(b) * p.Hq + g * p.G) * D;
-  const uint32_t pos = static_cast<uint32_t>(p.positions[b]);
-  float x1[KM], x2[KM];
-#pragma unroll
-  for (int k = 0; k < KM; ++k) {
-    const int e = tid + k * NTHR;
-    const int h = e / half, i = e - h * half;
-    x1[k] = e < npairs ? to_f32(q[h * D + i]) : 0.f;
-    x2[k] = e < npairs ? to_f32(q[h * D + half + i]) : 0.f;
-  }
   T *qo = static_cast<T *>(p.q_rot_out) + (static_cast<size_t>(b) * p.Hq + g * p.G) * D;
 #pragma unroll
   for (int k = 0; k < KM; ++k) {
@@ -673,7 +663,7 @@ __device__ __forceinline__ void fused_rotate_q(const AttnParams &p, int b, int g
       const int h = e / half, i = e - h * half;
       float c, s, y1, y2;
       rope_cossin(pos, p.turns[i], &c, &s);
-      rope_rotate(x1[k], x2[k], c, s, &y1, &y2);
+      rope_rotate(to_f32(qs[h * D + i]), to_f32(qs[h * D + half + i]), c, s, &y1, &y2);
       const T t1 = from_f32<T>(y1), t2 = from_f32<T>(y2);
       qs[h * D + i] = t1;
       qs[h * D + half + i] = t2;
@@ -1127,6 +1117,21 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
       u.off = rowoff * p.Hkv + static_cast<long long>(u.g) * (u.n + A);   // first position
     }
     const uint32_t qbytes = static_cast<uint32_t>(p.G * D * sizeof(T));
+    // FUSE: the raw query rows of the next segment's unit (16-byte pieces,
+    // lane-strided) and its row's position, loaded while the current segment
+    // streams and stored into the segment slot when it is handed over
+    constexpr int kQV = FUSE ? (8 * D * static_cast<int>(sizeof(T))) / (16 * 32) : 1;
+    uint4 qraw[kQV];
+    uint32_t qpos = 0;
+    auto fetch_q = [&](int b, int g) {
+      const uint4 *src = reinterpret_cast<const uint4 *>(
+          static_cast<const T *>(p.q_new) + (static_cast<size_t>(b) * p.Hq + g * p.G) * D);
+      const int nv = static_cast<int>(qbytes / 16);
+#pragma unroll
+      for (int i = 0; i < kQV; ++i)
+        qraw[i] = lane + 32 * i < nv ? src[lane + 32 * i] : make_uint4(0u, 0u, 0u, 0u);
+      qpos = static_cast<uint32_t>(p.positions[b]);
+    };
     int x = 0, k = 0;
     bool aborted = false, waited = FUSE;
     // pages [j0, j1) of unit u lie in this part's positions [start, end); the
@@ -1152,6 +1157,11 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
       if (use_plan && lane < kPlanIds && j0 + lane < j1 && plan_ids != ids)
         set_dev_err(p.err, PKV_DEVERR_BAD_PLAN);
     }
+    if constexpr (FUSE) {
+#pragma unroll
+      for (int i = 0; i < kQV; ++i) qraw[i] = make_uint4(0u, 0u, 0u, 0u);
+      if (j1 > j0) fetch_q(u.b, u.g);
+    }
     while (!aborted) {
       const int32_t *bt = p.block_tables + static_cast<size_t>(u.b) * p.bt_stride;
       // read ahead: the next unit (if the part reaches its pages) and its
@@ -1175,20 +1185,37 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
       // the segment slot: header, then the query rows (after the first batch
       // of pages, so the first pages are on their way before any wait)
       auto send_segment = [&]() {
+        const int slot = k % Q::kSegSlots;
+        unsigned char *sp = smem + Q::kOffSeg + slot * Q::kSegBytes;
+        bool dead = false;
         if (lane == 0) {
-          const int slot = k % Q::kSegSlots;
           const uint32_t sph = static_cast<uint32_t>(k / Q::kSegSlots) & 1u;
-          bool dead = misc[2] != 0;
+          dead = misc[2] != 0;
           if (!dead && !mbar_wait_bounded(&segempty[slot], sph ^ 1u, p.wait_limit)) {
             misc[2] = 1;
             dead = true;
             set_dev_err(p.err, PKV_DEVERR_TIMEOUT);
           }
+        }
+        if constexpr (FUSE) {
+          // the raw query rows, by every lane, once lane 0 has seen the slot
+          // free (the warp barrier orders its wait before the other lanes'
+          // stores)
+          __syncwarp();
+          if (!__shfl_sync(0xffffffffu, dead, 0)) {
+            uint4 *dst = reinterpret_cast<uint4 *>(sp + 64);
+            const int nv = static_cast<int>(qbytes / 16);
+#pragma unroll
+            for (int i = 0; i < kQV; ++i)
+              if (lane + 32 * i < nv) dst[lane + 32 * i] = qraw[i];
+          }
+          __syncwarp();
+        }
+        if (lane == 0) {
           // once anything has given up, nothing more is handed over (the
           // consumers stop too), so no barrier gets an arrival for a phase the
           // other side never finished
           if (!dead) {
-            unsigned char *sp = smem + Q::kOffSeg + slot * Q::kSegBytes;
             int *h = reinterpret_cast<int *>(sp);
             h[0] = u.b;
             h[1] = u.g;
@@ -1203,6 +1230,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
             h[8] = cf;
             h[9] = part_of(u.off + A + u.n - 1, P, C) - cf + 1;
             h[10] = last ? 1 : 0;
+            h[11] = static_cast<int>(qpos);
             if (!FUSE) {
               if (!waited) {
                 pdl_wait();   // the query rows come from the kernel before this one
@@ -1275,11 +1303,19 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
           if (!sent) {
             send_segment();
             sent = true;
+            if constexpr (FUSE) {
+              if (more) fetch_q(nx.b, nx.g);
+            }
           }
         }
         aborted = __shfl_sync(0xffffffffu, misc[2], 0) != 0;
       }
-      if (!sent) send_segment();   // (a part with no page, or aborted before a batch)
+      if (!sent) {   // (a part with no page, or aborted before a batch)
+        send_segment();
+        if constexpr (FUSE) {
+          if (more) fetch_q(nx.b, nx.g);
+        }
+      }
       x += j1 - j0;
       ++k;
       if (!more) break;
@@ -1351,11 +1387,10 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
     if constexpr (KIND == 0) {
       MmaState<D> s;
       if constexpr (FUSE) {
-        T *qs = reinterpret_cast<T *>(red_acc);
-        fused_rotate_q<T, D, kConsumers>(p, u.b, u.g, j0 == 0, qs, tid);
+        T *qs = reinterpret_cast<T *>(const_cast<unsigned char *>(sp) + 64);
+        fused_rotate_q<T, D, kConsumers>(p, u.b, u.g, static_cast<uint32_t>(hdr[11]), j0 == 0, qs,
+                                         tid);
         mma_begin_smem<D>(s, reinterpret_cast<const __nv_bfloat16 *>(qs), p.G, lane);
-        // qs sits in the reduction buffer: nobody stashes before all have read
-        asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
       } else {
         mma_begin_smem<D>(s, reinterpret_cast<const __nv_bfloat16 *>(qslot), p.G, lane);
       }
@@ -1385,10 +1420,10 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
     } else {
       SimtState<T, D, G> s;
       if constexpr (FUSE) {
-        T *qs = reinterpret_cast<T *>(red_acc);
-        fused_rotate_q<T, D, kConsumers>(p, u.b, u.g, j0 == 0, qs, tid);
+        T *qs = reinterpret_cast<T *>(const_cast<unsigned char *>(sp) + 64);
+        fused_rotate_q<T, D, kConsumers>(p, u.b, u.g, static_cast<uint32_t>(hdr[11]), j0 == 0, qs,
+                                         tid);
         simt_begin_smem<T, D, G>(s, qs, p.G, p.scale_log2, lane);
-        asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
       } else {
         simt_begin_smem<T, D, G>(s, qslot, p.G, p.scale_log2, lane);
       }

@@ -537,7 +537,7 @@ def test_graph_replay_matches_eager_steps(metadata):
     assert eager.device_errors() == 0 and graph.device_errors() == 0
 
 
-@pytest.mark.parametrize("name", ["tiny", "decode16", "ragged64", "long131k"])
+@pytest.mark.parametrize("name", ["tiny", "decode16", "ragged64", "churn256", "long131k"])
 def test_whole_step_kernel_equals_split_launch(name):
     """The one-launch step (RoPE and append inside the attention kernel) gives
     bit-identical q_rot, k_rot, caches and output to the default two launches
@@ -547,6 +547,22 @@ def test_whole_step_kernel_equals_split_launch(name):
     tokens = workloads.make_new_tokens(w, 0, "cpu")
     fused = gpu_single_step(w, caches=caches, tokens=tokens, flags=binding.STEP_FUSED)
     split = gpu_single_step(w, caches=caches, tokens=tokens)
+    for key in ("out", "q_rot", "k_rot", "k_cache", "v_cache"):
+        assert torch.equal(fused[key], split[key]), key
+    assert fused["err"] == 0 and split["err"] == 0
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_whole_step_kernel_random_shapes(seed):
+    """The one-launch step on the random batches, head groupings, head sizes,
+    dtypes and partition counts: bit-identical to the two launches."""
+    lens, hq, hkv, d, dtype, parts = _random_case(seed)
+    w = workloads.custom_workload(f"rand{seed}", lens, hq, hkv, d, dtype, seed=seed)
+    caches = workloads.make_caches(w, "cpu")
+    tokens = workloads.make_new_tokens(w, 0, "cpu")
+    fused = gpu_single_step(w, caches=caches, tokens=tokens, num_parts=parts,
+                            flags=binding.STEP_FUSED)
+    split = gpu_single_step(w, caches=caches, tokens=tokens, num_parts=parts)
     for key in ("out", "q_rot", "k_rot", "k_cache", "v_cache"):
         assert torch.equal(fused[key], split[key]), key
     assert fused["err"] == 0 and split["err"] == 0
