@@ -430,7 +430,10 @@ struct Geo {
   // row lengths of the first kLensCache rows, as the prologue read them
   static constexpr int kLensCache = 256;
   static constexpr int kOffLens = kOffSegBars + 2 * kSegSlots * 8;
-  static constexpr int kSmemBytes = kOffLens + kLensCache * 4 + 1024;   // + alignment slack
+  // whole-step kernels: the RoPE turn table, copied from the parameters once
+  // (threads index it by pair, which the parameter bank would serialise)
+  static constexpr int kOffTurns = kOffLens + kLensCache * 4;
+  static constexpr int kSmemBytes = kOffTurns + (D / 2) * 8 + 1024;   // + alignment slack
   static_assert(kSubs >= 1 && D * kElem % 128 == 0, "row must be whole 128-B lines");
   static_assert(NS % NW == 0, "a stage must always feed the same consumer warp");
 };
@@ -650,8 +653,9 @@ __device__ __forceinline__ void simt_load_row(const char *tile, int row, int lan
 // T, rounded once as pkv_rope does; the part that owns the unit's first page
 // also reports the rotated rows in q_rot_out.
 template <typename T, int D, int NTHR>
-__device__ __forceinline__ void fused_rotate_q(const AttnParams &p, int b, int g, uint32_t pos,
-                                               bool report, T *qs, int tid) {
+__device__ __forceinline__ void fused_rotate_q(const AttnParams &p, const unsigned long long *turns,
+                                               int b, int g, uint32_t pos, bool report, T *qs,
+                                               int tid) {
   constexpr int half = D / 2;
   constexpr int KM = (8 * half + NTHR - 1) / NTHR;   // pairs per thread (G <= 8)
   const int npairs = p.G * half;
@@ -662,7 +666,7 @@ __device__ __forceinline__ void fused_rotate_q(const AttnParams &p, int b, int g
     if (e < npairs) {
       const int h = e / half, i = e - h * half;
       float c, s, y1, y2;
-      rope_cossin(pos, p.turns[i], &c, &s);
+      rope_cossin(pos, turns[i], &c, &s);
       rope_rotate(to_f32(qs[h * D + i]), to_f32(qs[h * D + half + i]), c, s, &y1, &y2);
       const T t1 = from_f32<T>(y1), t2 = from_f32<T>(y2);
       qs[h * D + i] = t1;
@@ -686,7 +690,7 @@ template <typename T, int D>
 struct FusedAppend {
   static constexpr int KP = (D / 2 + 31) / 32;   // pairs per lane
   static constexpr int KV = (D + 31) / 32;       // values per lane
-  float x1[KP], x2[KP], v[KV];
+  T x1[KP], x2[KP], v[KV];   // as loaded: converted only when put() needs them
   long long slot;
   uint32_t pos;
 
@@ -699,17 +703,20 @@ struct FusedAppend {
 #pragma unroll
     for (int k = 0; k < KP; ++k) {
       const int i = lane + 32 * k;
-      x1[k] = i < half ? to_f32(kn[i]) : 0.f;
-      x2[k] = i < half ? to_f32(kn[half + i]) : 0.f;
+      if (i < half) {
+        x1[k] = kn[i];
+        x2[k] = kn[half + i];
+      }
     }
 #pragma unroll
     for (int k = 0; k < KV; ++k) {
       const int i = lane + 32 * k;
-      v[k] = i < D ? to_f32(vn[i]) : 0.f;
+      if (i < D) v[k] = vn[i];
     }
   }
 
-  __device__ __forceinline__ void put(const AttnParams &p, int b, int g, int lane) {
+  __device__ __forceinline__ void put(const AttnParams &p, const unsigned long long *turns, int b,
+                                      int g, int lane) {
     constexpr int half = D / 2;
     if (slot >= p.num_slots) {
       if (lane == 0) set_dev_err(p.err, PKV_DEVERR_BAD_SLOT);
@@ -725,8 +732,8 @@ struct FusedAppend {
         const int i = lane + 32 * k;
         if (i < half) {
           float c, s, y1, y2;
-          rope_cossin(pos, p.turns[i], &c, &s);
-          rope_rotate(x1[k], x2[k], c, s, &y1, &y2);
+          rope_cossin(pos, turns[i], &c, &s);
+          rope_rotate(to_f32(x1[k]), to_f32(x2[k]), c, s, &y1, &y2);
           const T t1 = from_f32<T>(y1), t2 = from_f32<T>(y2);
           kc[i] = t1;
           kc[half + i] = t2;
@@ -737,7 +744,7 @@ struct FusedAppend {
 #pragma unroll
       for (int k = 0; k < KV; ++k) {
         const int i = lane + 32 * k;
-        if (i < D) vc[i] = from_f32<T>(v[k]);
+        if (i < D) vc[i] = v[k];
       }
       asm volatile("fence.proxy.async.global;" ::: "memory");
     }
@@ -912,6 +919,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
   volatile int *stage_bad = reinterpret_cast<volatile int *>(smem + Q::kOffBad);
   int *scan = reinterpret_cast<int *>(smem + Q::kOffScan);
   int *lens_s = reinterpret_cast<int *>(smem + Q::kOffLens);
+  unsigned long long *turns_s = reinterpret_cast<unsigned long long *>(smem + Q::kOffTurns);
   volatile int *misc = reinterpret_cast<volatile int *>(smem + Q::kOffMisc);  // b0, rowoff0, abort
   int *stage_pg = reinterpret_cast<int *>(smem + Q::kOffPg);   // [NS], then [kSegSlots]
   int *slot_seg = stage_pg + NS;
@@ -945,6 +953,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
   if (warp == NW && lane == 0) {
     prefetch_tmap(&tmap_k);
     prefetch_tmap(&tmap_v);
+  }
+  if constexpr (FUSE) {   // read after the block-wide barrier below
+    for (int i = tid; i < D / 2; i += Q::kThreads) turns_s[i] = p.turns[i];
   }
 
   // The partition balances pages plus seg_cost per unit: a unit of n pages
@@ -1261,7 +1272,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
             // this part owns the unit's last page: append the step's token
             // before the batch that loads that page
             if (j1 == u.n && jb + i <= u.n - 1 && u.n - 1 < jb + i + kBatch)
-              app.put(p, u.b, u.g, lane);
+              app.put(p, turns_s, u.b, u.g, lane);
           }
           const int blk = __shfl_sync(0xffffffffu, cur_ids, (i + lane) & 31);
           if (lane < kBatch && i + lane < cnt) {
@@ -1388,8 +1399,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
       MmaState<D> s;
       if constexpr (FUSE) {
         T *qs = reinterpret_cast<T *>(const_cast<unsigned char *>(sp) + 64);
-        fused_rotate_q<T, D, kConsumers>(p, u.b, u.g, static_cast<uint32_t>(hdr[11]), j0 == 0, qs,
-                                         tid);
+        fused_rotate_q<T, D, kConsumers>(p, turns_s, u.b, u.g, static_cast<uint32_t>(hdr[11]),
+                                         j0 == 0, qs, tid);
         mma_begin_smem<D>(s, reinterpret_cast<const __nv_bfloat16 *>(qs), p.G, lane);
       } else {
         mma_begin_smem<D>(s, reinterpret_cast<const __nv_bfloat16 *>(qslot), p.G, lane);
@@ -1421,8 +1432,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
       SimtState<T, D, G> s;
       if constexpr (FUSE) {
         T *qs = reinterpret_cast<T *>(const_cast<unsigned char *>(sp) + 64);
-        fused_rotate_q<T, D, kConsumers>(p, u.b, u.g, static_cast<uint32_t>(hdr[11]), j0 == 0, qs,
-                                         tid);
+        fused_rotate_q<T, D, kConsumers>(p, turns_s, u.b, u.g, static_cast<uint32_t>(hdr[11]),
+                                         j0 == 0, qs, tid);
         simt_begin_smem<T, D, G>(s, qs, p.G, p.scale_log2, lane);
       } else {
         simt_begin_smem<T, D, G>(s, qslot, p.G, p.scale_log2, lane);
