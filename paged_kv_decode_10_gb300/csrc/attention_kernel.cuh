@@ -417,8 +417,9 @@ struct Geo {
   static constexpr int kOffScan = kOffBad + NS * 4;
   static constexpr int kOffMisc = kOffScan + (kThreads / 32) * 4;   // 16 ints
   // segment slots: the producer hands each unit segment to the consumers as a
-  // 64-byte header (row, KV head, pages, length, page range, first page) and
-  // the unit's query rows (up to 8 heads), bulk-copied from global memory
+  // 64-byte header (row, KV head, pages, length, page range, first page; FUSE:
+  // the row's position) and the unit's query rows (up to 8 heads): rotated
+  // rows bulk-copied from global memory, or (FUSE) the raw rows it loaded
   static constexpr int kSegSlots = 4;
   static constexpr int kSegQBytes = 8 * D * kElem;
   static constexpr int kSegBytes = 64 + kSegQBytes;
@@ -1086,7 +1087,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, KIND == 0 ? 2 : 1)
   if (warp == NW) {
     // ======================= producer warp =======================
     // Walks the part's unit segments.  For each it hands the consumers a
-    // segment slot (header + the unit's query rows, bulk-copied) and streams
+    // segment slot (header + the unit's query rows) and streams
     // the pages into the ring.  Row lengths of the part's first 64 rows and the
     // next segment's first block ids are read ahead, so a unit boundary costs
     // no dependent global read.
