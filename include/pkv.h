@@ -545,12 +545,19 @@ int pkv_step_graph_launch(pkv_step_graph *g, void *stream);
  * set i%2 (a0, the plan, the new q/k/v), enqueue its graph, then wait for the
  * graph of step i-1 and read its output while the GPU runs step i.  Host
  * buffers a queued or running launch reads or writes must not be touched until
- * pkv_step_graph_wait has returned for that graph.
+ * pkv_step_graph_wait has returned for that graph.  The graphs of one loop
+ * share the device buffers of dev (scratch, caches), so they go on one stream.
+ * Errors: PKV_ERR_INVALID_ARG for a NULL graph; PKV_ERR_CUDA if the launch or
+ * the event record fails (the message names the call).
  */
 int pkv_step_graph_enqueue(pkv_step_graph *g, void *stream);
-/* Waits for the last pkv_step_graph_enqueue of g (host->out is then set);
- * returns at once if g was never enqueued. */
+/* Waits (blocking the calling thread) for the last pkv_step_graph_enqueue of
+ * g; host->out then holds that step's output.  Returns at once if g was never
+ * enqueued.  Errors: PKV_ERR_INVALID_ARG for a NULL graph; PKV_ERR_CUDA if the
+ * step failed on the device (a sticky CUDA error: the context is then lost). */
 int pkv_step_graph_wait(pkv_step_graph *g);
+/* Frees the graph and its event (NULL is ignored); no launch of g may be in
+ * flight. */
 void pkv_step_graph_destroy(pkv_step_graph *g);
 
 /* ======================================================================== */
